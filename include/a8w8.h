@@ -1,0 +1,302 @@
+/*
+ * a8w8.h -- C ABI of the GB300 (sm_103a) A8W8 decode library (liba8w8.so).
+ *
+ * The library runs the decode hot path of a Qwen3-14B-shaped transformer with
+ * INT8 weights and dynamically quantised INT8 activations on one GPU:
+ * per-row activation quantisation, INT8 x INT8 -> INT32 projections with FP32
+ * dequantisation, RMSNorm, per-head QK-RMSNorm + RoPE, a paged BF16 KV cache,
+ * GQA decode attention, SwiGLU, and the LM head with greedy argmax.
+ *
+ * Sources, cited by page title and section:
+ *   [LIB-810] "perf(qwen3-a8w8): optimize decode scheduling and data paths"
+ *             (pypto-lib PR #810): "Decode scheduling", "Gate/Up INT8 path",
+ *             "BF16 KV cache", "Integration note", "Validation".
+ *   [SRV-48]  "Add native Qwen3 14B A8W8 serving path" (pypto-serving PR #48):
+ *             loader review (per-output-channel scales), "Summary" (physical
+ *             decode batch 16, startup validation), "Performance" settings.
+ *   [SRV-52]  "[Feature] Add native Qwen3-14B A8W8 serving path"
+ *             (pypto-serving issue #52): "Current behavior" (fused QK norm +
+ *             Q RoPE), "Measurement basis" (gate/up/silu/down MLP).
+ *   [SRV-61]  "Add Qwen3 A8W8 L2 runner foundation" (pypto-serving PR #61):
+ *             "Summary" (block table / slot mapping packing, padded decode
+ *             rows, KV page bounds validated on the host before dispatch).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller unless a
+ *     parameter says "host". The library never allocates or frees device
+ *     memory on these paths and never synchronises the stream, except where
+ *     an entry point says so.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Work is enqueued asynchronously on it.
+ *   - a8w8_bf16 holds a BF16 bit pattern. Matrices are row-major; weight
+ *     matrices are [N, K] with K contiguous (one row per output channel).
+ *   - Host-side argument validation runs before any launch; on failure
+ *     nothing is enqueued and a negative a8w8_status is returned, with a
+ *     message in a8w8_last_error(). Data-dependent checks (slot, block id,
+ *     context length, token id, RoPE position) run on the device: the
+ *     offending access is skipped and a bit is set in the device error word,
+ *     read with a8w8_read_device_errors(). No kernel traps.
+ *   - Pointers handed to the library must be 16-byte aligned.
+ */
+#ifndef A8W8_H
+#define A8W8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t a8w8_bf16;
+
+typedef enum {
+    A8W8_OK = 0,
+    A8W8_ERR_INVALID_ARG = -1,       /* null pointer, negative size, bad enum */
+    A8W8_ERR_UNSUPPORTED_SHAPE = -2, /* shape outside what the kernels handle */
+    A8W8_ERR_BOUNDS = -3,            /* an index known on the host is out of range */
+    A8W8_ERR_WORKSPACE = -4,         /* workspace missing or too small */
+    A8W8_ERR_CUDA = -5               /* a CUDA runtime call failed */
+} a8w8_status;
+
+/* Device error bits (a8w8_read_device_errors). */
+#define A8W8_DEVERR_SLOT 0x1u        /* slot_mapping entry >= num_blocks * page */
+#define A8W8_DEVERR_BLOCK 0x2u       /* block_table entry outside [0, num_blocks) */
+#define A8W8_DEVERR_CTX 0x4u         /* ctx_len outside [0, max_blocks * page] */
+#define A8W8_DEVERR_TOKEN 0x8u       /* token id outside [0, vocab) */
+#define A8W8_DEVERR_POS 0x10u        /* RoPE position outside the table */
+
+/* Message of the last failed call on this host thread ("" if none). */
+const char* a8w8_last_error(void);
+
+/* ABI version (major * 100 + minor). */
+int a8w8_version(void);
+
+/* Synchronises `stream`, then returns in *bits (host pointer) the device error
+ * word of the current device accumulated since the previous read, and clears
+ * it. */
+a8w8_status a8w8_read_device_errors(unsigned* bits, void* stream);
+
+/* ------------------------------------------------------------------------- */
+/* Model description                                                         */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+    int hidden;           /* H (multiple of 16) */
+    int num_q_heads;      /* Hq */
+    int num_kv_heads;     /* Hkv, divides Hq, Hq / Hkv <= 8 */
+    int head_dim;         /* D: 64 or 128 */
+    int intermediate;     /* I (multiple of 16) */
+    int num_layers;
+    int vocab;
+    int page_size;        /* tokens per KV page */
+    int down_k_splits;    /* 1 or 2 (2 = the pages' two-way split-K down) */
+    float rms_eps;
+} a8w8_config;
+
+/* One layer's weights ([LIB-810] "Gate/Up INT8 path", "Integration note":
+ * INT8 matrices plus FP32 per-output-channel scales; [SRV-48] loader review:
+ * scales broadcast over output channels). */
+typedef struct {
+    const a8w8_bf16* input_norm_w;   /* [H] */
+    const int8_t* w_qkv;             /* [Hq*D + 2*Hkv*D, H]: Q heads, K heads, V heads */
+    const float* s_qkv;              /* [Hq*D + 2*Hkv*D] */
+    const a8w8_bf16* q_norm_w;       /* [D] */
+    const a8w8_bf16* k_norm_w;       /* [D] */
+    const int8_t* w_o;               /* [H, Hq*D] */
+    const float* s_o;                /* [H] */
+    const a8w8_bf16* post_norm_w;    /* [H] */
+    const int8_t* w_gate_up;         /* [2I, H]: gate rows [0, I), up rows [I, 2I) */
+    const float* s_gate_up;          /* [2I] */
+    const int8_t* w_down;            /* [H, I] */
+    const float* s_down;             /* [H] */
+} a8w8_layer_weights;
+
+typedef struct {
+    const a8w8_bf16* embed;              /* [vocab, H] */
+    const a8w8_layer_weights* layers;    /* HOST array of num_layers structs */
+    const a8w8_bf16* final_norm_w;       /* [H] */
+    const a8w8_bf16* lm_head;            /* [vocab, H] */
+} a8w8_model;
+
+/* Optional device buffers that receive a layer's intermediates (any may be
+ * NULL). They serve numerical diagnosis the way the pages' kernel
+ * debug-stage switches do ([SRV-48], quoted kernel PR summary). */
+typedef struct {
+    a8w8_bf16* xn;                     /* [B, H] input RMSNorm output (BF16) */
+    int8_t* xq;        float* xs;      /* [B, H], [B]: its quantised rows */
+    a8w8_bf16* qkv;                    /* [B, Hq*D + 2*Hkv*D]: QKV projection */
+    a8w8_bf16* q_rot;  a8w8_bf16* k_rot;  /* [B, Hq, D], [B, Hkv, D] after norm + RoPE */
+    a8w8_bf16* attn;                   /* [B, Hq*D] attention output */
+    int8_t* aq;        float* as;      /* [B, Hq*D], [B] quantised attention rows */
+    a8w8_bf16* h1;                     /* [B, H] hidden after O + residual */
+    a8w8_bf16* hn;                     /* [B, H] post-attention RMSNorm output */
+    int8_t* hq;        float* hs;      /* [B, H], [B] its quantised rows */
+    a8w8_bf16* act;                    /* [B, I] SwiGLU output */
+    int8_t* actq;      float* acts;    /* [B, I], [B] quantised act rows */
+} a8w8_layer_taps;
+
+/* ------------------------------------------------------------------------- */
+/* Operations                                                                */
+/* ------------------------------------------------------------------------- */
+
+/* Per-row dynamic symmetric INT8 quantisation ([LIB-810] "Decode scheduling":
+ * activation quantisation batched across decode rows; "Gate/Up INT8 path":
+ * quantised once per row). For each row r of x ([rows, cols] BF16, row stride
+ * ldx elements): s = absmax / 127 (IEEE float32 division), q = clamp(rne(x/s),
+ * -127, 127) (IEEE float32 division, ties to even); a zero row gives s = 0,
+ * q = 0. Outputs q [rows, cols] int8 (dense) and row_scale [rows] float.
+ * cols must be a multiple of 8 and ldx a multiple of 8 with ldx >= cols. */
+a8w8_status a8w8_quant_rows(const a8w8_bf16* x, int rows, int cols, int ldx,
+                            int8_t* q, float* row_scale, void* stream);
+
+/* A8W8 projection ([LIB-810] "Gate/Up INT8 path": INT8 x INT8 -> INT32 with
+ * FP32 dequantisation; "Decode scheduling": two-way K parallelism of the down
+ * projection with independent partial accumulators; review "Changes": FP32
+ * partials accumulated, then cast with the residual).
+ *   acc_j[m][n] = sum_{k in split j} xq[m][k] * W[n][k]     (int32, exact)
+ *   p_j = (float(acc_j) * x_scale[m]) * w_scale[n]            (float32)
+ *   y[m][n] = bf16_rne( ((p_0 + p_1) ...) + float(residual[m][n]) )
+ * xq [M, K] int8, x_scale [M], W [N, K] int8, w_scale [N], residual [M, N]
+ * (nullable; may alias y), y [M, N] BF16. acc_out [M, N] int32 (nullable)
+ * receives the full-K sum of the split accumulators. k_splits is 1 or 2 and
+ * splits K into equal contiguous halves. 1 <= M; K a multiple of 16 with K /
+ * k_splits a multiple of 16; N >= 1. */
+a8w8_status a8w8_linear(const int8_t* xq, const float* x_scale, int M, int K,
+                        const int8_t* W, const float* w_scale, int N, int k_splits,
+                        const a8w8_bf16* residual, a8w8_bf16* y, int32_t* acc_out,
+                        void* stream);
+
+/* Fused Gate/Up projection with SwiGLU ([LIB-810] "Gate/Up INT8 path"; [SRV-52]
+ * "Measurement basis"). W_gu [2I, K]: rows [0, I) gate, [I, 2I) up.
+ *   g = (float(acc_gate) * x_scale[m]) * s_gu[j],  u likewise with s_gu[I + j]
+ *   act[m][j] = bf16_rne( silu(g) * u ),  silu(g) = g / (1 + exp(-g)), float32.
+ * acc_out [M, 2I] int32 (nullable). Shape rules as a8w8_linear. */
+a8w8_status a8w8_gate_up_swiglu(const int8_t* xq, const float* x_scale, int M, int K,
+                                const int8_t* W_gu, const float* s_gu, int I,
+                                a8w8_bf16* act, int32_t* acc_out, void* stream);
+
+/* Writes k, v ([T, Hkv, D] BF16) into the paged caches at
+ * slot_mapping[t] ([LIB-810] "BF16 KV cache": BF16 storage, no scale tensors;
+ * [SRV-61] "Summary": slot mapping). Caches are [num_blocks * page_size, Hkv,
+ * D] BF16. slot < 0 skips the token (padded row); slot >= num_blocks *
+ * page_size is skipped and flags A8W8_DEVERR_SLOT. */
+a8w8_status paged_kv_write(const a8w8_bf16* k, const a8w8_bf16* v, int T, int Hkv, int D,
+                           const int32_t* slot_mapping, a8w8_bf16* k_cache,
+                           a8w8_bf16* v_cache, int num_blocks, int page_size, void* stream);
+
+/* GQA decode attention over the paged BF16 cache ([LIB-810] "BF16 KV cache":
+ * attention loads BF16 K/V with no per-row dequantisation; [SRV-61]: block
+ * table). For request b, query head h (KV head h / (Hq / Hkv)) and its
+ * ctx_lens[b] tokens t at slot block_table[b][t / page] * page + t % page:
+ *   out = sum_t softmax_t(softmax_scale * <q, K_t>) V_t   (float32, split-KV
+ *   with online-softmax partials), narrowed to BF16 once.
+ * q [B, Hq, D]; block_table [B, max_blocks]; ctx_lens [B] (0 = padded row,
+ * zero output); out [B, Hq, D]. ws: device workspace of at least
+ * a8w8_attention_workspace_bytes(B, Hq, D, max_blocks * page_size) bytes
+ * (split-KV partials; may be NULL when that is 0). D is 64 or 128, Hq / Hkv
+ * <= 8. Calls that share a workspace must not overlap on the GPU. */
+a8w8_status paged_decode_attention_bf16(const a8w8_bf16* q, const a8w8_bf16* k_cache,
+                                        const a8w8_bf16* v_cache,
+                                        const int32_t* block_table, const int32_t* ctx_lens,
+                                        int B, int Hq, int Hkv, int D, int page_size,
+                                        int max_blocks, int num_blocks, float softmax_scale,
+                                        a8w8_bf16* out, void* ws, size_t ws_bytes,
+                                        void* stream);
+
+size_t a8w8_attention_workspace_bytes(int B, int Hq, int D, int max_ctx);
+
+/* Fills the RoPE table used by the layer: rope[p][i] = cos(p * theta^(-2i/D))
+ * and rope[p][D/2 + i] = sin(p * theta^(-2i/D)) for i < D/2, p < max_pos,
+ * computed in double and rounded to float ([SRV-52] "Current behavior": Q/K
+ * RoPE of the fused QK-norm path; reading: Qwen3 rotate-half, theta from the
+ * model). rope: device [max_pos, D] float. */
+a8w8_status a8w8_rope_table(float* rope, int max_pos, int D, double theta, void* stream);
+
+/* Bytes of workspace a8w8_decode_layer / a8w8_decode_step need for batches of
+ * up to max_B rows and block tables of max_blocks entries. */
+size_t a8w8_workspace_bytes(const a8w8_config* cfg, int max_B, int max_blocks);
+
+/* One A8W8 decode layer on B rows (the method's steps, in order): input
+ * RMSNorm, per-row INT8 quantisation, QKV projection, per-head QK RMSNorm,
+ * RoPE at position ctx_lens[b] - 1, KV write at slot_mapping[b], paged GQA
+ * attention over ctx_lens[b] tokens (the decoded token included), quantisation,
+ * O projection + residual, post-attention RMSNorm + quantisation, Gate/Up +
+ * SwiGLU, quantisation, split-K down projection + residual.
+ * hidden [B, H] BF16 is updated in place. k_cache / v_cache: this layer's
+ * [num_blocks * page, Hkv, D] caches. slot_mapping [B], block_table
+ * [B, max_blocks], ctx_lens [B]: padded rows ([SRV-61]) have slot -1 and
+ * ctx_len 0; they write no KV and attend to nothing. rope: table from
+ * a8w8_rope_table with max_pos rows. ws / ws_bytes: a8w8_workspace_bytes.
+ * taps: NULL, or intermediates to capture. 1 <= B <= 64. */
+a8w8_status a8w8_decode_layer(const a8w8_layer_weights* w, const a8w8_config* cfg, int B,
+                              a8w8_bf16* hidden, const int32_t* slot_mapping,
+                              const int32_t* block_table, int max_blocks, int num_blocks,
+                              const int32_t* ctx_lens, a8w8_bf16* k_cache, a8w8_bf16* v_cache,
+                              const float* rope, int max_pos, void* ws, size_t ws_bytes,
+                              const a8w8_layer_taps* taps, void* stream);
+
+/* One decode step: embedding gather of token_ids [B], the num_layers layers,
+ * final RMSNorm, BF16 LM head with FP32 logits and greedy argmax (lowest index
+ * on ties) into next_tokens [B] int32 ([SRV-48] "Performance": temperature 0,
+ * top_p 1; [SRV-61] "Related": device-side embedding and sampling).
+ * k_caches / v_caches: HOST arrays of num_layers device cache pointers.
+ * logits [B, vocab] float (nullable), final_hidden [B, H] BF16 (nullable:
+ * the normalised last hidden state). Other arguments as a8w8_decode_layer. */
+a8w8_status a8w8_decode_step(const a8w8_model* m, const a8w8_config* cfg, int B,
+                             const int32_t* token_ids, const int32_t* slot_mapping,
+                             const int32_t* block_table, int max_blocks, int num_blocks,
+                             const int32_t* ctx_lens, a8w8_bf16* const* k_caches,
+                             a8w8_bf16* const* v_caches, const float* rope, int max_pos,
+                             int32_t* next_tokens, float* logits, a8w8_bf16* final_hidden,
+                             void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------- */
+/* Replayable decode step                                                    */
+/* ------------------------------------------------------------------------- */
+
+/* A decode step captured once into a CUDA graph with programmatic dependent
+ * launches between its kernels, then replayed. The graph reads its per-step
+ * inputs from caller-owned device buffers given at creation -- token_ids [B],
+ * slot_mapping [B], block_table [B, max_blocks], ctx_lens [B] -- and writes
+ * next_tokens [B]; the caller may rewrite the inputs between replays.
+ * With device_loop != 0 the graph ends with a kernel that prepares the next
+ * step on the device: token_ids = next_tokens, and for every live row
+ * (ctx_len > 0) the context grows by one token whose slot is taken from the
+ * block table; a row whose context is full becomes a padded row (ctx_len 0,
+ * slot -1). Replaying such a graph n times decodes n tokens greedily with no
+ * host involvement. Creation captures on a private stream after
+ * synchronising `stream`; it must not run while `stream` is being captured.
+ * The model, caches, rope table, workspace, input/output buffers and optional
+ * logits / final_hidden are borrowed and must outlive the graph. */
+typedef struct a8w8_step_graph a8w8_step_graph;
+
+a8w8_status a8w8_step_graph_create(a8w8_step_graph** out, const a8w8_model* m,
+                                   const a8w8_config* cfg, int B, int max_blocks,
+                                   int num_blocks, a8w8_bf16* const* k_caches,
+                                   a8w8_bf16* const* v_caches, const float* rope,
+                                   int max_pos, int32_t* token_ids, int32_t* slot_mapping,
+                                   int32_t* block_table, int32_t* ctx_lens,
+                                   int32_t* next_tokens, float* logits,
+                                   a8w8_bf16* final_hidden, int device_loop, void* ws,
+                                   size_t ws_bytes, void* stream);
+
+/* Replays the step on `stream`. */
+a8w8_status a8w8_step_graph_launch(a8w8_step_graph* g, void* stream);
+
+/* End-to-end step from HOST buffers: copies token_ids [B], slot_mapping [B],
+ * block_table [B, max_blocks] and ctx_lens [B] from host memory (pinned for
+ * best speed) into the graph's device input buffers, replays the step, copies
+ * next_tokens [B] back to host memory, and synchronises `stream`. */
+a8w8_status a8w8_step_graph_run_host(a8w8_step_graph* g, const int32_t* token_ids,
+                                     const int32_t* slot_mapping,
+                                     const int32_t* block_table, const int32_t* ctx_lens,
+                                     int32_t* next_tokens, void* stream);
+
+void a8w8_step_graph_destroy(a8w8_step_graph* g);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* A8W8_H */

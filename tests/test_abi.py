@@ -1,0 +1,142 @@
+"""The C-ABI library loads, exports every declared entry point, and rejects bad
+arguments on the host before touching the GPU (no compute call is made)."""
+import ctypes
+
+import pytest
+
+import synth
+import w8a8_quantized_decode_gb300 as a8w8
+
+
+@pytest.fixture(scope="module")
+def lib():
+    a8w8.build()
+    return a8w8.lib()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = a8w8.header_functions()
+    assert len(names) >= 17
+    for n in names:
+        assert hasattr(lib, n), n
+    # the binding wraps every declared entry point
+    assert set(names) <= set(a8w8._SIGNATURES)
+
+
+def test_version(lib):
+    assert lib.a8w8_version() == 100
+
+
+FAKE = 0x10000   # a 16-byte aligned non-null address; never dereferenced by the host checks
+
+
+def test_linear_validation(lib):
+    L = lib
+    assert L.a8w8_linear(None, FAKE, 1, 32, FAKE, FAKE, 4, 1, None, FAKE, None, None) == a8w8.ERR_INVALID_ARG
+    assert b"NULL" in L.a8w8_last_error()
+    assert L.a8w8_linear(FAKE, FAKE, 1, 24, FAKE, FAKE, 4, 1, None, FAKE, None, None) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert L.a8w8_linear(FAKE, FAKE, 1, 32, FAKE, FAKE, 4, 3, None, FAKE, None, None) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert L.a8w8_linear(FAKE, FAKE, 1, 48, FAKE, FAKE, 4, 2, None, FAKE, None, None) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert L.a8w8_linear(FAKE + 4, FAKE, 1, 32, FAKE, FAKE, 4, 1, None, FAKE, None, None) == a8w8.ERR_INVALID_ARG
+    assert L.a8w8_linear(FAKE, FAKE, -1, 32, FAKE, FAKE, 4, 1, None, FAKE, None, None) == a8w8.ERR_INVALID_ARG
+    # empty problems are a no-op
+    assert L.a8w8_linear(None, None, 0, 32, None, None, 4, 1, None, None, None, None) == a8w8.OK
+    assert L.a8w8_gate_up_swiglu(FAKE, FAKE, 1, 20, FAKE, FAKE, 4, FAKE, None, None) == a8w8.ERR_UNSUPPORTED_SHAPE
+
+
+def test_quant_and_kv_validation(lib):
+    L = lib
+    assert L.a8w8_quant_rows(FAKE, 2, 12, 12, FAKE, FAKE, None) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert L.a8w8_quant_rows(FAKE, 2, 16, 8, FAKE, FAKE, None) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert L.a8w8_quant_rows(None, 2, 16, 16, FAKE, FAKE, None) == a8w8.ERR_INVALID_ARG
+    assert L.a8w8_quant_rows(None, 0, 16, 16, None, None, None) == a8w8.OK
+    assert L.paged_kv_write(FAKE, FAKE, 1, 1, 4, FAKE, FAKE, FAKE, 1, 16, None) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert L.paged_kv_write(None, FAKE, 1, 2, 64, FAKE, FAKE, FAKE, 1, 16, None) == a8w8.ERR_INVALID_ARG
+    assert L.paged_kv_write(None, None, 0, 2, 64, None, None, None, 1, 16, None) == a8w8.OK
+
+
+def test_attention_validation(lib):
+    L = lib
+    args = lambda D, Hq, Hkv, ws, wsb: (FAKE, FAKE, FAKE, FAKE, FAKE, 2, Hq, Hkv, D, 128, 40, 100,
+                                        0.1, FAKE, ws, wsb, None)
+    assert L.paged_decode_attention_bf16(*args(96, 8, 2, None, 0)) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert L.paged_decode_attention_bf16(*args(128, 9, 2, None, 0)) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert L.paged_decode_attention_bf16(*args(128, 32, 2, None, 0)) == a8w8.ERR_UNSUPPORTED_SHAPE
+    # 40 blocks of 128 tokens need split-KV partials: a missing workspace is reported
+    need = L.a8w8_attention_workspace_bytes(2, 8, 128, 40 * 128)
+    assert need > 0
+    assert L.paged_decode_attention_bf16(*args(128, 8, 2, None, 0)) == a8w8.ERR_WORKSPACE
+    assert L.paged_decode_attention_bf16(*args(128, 8, 2, FAKE, need - 1)) == a8w8.ERR_WORKSPACE
+    # short contexts need none
+    assert L.a8w8_attention_workspace_bytes(1, 40, 128, 256) == 0
+
+
+def _cfg(c):
+    return ctypes.byref(a8w8.make_config(c))
+
+
+def test_workspace_sizes(lib):
+    q = synth.QWEN3_14B
+    small = lib.a8w8_workspace_bytes(_cfg(q), 1, 2)
+    big = lib.a8w8_workspace_bytes(_cfg(q), 16, 33)
+    assert 0 < small < big
+    # at least the activations the layer keeps: qkv, attention output, SwiGLU output, hidden
+    H, I = q["hidden"], q["intermediate"]
+    assert small >= 2 * (H + 7168 + 40 * 128 + I)
+    assert lib.a8w8_workspace_bytes(None, 1, 1) == 0
+    assert lib.a8w8_workspace_bytes(_cfg(q), 0, 1) == 0
+
+
+def test_layer_and_step_validation(lib):
+    L = lib
+    q = synth.QWEN3_14B
+    w = a8w8.LayerWeights(*([FAKE] * len(a8w8.WEIGHT_FIELDS)))
+    base = dict(B=1, max_blocks=2, num_blocks=4, rope=FAKE, max_pos=256, ws=FAKE, wsb=1 << 30)
+
+    def call(cfg, w=w, **kw):
+        a = dict(base, **kw)
+        return L.a8w8_decode_layer(ctypes.byref(w), _cfg(cfg), a["B"], FAKE, FAKE, FAKE,
+                                   a["max_blocks"], a["num_blocks"], FAKE, FAKE, FAKE, a["rope"],
+                                   a["max_pos"], a["ws"], a["wsb"], None, None)
+    assert call(dict(q, head_dim=96)) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert call(dict(q, num_kv_heads=7)) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert call(dict(q, down_k_splits=3)) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert call(dict(q, hidden=5128)) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert call(q, B=0) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert call(q, B=65) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert call(q, rope=None) == a8w8.ERR_INVALID_ARG
+    assert call(q, wsb=1000) == a8w8.ERR_WORKSPACE
+    bad = a8w8.LayerWeights(*([FAKE] * len(a8w8.WEIGHT_FIELDS)))
+    bad.w_down = None
+    assert call(q, w=bad) == a8w8.ERR_INVALID_ARG
+    assert L.a8w8_decode_layer(None, _cfg(q), 1, FAKE, FAKE, FAKE, 2, 4, FAKE, FAKE, FAKE, FAKE,
+                               256, FAKE, 1 << 30, None, None) == a8w8.ERR_INVALID_ARG
+
+    # step: null model, and vocab must be set
+    caches = (ctypes.c_void_p * 1)(FAKE)
+    assert L.a8w8_decode_step(None, _cfg(dict(q, num_layers=1)), 1, FAKE, FAKE, FAKE, 2, 4, FAKE,
+                              caches, caches, FAKE, 256, FAKE, None, None, FAKE, 1 << 30,
+                              None) == a8w8.ERR_INVALID_ARG
+    layers = (a8w8.LayerWeights * 1)(w)
+    m = a8w8.Model(FAKE, ctypes.cast(layers, ctypes.c_void_p), FAKE, FAKE)
+    assert L.a8w8_decode_step(ctypes.byref(m), _cfg(dict(q, num_layers=1, vocab=0)), 1, FAKE, FAKE,
+                              FAKE, 2, 4, FAKE, caches, caches, FAKE, 256, FAKE, None, None, FAKE,
+                              1 << 30, None) == a8w8.ERR_INVALID_ARG
+    assert L.a8w8_decode_step(ctypes.byref(m), _cfg(dict(q, num_layers=1)), 1, FAKE, FAKE, FAKE, 2,
+                              4, FAKE, caches, caches, FAKE, 256, FAKE, None, None, FAKE, 100,
+                              None) == a8w8.ERR_WORKSPACE
+    # graph creation validates the same way and returns no handle
+    out = ctypes.c_void_p(123)
+    assert L.a8w8_step_graph_create(ctypes.byref(out), ctypes.byref(m),
+                                    _cfg(dict(q, num_layers=1)), 1, 2, 4, caches, caches, FAKE,
+                                    256, None, None, FAKE, 100, None) == a8w8.ERR_WORKSPACE
+    assert out.value is None
+    assert L.a8w8_step_graph_launch(None, None) == a8w8.ERR_INVALID_ARG
+    L.a8w8_step_graph_destroy(None)
+
+
+def test_rope_table_validation(lib):
+    assert lib.a8w8_rope_table(FAKE, 16, 63, 1e6, None) == a8w8.ERR_INVALID_ARG
+    assert lib.a8w8_rope_table(FAKE, 16, 64, 0.0, None) == a8w8.ERR_INVALID_ARG
+    assert lib.a8w8_rope_table(None, 16, 64, 1e6, None) == a8w8.ERR_INVALID_ARG
+    assert lib.a8w8_rope_table(None, 0, 64, 1e6, None) == a8w8.OK

@@ -1,0 +1,157 @@
+"""GPU parity of the fused decode layer against the oracle.
+
+Stage by stage (through the layer's taps), every integer decision is checked
+bit for bit on the GPU's own inputs: the INT8 codes and scales of each
+quantised row, and every projection output given the GPU's quantised rows.
+Floating-point stages are checked against the oracle within a few BF16 units,
+and the whole layer against the oracle's layer at the stated bar.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import (assert_layer_close, bf16_to_f64, bf16_ulp_diff, rel_l2, to_dev,
+                      to_host)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def a8w8():
+    import w8a8_quantized_decode_gb300 as m
+    m.build()
+    return m
+
+
+def _run_gpu_layer(a8w8, cfg, case, with_taps=True):
+    import torch
+    w = {k: to_dev(v) for k, v in case["weights"].items()}
+    hidden = to_dev(case["hidden"])
+    kc, vc = to_dev(case["k_cache"]), to_dev(case["v_cache"])
+    bt = to_dev(case["block_table"])
+    max_pos = int(case["block_table"].shape[1] * cfg["page_size"])
+    rope = a8w8.a8w8_rope_table(max_pos, cfg["head_dim"], cfg["rope_theta"])
+    ws = a8w8.alloc_workspace(cfg, hidden.shape[0], bt.shape[1])
+    taps = a8w8.make_taps(cfg, hidden.shape[0]) if with_taps else None
+    a8w8.read_device_errors()
+    a8w8.a8w8_decode_layer(w, cfg, hidden, to_dev(case["slot_mapping"]), bt,
+                           to_dev(case["ctx_lens"]), kc, vc, rope, ws, taps=taps)
+    torch.cuda.synchronize()
+    assert a8w8.read_device_errors() == 0
+    t = {k: to_host(v) for k, v in taps.items()} if taps else None
+    return to_host(hidden), t, to_host(kc), to_host(vc)
+
+
+def _check_stages(cfg, case, out, t, kc, vc):
+    """Each stage recomputed by the oracle from the GPU's own previous stage."""
+    w = case["weights"]
+    eps, D = cfg["rms_eps"], cfg["head_dim"]
+    Hq, Hkv, I = cfg["num_q_heads"], cfg["num_kv_heads"], cfg["intermediate"]
+    B = case["hidden"].shape[0]
+    NQ, NK = Hq * D, Hkv * D
+    report = {}
+    # a2: input RMSNorm (float32 vs double): within one BF16 ulp
+    xn = oracle.rmsnorm(case["hidden"], w["input_norm_w"], eps)
+    d = bf16_ulp_diff(t["xn"], xn)
+    assert d.max() <= 1, d.max()
+    report["xn_ulp_eq"] = float((d == 0).mean())
+    # a3: quantisation of the GPU's row -- bit exact
+    q, s = oracle.quant_rows(t["xn"])
+    assert np.array_equal(t["xq"], q) and np.array_equal(t["xs"], s)
+    # a4: QKV of the GPU's codes -- bit exact
+    qkv, _ = oracle.linear(t["xq"], t["xs"], w["w_qkv"], w["s_qkv"])
+    assert np.array_equal(t["qkv"], qkv)
+    # a5-a6: QK norm + RoPE of the GPU's qkv (float32 vs double)
+    pos = case["ctx_lens"].astype(np.int32) - 1
+    live = case["ctx_lens"] > 0
+    qh = oracle.rope(oracle.rmsnorm(t["qkv"][:, :NQ].reshape(B, Hq, D), w["q_norm_w"], eps),
+                     np.maximum(pos, 0), cfg["rope_theta"])
+    kh = oracle.rope(oracle.rmsnorm(t["qkv"][:, NQ:NQ + NK].reshape(B, Hkv, D), w["k_norm_w"], eps),
+                     np.maximum(pos, 0), cfg["rope_theta"])
+    assert bf16_ulp_diff(t["q_rot"][live], qh[live]).max() <= 2
+    assert bf16_ulp_diff(t["k_rot"][live], kh[live]).max() <= 2
+    # a7: the new token's K/V landed in its slot, nothing else changed
+    for b in range(B):
+        sl = case["slot_mapping"][b]
+        if sl >= 0:
+            assert np.array_equal(kc[sl], t["k_rot"][b])
+            assert np.array_equal(vc[sl], t["qkv"][b, NQ + NK:].reshape(Hkv, D))
+    mask = np.ones(kc.shape[0], bool)
+    mask[case["slot_mapping"][case["slot_mapping"] >= 0]] = False
+    assert np.array_equal(kc[mask], case["k_cache"][mask])
+    assert np.array_equal(vc[mask], case["v_cache"][mask])
+    # a8: attention over the GPU's cache with the GPU's rotated q
+    att, rc = oracle.paged_attention(t["q_rot"], kc, vc, case["block_table"], case["ctx_lens"],
+                                     cfg["page_size"])
+    assert rc == 0
+    att = att.reshape(B, NQ)
+    assert rel_l2(bf16_to_f64(t["attn"]), bf16_to_f64(att)) <= 2e-3
+    assert bf16_ulp_diff(t["attn"], att).max() <= 2
+    # a9-a10: quantisation and O projection + residual -- bit exact
+    aq, as_ = oracle.quant_rows(t["attn"])
+    assert np.array_equal(t["aq"], aq) and np.array_equal(t["as"], as_)
+    h1, _ = oracle.linear(t["aq"], t["as"], w["w_o"], w["s_o"], 1, case["hidden"])
+    assert np.array_equal(t["h1"], h1)
+    # a11: post-attention norm (one ulp) and its quantisation (exact)
+    hn = oracle.rmsnorm(t["h1"], w["post_norm_w"], eps)
+    assert bf16_ulp_diff(t["hn"], hn).max() <= 1
+    hq, hs = oracle.quant_rows(t["hn"])
+    assert np.array_equal(t["hq"], hq) and np.array_equal(t["hs"], hs)
+    # a12: gate/up + SwiGLU of the GPU's codes (silu float32 vs double: one ulp)
+    act, _ = oracle.gate_up_swiglu(t["hq"], t["hs"], w["w_gate_up"], w["s_gate_up"])
+    assert bf16_ulp_diff(t["act"], act).max() <= 1
+    # a13-a14: quantisation and split-K down projection + residual -- bit exact
+    dq, ds = oracle.quant_rows(t["act"])
+    assert np.array_equal(t["actq"], dq) and np.array_equal(t["acts"], ds)
+    o, _ = oracle.linear(t["actq"], t["acts"], w["w_down"], w["s_down"], cfg["down_k_splits"],
+                         t["h1"])
+    assert np.array_equal(out, o)
+    return report
+
+
+def _layer_parity(a8w8, cfg, case):
+    out, t, kc, vc = _run_gpu_layer(a8w8, cfg, case)
+    _check_stages(cfg, case, out, t, kc, vc)
+    # whole layer against the oracle's own layer from the same inputs
+    okc, ovc = case["k_cache"].copy(), case["v_cache"].copy()
+    ref, _, rc = oracle.decode_layer(case["weights"], cfg, case["hidden"], case["slot_mapping"],
+                                     case["block_table"], case["ctx_lens"], okc, ovc)
+    assert rc == 0
+    return assert_layer_close(out, ref, "layer output")
+
+
+def test_tiny_layer_b1_ctx16(a8w8):
+    # 16 tokens in one 16-token page, the decoded token included
+    cfg = synth.TINY
+    _layer_parity(a8w8, cfg, synth.decode_layer_case(cfg, 1, [16], seed_base=101))
+
+
+def test_tiny_layer_b1_two_pages(a8w8):
+    # 16 cached tokens plus the decoded one at position 16, on a second page
+    cfg = synth.TINY
+    _layer_parity(a8w8, cfg, synth.decode_layer_case(cfg, 1, [17], seed_base=102))
+
+
+def test_tiny_layer_batched_with_padding(a8w8):
+    cfg = synth.TINY
+    case = synth.decode_layer_case(cfg, 16, list(range(1, 17)), seed_base=103, padded_rows=(3, 9))
+    _layer_parity(a8w8, cfg, case)
+
+
+def test_qwen3_14b_layer_b1_ctx256(a8w8):
+    cfg = dict(synth.QWEN3_14B, num_layers=1)
+    _layer_parity(a8w8, cfg, synth.decode_layer_case(cfg, 1, [256], seed_base=104))
+
+
+def test_qwen3_14b_layer_b4_mixed_ctx(a8w8):
+    cfg = dict(synth.QWEN3_14B, num_layers=1)
+    case = synth.decode_layer_case(cfg, 4, [1, 77, 256, 129], seed_base=105)
+    _layer_parity(a8w8, cfg, case)
+
+
+def test_qwen3_14b_layer_b16_long_ctx(a8w8):
+    cfg = dict(synth.QWEN3_14B, num_layers=1)
+    ctx = synth.batched_ctx_lens(106, 16)
+    case = synth.decode_layer_case(cfg, 16, list(ctx), seed_base=106)
+    _layer_parity(a8w8, cfg, case)

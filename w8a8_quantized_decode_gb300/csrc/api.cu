@@ -1,0 +1,689 @@
+// api.cu -- the C ABI of liba8w8.so: argument validation, workspace layout,
+// orchestration of the decode layer and step, and the replayable step graph.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/a8w8.h"
+#include "kernels.cuh"
+
+using namespace a8w8;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+a8w8_status fail(a8w8_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+a8w8_status fail(a8w8_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+a8w8_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(A8W8_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define CUDA_TRY(expr, what)                          \
+    do {                                              \
+        cudaError_t e_ = (expr);                      \
+        if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+    } while (0)
+
+__device__ unsigned g_device_error;
+
+int num_sms_current() {
+    static int cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev < 0 || dev >= 64) return 0;
+    if (cached[dev] == 0) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+unsigned* device_error_word() {
+    static unsigned* cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (!cached[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+        cached[dev] = static_cast<unsigned*>(p);
+    }
+    return cached[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+Launch make_launch(void* stream, bool pdl) {
+    Launch L;
+    L.stream = static_cast<cudaStream_t>(stream);
+    L.num_sms = num_sms_current();
+    L.pdl = pdl;
+    return L;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Workspace layout shared by the layer and the step.
+struct WsLayout {
+    size_t hid, qkv, attn, act, part, keys, ticket, total;
+};
+
+WsLayout ws_layout(const a8w8_config& c, int B, int max_blocks) {
+    const int D = c.head_dim;
+    const size_t nqkv = (size_t)(c.num_q_heads + 2 * c.num_kv_heads) * D;
+    WsLayout w;
+    size_t o = 0;
+    w.hid = o;
+    o = round_up(o + (size_t)B * c.hidden * 2, 256);
+    w.qkv = o;
+    o = round_up(o + (size_t)B * nqkv * 2, 256);
+    w.attn = o;
+    o = round_up(o + (size_t)B * c.num_q_heads * D * 2, 256);
+    w.act = o;
+    o = round_up(o + (size_t)B * c.intermediate * 2, 256);
+    w.part = o;
+    o = round_up(o + attn_part_bytes(B, c.num_q_heads, D, max_blocks * c.page_size), 256);
+    w.keys = o;
+    o = round_up(o + (size_t)B * 8, 256);
+    w.ticket = o;
+    o = round_up(o + 16, 256);
+    w.total = o;
+    return w;
+}
+
+a8w8_status check_config(const a8w8_config* c) {
+    if (!c) return fail(A8W8_ERR_INVALID_ARG, "config is NULL");
+    if (c->hidden <= 0 || c->num_q_heads <= 0 || c->num_kv_heads <= 0 || c->intermediate <= 0 ||
+        c->page_size <= 0 || c->num_layers < 0)
+        return fail(A8W8_ERR_INVALID_ARG, "config sizes must be positive");
+    if (c->head_dim != 64 && c->head_dim != 128)
+        return fail(A8W8_ERR_UNSUPPORTED_SHAPE, "head_dim %d not supported (64 or 128)", c->head_dim);
+    if (c->num_q_heads % c->num_kv_heads != 0 || c->num_q_heads / c->num_kv_heads > 8)
+        return fail(A8W8_ERR_UNSUPPORTED_SHAPE, "Hq/Hkv must be an integer <= 8 (Hq=%d Hkv=%d)",
+                    c->num_q_heads, c->num_kv_heads);
+    if (c->hidden % 16 || c->intermediate % 16)
+        return fail(A8W8_ERR_UNSUPPORTED_SHAPE, "hidden and intermediate must be multiples of 16");
+    if (c->down_k_splits != 1 && c->down_k_splits != 2)
+        return fail(A8W8_ERR_UNSUPPORTED_SHAPE, "down_k_splits must be 1 or 2");
+    if (c->intermediate % (16 * c->down_k_splits))
+        return fail(A8W8_ERR_UNSUPPORTED_SHAPE, "intermediate / down_k_splits must be a multiple of 16");
+    if (!(c->rms_eps >= 0.0f)) return fail(A8W8_ERR_INVALID_ARG, "rms_eps must be >= 0");
+    return A8W8_OK;
+}
+
+a8w8_status check_ptrs(std::initializer_list<const void*> ptrs, const char* what) {
+    for (const void* p : ptrs) {
+        if (!p) return fail(A8W8_ERR_INVALID_ARG, "%s: required pointer is NULL", what);
+        if (!aligned16(p)) return fail(A8W8_ERR_INVALID_ARG, "%s: pointer not 16-byte aligned", what);
+    }
+    return A8W8_OK;
+}
+
+a8w8_status check_layer_weights(const a8w8_layer_weights* w) {
+    if (!w) return fail(A8W8_ERR_INVALID_ARG, "layer weights are NULL");
+    return check_ptrs({w->input_norm_w, w->w_qkv, w->s_qkv, w->q_norm_w, w->k_norm_w, w->w_o, w->s_o,
+                       w->post_norm_w, w->w_gate_up, w->s_gate_up, w->w_down, w->s_down},
+                      "layer weights");
+}
+
+// Runs a projection over batch tiles.
+cudaError_t run_gemv(int pro, int epi, int ks, GemvParams p, int M, const Launch& L) {
+    const int tile = gemv_max_batch_tile(p.K);
+    const int Ntot = (epi == EPI_SWIGLU) ? 2 * p.N : p.N;
+    for (int b0 = 0; b0 < M; b0 += tile) {
+        GemvParams q = p;
+        q.M = M - b0 < tile ? M - b0 : tile;
+        if (p.xq) q.xq = p.xq + (size_t)b0 * p.K;
+        if (p.x_scale) q.x_scale = p.x_scale + b0;
+        if (p.x) q.x = p.x + (size_t)b0 * p.ldx;
+        if (p.residual) q.residual = p.residual + (size_t)b0 * p.ldy;
+        q.y = p.y + (size_t)b0 * p.ldy;
+        if (p.acc_out) q.acc_out = p.acc_out + (size_t)b0 * Ntot;
+        if (p.tap_q) q.tap_q = p.tap_q + (size_t)b0 * p.K;
+        if (p.tap_x) q.tap_x = p.tap_x + (size_t)b0 * p.K;
+        if (p.tap_s) q.tap_s = p.tap_s + b0;
+        cudaError_t e = launch_gemv(pro, epi, ks, q, L);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+// Enqueues one decode layer (no validation).
+a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int B, bf16* hidden,
+                          const int32_t* slot_mapping, const int32_t* block_table, int max_blocks,
+                          int num_blocks, const int32_t* ctx_lens, bf16* k_cache, bf16* v_cache,
+                          const float* rope, int max_pos, unsigned char* ws, const WsLayout& lay,
+                          const a8w8_layer_taps* taps, const Launch& L) {
+    const int H = c.hidden, D = c.head_dim, Hq = c.num_q_heads, Hkv = c.num_kv_heads;
+    const int I = c.intermediate, NQ = Hq * D, NQKV = NQ + 2 * Hkv * D;
+    bf16* qkv = reinterpret_cast<bf16*>(ws + lay.qkv);
+    bf16* attn = reinterpret_cast<bf16*>(ws + lay.attn);
+    bf16* act = reinterpret_cast<bf16*>(ws + lay.act);
+    float* part = reinterpret_cast<float*>(ws + lay.part);
+    const a8w8_layer_taps none = {};
+    const a8w8_layer_taps& T = taps ? *taps : none;
+
+    // a2-a4: input RMSNorm + quantisation (prologue) + QKV projection
+    GemvParams g = {};
+    g.W = w->w_qkv;
+    g.w_scale = w->s_qkv;
+    g.K = H;
+    g.N = NQKV;
+    g.x = reinterpret_cast<const bf16*>(hidden);
+    g.ldx = H;
+    g.norm_w = reinterpret_cast<const bf16*>(w->input_norm_w);
+    g.eps = c.rms_eps;
+    g.y = qkv;
+    g.ldy = NQKV;
+    g.tap_x = reinterpret_cast<bf16*>(T.xn);
+    g.tap_q = T.xq;
+    g.tap_s = T.xs;
+    cudaError_t e = run_gemv(PRO_NORM_QUANT, EPI_STORE, 1, g, B, L);
+    if (e != cudaSuccess) return cuda_fail(e, "QKV projection");
+    if (T.qkv) {
+        e = cudaMemcpyAsync(T.qkv, qkv, (size_t)B * NQKV * 2, cudaMemcpyDeviceToDevice, L.stream);
+        if (e != cudaSuccess) return cuda_fail(e, "tap qkv");
+    }
+
+    // a5-a8: QK norm, RoPE, KV write, paged attention
+    AttnParams a = {};
+    a.q = qkv;
+    a.q_stride = NQKV;
+    a.fused = true;
+    a.q_norm_w = reinterpret_cast<const bf16*>(w->q_norm_w);
+    a.k_norm_w = reinterpret_cast<const bf16*>(w->k_norm_w);
+    a.rope = rope;
+    a.max_pos = max_pos;
+    a.eps = c.rms_eps;
+    a.slot_mapping = slot_mapping;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_table = block_table;
+    a.ctx_lens = ctx_lens;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.D = D;
+    a.page = c.page_size;
+    a.max_blocks = max_blocks;
+    a.num_blocks = num_blocks;
+    a.scale = 1.0f / sqrtf((float)D);
+    a.out = attn;
+    a.part = part;
+    a.err = device_error_word();
+    a.tap_q_rot = reinterpret_cast<bf16*>(T.q_rot);
+    a.tap_k_rot = reinterpret_cast<bf16*>(T.k_rot);
+    e = launch_attention(a, L);
+    if (e != cudaSuccess) return cuda_fail(e, "attention");
+    if (T.attn) {
+        e = cudaMemcpyAsync(T.attn, attn, (size_t)B * NQ * 2, cudaMemcpyDeviceToDevice, L.stream);
+        if (e != cudaSuccess) return cuda_fail(e, "tap attn");
+    }
+
+    // a9-a10: quantisation (prologue) + O projection + residual (in place)
+    g = GemvParams{};
+    g.W = w->w_o;
+    g.w_scale = w->s_o;
+    g.K = NQ;
+    g.N = H;
+    g.x = attn;
+    g.ldx = NQ;
+    g.residual = hidden;
+    g.y = hidden;
+    g.ldy = H;
+    g.tap_q = T.aq;
+    g.tap_s = T.as;
+    e = run_gemv(PRO_QUANT, EPI_STORE, 1, g, B, L);
+    if (e != cudaSuccess) return cuda_fail(e, "O projection");
+    if (T.h1) {
+        e = cudaMemcpyAsync(T.h1, hidden, (size_t)B * H * 2, cudaMemcpyDeviceToDevice, L.stream);
+        if (e != cudaSuccess) return cuda_fail(e, "tap h1");
+    }
+
+    // a11-a12: post-attention RMSNorm + quantisation (prologue) + Gate/Up + SwiGLU
+    g = GemvParams{};
+    g.W = w->w_gate_up;
+    g.w_scale = w->s_gate_up;
+    g.K = H;
+    g.N = I;
+    g.x = hidden;
+    g.ldx = H;
+    g.norm_w = reinterpret_cast<const bf16*>(w->post_norm_w);
+    g.eps = c.rms_eps;
+    g.y = act;
+    g.ldy = I;
+    g.tap_x = reinterpret_cast<bf16*>(T.hn);
+    g.tap_q = T.hq;
+    g.tap_s = T.hs;
+    e = run_gemv(PRO_NORM_QUANT, EPI_SWIGLU, 1, g, B, L);
+    if (e != cudaSuccess) return cuda_fail(e, "Gate/Up projection");
+    if (T.act) {
+        e = cudaMemcpyAsync(T.act, act, (size_t)B * I * 2, cudaMemcpyDeviceToDevice, L.stream);
+        if (e != cudaSuccess) return cuda_fail(e, "tap act");
+    }
+
+    // a13-a14: quantisation (prologue) + split-K down projection + residual
+    g = GemvParams{};
+    g.W = w->w_down;
+    g.w_scale = w->s_down;
+    g.K = I;
+    g.N = H;
+    g.x = act;
+    g.ldx = I;
+    g.residual = hidden;
+    g.y = hidden;
+    g.ldy = H;
+    g.tap_q = T.actq;
+    g.tap_s = T.acts;
+    e = run_gemv(PRO_QUANT, EPI_STORE, c.down_k_splits, g, B, L);
+    if (e != cudaSuccess) return cuda_fail(e, "down projection");
+    return A8W8_OK;
+}
+
+a8w8_status check_layer_common(const a8w8_config* cfg, int B, int max_blocks, int num_blocks,
+                               const float* rope, int max_pos) {
+    a8w8_status s = check_config(cfg);
+    if (s != A8W8_OK) return s;
+    if (B < 1 || B > 64) return fail(A8W8_ERR_UNSUPPORTED_SHAPE, "B=%d outside [1, 64]", B);
+    if (max_blocks < 1 || num_blocks < 1)
+        return fail(A8W8_ERR_INVALID_ARG, "max_blocks and num_blocks must be >= 1");
+    if ((long long)max_blocks * cfg->page_size > (1 << 24))
+        return fail(A8W8_ERR_UNSUPPORTED_SHAPE, "context longer than 2^24 tokens");
+    if (!rope || max_pos < 1) return fail(A8W8_ERR_INVALID_ARG, "rope table missing");
+    return A8W8_OK;
+}
+
+}  // namespace
+
+// ===========================================================================
+// C ABI
+// ===========================================================================
+
+extern "C" {
+
+const char* a8w8_last_error(void) { return g_last_error.c_str(); }
+
+int a8w8_version(void) { return 100; }
+
+a8w8_status a8w8_read_device_errors(unsigned* bits, void* stream) {
+    if (!bits) return fail(A8W8_ERR_INVALID_ARG, "bits is NULL");
+    CUDA_TRY(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "stream synchronize");
+    unsigned* w = device_error_word();
+    if (!w) return fail(A8W8_ERR_CUDA, "device error word unavailable");
+    unsigned h = 0;
+    CUDA_TRY(cudaMemcpy(&h, w, sizeof h, cudaMemcpyDeviceToHost), "read device error word");
+    CUDA_TRY(cudaMemset(w, 0, sizeof h), "clear device error word");
+    *bits = h;
+    return A8W8_OK;
+}
+
+a8w8_status a8w8_quant_rows(const a8w8_bf16* x, int rows, int cols, int ldx, int8_t* q,
+                            float* row_scale, void* stream) {
+    if (rows < 0 || cols < 0) return fail(A8W8_ERR_INVALID_ARG, "negative size");
+    if (rows == 0) return A8W8_OK;
+    if (cols == 0 || cols % 8 || ldx % 8 || ldx < cols)
+        return fail(A8W8_ERR_UNSUPPORTED_SHAPE, "cols and ldx must be positive multiples of 8, ldx >= cols");
+    a8w8_status s = check_ptrs({x, q, row_scale}, "a8w8_quant_rows");
+    if (s != A8W8_OK) return s;
+    cudaError_t e = launch_quant_rows(reinterpret_cast<const bf16*>(x), rows, cols, ldx, q, row_scale,
+                                      make_launch(stream, false));
+    return e == cudaSuccess ? A8W8_OK : cuda_fail(e, "a8w8_quant_rows");
+}
+
+static a8w8_status linear_common(const int8_t* xq, const float* x_scale, int M, int K,
+                                 const int8_t* W, const float* w_scale, int N, int k_splits,
+                                 const a8w8_bf16* residual, a8w8_bf16* y, int32_t* acc_out,
+                                 bool swiglu, void* stream, const char* name) {
+    if (M < 0 || K < 0 || N < 0) return fail(A8W8_ERR_INVALID_ARG, "%s: negative size", name);
+    if (M == 0 || N == 0) return A8W8_OK;
+    if (K == 0 || K % 16) return fail(A8W8_ERR_UNSUPPORTED_SHAPE, "%s: K must be a positive multiple of 16", name);
+    if (k_splits != 1 && k_splits != 2) return fail(A8W8_ERR_UNSUPPORTED_SHAPE, "%s: k_splits must be 1 or 2", name);
+    if ((K / k_splits) % 16 || K % k_splits)
+        return fail(A8W8_ERR_UNSUPPORTED_SHAPE, "%s: K / k_splits must be a multiple of 16", name);
+    a8w8_status s = check_ptrs({xq, x_scale, W, w_scale, y}, name);
+    if (s != A8W8_OK) return s;
+    if (residual && !aligned16(residual)) return fail(A8W8_ERR_INVALID_ARG, "%s: residual misaligned", name);
+    Launch L = make_launch(stream, false);
+    if (L.num_sms <= 0) return fail(A8W8_ERR_CUDA, "%s: no CUDA device", name);
+    GemvParams g = {};
+    g.W = W;
+    g.w_scale = w_scale;
+    g.K = K;
+    g.N = N;
+    g.xq = xq;
+    g.x_scale = x_scale;
+    g.residual = reinterpret_cast<const bf16*>(residual);
+    g.y = reinterpret_cast<bf16*>(y);
+    g.ldy = N;
+    g.acc_out = acc_out;
+    cudaError_t e = run_gemv(PRO_I8, swiglu ? EPI_SWIGLU : EPI_STORE, k_splits, g, M, L);
+    return e == cudaSuccess ? A8W8_OK : cuda_fail(e, name);
+}
+
+a8w8_status a8w8_linear(const int8_t* xq, const float* x_scale, int M, int K, const int8_t* W,
+                        const float* w_scale, int N, int k_splits, const a8w8_bf16* residual,
+                        a8w8_bf16* y, int32_t* acc_out, void* stream) {
+    return linear_common(xq, x_scale, M, K, W, w_scale, N, k_splits, residual, y, acc_out, false,
+                         stream, "a8w8_linear");
+}
+
+a8w8_status a8w8_gate_up_swiglu(const int8_t* xq, const float* x_scale, int M, int K,
+                                const int8_t* W_gu, const float* s_gu, int I, a8w8_bf16* act,
+                                int32_t* acc_out, void* stream) {
+    return linear_common(xq, x_scale, M, K, W_gu, s_gu, I, 1, nullptr, act, acc_out, true, stream,
+                         "a8w8_gate_up_swiglu");
+}
+
+a8w8_status paged_kv_write(const a8w8_bf16* k, const a8w8_bf16* v, int T, int Hkv, int D,
+                           const int32_t* slot_mapping, a8w8_bf16* k_cache, a8w8_bf16* v_cache,
+                           int num_blocks, int page_size, void* stream) {
+    if (T < 0 || Hkv <= 0 || D <= 0 || num_blocks < 0 || page_size <= 0)
+        return fail(A8W8_ERR_INVALID_ARG, "paged_kv_write: bad size");
+    if (T == 0) return A8W8_OK;
+    if ((Hkv * D) % 8) return fail(A8W8_ERR_UNSUPPORTED_SHAPE, "paged_kv_write: Hkv*D must be a multiple of 8");
+    a8w8_status s = check_ptrs({k, v, slot_mapping, k_cache, v_cache}, "paged_kv_write");
+    if (s != A8W8_OK) return s;
+    cudaError_t e = launch_kv_write(reinterpret_cast<const bf16*>(k), reinterpret_cast<const bf16*>(v), T,
+                                    Hkv, D, slot_mapping, reinterpret_cast<bf16*>(k_cache),
+                                    reinterpret_cast<bf16*>(v_cache), (long)num_blocks * page_size,
+                                    device_error_word(), make_launch(stream, false));
+    return e == cudaSuccess ? A8W8_OK : cuda_fail(e, "paged_kv_write");
+}
+
+size_t a8w8_attention_workspace_bytes(int B, int Hq, int D, int max_ctx) {
+    if (B <= 0 || Hq <= 0 || D <= 0 || max_ctx <= 0) return 0;
+    return attn_part_bytes(B, Hq, D, max_ctx);
+}
+
+a8w8_status paged_decode_attention_bf16(const a8w8_bf16* q, const a8w8_bf16* k_cache,
+                                        const a8w8_bf16* v_cache, const int32_t* block_table,
+                                        const int32_t* ctx_lens, int B, int Hq, int Hkv, int D,
+                                        int page_size, int max_blocks, int num_blocks,
+                                        float softmax_scale, a8w8_bf16* out, void* ws,
+                                        size_t ws_bytes, void* stream) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || page_size <= 0 || max_blocks <= 0 || num_blocks <= 0)
+        return fail(A8W8_ERR_INVALID_ARG, "paged_decode_attention_bf16: bad size");
+    if (B == 0) return A8W8_OK;
+    if (D != 64 && D != 128) return fail(A8W8_ERR_UNSUPPORTED_SHAPE, "head_dim %d not supported", D);
+    if (Hq % Hkv || Hq / Hkv > 8) return fail(A8W8_ERR_UNSUPPORTED_SHAPE, "Hq/Hkv must be an integer <= 8");
+    if ((long long)max_blocks * page_size > (1 << 24))
+        return fail(A8W8_ERR_UNSUPPORTED_SHAPE, "context longer than 2^24 tokens");
+    a8w8_status s = check_ptrs({q, k_cache, v_cache, block_table, ctx_lens, out}, "paged_decode_attention_bf16");
+    if (s != A8W8_OK) return s;
+    const size_t need = attn_part_bytes(B, Hq, D, max_blocks * page_size);
+    if (need > 0 && (!ws || ws_bytes < need || !aligned16(ws)))
+        return fail(A8W8_ERR_WORKSPACE, "attention workspace needs %zu bytes", need);
+    AttnParams a = {};
+    a.q = reinterpret_cast<const bf16*>(q);
+    a.q_stride = Hq * D;
+    a.fused = false;
+    a.k_cache = const_cast<bf16*>(reinterpret_cast<const bf16*>(k_cache));
+    a.v_cache = const_cast<bf16*>(reinterpret_cast<const bf16*>(v_cache));
+    a.block_table = block_table;
+    a.ctx_lens = ctx_lens;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.D = D;
+    a.page = page_size;
+    a.max_blocks = max_blocks;
+    a.num_blocks = num_blocks;
+    a.scale = softmax_scale;
+    a.out = reinterpret_cast<bf16*>(out);
+    a.part = static_cast<float*>(ws);
+    a.err = device_error_word();
+    cudaError_t e = launch_attention(a, make_launch(stream, false));
+    return e == cudaSuccess ? A8W8_OK : cuda_fail(e, "paged_decode_attention_bf16");
+}
+
+a8w8_status a8w8_rope_table(float* rope, int max_pos, int D, double theta, void* stream) {
+    if (max_pos < 0 || D <= 0 || D % 2 || D > 2048 || !(theta > 0.0))
+        return fail(A8W8_ERR_INVALID_ARG, "a8w8_rope_table: bad arguments");
+    if (max_pos == 0) return A8W8_OK;
+    a8w8_status s = check_ptrs({rope}, "a8w8_rope_table");
+    if (s != A8W8_OK) return s;
+    cudaError_t e = launch_rope_table(rope, max_pos, D, theta, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? A8W8_OK : cuda_fail(e, "a8w8_rope_table");
+}
+
+size_t a8w8_workspace_bytes(const a8w8_config* cfg, int max_B, int max_blocks) {
+    if (!cfg || max_B <= 0 || max_blocks <= 0) return 0;
+    return ws_layout(*cfg, max_B, max_blocks).total;
+}
+
+a8w8_status a8w8_decode_layer(const a8w8_layer_weights* w, const a8w8_config* cfg, int B,
+                              a8w8_bf16* hidden, const int32_t* slot_mapping,
+                              const int32_t* block_table, int max_blocks, int num_blocks,
+                              const int32_t* ctx_lens, a8w8_bf16* k_cache, a8w8_bf16* v_cache,
+                              const float* rope, int max_pos, void* ws, size_t ws_bytes,
+                              const a8w8_layer_taps* taps, void* stream) {
+    a8w8_status s = check_layer_common(cfg, B, max_blocks, num_blocks, rope, max_pos);
+    if (s != A8W8_OK) return s;
+    if ((s = check_layer_weights(w)) != A8W8_OK) return s;
+    if ((s = check_ptrs({hidden, slot_mapping, block_table, ctx_lens, k_cache, v_cache, rope},
+                        "a8w8_decode_layer")) != A8W8_OK)
+        return s;
+    const WsLayout lay = ws_layout(*cfg, B, max_blocks);
+    if (!ws || ws_bytes < lay.total || !aligned16(ws))
+        return fail(A8W8_ERR_WORKSPACE, "decode layer workspace needs %zu bytes", lay.total);
+    Launch L = make_launch(stream, true);
+    if (L.num_sms <= 0) return fail(A8W8_ERR_CUDA, "no CUDA device");
+    return enqueue_layer(w, *cfg, B, reinterpret_cast<bf16*>(hidden), slot_mapping, block_table,
+                         max_blocks, num_blocks, ctx_lens, reinterpret_cast<bf16*>(k_cache),
+                         reinterpret_cast<bf16*>(v_cache), rope, max_pos,
+                         static_cast<unsigned char*>(ws), lay, taps, L);
+}
+
+static a8w8_status check_step(const a8w8_model* m, const a8w8_config* cfg, int B, int max_blocks,
+                              int num_blocks, a8w8_bf16* const* k_caches,
+                              a8w8_bf16* const* v_caches, const float* rope, int max_pos,
+                              size_t ws_bytes, const void* ws) {
+    a8w8_status s = check_layer_common(cfg, B, max_blocks, num_blocks, rope, max_pos);
+    if (s != A8W8_OK) return s;
+    if (!m) return fail(A8W8_ERR_INVALID_ARG, "model is NULL");
+    if (cfg->vocab <= 0 || cfg->num_layers < 1) return fail(A8W8_ERR_INVALID_ARG, "vocab and num_layers must be >= 1");
+    if ((s = check_ptrs({m->embed, m->final_norm_w, m->lm_head}, "model")) != A8W8_OK) return s;
+    if (!m->layers || !k_caches || !v_caches) return fail(A8W8_ERR_INVALID_ARG, "layer arrays are NULL");
+    for (int l = 0; l < cfg->num_layers; ++l) {
+        if ((s = check_layer_weights(&m->layers[l])) != A8W8_OK) return s;
+        if ((s = check_ptrs({k_caches[l], v_caches[l]}, "KV caches")) != A8W8_OK) return s;
+    }
+    const WsLayout lay = ws_layout(*cfg, B, max_blocks);
+    if (!ws || ws_bytes < lay.total || !aligned16(ws))
+        return fail(A8W8_ERR_WORKSPACE, "decode step workspace needs %zu bytes", lay.total);
+    return A8W8_OK;
+}
+
+static a8w8_status enqueue_step(const a8w8_model* m, const a8w8_config& c, int B,
+                                const int32_t* token_ids, const int32_t* slot_mapping,
+                                const int32_t* block_table, int max_blocks, int num_blocks,
+                                const int32_t* ctx_lens, a8w8_bf16* const* k_caches,
+                                a8w8_bf16* const* v_caches, const float* rope, int max_pos,
+                                int32_t* next_tokens, float* logits, a8w8_bf16* final_hidden,
+                                unsigned char* ws, const Launch& L) {
+    const WsLayout lay = ws_layout(c, B, max_blocks);
+    bf16* hidden = reinterpret_cast<bf16*>(ws + lay.hid);
+    unsigned long long* keys = reinterpret_cast<unsigned long long*>(ws + lay.keys);
+    unsigned* ticket = reinterpret_cast<unsigned*>(ws + lay.ticket);
+    cudaError_t e = launch_embed(reinterpret_cast<const bf16*>(m->embed), c.vocab, c.hidden, token_ids,
+                                 B, hidden, keys, ticket, device_error_word(), L);
+    if (e != cudaSuccess) return cuda_fail(e, "embedding");
+    for (int l = 0; l < c.num_layers; ++l) {
+        a8w8_status s = enqueue_layer(&m->layers[l], c, B, hidden, slot_mapping, block_table, max_blocks,
+                                      num_blocks, ctx_lens, reinterpret_cast<bf16*>(k_caches[l]),
+                                      reinterpret_cast<bf16*>(v_caches[l]), rope, max_pos, ws, lay,
+                                      nullptr, L);
+        if (s != A8W8_OK) return s;
+    }
+    const int tile = lmhead_max_batch_tile();
+    for (int b0 = 0; b0 < B; b0 += tile) {
+        LmHeadParams p = {};
+        p.hidden = hidden + (size_t)b0 * c.hidden;
+        p.norm_w = reinterpret_cast<const bf16*>(m->final_norm_w);
+        p.eps = c.rms_eps;
+        p.W = reinterpret_cast<const bf16*>(m->lm_head);
+        p.H = c.hidden;
+        p.V = c.vocab;
+        p.M = B - b0 < tile ? B - b0 : tile;
+        p.logits = logits ? logits + (size_t)b0 * c.vocab : nullptr;
+        p.final_hidden = final_hidden ? reinterpret_cast<bf16*>(final_hidden) + (size_t)b0 * c.hidden : nullptr;
+        p.keys = keys + b0;
+        p.ticket = ticket;
+        p.next_tokens = next_tokens + b0;
+        e = launch_lmhead_argmax(p, L);
+        if (e != cudaSuccess) return cuda_fail(e, "LM head");
+    }
+    return A8W8_OK;
+}
+
+a8w8_status a8w8_decode_step(const a8w8_model* m, const a8w8_config* cfg, int B,
+                             const int32_t* token_ids, const int32_t* slot_mapping,
+                             const int32_t* block_table, int max_blocks, int num_blocks,
+                             const int32_t* ctx_lens, a8w8_bf16* const* k_caches,
+                             a8w8_bf16* const* v_caches, const float* rope, int max_pos,
+                             int32_t* next_tokens, float* logits, a8w8_bf16* final_hidden,
+                             void* ws, size_t ws_bytes, void* stream) {
+    a8w8_status s = check_step(m, cfg, B, max_blocks, num_blocks, k_caches, v_caches, rope, max_pos,
+                               ws_bytes, ws);
+    if (s != A8W8_OK) return s;
+    if ((s = check_ptrs({token_ids, slot_mapping, block_table, ctx_lens, next_tokens}, "a8w8_decode_step")) != A8W8_OK)
+        return s;
+    if ((logits && !aligned16(logits)) || (final_hidden && !aligned16(final_hidden)))
+        return fail(A8W8_ERR_INVALID_ARG, "logits / final_hidden misaligned");
+    Launch L = make_launch(stream, true);
+    if (L.num_sms <= 0) return fail(A8W8_ERR_CUDA, "no CUDA device");
+    return enqueue_step(m, *cfg, B, token_ids, slot_mapping, block_table, max_blocks, num_blocks,
+                        ctx_lens, k_caches, v_caches, rope, max_pos, next_tokens, logits,
+                        final_hidden, static_cast<unsigned char*>(ws), L);
+}
+
+// ---------------------------------------------------------------------------
+// Replayable step
+// ---------------------------------------------------------------------------
+
+struct a8w8_step_graph {
+    int device;
+    int B, max_blocks;
+    int32_t *tok, *slot, *table, *ctx, *next;
+    cudaGraph_t graph;
+    cudaGraphExec_t exec;
+};
+
+a8w8_status a8w8_step_graph_create(a8w8_step_graph** out, const a8w8_model* m,
+                                   const a8w8_config* cfg, int B, int max_blocks, int num_blocks,
+                                   a8w8_bf16* const* k_caches, a8w8_bf16* const* v_caches,
+                                   const float* rope, int max_pos, int32_t* token_ids,
+                                   int32_t* slot_mapping, int32_t* block_table, int32_t* ctx_lens,
+                                   int32_t* next_tokens, float* logits, a8w8_bf16* final_hidden,
+                                   int device_loop, void* ws, size_t ws_bytes, void* stream) {
+    if (!out) return fail(A8W8_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    a8w8_status s = check_step(m, cfg, B, max_blocks, num_blocks, k_caches, v_caches, rope, max_pos,
+                               ws_bytes, ws);
+    if (s != A8W8_OK) return s;
+    if ((s = check_ptrs({token_ids, slot_mapping, block_table, ctx_lens, next_tokens},
+                        "a8w8_step_graph_create")) != A8W8_OK)
+        return s;
+    if ((logits && !aligned16(logits)) || (final_hidden && !aligned16(final_hidden)))
+        return fail(A8W8_ERR_INVALID_ARG, "logits / final_hidden misaligned");
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    CUDA_TRY(cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cs), "capture status");
+    if (cs != cudaStreamCaptureStatusNone)
+        return fail(A8W8_ERR_INVALID_ARG, "a8w8_step_graph_create called during stream capture");
+    CUDA_TRY(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)), "stream synchronize");
+    cudaStream_t cap = nullptr;
+    CUDA_TRY(cudaStreamCreateWithFlags(&cap, cudaStreamNonBlocking), "capture stream");
+    a8w8_step_graph* g = new a8w8_step_graph();
+    cudaGetDevice(&g->device);
+    g->B = B;
+    g->max_blocks = max_blocks;
+    g->tok = token_ids;
+    g->slot = slot_mapping;
+    g->table = block_table;
+    g->ctx = ctx_lens;
+    g->next = next_tokens;
+    cudaError_t e = cudaStreamBeginCapture(cap, cudaStreamCaptureModeThreadLocal);
+    if (e == cudaSuccess) {
+        Launch L = make_launch(cap, true);
+        s = enqueue_step(m, *cfg, B, g->tok, g->slot, g->table, max_blocks, num_blocks, g->ctx,
+                         k_caches, v_caches, rope, max_pos, g->next, logits, final_hidden,
+                         static_cast<unsigned char*>(ws), L);
+        if (s == A8W8_OK && device_loop) {
+            cudaError_t e3 = launch_advance(g->tok, g->slot, g->table, g->ctx, g->next, B, max_blocks,
+                                            cfg->page_size, L);
+            if (e3 != cudaSuccess) s = cuda_fail(e3, "advance kernel");
+        }
+        cudaGraph_t graph = nullptr;
+        cudaError_t e2 = cudaStreamEndCapture(cap, &graph);
+        if (s == A8W8_OK && e2 != cudaSuccess) s = cuda_fail(e2, "end capture");
+        if (s == A8W8_OK) {
+            g->graph = graph;
+            e2 = cudaGraphInstantiate(&g->exec, graph, 0);
+            if (e2 != cudaSuccess) s = cuda_fail(e2, "graph instantiate");
+        } else if (graph) {
+            cudaGraphDestroy(graph);
+        }
+    } else {
+        s = cuda_fail(e, "begin capture");
+    }
+    cudaStreamDestroy(cap);
+    if (s != A8W8_OK) {
+        if (g->graph) cudaGraphDestroy(g->graph);
+        delete g;
+        return s;
+    }
+    *out = g;
+    return A8W8_OK;
+}
+
+a8w8_status a8w8_step_graph_launch(a8w8_step_graph* g, void* stream) {
+    if (!g) return fail(A8W8_ERR_INVALID_ARG, "graph is NULL");
+    CUDA_TRY(cudaGraphLaunch(g->exec, static_cast<cudaStream_t>(stream)), "graph launch");
+    return A8W8_OK;
+}
+
+a8w8_status a8w8_step_graph_run_host(a8w8_step_graph* g, const int32_t* token_ids,
+                                     const int32_t* slot_mapping, const int32_t* block_table,
+                                     const int32_t* ctx_lens, int32_t* next_tokens, void* stream) {
+    if (!g) return fail(A8W8_ERR_INVALID_ARG, "graph is NULL");
+    if (!token_ids || !slot_mapping || !block_table || !ctx_lens || !next_tokens)
+        return fail(A8W8_ERR_INVALID_ARG, "a8w8_step_graph_run_host: NULL host buffer");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t b4 = (size_t)g->B * sizeof(int32_t);
+    CUDA_TRY(cudaMemcpyAsync(g->tok, token_ids, b4, cudaMemcpyHostToDevice, st), "H2D tokens");
+    CUDA_TRY(cudaMemcpyAsync(g->slot, slot_mapping, b4, cudaMemcpyHostToDevice, st), "H2D slots");
+    CUDA_TRY(cudaMemcpyAsync(g->table, block_table, b4 * g->max_blocks, cudaMemcpyHostToDevice, st),
+             "H2D block table");
+    CUDA_TRY(cudaMemcpyAsync(g->ctx, ctx_lens, b4, cudaMemcpyHostToDevice, st), "H2D ctx lens");
+    CUDA_TRY(cudaGraphLaunch(g->exec, st), "graph launch");
+    CUDA_TRY(cudaMemcpyAsync(next_tokens, g->next, b4, cudaMemcpyDeviceToHost, st), "D2H next tokens");
+    CUDA_TRY(cudaStreamSynchronize(st), "stream synchronize");
+    return A8W8_OK;
+}
+
+void a8w8_step_graph_destroy(a8w8_step_graph* g) {
+    if (!g) return;
+    int cur = 0;
+    cudaGetDevice(&cur);
+    cudaSetDevice(g->device);
+    if (g->exec) cudaGraphExecDestroy(g->exec);
+    if (g->graph) cudaGraphDestroy(g->graph);
+    cudaSetDevice(cur);
+    delete g;
+}
+
+}  // extern "C"

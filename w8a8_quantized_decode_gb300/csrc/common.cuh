@@ -1,0 +1,89 @@
+// common.cuh -- device helpers shared by the A8W8 decode kernels (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace a8w8 {
+
+typedef __nv_bfloat16 bf16;
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialization may start while its predecessor is still running; it must
+// call pdl_wait() before it reads anything the predecessor writes and before
+// it writes anything. Every kernel here reads only immutable inputs (weights,
+// cached K/V of earlier tokens, tables) before that point. In a kernel
+// launched without the attribute both instructions are no-ops.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// 16-byte streaming load of data read once (weights): bypasses L1.
+__device__ __forceinline__ int4 ld_stream_v4(const void* p) {
+    int4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.s32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// 16-byte load through the read-only path (inputs reused across CTAs).
+__device__ __forceinline__ int4 ld_nc_v4(const void* p) {
+    return __ldg(reinterpret_cast<const int4*>(p));
+}
+
+// Asynchronous 16-byte global -> shared copy (cp.async, L2 only).
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ int warp_sum_i(int v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float bf2f(bf16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ bf16 f2bf(float v) { return __float2bfloat16_rn(v); }
+
+// Unpack 8 BF16 values held in an int4.
+__device__ __forceinline__ void unpack8(const int4& v, float (&f)[8]) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        float2 t = __bfloat1622float2(h[i]);
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+
+// Per-row INT8 code of x with row scale s: clamp(rne(x / s), -127, 127) with
+// an IEEE float32 division; s == 0 gives 0.
+__device__ __forceinline__ int quant_code(float x, float s) {
+    if (s == 0.0f) return 0;
+    int q = __float2int_rn(__fdiv_rn(x, s));
+    return max(-127, min(127, q));
+}
+
+__device__ __forceinline__ void set_error(unsigned* err, unsigned bit) {
+    if (err) atomicOr(err, bit);
+}
+
+}  // namespace a8w8

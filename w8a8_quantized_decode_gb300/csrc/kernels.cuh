@@ -1,0 +1,129 @@
+// kernels.cuh -- parameter blocks and launchers of the A8W8 decode kernels.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace a8w8 {
+
+// Launch context: device properties and whether to chain with programmatic
+// dependent launch.
+struct Launch {
+    cudaStream_t stream;
+    int num_sms;
+    bool pdl;
+};
+
+// ---------------------------------------------------------------------------
+// Per-row quantisation
+// ---------------------------------------------------------------------------
+cudaError_t launch_quant_rows(const bf16* x, int rows, int cols, int ldx, int8_t* q,
+                              float* s, const Launch& L);
+
+// ---------------------------------------------------------------------------
+// A8W8 GEMV (decode projections)
+// ---------------------------------------------------------------------------
+enum Prologue { PRO_I8 = 0, PRO_QUANT = 1, PRO_NORM_QUANT = 2 };
+enum Epilogue { EPI_STORE = 0, EPI_SWIGLU = 1 };
+
+struct GemvParams {
+    const int8_t* W;        // [rows, K]; SwiGLU: rows [0, N) gate, [N, 2N) up
+    const float* w_scale;   // per weight row
+    int K;
+    int N;                  // outputs per batch row
+    int M;                  // batch rows of this launch
+    // PRO_I8 input
+    const int8_t* xq;       // [M, K]
+    const float* x_scale;   // [M]
+    // PRO_QUANT / PRO_NORM_QUANT input
+    const bf16* x;          // [M, ldx]
+    int ldx;
+    const bf16* norm_w;     // [K] (PRO_NORM_QUANT)
+    float eps;
+    // epilogue
+    const bf16* residual;   // [M, ldy] or null (may alias y)
+    bf16* y;                // [M, ldy]
+    int ldy;
+    int32_t* acc_out;       // [M, N] (SwiGLU: [M, 2N]) or null
+    // taps of the quantised input (written by CTA 0), may be null
+    bf16* tap_x;            // [M, K] normalised BF16 row (PRO_NORM_QUANT)
+    int8_t* tap_q;          // [M, K]
+    float* tap_s;           // [M]
+};
+
+// Largest batch tile one launch handles; bigger batches are tiled by the host.
+int gemv_max_batch_tile(int K);
+cudaError_t launch_gemv(int prologue, int epilogue, int k_splits, const GemvParams& p,
+                        const Launch& L);
+
+// ---------------------------------------------------------------------------
+// KV write and paged decode attention
+// ---------------------------------------------------------------------------
+cudaError_t launch_kv_write(const bf16* k, const bf16* v, int T, int Hkv, int D,
+                            const int32_t* slot_mapping, bf16* k_cache, bf16* v_cache,
+                            long num_slots, unsigned* err, const Launch& L);
+
+struct AttnParams {
+    // query source: q [B, q_stride] (head h at h*D), or, when fused, the QKV
+    // projection rows [B, q_stride] with Q heads, then K heads, then V heads.
+    const bf16* q;
+    int q_stride;
+    bool fused;
+    const bf16* q_norm_w;   // fused: [D]
+    const bf16* k_norm_w;   // fused: [D]
+    const float* rope;      // fused: [max_pos, D]
+    int max_pos;
+    float eps;
+    const int32_t* slot_mapping;  // fused: [B]
+    bf16* k_cache;          // [num_blocks*page, Hkv, D]
+    bf16* v_cache;
+    const int32_t* block_table;   // [B, max_blocks]
+    const int32_t* ctx_lens;      // [B]
+    int B, Hq, Hkv, D, page, max_blocks, num_blocks;
+    float scale;
+    bf16* out;              // [B, Hq*D]
+    float* part;            // split partials, [B, Hq, splits, D + 2]
+    unsigned* err;
+    bf16* tap_q_rot;        // [B, Hq, D] or null
+    bf16* tap_k_rot;        // [B, Hkv, D] or null
+};
+
+// Tokens per attention CTA and the number of CTAs per (request, KV head).
+int attn_chunk(int max_ctx);
+int attn_splits(int max_ctx);
+size_t attn_part_bytes(int B, int Hq, int D, int max_ctx);
+cudaError_t launch_attention(const AttnParams& p, const Launch& L);
+
+// ---------------------------------------------------------------------------
+// Embedding, RoPE table, LM head + argmax
+// ---------------------------------------------------------------------------
+cudaError_t launch_embed(const bf16* embed, int vocab, int H, const int32_t* token_ids, int B,
+                         bf16* hidden, unsigned long long* argmax_keys, unsigned* argmax_ticket,
+                         unsigned* err, const Launch& L);
+
+cudaError_t launch_rope_table(float* rope, int max_pos, int D, double theta, cudaStream_t s);
+
+struct LmHeadParams {
+    const bf16* hidden;     // [M, H] (pre final norm)
+    const bf16* norm_w;     // [H]
+    float eps;
+    const bf16* W;          // [V, H]
+    int H, V, M;
+    float* logits;          // [M, V] or null
+    bf16* final_hidden;     // [M, H] or null
+    unsigned long long* keys;   // [M] argmax keys (zero on entry)
+    unsigned* ticket;       // zero on entry
+    int32_t* next_tokens;   // [M]
+};
+int lmhead_max_batch_tile();
+
+// Device-side decode loop: next step's token ids from this step's argmax, the
+// context advanced by one position with its slot from the block table.
+cudaError_t launch_advance(int32_t* token_ids, int32_t* slot_mapping, const int32_t* block_table,
+                           int32_t* ctx_lens, const int32_t* next_tokens, int B, int max_blocks,
+                           int page, const Launch& L);
+cudaError_t launch_lmhead_argmax(const LmHeadParams& p, const Launch& L);
+
+}  // namespace a8w8
