@@ -1,0 +1,416 @@
+"""Benchmark of the A8W8 decode step on GB300.
+
+Workload (default): a 40-layer Qwen3-14B-shaped A8W8 decode step with the BF16
+LM head and greedy argmax, batch 1. A 16-token seeded prompt is decoded token by
+token to fill the paged BF16 KV cache, then W warm-up steps and K timed steps
+follow (max_seq_len 256). Weights are random-init (seeded, drawn on the device),
+14.8 GB per step, far larger than L2, so no step can hit in L2 for weights.
+
+value    : TPOT (ms/token) of K replays of the captured step graph whose inputs
+           stay in HBM (the graph feeds each argmax back as the next token).
+e2e      : TPOT through the C ABI with HOST buffers: every step copies its
+           inputs from pinned host memory and reads the next token back.
+roofline : the Gate/Up projection kernel (54% of the step's bytes), timed live
+           with CUDA events over the 40 layers' Gate/Up weights.
+cpu_baseline / --impl reference : the CPU oracle, timed on one decode step.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+PROMPT_LEN = 16
+MAX_SEQ = 256
+SEED = 2026
+WORKLOAD = "qwen3_14b_a8w8_decode_step_b1"
+METRIC = "A8W8 decode TPOT (ms/token, 40 layers, bs=1)"
+
+# DRAM traffic per launch of the Gate/Up kernel from the committed ncu summary
+# (profiles/); None until a capture of the current kernel exists.
+GATE_UP_NCU_TRAFFIC_BYTES = None
+
+
+def step_bytes(cfg, ctx_lens) -> dict:
+    """Algorithmic bytes of one decode step (weights, norms, KV read + write)."""
+    H, V, L = cfg["hidden"], cfg["vocab"], cfg["num_layers"]
+    Hkv, D = cfg["num_kv_heads"], cfg["head_dim"]
+    layer = synth.layer_weight_bytes(cfg)
+    kv_row = 2 * Hkv * D * 2            # K and V of one token, one layer
+    kv = sum(int(c) for c in ctx_lens) * kv_row * L   # read (the new token is written once)
+    head = V * H * 2 + H * 2
+    return {"layers": layer * L, "lm_head": head, "kv": kv, "total": layer * L + head + kv}
+
+
+def gate_up_bytes(cfg) -> int:
+    H, I = cfg["hidden"], cfg["intermediate"]
+    return 2 * I * H + 2 * I * 4
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines: list[str] = []
+
+    def __enter__(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "20"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def build_model(cfg, device):
+    import torch
+    m = synth.t_model_weights(cfg, SEED, device)
+    torch.cuda.synchronize()
+    return m
+
+
+def host_model(model) -> dict:
+    """Copy a device model to numpy (BF16 as uint16) for the oracle."""
+    import torch
+
+    def h(t):
+        t = t.detach().cpu()
+        if t.dtype == torch.bfloat16:
+            return t.view(torch.int16).numpy().view(np.uint16)
+        return t.numpy()
+    return dict(embed=h(model["embed"]), final_norm_w=h(model["final_norm_w"]),
+                lm_head=h(model["lm_head"]),
+                layers=[{k: h(v) for k, v in l.items()} for l in model["layers"]])
+
+
+def time_oracle_steps(hm, cfg, n_steps: int, budget_s: float):
+    """Oracle decode steps (batch 1) from a prompt of PROMPT_LEN tokens; returns
+    (seconds per step list, threads)."""
+    import oracle
+    page = cfg["page_size"]
+    max_blocks = MAX_SEQ // page
+    bt = np.arange(max_blocks, dtype=np.int32)[None, :]
+    Hkv, D = cfg["num_kv_heads"], cfg["head_dim"]
+    L = cfg["num_layers"]
+    kc = [np.zeros((max_blocks * page, Hkv, D), np.uint16) for _ in range(L)]
+    vc = [np.zeros((max_blocks * page, Hkv, D), np.uint16) for _ in range(L)]
+    tok = synth.prompt_ids(SEED + 5, 1, cfg["vocab"])
+    times = []
+    t_start = time.perf_counter()
+    for s in range(n_steps):
+        ctx = np.array([PROMPT_LEN + s + 1], np.int32)
+        slots = synth.slots_for(bt, ctx - 1, page)
+        t0 = time.perf_counter()
+        nxt, _, _, rc = oracle.decode_step(hm, cfg, tok, slots, bt, ctx, kc, vc)
+        times.append(time.perf_counter() - t0)
+        tok = nxt
+        if time.perf_counter() - t_start > budget_s:
+            break
+    return times, oracle.num_threads()
+
+
+def run_reference(args, cfg):
+    """The oracle as the reference arm (rank 0 only)."""
+    import torch
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    device = torch.device(f"cuda:{local}") if torch.cuda.is_available() else None
+    if device is not None:
+        torch.cuda.set_device(device)
+        model = build_model(cfg, device)
+        hm = host_model(model)
+        del model
+        torch.cuda.empty_cache()
+    else:
+        hm = synth.model_weights_host(cfg, SEED)
+    import oracle
+    oracle.build()
+    n = args.warmup + args.steps
+    times, threads = time_oracle_steps(hm, cfg, n, budget_s=240.0)
+    timed = times[args.warmup:] if len(times) > args.warmup else times
+    tpot = 1000.0 * sum(timed) / len(timed)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tpot, "unit": "ms/token",
+        "n_gpus": args.gpus, "steps": len(timed), "warmup": min(args.warmup, len(times)),
+        "ms_per_step": tpot, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8/int32/f32/f64", "data": "synthetic (seeded random-init weights)",
+        "config": {"workload": WORKLOAD, "batch": 1, "prompt_len": PROMPT_LEN,
+                   "max_seq_len": MAX_SEQ, "layers": cfg["num_layers"]},
+        "cpu_baseline": {"value": tpot, "unit": "ms/token", "cores": threads, "kind": "oracle",
+                         "sample": f"{len(timed)} oracle decode steps (40 layers + LM head, "
+                                   f"batch 1, context {PROMPT_LEN + 1}..)"},
+        "e2e": {"value": tpot, "unit": "ms/token", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, cfg):
+    import torch
+    import w8a8_quantized_decode_gb300 as a8w8
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    a8w8.build()
+    B = 1
+    page = cfg["page_size"]
+    max_blocks = MAX_SEQ // page
+    n_total = PROMPT_LEN + args.warmup + args.steps
+    if n_total > MAX_SEQ:
+        raise SystemExit(f"prompt + warmup + steps = {n_total} exceeds max_seq_len {MAX_SEQ}")
+
+    model = build_model(cfg, device)
+    Hkv, D, L = cfg["num_kv_heads"], cfg["head_dim"], cfg["num_layers"]
+    nblk = max_blocks + 1
+    perm = np.random.default_rng(SEED + 1).permutation(nblk).astype(np.int32)
+    bt = perm[:max_blocks][None, :]
+    kc = [torch.zeros((nblk * page, Hkv, D), dtype=torch.bfloat16, device=device) for _ in range(L)]
+    vc = [torch.zeros((nblk * page, Hkv, D), dtype=torch.bfloat16, device=device) for _ in range(L)]
+    rope = a8w8.a8w8_rope_table(MAX_SEQ, D, cfg["rope_theta"], device=device)
+    ws = a8w8.alloc_workspace(cfg, B, max_blocks, device=device)
+    stream = torch.cuda.Stream(device)
+
+    # device-resident decode loop: the graph feeds each argmax back on the device
+    with torch.cuda.stream(stream):
+        g = a8w8.StepGraph(model, cfg, B, max_blocks, kc, vc, rope, ws, device_loop=True,
+                           stream=stream)
+        prompt = synth.prompt_ids(SEED + 5, PROMPT_LEN, cfg["vocab"])
+        # prompt: one step per token, the next prompt token overriding the argmax
+        g.block_table.copy_(torch.from_numpy(bt))
+        for i in range(PROMPT_LEN):
+            ctx = np.array([i + 1], np.int32)
+            g.token_ids.copy_(torch.from_numpy(prompt[i:i + 1]))
+            g.ctx_lens.copy_(torch.from_numpy(ctx))
+            g.slot_mapping.copy_(torch.from_numpy(synth.slots_for(bt, ctx - 1, page)))
+            g.launch(stream)
+        for _ in range(args.warmup):
+            g.launch(stream)
+        stream.synchronize()
+        gpu_uuid = None
+        try:
+            gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+        except Exception:
+            pass
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        with ClockSampler(gpu_uuid) as clocks:
+            ev0.record(stream)
+            for _ in range(args.steps):
+                g.launch(stream)
+            ev1.record(stream)
+            ev1.synchronize()
+        torch.cuda.synchronize()
+        ms = ev0.elapsed_time(ev1)
+        ctx_timed = [PROMPT_LEN + args.warmup + i + 1 for i in range(args.steps)]
+        if world > 1:
+            t = torch.tensor([ms], device=device)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ms = float(t.item())
+        tpot = ms / args.steps
+        errs = a8w8.read_device_errors(stream)
+
+        # e2e: host buffers through the C ABI, inputs H2D + next token D2H every step
+        e2e_graph = a8w8.StepGraph(model, cfg, B, max_blocks, kc, vc, rope, ws, device_loop=False,
+                                   stream=stream)
+        h_tok = torch.zeros(B, dtype=torch.int32).pin_memory()
+        h_slot = torch.zeros(B, dtype=torch.int32).pin_memory()
+        h_bt = torch.from_numpy(bt.copy()).pin_memory()
+        h_ctx = torch.zeros(B, dtype=torch.int32).pin_memory()
+        h_next = torch.zeros(B, dtype=torch.int32).pin_memory()
+        h_tok[0] = int(prompt[-1])
+
+        def e2e_step(pos):
+            h_ctx[0] = pos + 1
+            h_slot[0] = int(bt[0, pos // page]) * page + pos % page
+            e2e_graph.run_host(h_tok, h_slot, h_bt, h_ctx, h_next, stream=stream)
+            h_tok[0] = int(h_next[0])
+
+        for i in range(args.warmup):
+            e2e_step(PROMPT_LEN + i)
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            e2e_step(PROMPT_LEN + args.warmup + i)
+        e2e_ms = (time.perf_counter() - t0) * 1000.0 / args.steps
+        h2d = (B + B + B * max_blocks + B) * 4
+        d2h = B * 4
+        e2e_graph.close()
+
+        # roofline of the dominant kernel: Gate/Up over the 40 layers' weights
+        gu_bytes = gate_up_bytes(cfg)
+        xq = torch.randint(-127, 128, (B, cfg["hidden"]), dtype=torch.int8, device=device)
+        xs = torch.full((B,), 0.01, dtype=torch.float32, device=device)
+        for l in range(3):
+            a8w8.a8w8_gate_up_swiglu(xq, xs, model["layers"][l]["w_gate_up"],
+                                     model["layers"][l]["s_gate_up"], stream=stream)
+        reps = 2
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            for l in range(L):
+                a8w8.a8w8_gate_up_swiglu(xq, xs, model["layers"][l]["w_gate_up"],
+                                         model["layers"][l]["s_gate_up"], stream=stream)
+        e1.record(stream)
+        e1.synchronize()
+        gu_ms = e0.elapsed_time(e1) / (reps * L)
+
+    peaks = measured_peaks()
+    sb = step_bytes(cfg, ctx_timed)
+    per_step_bytes = sb["layers"] + sb["lm_head"] + sb["kv"] / args.steps
+    achieved = gu_bytes / (gu_ms * 1e-3) / 1e9
+    n_launch = 1 + L * 5 + 1 + 1     # embed, 5 per layer, LM head, device-loop advance
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(model, cfg)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": tpot, "unit": "ms/token", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tpot,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int8 x int8 -> int32, f32 dequant, bf16 activations",
+            "data": "synthetic (seeded random-init weights drawn on the device)",
+            "config": {"workload": WORKLOAD, "batch": 1, "layers": L, "hidden": cfg["hidden"],
+                       "intermediate": cfg["intermediate"], "vocab": cfg["vocab"],
+                       "prompt_len": PROMPT_LEN, "max_seq_len": MAX_SEQ, "page_size": page,
+                       "parallelism": "replicas" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2 (14.8 GB of weights per step)"},
+            "tokens_per_s": 1000.0 / tpot * world,
+            "step_bytes": per_step_bytes,
+            "step_hbm_gbs": per_step_bytes / (tpot * 1e-3) / 1e9,
+            "step_frac_of_peak": per_step_bytes / (tpot * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "e2e": {"value": e2e_ms, "unit": "ms/token", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": n_launch * args.steps,
+            "roofline": {"bound": "hbm", "kernel": "Gate/Up projection + SwiGLU (gemv_kernel)",
+                         "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"],
+                         "traffic": GATE_UP_NCU_TRAFFIC_BYTES,
+                         "bytes_per_launch": gu_bytes, "ms_per_launch": gu_ms,
+                         "peak_source": peaks["source"] + " (HBM copy GB/s, MEASURED_PEAKS.json)"},
+            "clocks": clocks.summary(),
+            "device_errors": errs,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def cpu_baseline(model, cfg):
+    """The oracle on a bounded sample: decode steps until about 20 s of CPU time."""
+    import torch
+    hm = host_model(model)
+    import oracle
+    oracle.build()
+    times, threads = time_oracle_steps(hm, cfg, n_steps=8, budget_s=20.0)
+    del hm
+    return {"value": 1000.0 * sum(times) / len(times), "unit": "ms/token", "cores": threads,
+            "kind": "oracle",
+            "sample": f"{len(times)} oracle decode steps of the same workload (40 layers + LM "
+                      f"head, batch 1, contexts {PROMPT_LEN + 1}..{PROMPT_LEN + len(times)})"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=48)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=40, help=argparse.SUPPRESS)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("warmup must be >= 3")
+    cfg = dict(synth.QWEN3_14B, num_layers=args.layers)
+    if args.impl == "reference":
+        run_reference(args, cfg)
+    else:
+        run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    main()

@@ -65,6 +65,7 @@ typedef enum {
 #define A8W8_DEVERR_CTX 0x4u         /* ctx_len outside [0, max_blocks * page] */
 #define A8W8_DEVERR_TOKEN 0x8u       /* token id outside [0, vocab) */
 #define A8W8_DEVERR_POS 0x10u        /* RoPE position outside the table */
+#define A8W8_DEVERR_TIMEOUT 0x20u    /* a bounded wait on an asynchronous copy gave up */
 
 /* Message of the last failed call on this host thread ("" if none). */
 const char* a8w8_last_error(void);

@@ -61,3 +61,17 @@ def assert_layer_close(gpu_bf16, ref_bf16, what=""):
     assert r <= LAYER_REL_L2, f"{what}: rel-L2 {r:.3e} > {LAYER_REL_L2}"
     assert m <= LAYER_NORM_MAX_ABS, f"{what}: normalised max-abs {m:.3e} > {LAYER_NORM_MAX_ABS}"
     return r, m
+
+
+def bf16_close(gpu_bf16, ref_bf16, ulps: float, rel_floor: float) -> np.ndarray:
+    """Elementwise |a - b| <= ulps BF16 units of max(|b|, rel_floor * rms(b)).
+
+    Plain unit-in-the-last-place distances blow up for values near zero
+    (cancellation, or a float32 exp that underflows where the double one does
+    not); the floor measures those against the tensor's own scale."""
+    a = bf16_to_f64(gpu_bf16)
+    b = bf16_to_f64(ref_bf16)
+    rms = np.sqrt(np.mean(b * b)) if b.size else 0.0
+    mag = np.maximum(np.abs(b), max(rel_floor * rms, 1e-30))
+    ulp = 2.0 ** (np.floor(np.log2(mag)) - 7)
+    return np.abs(a - b) <= ulps * ulp

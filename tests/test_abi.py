@@ -129,7 +129,8 @@ def test_layer_and_step_validation(lib):
     out = ctypes.c_void_p(123)
     assert L.a8w8_step_graph_create(ctypes.byref(out), ctypes.byref(m),
                                     _cfg(dict(q, num_layers=1)), 1, 2, 4, caches, caches, FAKE,
-                                    256, None, None, FAKE, 100, None) == a8w8.ERR_WORKSPACE
+                                    256, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, 1, FAKE, 100,
+                                    None) == a8w8.ERR_WORKSPACE
     assert out.value is None
     assert L.a8w8_step_graph_launch(None, None) == a8w8.ERR_INVALID_ARG
     L.a8w8_step_graph_destroy(None)

@@ -142,7 +142,7 @@ a8w8_status check_layer_weights(const a8w8_layer_weights* w) {
 
 // Runs a projection over batch tiles.
 cudaError_t run_gemv(int pro, int epi, int ks, GemvParams p, int M, const Launch& L) {
-    const int tile = gemv_max_batch_tile(p.K);
+    const int tile = gemv_max_batch_tile(p.K, ks);
     const int Ntot = (epi == EPI_SWIGLU) ? 2 * p.N : p.N;
     for (int b0 = 0; b0 < M; b0 += tile) {
         GemvParams q = p;
@@ -155,6 +155,7 @@ cudaError_t run_gemv(int pro, int epi, int ks, GemvParams p, int M, const Launch
         if (p.acc_out) q.acc_out = p.acc_out + (size_t)b0 * Ntot;
         if (p.tap_q) q.tap_q = p.tap_q + (size_t)b0 * p.K;
         if (p.tap_x) q.tap_x = p.tap_x + (size_t)b0 * p.K;
+        q.err = device_error_word();
         if (p.tap_s) q.tap_s = p.tap_s + b0;
         cudaError_t e = launch_gemv(pro, epi, ks, q, L);
         if (e != cudaSuccess) return e;

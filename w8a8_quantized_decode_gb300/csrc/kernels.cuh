@@ -51,10 +51,11 @@ struct GemvParams {
     bf16* tap_x;            // [M, K] normalised BF16 row (PRO_NORM_QUANT)
     int8_t* tap_q;          // [M, K]
     float* tap_s;           // [M]
+    unsigned* err;          // device error word (timeouts)
 };
 
 // Largest batch tile one launch handles; bigger batches are tiled by the host.
-int gemv_max_batch_tile(int K);
+int gemv_max_batch_tile(int K, int k_splits);
 cudaError_t launch_gemv(int prologue, int epilogue, int k_splits, const GemvParams& p,
                         const Launch& L);
 
