@@ -43,7 +43,7 @@ METRIC = "A8W8 decode TPOT (ms/token, 40 layers, bs=1)"
 
 # DRAM traffic per launch of the Gate/Up kernel from the committed ncu summary
 # (profiles/); None until a capture of the current kernel exists.
-GATE_UP_NCU_TRAFFIC_BYTES = None
+GATE_UP_NCU_TRAFFIC_BYTES = 181244672   # profiles/gemv_stream_gate_up_b1.md
 
 
 def step_bytes(cfg, ctx_lens) -> dict:
@@ -319,24 +319,34 @@ def run_ours(args, cfg):
         d2h = B * 4
         e2e_graph.close()
 
-        # roofline of the dominant kernel: Gate/Up over the 40 layers' weights
+        # roofline of the dominant kernel: Gate/Up over the 40 layers' weights,
+        # its 40 launches replayed as one CUDA graph (no host launch overhead)
         gu_bytes = gate_up_bytes(cfg)
         xq = torch.randint(-127, 128, (B, cfg["hidden"]), dtype=torch.int8, device=device)
         xs = torch.full((B,), 0.01, dtype=torch.float32, device=device)
-        for l in range(3):
-            a8w8.a8w8_gate_up_swiglu(xq, xs, model["layers"][l]["w_gate_up"],
-                                     model["layers"][l]["s_gate_up"], stream=stream)
-        reps = 2
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(reps):
+
+        def gate_up_all():
             for l in range(L):
                 a8w8.a8w8_gate_up_swiglu(xq, xs, model["layers"][l]["w_gate_up"],
-                                         model["layers"][l]["s_gate_up"], stream=stream)
-        e1.record(stream)
+                                         model["layers"][l]["s_gate_up"])
+        gate_up_all()
+        torch.cuda.synchronize()
+        gg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gg):
+            gate_up_all()
+        for _ in range(2):
+            gg.replay()
+        reps = 3
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        cs = torch.cuda.current_stream()
+        e0.record(cs)
+        for _ in range(reps):
+            gg.replay()
+        e1.record(cs)
         e1.synchronize()
         gu_ms = e0.elapsed_time(e1) / (reps * L)
+        del gg
 
     peaks = measured_peaks()
     sb = step_bytes(cfg, ctx_timed)
@@ -365,7 +375,7 @@ def run_ours(args, cfg):
             "e2e": {"value": e2e_ms, "unit": "ms/token", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": n_launch * args.steps,
-            "roofline": {"bound": "hbm", "kernel": "Gate/Up projection + SwiGLU (gemv_kernel)",
+            "roofline": {"bound": "hbm", "kernel": "Gate/Up projection + SwiGLU (gemv_stream_kernel)",
                          "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / peaks["hbm_gbs"],
                          "traffic": GATE_UP_NCU_TRAFFIC_BYTES,

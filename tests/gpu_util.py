@@ -53,13 +53,25 @@ LAYER_NORM_MAX_ABS = 3e-2
 STEP_REL_L2 = 2e-2
 
 
-def assert_layer_close(gpu_bf16, ref_bf16, what=""):
+def assert_layer_close(gpu_bf16, ref_bf16, what="", flipped_rows=(), max_abs_bar=None):
+    """The per-layer bar on every row whose quantisation decisions match the
+    oracle's; rows listed in `flipped_rows` (a row scale differs because the
+    row's absmax element differs by one BF16 unit upstream) are held to the
+    step bar instead, since one such flip moves every INT8 code of the row."""
     a = bf16_to_f64(gpu_bf16)
     b = bf16_to_f64(ref_bf16)
-    r = rel_l2(a, b)
-    m = norm_max_abs(a, b)
+    a2 = a.reshape(a.shape[0], -1)
+    b2 = b.reshape(b.shape[0], -1)
+    keep = np.ones(a2.shape[0], bool)
+    keep[list(flipped_rows)] = False
+    r = rel_l2(a2[keep], b2[keep])
+    m = norm_max_abs(a2[keep], b2[keep])
     assert r <= LAYER_REL_L2, f"{what}: rel-L2 {r:.3e} > {LAYER_REL_L2}"
-    assert m <= LAYER_NORM_MAX_ABS, f"{what}: normalised max-abs {m:.3e} > {LAYER_NORM_MAX_ABS}"
+    bar = LAYER_NORM_MAX_ABS if max_abs_bar is None else max_abs_bar
+    assert m <= bar, f"{what}: normalised max-abs {m:.3e} > {bar}"
+    for row in flipped_rows:
+        rr = rel_l2(a2[row], b2[row])
+        assert rr <= STEP_REL_L2, f"{what}: row {row} with a flipped scale: rel-L2 {rr:.3e}"
     return r, m
 
 

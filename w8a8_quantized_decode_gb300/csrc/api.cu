@@ -8,7 +8,7 @@
 #include <string>
 #include <vector>
 
-#include "../../include/a8w8.h"
+#include "a8w8.h"
 #include "kernels.cuh"
 
 using namespace a8w8;

@@ -8,57 +8,53 @@
 // or, for the fused Gate/Up, act = bf16_rne( silu(g) * u ) from the gate and
 // up dequantised values. The two-way split-K of the down projection keeps two
 // independent INT32 accumulators over the two K halves, as the pages do; the
-// halves stay inside one warp because the 5120 output rows already give every
-// SM enough independent rows, so the partials never leave registers.
+// halves are consecutive pieces of the same row stream, so the partials never
+// leave the CTA.
 //
-// Design (decode, batch 1..8 rows per launch):
-//   * One CTA per SM, 16 warps. CTA c owns output channels [c*N/G, (c+1)*N/G)
-//     (balanced to one row). The CTA's weight bytes are cut into 512-byte
-//     units (one 16-byte load per lane) and every warp streams an equal,
-//     contiguous run of units with 128-bit L1-bypassing loads, kUnroll units
-//     in flight per warp (64 KB per SM). Row boundaries inside a run flush
-//     the warp's INT32 partial sums into shared memory with an atomic add,
-//     which is exact, so the split of rows across warps does not change the
-//     result.
+// Design (decode, batch 1..8 rows per launch; one CTA per SM):
+//   * CTA c owns output channels [c*N/G, (c+1)*N/G) (balanced to one row);
+//     for the fused Gate/Up it owns the same channels of both halves. Its
+//     weight rows are contiguous, so they form one byte stream (two for
+//     Gate/Up) cut into 512-byte units, one 16-byte load per lane. Every warp
+//     streams an equal contiguous run of units: the load pointer just advances
+//     by 512 bytes per unit, with L1-bypassing 128-bit loads, double-buffered
+//     (the next batch is in flight while the current one is multiplied).
+//   * Row (and split) boundaries inside a run flush the warp's INT32 partial
+//     sums into shared memory with an atomic add, which is exact, so how the
+//     rows are split across warps does not change the result.
 //   * The first batch of weight loads is issued before griddepcontrol.wait:
-//     weights do not depend on the previous kernel, so with programmatic
+//     weights do not depend on the previous kernel, so under programmatic
 //     dependent launch the weight stream starts while the previous kernel
 //     drains.
 //   * The activation rows are quantised in the prologue by every CTA
 //     (redundantly, from L2): optional RMSNorm (float32, rounded to BF16),
-//     absmax, then INT8 codes into shared memory. INT8 x INT8 products run on
-//     dp4a with the activation read from shared memory.
+//     absmax, then INT8 codes into shared memory. INT8 products use dp4a in
+//     two independent chains.
+//   * K not a multiple of 512 * k_splits falls back to a general kernel that
+//     masks partial units (small shapes only).
 #include "kernels.cuh"
 
 namespace a8w8 {
 
 namespace {
 
-constexpr int kThreads = 512;
-constexpr int kWarps = kThreads / 32;
-constexpr int kUnit = 512;      // bytes per warp-wide load
-constexpr int kUnroll = 8;
+constexpr int kUnit = 512;                // bytes per warp-wide load
+constexpr int kMaxWarps = 32;
 constexpr size_t kSmemActBudget = 96 * 1024;
+
+// Streaming kernel: 4 units per batch, two batches in flight; 32 warps for
+// batch tiles up to 4 rows (64 registers), 16 warps for 8-row tiles.
+__host__ __device__ constexpr int stream_threads(int BT) { return BT >= 8 ? 512 : 1024; }
+constexpr int kStreamUnroll = 4;
+// General kernel (any K multiple of 16).
+constexpr int kGenThreads = 512;
+constexpr int kGenUnroll = 8;
 
 __host__ __device__ __forceinline__ size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
-struct Cursor {
-    int seg, r, ch;
-};
-
-__device__ __forceinline__ void advance(Cursor& c, int upr, int nrows) {
-    if (++c.ch == upr) {
-        c.ch = 0;
-        if (++c.r == nrows) {
-            c.r = 0;
-            ++c.seg;
-        }
-    }
-}
-
 template <int BT>
 __device__ __forceinline__ void block_sum(float (&v)[BT], float* red) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
 #pragma unroll
     for (int b = 0; b < BT; ++b) {
         float s = warp_sum(v[b]);
@@ -68,8 +64,7 @@ __device__ __forceinline__ void block_sum(float (&v)[BT], float* red) {
 #pragma unroll
     for (int b = 0; b < BT; ++b) {
         float s = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) s += red[w * BT + b];
+        for (int w = 0; w < nw; ++w) s += red[w * BT + b];
         v[b] = s;
     }
     __syncthreads();
@@ -77,7 +72,7 @@ __device__ __forceinline__ void block_sum(float (&v)[BT], float* red) {
 
 template <int BT>
 __device__ __forceinline__ void block_max(float (&v)[BT], float* red) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
 #pragma unroll
     for (int b = 0; b < BT; ++b) {
         float s = warp_max(v[b]);
@@ -87,8 +82,7 @@ __device__ __forceinline__ void block_max(float (&v)[BT], float* red) {
 #pragma unroll
     for (int b = 0; b < BT; ++b) {
         float s = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) s = fmaxf(s, red[w * BT + b]);
+        for (int w = 0; w < nw; ++w) s = fmaxf(s, red[w * BT + b]);
         v[b] = s;
     }
     __syncthreads();
@@ -98,9 +92,10 @@ __device__ __forceinline__ void block_max(float (&v)[BT], float* red) {
 template <int BT, int PRO>
 __device__ __forceinline__ void prologue(const GemvParams& p, int8_t* act, float* xs, float* red) {
     const int K = p.K, M = p.M;
+    const int nt = blockDim.x;
     if (PRO == PRO_I8) {
         const int vec = K / 16;
-        for (int i = threadIdx.x; i < BT * vec; i += kThreads) {
+        for (int i = threadIdx.x; i < BT * vec; i += nt) {
             const int b = i / vec, j = i - b * vec;
             int4 v = make_int4(0, 0, 0, 0);
             if (b < M) v = ld_nc_v4(p.xq + (size_t)b * K + 16 * j);
@@ -118,7 +113,7 @@ __device__ __forceinline__ void prologue(const GemvParams& p, int8_t* act, float
         float ss[BT];
 #pragma unroll
         for (int b = 0; b < BT; ++b) ss[b] = 0.0f;
-        for (int j = threadIdx.x; j < vec; j += kThreads) {
+        for (int j = threadIdx.x; j < vec; j += nt) {
 #pragma unroll
             for (int b = 0; b < BT; ++b) {
                 if (b < M) {
@@ -138,7 +133,7 @@ __device__ __forceinline__ void prologue(const GemvParams& p, int8_t* act, float
     float am[BT];
 #pragma unroll
     for (int b = 0; b < BT; ++b) am[b] = 0.0f;
-    for (int j = threadIdx.x; j < vec; j += kThreads) {
+    for (int j = threadIdx.x; j < vec; j += nt) {
         float w[8];
         if (PRO == PRO_NORM_QUANT) unpack8(ld_nc_v4(p.norm_w + 8 * j), w);
 #pragma unroll
@@ -171,7 +166,7 @@ __device__ __forceinline__ void prologue(const GemvParams& p, int8_t* act, float
         for (int b = 0; b < BT; ++b)
             if (b == (int)threadIdx.x) p.tap_s[b] = sc[b];
     }
-    for (int j = threadIdx.x; j < vec; j += kThreads) {
+    for (int j = threadIdx.x; j < vec; j += nt) {
         float w[8];
         if (PRO == PRO_NORM_QUANT) unpack8(ld_nc_v4(p.norm_w + 8 * j), w);
 #pragma unroll
@@ -200,21 +195,8 @@ __device__ __forceinline__ void prologue(const GemvParams& p, int8_t* act, float
     __syncthreads();
 }
 
-template <int BT, int KS>
-__device__ __forceinline__ void flush(int (&acc)[KS][BT], int32_t* accs, int seg, int r,
-                                      int rows_max, int lane) {
-#pragma unroll
-    for (int s = 0; s < KS; ++s) {
-#pragma unroll
-        for (int b = 0; b < BT; ++b) {
-            const int v = warp_sum_i(acc[s][b]);
-            if (lane == 0) atomicAdd(&accs[((seg * rows_max + r) * KS + s) * BT + b], v);
-            acc[s][b] = 0;
-        }
-    }
-}
-
 // Dequantise in float32, add the residual or apply SwiGLU, narrow to BF16.
+// accs layout: [seg][rows_max][KS][BT].
 template <int BT, int EPI, int KS>
 __device__ __forceinline__ void epilogue(const GemvParams& p, const int32_t* accs, const float* xs,
                                          int o0, int nrows, int rows_max) {
@@ -254,202 +236,214 @@ __device__ __forceinline__ void epilogue(const GemvParams& p, const int32_t* acc
     }
 }
 
-// ---------------------------------------------------------------------------
-// Streaming through shared memory with the bulk-copy (TMA) engine, for
-// K a multiple of 512 * k_splits (every Qwen3-14B projection). The CTA's rows
-// are cut into stages of whole rows (about 20 KB) held in a ring of
-// `stages` buffers (about 120 KB). Thread 0 issues one bulk copy per stage;
-// the first ring-full is issued before griddepcontrol.wait, so the weights of
-// this projection stream in while the previous kernel finishes. Consumers
-// (all 16 warps) split each stage into 512-byte units (16 bytes per lane),
-// accumulate dp4a partial sums and merge rows with shared-memory INT32
-// atomics; after a stage every warp arrives on its "empty" barrier and thread
-// 0 refills it with the stage `stages` ahead.
-// ---------------------------------------------------------------------------
-struct TmaPlan {
-    int rows_per_stage;
-    int stages;
-    size_t stage_bytes;
+// Shared-memory layout common to both kernels.
+struct SmemLayout {
+    size_t act, accs, xs, red, total;
 };
-
-constexpr size_t kStageTarget = 20 * 1024;
-constexpr size_t kRingTarget = 120 * 1024;
-constexpr int kMaxStages = 8;
-
-__host__ __device__ __forceinline__ TmaPlan tma_plan(int K) {
-    TmaPlan t;
-    t.rows_per_stage = (int)(kStageTarget / (size_t)K);
-    if (t.rows_per_stage < 1) t.rows_per_stage = 1;
-    t.stage_bytes = (size_t)t.rows_per_stage * K;
-    t.stages = (int)(kRingTarget / t.stage_bytes);
-    if (t.stages > kMaxStages) t.stages = kMaxStages;
-    if (t.stages < 2) t.stages = 2;
-    return t;
+__host__ __device__ __forceinline__ SmemLayout smem_layout(int BT, int nseg, int KS, int K, int N,
+                                                           int G) {
+    const int rows_max = (N + G - 1) / G;
+    SmemLayout s;
+    s.act = 0;
+    s.accs = align16((size_t)BT * K);
+    s.xs = s.accs + align16((size_t)nseg * rows_max * KS * BT * 4);
+    s.red = s.xs + align16((size_t)BT * 4);
+    s.total = s.red + (size_t)kMaxWarps * BT * 4;
+    return s;
 }
 
+// ---------------------------------------------------------------------------
+// Streaming kernel (K a multiple of 512 * KS).
+// ---------------------------------------------------------------------------
 template <int BT, int PRO, int EPI, int KS>
-__global__ void __launch_bounds__(kThreads, 1) gemv_tma_kernel(const GemvParams p) {
+__global__ void __launch_bounds__(stream_threads(BT), 1) gemv_stream_kernel(const GemvParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
     constexpr int NSEG = (EPI == EPI_SWIGLU) ? 2 : 1;
+    constexpr int UNR = kStreamUnroll;
+    constexpr int NW = stream_threads(BT) / 32;
     const int K = p.K, N = p.N;
     const int G = gridDim.x;
     const int o0 = (int)(((long long)N * blockIdx.x) / G);
     const int o1 = (int)(((long long)N * (blockIdx.x + 1)) / G);
     const int nrows = o1 - o0;
     const int rows_max = (N + G - 1) / G;
-    const TmaPlan plan = tma_plan(K);
-    const int R = plan.rows_per_stage, NS = plan.stages;
-    unsigned char* ring = smem;
-    int8_t* act = reinterpret_cast<int8_t*>(smem + plan.stage_bytes * NS);
-    int32_t* accs = reinterpret_cast<int32_t*>(smem + plan.stage_bytes * NS + align16((size_t)BT * K));
-    const int acc_n = NSEG * rows_max * KS * BT;
-    float* xs = reinterpret_cast<float*>(accs + acc_n);
-    float* red = xs + BT;
-    uint64_t* full = reinterpret_cast<uint64_t*>(
-        (reinterpret_cast<uintptr_t>(red + kWarps * BT) + 7) & ~uintptr_t(7));
-    uint64_t* empty = full + NS;
-    __shared__ volatile int s_abort;
+    const SmemLayout L = smem_layout(BT, NSEG, KS, K, N, G);
+    int8_t* act = reinterpret_cast<int8_t*>(smem + L.act);
+    int32_t* accs = reinterpret_cast<int32_t*>(smem + L.accs);
+    float* xs = reinterpret_cast<float*>(smem + L.xs);
+    float* red = reinterpret_cast<float*>(smem + L.red);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int upr = K / kUnit;                 // units per row
-    const int per_seg = (nrows + R - 1) / R;   // stages per segment
-    const int C = NSEG * per_seg;              // stages in total
-    const int Ks_units = upr / KS;             // units per K split
+    const int upr = K / kUnit;            // units per row
+    const int upp = upr / KS;             // units per piece (row split)
+    const int useg = nrows * upr;         // units per segment
+    const int U = NSEG * useg;
+    const int u0 = (int)(((long long)U * warp) / NW);
+    const int u1 = (int)(((long long)U * (warp + 1)) / NW);
+    const int n = u1 - u0;
 
-    if (threadIdx.x == 0) {
-        s_abort = 0;
-        for (int i = 0; i < NS; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kWarps);
+    // load stream: contiguous bytes inside a segment
+    int lseg = 0, lleft = 0;
+    const int8_t* lp = p.W;
+    if (n > 0) {
+        lseg = u0 / useg;
+        const int off = u0 - lseg * useg;
+        lleft = useg - off;
+        lp = p.W + ((size_t)(lseg * N + o0) * K + (size_t)off * kUnit + lane * 16);
+    }
+    auto load_batch = [&](int4 (&dst)[UNR], int count) {
+#pragma unroll
+        for (int i = 0; i < UNR; ++i) {
+            if (i < count) {
+                dst[i] = ld_stream_v4(lp);
+                lp += kUnit;
+                if (--lleft == 0) {
+                    ++lseg;
+                    lleft = useg;
+                    lp = p.W + ((size_t)(lseg * N + o0) * K + lane * 16);
+                }
+            }
         }
-        fence_barrier_init();
-    }
-    __syncthreads();
-
-    uint64_t policy = 0;
-    int issued = 0;   // stages issued so far (thread 0 only)
-    auto issue = [&](int c) {
-        ++issued;
-        const int seg = c / per_seg;
-        const int rf = (c - seg * per_seg) * R;
-        const int rows = min(R, nrows - rf);
-        const unsigned bytes = (unsigned)(rows * K);
-        const int s = c % NS;
-        mbar_arrive_expect_tx(&full[s], bytes);
-        bulk_g2s(ring + (size_t)s * plan.stage_bytes, p.W + (size_t)(seg * N + o0 + rf) * K, bytes,
-                 &full[s], policy);
     };
-    if (threadIdx.x == 0) {
-        policy = l2_evict_first_policy();
-        const int first = C < NS ? C : NS;
-        for (int c = 0; c < first; ++c) issue(c);
-    }
+
+    int4 wa[UNR], wb[UNR];
+    load_batch(wa, n < UNR ? n : UNR);
 
     pdl_wait();
     pdl_trigger();
 
-    for (int i = threadIdx.x; i < acc_n; i += kThreads) accs[i] = 0;
+    const int acc_n = NSEG * rows_max * KS * BT;
+    for (int i = threadIdx.x; i < acc_n; i += blockDim.x) accs[i] = 0;
     prologue<BT, PRO>(p, act, xs, red);
 
-    int acc[KS][BT];
+    // compute stream: piece = (segment, row, split)
+    int cpiece = 0, pleft = 0, rleft = 0, aoff = 0;
+    if (n > 0) {
+        cpiece = u0 / upp;
+        pleft = upp - (u0 - cpiece * upp);
+        const int ju = u0 % upr;                    // unit inside the row
+        rleft = upr - ju;
+        aoff = ju * kUnit + lane * 16;
+    }
+    int acc0[BT], acc1[BT];
 #pragma unroll
-    for (int s = 0; s < KS; ++s)
-#pragma unroll
-        for (int b = 0; b < BT; ++b) acc[s][b] = 0;
+    for (int b = 0; b < BT; ++b) acc0[b] = acc1[b] = 0;
 
-    bool ok = true;
-    for (int c = 0; c < C; ++c) {
-        const int s = c % NS;
-        const unsigned par = (unsigned)((c / NS) & 1);
-        if (!mbar_wait(&full[s], par)) {
-            ok = false;
-            break;
+    auto flush = [&]() {
+        // piece index -> (segment, row, split) -> shared accumulator slot
+        const int split = cpiece % KS;
+        const int rowg = cpiece / KS;               // segment * nrows + row
+        const int seg = rowg / nrows;
+        const int r = rowg - seg * nrows;
+        int32_t* dst = accs + ((seg * rows_max + r) * KS + split) * BT;
+#pragma unroll
+        for (int b = 0; b < BT; ++b) {
+            const int v = warp_sum_i(acc0[b] + acc1[b]);
+            if (lane == 0) atomicAdd(&dst[b], v);
+            acc0[b] = acc1[b] = 0;
         }
-        const int seg = c / per_seg;
-        const int rf = (c - seg * per_seg) * R;
-        const int rows = min(R, nrows - rf);
-        const int U = rows * upr;
-        const int u0 = (U * warp) / kWarps, u1 = (U * (warp + 1)) / kWarps;
-        if (u0 < u1) {
-            int r = u0 / upr, j = u0 - r * upr;
-            int kr = r;
-            const unsigned char* stage = ring + (size_t)s * plan.stage_bytes;
-            for (int u = u0; u < u1; ++u) {
-                if (r != kr) {
-                    flush<BT, KS>(acc, accs, seg, rf + kr, rows_max, lane);
-                    kr = r;
-                }
-                const int4 w = *reinterpret_cast<const int4*>(stage + (size_t)r * K + j * kUnit + lane * 16);
-                const int k = j * kUnit + lane * 16;
+    };
+    auto compute_batch = [&](const int4 (&w)[UNR], int count) {
+#pragma unroll
+        for (int i = 0; i < UNR; ++i) {
+            if (i < count) {
 #pragma unroll
                 for (int b = 0; b < BT; ++b) {
-                    const int4 a = *reinterpret_cast<const int4*>(act + (size_t)b * K + k);
-                    int t = 0;
-                    t = __dp4a(w.x, a.x, t);
-                    t = __dp4a(w.y, a.y, t);
-                    t = __dp4a(w.z, a.z, t);
-                    t = __dp4a(w.w, a.w, t);
-                    if (KS == 1 || j < Ks_units) acc[0][b] += t;
-                    else acc[KS - 1][b] += t;
+                    const int4 a = *reinterpret_cast<const int4*>(act + (size_t)b * K + aoff);
+                    acc0[b] = __dp4a(w[i].x, a.x, acc0[b]);
+                    acc1[b] = __dp4a(w[i].y, a.y, acc1[b]);
+                    acc0[b] = __dp4a(w[i].z, a.z, acc0[b]);
+                    acc1[b] = __dp4a(w[i].w, a.w, acc1[b]);
                 }
-                if (++j == upr) {
-                    j = 0;
-                    ++r;
+                aoff += kUnit;
+                if (--rleft == 0) {
+                    rleft = upr;
+                    aoff = lane * 16;
+                }
+                if (--pleft == 0) {
+                    flush();
+                    ++cpiece;
+                    pleft = upp;
                 }
             }
-            flush<BT, KS>(acc, accs, seg, rf + kr, rows_max, lane);
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-        if (threadIdx.x == 0 && c + NS < C) {
-            if (mbar_wait(&empty[s], par)) {
-                issue(c + NS);
-            } else {
-                ok = false;
-            }
-        }
-        __syncwarp();
-        if (!ok || s_abort) break;
+    };
+
+    int done = 0;
+    while (done < n) {
+        const int ca = n - done < UNR ? n - done : UNR;
+        const int rest = n - done - ca;
+        const int cb = rest < UNR ? rest : UNR;
+        load_batch(wb, cb);
+        compute_batch(wa, ca);
+        done += ca;
+        if (done >= n) break;
+        const int rest2 = n - done - cb;
+        const int ca2 = rest2 < UNR ? rest2 : UNR;
+        load_batch(wa, ca2);
+        compute_batch(wb, cb);
+        done += cb;
     }
-    if (!ok) {
-        s_abort = 1;
-        set_error(p.err, 0x20u);
-    }
+    if (n > 0 && pleft != upp) flush();
     __syncthreads();
-    if (s_abort) {
-        // let every issued copy land before the CTA's shared memory is released
-        if (threadIdx.x == 0) {
-            for (int c = issued - NS < 0 ? 0 : issued - NS; c < issued; ++c)
-                (void)mbar_wait(&full[c % NS], (unsigned)((c / NS) & 1));
-        }
-        __syncthreads();
-        return;
-    }
     epilogue<BT, EPI, KS>(p, accs, xs, o0, nrows, rows_max);
 }
 
+// ---------------------------------------------------------------------------
+// General kernel (any K that is a multiple of 16; partial units are masked).
+// ---------------------------------------------------------------------------
+struct Cursor {
+    int seg, r, ch;
+};
+
+__device__ __forceinline__ void advance(Cursor& c, int upr, int nrows) {
+    if (++c.ch == upr) {
+        c.ch = 0;
+        if (++c.r == nrows) {
+            c.r = 0;
+            ++c.seg;
+        }
+    }
+}
+
+template <int BT, int KS>
+__device__ __forceinline__ void flush_gen(int (&acc)[KS][BT], int32_t* accs, int seg, int r,
+                                          int rows_max, int lane) {
+#pragma unroll
+    for (int s = 0; s < KS; ++s) {
+#pragma unroll
+        for (int b = 0; b < BT; ++b) {
+            const int v = warp_sum_i(acc[s][b]);
+            if (lane == 0) atomicAdd(&accs[((seg * rows_max + r) * KS + s) * BT + b], v);
+            acc[s][b] = 0;
+        }
+    }
+}
+
 template <int BT, int PRO, int EPI, int KS>
-__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
+__global__ void __launch_bounds__(kGenThreads, 1) gemv_kernel(const GemvParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
     constexpr int NSEG = (EPI == EPI_SWIGLU) ? 2 : 1;
+    constexpr int NW = kGenThreads / 32;
     const int K = p.K, N = p.N;
     const int G = gridDim.x;
     const int o0 = (int)(((long long)N * blockIdx.x) / G);
     const int o1 = (int)(((long long)N * (blockIdx.x + 1)) / G);
     const int nrows = o1 - o0;
     const int rows_max = (N + G - 1) / G;
-    int8_t* act = reinterpret_cast<int8_t*>(smem);
-    int32_t* accs = reinterpret_cast<int32_t*>(smem + align16((size_t)BT * K));
+    const SmemLayout L = smem_layout(BT, NSEG, KS, K, N, G);
+    int8_t* act = reinterpret_cast<int8_t*>(smem + L.act);
+    int32_t* accs = reinterpret_cast<int32_t*>(smem + L.accs);
+    float* xs = reinterpret_cast<float*>(smem + L.xs);
+    float* red = reinterpret_cast<float*>(smem + L.red);
     const int acc_n = NSEG * rows_max * KS * BT;
-    float* xs = reinterpret_cast<float*>(accs + acc_n);
-    float* red = xs + BT;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int upr = (K + kUnit - 1) / kUnit;
     const int per_seg = nrows * upr;
     const int U = NSEG * per_seg;
-    const int u0 = (int)((long long)U * warp / kWarps);
-    const int u1 = (int)((long long)U * (warp + 1) / kWarps);
+    const int u0 = (int)((long long)U * warp / NW);
+    const int u1 = (int)((long long)U * (warp + 1) / NW);
     const int Ks = K / KS;
     const int lane_off = lane * 16;
 
@@ -462,9 +456,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
     }
     Cursor cur = ld;
 
-    int4 wv[kUnroll];
+    int4 wv[kGenUnroll];
 #pragma unroll
-    for (int i = 0; i < kUnroll; ++i) {
+    for (int i = 0; i < kGenUnroll; ++i) {
         wv[i] = make_int4(0, 0, 0, 0);
         if (u0 + i < u1) {
             const int k = ld.ch * kUnit + lane_off;
@@ -476,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
     pdl_wait();
     pdl_trigger();
 
-    for (int i = threadIdx.x; i < acc_n; i += kThreads) accs[i] = 0;
+    for (int i = threadIdx.x; i < acc_n; i += blockDim.x) accs[i] = 0;
     prologue<BT, PRO>(p, act, xs, red);
 
     int acc[KS][BT];
@@ -486,12 +480,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
         for (int b = 0; b < BT; ++b) acc[s][b] = 0;
     int kseg = cur.seg, kr = cur.r;
 
-    for (int ub = u0; ub < u1; ub += kUnroll) {
+    for (int ub = u0; ub < u1; ub += kGenUnroll) {
 #pragma unroll
-        for (int i = 0; i < kUnroll; ++i) {
+        for (int i = 0; i < kGenUnroll; ++i) {
             if (ub + i < u1) {
                 if (cur.seg != kseg || cur.r != kr) {
-                    flush<BT, KS>(acc, accs, kseg, kr, rows_max, lane);
+                    flush_gen<BT, KS>(acc, accs, kseg, kr, rows_max, lane);
                     kseg = cur.seg;
                     kr = cur.r;
                 }
@@ -501,31 +495,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
 #pragma unroll
                     for (int b = 0; b < BT; ++b) {
                         const int4 a = *reinterpret_cast<const int4*>(act + (size_t)b * K + k);
-                        if (KS == 1) {
-                            int t = acc[0][b];
-                            t = __dp4a(w.x, a.x, t);
-                            t = __dp4a(w.y, a.y, t);
-                            t = __dp4a(w.z, a.z, t);
-                            t = __dp4a(w.w, a.w, t);
-                            acc[0][b] = t;
-                        } else {
-                            int t = 0;
-                            t = __dp4a(w.x, a.x, t);
-                            t = __dp4a(w.y, a.y, t);
-                            t = __dp4a(w.z, a.z, t);
-                            t = __dp4a(w.w, a.w, t);
-                            if (k < Ks) acc[0][b] += t;
-                            else acc[KS - 1][b] += t;
-                        }
+                        int t = 0;
+                        t = __dp4a(w.x, a.x, t);
+                        t = __dp4a(w.y, a.y, t);
+                        t = __dp4a(w.z, a.z, t);
+                        t = __dp4a(w.w, a.w, t);
+                        if (KS == 1 || k < Ks) acc[0][b] += t;
+                        else acc[KS - 1][b] += t;
                     }
                 }
                 advance(cur, upr, nrows);
             }
         }
-        if (ub + kUnroll < u1) {
+        if (ub + kGenUnroll < u1) {
 #pragma unroll
-            for (int i = 0; i < kUnroll; ++i) {
-                if (ub + kUnroll + i < u1) {
+            for (int i = 0; i < kGenUnroll; ++i) {
+                if (ub + kGenUnroll + i < u1) {
                     const int k = ld.ch * kUnit + lane_off;
                     wv[i] = make_int4(0, 0, 0, 0);
                     if (k < K) wv[i] = ld_stream_v4(p.W + (size_t)(ld.seg * N + o0 + ld.r) * K + k);
@@ -534,49 +519,36 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const GemvParams p) {
             }
         }
     }
-    if (u0 < u1) flush<BT, KS>(acc, accs, kseg, kr, rows_max, lane);
+    if (u0 < u1) flush_gen<BT, KS>(acc, accs, kseg, kr, rows_max, lane);
     __syncthreads();
-
     epilogue<BT, EPI, KS>(p, accs, xs, o0, nrows, rows_max);
 }
 
-size_t gemv_smem_bytes(int BT, int nseg, int KS, int K, int N, int G) {
-    const int rows_max = (N + G - 1) / G;
-    return align16((size_t)BT * K) + (size_t)nseg * rows_max * KS * BT * 4 + (size_t)BT * 4 +
-           (size_t)kWarps * BT * 4;
-}
-
-bool use_tma(int K, int KS) { return K % (kUnit * KS) == 0; }
-
-size_t gemv_tma_smem_bytes(int BT, int nseg, int KS, int K, int N, int G) {
-    const TmaPlan t = tma_plan(K);
-    return t.stage_bytes * t.stages + gemv_smem_bytes(BT, nseg, KS, K, N, G) + 8 + 16 * t.stages;
-}
+bool use_stream(int K, int KS) { return K % (kUnit * KS) == 0; }
 
 template <int BT, int PRO, int EPI, int KS>
 cudaError_t launch_t(const GemvParams& p, const Launch& L) {
-    const bool tma = use_tma(p.K, KS);
-    auto kern = tma ? gemv_tma_kernel<BT, PRO, EPI, KS> : gemv_kernel<BT, PRO, EPI, KS>;
+    const bool stream = use_stream(p.K, KS);
+    auto kern = stream ? gemv_stream_kernel<BT, PRO, EPI, KS> : gemv_kernel<BT, PRO, EPI, KS>;
     const int G = L.num_sms;
     const int nseg = EPI == EPI_SWIGLU ? 2 : 1;
-    const size_t smem = tma ? gemv_tma_smem_bytes(BT, nseg, KS, p.K, p.N, G)
-                            : gemv_smem_bytes(BT, nseg, KS, p.K, p.N, G);
+    const size_t smem = smem_layout(BT, nseg, KS, p.K, p.N, G).total;
     static int configured_dev = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_dev != dev) {
         cudaError_t e = cudaFuncSetAttribute(gemv_kernel<BT, PRO, EPI, KS>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(gemv_tma_kernel<BT, PRO, EPI, KS>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, 220 * 1024);
+            e = cudaFuncSetAttribute(gemv_stream_kernel<BT, PRO, EPI, KS>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
         if (e != cudaSuccess) return e;
         configured_dev = dev;
     }
-    if (smem > 220 * 1024) return cudaErrorInvalidValue;
+    if (smem > 200 * 1024) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(G);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(stream ? stream_threads(BT) : kGenThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = L.stream;
     cudaLaunchAttribute attr[1];
@@ -598,11 +570,9 @@ cudaError_t launch_bt(const GemvParams& p, const Launch& L) {
 }  // namespace
 
 int gemv_max_batch_tile(int K, int k_splits) {
-    const size_t budget = use_tma(K, k_splits)
-                              ? 200 * 1024 - tma_plan(K).stage_bytes * tma_plan(K).stages
-                              : kSmemActBudget;
+    (void)k_splits;
     int bt = 8;
-    while (bt > 1 && (size_t)bt * K > budget) bt >>= 1;
+    while (bt > 1 && (size_t)bt * K > kSmemActBudget) bt >>= 1;
     return bt;
 }
 
