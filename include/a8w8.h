@@ -207,6 +207,34 @@ a8w8_status paged_decode_attention_bf16(const a8w8_bf16* q, const a8w8_bf16* k_c
 
 size_t a8w8_attention_workspace_bytes(int B, int Hq, int D, int max_ctx);
 
+/* The same decode attention as paged_decode_attention_bf16, for callers that
+ * cannot allocate device memory: a plugin whose host framework owns all GPU
+ * memory and hands it no workspace, a serving loop whose memory budget is
+ * fixed at start-up, or a C caller with no device allocator of its own. It
+ * takes no workspace and calls no allocator (no cudaMalloc, cudaFree or
+ * allocating library routine); the caller still passes q, the caches, the
+ * tables and out. There is no counterpart on the source pages: this entry
+ * point exists for such callers only.
+ * Its split-KV partials live in one static device array built into the
+ * library, A8W8_NOALLOC_SCRATCH_BYTES (8 MiB) large, held on every GPU that
+ * loads the library until the process exits. A call whose partials would
+ * exceed it (a8w8_attention_workspace_bytes(B, Hq, D, max_blocks * page_size)
+ * > A8W8_NOALLOC_SCRATCH_BYTES) is rejected with A8W8_ERR_WORKSPACE before
+ * anything is launched. The first call on a device looks up the array's
+ * device address for that device (with that device current); make that first
+ * call before any stream capture. Every call shares the one array: calls that
+ * overlap on the GPU (other streams, other host threads) race on it and must
+ * be serialised by the caller. Nothing in it needs to start at zero: each call
+ * writes every partial it later reads. */
+#define A8W8_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+a8w8_status paged_decode_attention_bf16_noalloc(const a8w8_bf16* q, const a8w8_bf16* k_cache,
+                                                const a8w8_bf16* v_cache,
+                                                const int32_t* block_table,
+                                                const int32_t* ctx_lens, int B, int Hq, int Hkv,
+                                                int D, int page_size, int max_blocks,
+                                                int num_blocks, float softmax_scale,
+                                                a8w8_bf16* out, void* stream);
+
 /* Fills the RoPE table used by the layer: rope[p][i] = cos(p * theta^(-2i/D))
  * and rope[p][D/2 + i] = sin(p * theta^(-2i/D)) for i < D/2, p < max_pos,
  * computed in double and rounded to float ([SRV-52] "Current behavior": Q/K

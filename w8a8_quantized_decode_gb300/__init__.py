@@ -75,6 +75,8 @@ _SIGNATURES = {
     "paged_decode_attention_bf16": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p,
                                          _p, _sz, _p]),
     "a8w8_attention_workspace_bytes": (_sz, [_i, _i, _i, _i]),
+    "paged_decode_attention_bf16_noalloc": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i,
+                                                 _f, _p, _p]),
     "a8w8_rope_table": (_i, [_p, _i, _i, ctypes.c_double, _p]),
     "a8w8_workspace_bytes": (_sz, [_p, _i, _i]),
     "a8w8_decode_layer": (_i, [_p, _p, _i, _p, _p, _p, _i, _i, _p, _p, _p, _p, _i, _p, _sz, _p,
@@ -236,6 +238,29 @@ def paged_decode_attention_bf16(q, k_cache, v_cache, block_table, ctx_lens, page
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(ctx_lens), B, Hq, Hkv, D,
         page_size, max_blocks, num_blocks, scale, _ptr(o), _ptr(ws),
         0 if ws is None else ws.numel(), _stream(stream)))
+    return o
+
+
+NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def paged_decode_attention_bf16_noalloc(q, k_cache, v_cache, block_table, ctx_lens, page_size,
+                                        softmax_scale=None, out=None, stream=None):
+    """Decode attention for callers that cannot allocate device memory.
+
+    Same result as paged_decode_attention_bf16, with the split-KV partials in
+    the library's built-in 8 MiB device scratch instead of a caller workspace.
+    The first call on a device looks up that scratch's address (make it before
+    any stream capture); calls that overlap on the GPU share the scratch and
+    race, so serialise them."""
+    B, Hq, D = q.shape
+    Hkv = k_cache.shape[-2]
+    num_blocks = k_cache.numel() // (Hkv * D * page_size)
+    scale = (1.0 / D ** 0.5) if softmax_scale is None else softmax_scale
+    o = out if out is not None else _torch().empty_like(q)
+    _check(lib().paged_decode_attention_bf16_noalloc(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(ctx_lens), B, Hq, Hkv, D,
+        page_size, block_table.shape[1], num_blocks, scale, _ptr(o), _stream(stream)))
     return o
 
 

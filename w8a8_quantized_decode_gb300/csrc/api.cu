@@ -451,6 +451,91 @@ a8w8_status paged_decode_attention_bf16(const a8w8_bf16* q, const a8w8_bf16* k_c
     return e == cudaSuccess ? A8W8_OK : cuda_fail(e, "paged_decode_attention_bf16");
 }
 
+}  // extern "C"
+
+// Scratch of paged_decode_attention_bf16_noalloc: a fixed device array owned by
+// the library, so that callers with no way to allocate device memory can run
+// split-KV attention. Host code must not pass the array's name to a kernel (on
+// the host it is only a stand-in); the device address comes from
+// cudaGetSymbolAddress, once per device.
+static __device__ __align__(256) float g_noalloc_attn_scratch[A8W8_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+namespace {
+
+// Device address of the scratch array on the current device (looked up on
+// the first use per device), or nullptr with the error message set.
+float* noalloc_scratch_address(int dev) {
+    static float* addr[64];
+    if (dev < 0 || dev >= 64) return nullptr;
+    if (!addr[dev]) {
+        void* p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_attn_scratch);
+        if (e != cudaSuccess) {
+            cuda_fail(e, "paged_decode_attention_bf16_noalloc: scratch address");
+            return nullptr;
+        }
+        addr[dev] = static_cast<float*>(p);
+    }
+    return addr[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+a8w8_status paged_decode_attention_bf16_noalloc(const a8w8_bf16* q, const a8w8_bf16* k_cache,
+                                                const a8w8_bf16* v_cache,
+                                                const int32_t* block_table,
+                                                const int32_t* ctx_lens, int B, int Hq, int Hkv,
+                                                int D, int page_size, int max_blocks,
+                                                int num_blocks, float softmax_scale,
+                                                a8w8_bf16* out, void* stream) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || page_size <= 0 || max_blocks <= 0 || num_blocks <= 0)
+        return fail(A8W8_ERR_INVALID_ARG, "paged_decode_attention_bf16_noalloc: bad size");
+    if (B == 0) return A8W8_OK;
+    if (D != 64 && D != 128) return fail(A8W8_ERR_UNSUPPORTED_SHAPE, "head_dim %d not supported", D);
+    if (Hq % Hkv || Hq / Hkv > 8) return fail(A8W8_ERR_UNSUPPORTED_SHAPE, "Hq/Hkv must be an integer <= 8");
+    if ((long long)max_blocks * page_size > (1 << 24))
+        return fail(A8W8_ERR_UNSUPPORTED_SHAPE, "context longer than 2^24 tokens");
+    a8w8_status s = check_ptrs({q, k_cache, v_cache, block_table, ctx_lens, out},
+                               "paged_decode_attention_bf16_noalloc");
+    if (s != A8W8_OK) return s;
+    const size_t need = attn_part_bytes(B, Hq, D, max_blocks * page_size);
+    if (need > A8W8_NOALLOC_SCRATCH_BYTES)
+        return fail(A8W8_ERR_WORKSPACE,
+                    "paged_decode_attention_bf16_noalloc: split-KV partials need %zu bytes, more than "
+                    "the %zu-byte built-in scratch; use paged_decode_attention_bf16 with a workspace",
+                    need, (size_t)A8W8_NOALLOC_SCRATCH_BYTES);
+    int dev = 0;
+    CUDA_TRY(cudaGetDevice(&dev), "paged_decode_attention_bf16_noalloc: current device");
+    float* scratch = nullptr;
+    if (need > 0) {
+        scratch = noalloc_scratch_address(dev);
+        if (!scratch) return A8W8_ERR_CUDA;
+    }
+    AttnParams a = {};
+    a.q = reinterpret_cast<const bf16*>(q);
+    a.q_stride = Hq * D;
+    a.fused = false;
+    a.k_cache = const_cast<bf16*>(reinterpret_cast<const bf16*>(k_cache));
+    a.v_cache = const_cast<bf16*>(reinterpret_cast<const bf16*>(v_cache));
+    a.block_table = block_table;
+    a.ctx_lens = ctx_lens;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.D = D;
+    a.page = page_size;
+    a.max_blocks = max_blocks;
+    a.num_blocks = num_blocks;
+    a.scale = softmax_scale;
+    a.out = reinterpret_cast<bf16*>(out);
+    a.part = scratch;
+    a.err = device_error_word();
+    cudaError_t e = launch_attention(a, make_launch(stream, false));
+    return e == cudaSuccess ? A8W8_OK : cuda_fail(e, "paged_decode_attention_bf16_noalloc");
+}
+
 a8w8_status a8w8_rope_table(float* rope, int max_pos, int D, double theta, void* stream) {
     if (max_pos < 0 || D <= 0 || D % 2 || D > 2048 || !(theta > 0.0))
         return fail(A8W8_ERR_INVALID_ARG, "a8w8_rope_table: bad arguments");
