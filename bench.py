@@ -41,9 +41,10 @@ SEED = 2026
 WORKLOAD = "qwen3_14b_a8w8_decode_step_b1"
 METRIC = "A8W8 decode TPOT (ms/token, 40 layers, bs=1)"
 
-# DRAM traffic per launch of the Gate/Up kernel from the committed ncu summary
-# (profiles/); None until a capture of the current kernel exists.
-GATE_UP_NCU_TRAFFIC_BYTES = 181244672   # profiles/gemv_stream_gate_up_b1.md
+# DRAM bytes (read + write) per launch of the Gate/Up kernel, from an ncu
+# capture of the kernel as it is now built; None while no capture of the
+# current kernel exists.
+GATE_UP_NCU_TRAFFIC_BYTES = None
 
 
 def step_bytes(cfg, ctx_lens) -> dict:

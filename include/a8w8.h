@@ -93,7 +93,17 @@ typedef struct {
     int page_size;        /* tokens per KV page */
     int down_k_splits;    /* 1 or 2 (2 = the pages' two-way split-K down) */
     float rms_eps;
+    int flags;            /* A8W8_FLAG_* */
 } a8w8_config;
+
+/* a8w8_config.flags: run the decode step as one persistent cooperative
+ * kernel (one CTA per SM, phases separated by grid barriers) instead of one
+ * kernel per operation chained with programmatic dependent launch. Applies
+ * where the shape allows (batch <= 4, head_dim 128, two-way split-K down,
+ * hidden and Hq*head_dim multiples of 512, intermediate a multiple of 1024);
+ * otherwise the flag is ignored. Both give identical results; the separate
+ * kernels are the default because they are currently faster. */
+#define A8W8_FLAG_PERSISTENT_STEP 0x1
 
 /* One layer's weights ([LIB-810] "Gate/Up INT8 path", "Integration note":
  * INT8 matrices plus FP32 per-output-channel scales; [SRV-48] loader review:
@@ -269,6 +279,10 @@ a8w8_status a8w8_decode_layer(const a8w8_layer_weights* w, const a8w8_config* cf
  * final RMSNorm, BF16 LM head with FP32 logits and greedy argmax (lowest index
  * on ties) into next_tokens [B] int32 ([SRV-48] "Performance": temperature 0,
  * top_p 1; [SRV-61] "Related": device-side embedding and sampling).
+ * By default one kernel per operation, chained with programmatic dependent
+ * launch: each kernel's first weight loads are in flight before it waits on
+ * its predecessor. With A8W8_FLAG_PERSISTENT_STEP, where the shape allows,
+ * the whole step is one persistent cooperative kernel.
  * k_caches / v_caches: HOST arrays of num_layers device cache pointers.
  * logits [B, vocab] float (nullable), final_hidden [B, H] BF16 (nullable:
  * the normalised last hidden state). Other arguments as a8w8_decode_layer. */

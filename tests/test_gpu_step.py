@@ -170,3 +170,138 @@ def test_step_bad_token_id_is_flagged(a8w8):
     a8w8.a8w8_decode_step(s.gm, cfg, to_dev(tok), to_dev(slots), to_dev(s.bt), to_dev(ctx), s.gkc,
                           s.gvc, s.rope, s.ws, s.next)
     assert a8w8.read_device_errors() & a8w8.DEVERR_TOKEN
+
+
+# Shapes the persistent single-kernel step accepts (head_dim 128, hidden and
+# Hq * head_dim multiples of 512, intermediate a multiple of 1024), small enough
+# for the oracle.
+SMALL_PERSISTENT = dict(synth.TINY, hidden=512, num_q_heads=4, num_kv_heads=2, head_dim=128,
+                        intermediate=1024, num_layers=2, vocab=1000, page_size=16)
+
+
+def _run_steps(a8w8, cfg, B, max_seq, seed, n_steps, flags):
+    """n teacher-free steps through the direct entry point; returns per-step
+    (next tokens, final hidden, logits) and the caches."""
+    c = dict(cfg, flags=flags)
+    s = Session(a8w8, c, B, max_seq=max_seq, seed=seed)
+    tok, slots, ctx = s.inputs(synth.prompt_ids(seed + 7, B, cfg["vocab"]))
+    out = []
+    for _ in range(n_steps):
+        a8w8.a8w8_decode_step(s.gm, c, to_dev(tok), to_dev(slots), to_dev(s.bt), to_dev(ctx),
+                              s.gkc, s.gvc, s.rope, s.ws, s.next, logits=s.logits,
+                              final_hidden=s.fh)
+        out.append((to_host(s.next), to_host(s.fh), to_host(s.logits)))
+        tok = to_host(s.next)
+        ctx = ctx + 1
+        slots = synth.slots_for(s.bt, ctx - 1, s.page)
+    return out, [to_host(x) for x in s.gkc + s.gvc]
+
+
+@pytest.mark.parametrize("B,max_seq", [(1, 40), (2, 300), (4, 40)])
+def test_persistent_step_equals_separate_kernels(a8w8, B, max_seq):
+    # max_seq 300 gives 19 pages of 16 tokens: three 128-token KV chunks and a
+    # combine pass inside the persistent kernel
+    a, ca = _run_steps(a8w8, SMALL_PERSISTENT, B, max_seq, 600 + B, 6, a8w8.FLAG_PERSISTENT_STEP)
+    b, cb = _run_steps(a8w8, SMALL_PERSISTENT, B, max_seq, 600 + B, 6, 0)
+    for (n1, h1, l1), (n2, h2, l2) in zip(a, b):
+        assert np.array_equal(n1, n2)
+        assert np.array_equal(h1, h2)
+        assert np.array_equal(l1, l2)
+    for x, y in zip(ca, cb):
+        assert np.array_equal(x, y)
+    assert a8w8.read_device_errors() == 0
+
+
+@pytest.mark.parametrize("B", [1, 4])
+def test_persistent_step_teacher_forced_vs_oracle(a8w8, B):
+    s = Session(a8w8, dict(SMALL_PERSISTENT, flags=a8w8.FLAG_PERSISTENT_STEP), B, max_seq=48,
+                seed=700 + B)
+    tokens = synth.prompt_ids(701 + B, B, SMALL_PERSISTENT["vocab"])
+    for step in range(12):
+        r = s.step_both(tokens)
+        assert r["rel"] <= STEP_REL_L2, (step, r["rel"])
+        assert np.array_equal(r["g_next"], oracle.argmax_f32(r["g_logits"]))
+        assert rel_l2(r["g_logits"], r["o_logits"]) <= STEP_REL_L2
+        tokens = r["o_next"]
+    assert a8w8.read_device_errors() == 0
+
+
+def test_persistent_device_loop(a8w8):
+    cfg = dict(SMALL_PERSISTENT, flags=a8w8.FLAG_PERSISTENT_STEP)
+    B, n = 2, 10
+    s = Session(a8w8, cfg, B, max_seq=32, seed=800)
+    saved = [c.clone() for c in s.gkc + s.gvc]
+    tok0, slots0, ctx0 = s.inputs(synth.prompt_ids(801, B, cfg["vocab"]))
+    ref = []
+    tok, slots, ctx = tok0, slots0, ctx0
+    for _ in range(n):
+        a8w8.a8w8_decode_step(s.gm, cfg, to_dev(tok), to_dev(slots), to_dev(s.bt), to_dev(ctx),
+                              s.gkc, s.gvc, s.rope, s.ws, s.next)
+        ref.append(to_host(s.next))
+        tok, ctx = ref[-1], ctx + 1
+        slots = synth.slots_for(s.bt, ctx - 1, s.page)
+    for c, sv in zip(s.gkc + s.gvc, saved):
+        c.copy_(sv)
+    g = a8w8.StepGraph(s.gm, cfg, B, s.max_blocks, s.gkc, s.gvc, s.rope, s.ws, device_loop=True)
+    g.set_inputs(to_dev(tok0), to_dev(slots0), to_dev(s.bt), to_dev(ctx0))
+    got = []
+    for _ in range(n):
+        g.launch()
+        got.append(to_host(g.next_tokens))
+    assert np.array_equal(np.array(got), np.array(ref))
+    g.close()
+
+
+@pytest.mark.slow
+def test_qwen3_14b_40_layer_step_vs_oracle(a8w8):
+    """The benchmarked workload at full size: 40 Qwen3-14B-shaped layers and the
+    151936-token LM head at batch 1, weights drawn on the device as in the
+    benchmark, run through the persistent step graph; the oracle recomputes the
+    same steps (teacher forcing) on the host."""
+    import torch
+    cfg = dict(synth.QWEN3_14B)
+    dev = torch.device("cuda")
+    model = synth.t_model_weights(cfg, 2026, dev)
+    page, max_blocks = cfg["page_size"], 2
+    Hkv, D, L = cfg["num_kv_heads"], cfg["head_dim"], cfg["num_layers"]
+    kc = [torch.zeros((max_blocks * page, Hkv, D), dtype=torch.bfloat16, device=dev) for _ in range(L)]
+    vc = [torch.zeros_like(kc[0]) for _ in range(L)]
+    rope = a8w8.a8w8_rope_table(max_blocks * page, D, cfg["rope_theta"])
+    ws = a8w8.alloc_workspace(cfg, 1, max_blocks)
+    fh = torch.empty((1, cfg["hidden"]), dtype=torch.bfloat16, device=dev)
+    logits = torch.empty((1, cfg["vocab"]), dtype=torch.float32, device=dev)
+    g = a8w8.StepGraph(model, cfg, 1, max_blocks, kc, vc, rope, ws, logits=logits, final_hidden=fh)
+
+    def h(t):
+        t = t.detach().cpu()
+        return t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy()
+    hm = dict(embed=h(model["embed"]), final_norm_w=h(model["final_norm_w"]),
+              lm_head=h(model["lm_head"]),
+              layers=[{k: h(v) for k, v in l.items()} for l in model["layers"]])
+    okc = [np.zeros((max_blocks * page, Hkv, D), np.uint16) for _ in range(L)]
+    ovc = [np.zeros_like(okc[0]) for _ in range(L)]
+    bt = np.array([[0, 1]], np.int32)
+    tok = synth.prompt_ids(5, 1, cfg["vocab"])
+    for step in range(3):
+        ctx = np.array([step + 1], np.int32)
+        slots = synth.slots_for(bt, ctx - 1, page)
+        # both sides start each step from the same state: the GPU's KV caches
+        # (a step is 40 quantised layers deep, and differences carried in the
+        # caches from earlier steps would compound with the step's own)
+        for l in range(L):
+            okc[l][...] = to_host(kc[l])
+            ovc[l][...] = to_host(vc[l])
+        g.set_inputs(to_dev(tok), to_dev(slots), to_dev(bt), to_dev(ctx))
+        g.launch()
+        torch.cuda.synchronize()
+        o_next, o_fh, o_logits, rc = oracle.decode_step(hm, cfg, tok, slots, bt, ctx, okc, ovc,
+                                                        want_logits=True)
+        assert rc == 0
+        rel = rel_l2(bf16_to_f64(to_host(fh)), bf16_to_f64(o_fh))
+        assert rel <= STEP_REL_L2, (step, rel)
+        gl = to_host(logits)
+        assert rel_l2(gl, o_logits) <= STEP_REL_L2
+        assert np.array_equal(to_host(g.next_tokens), oracle.argmax_f32(gl))
+        tok = o_next
+    g.close()
+    assert a8w8.read_device_errors() == 0

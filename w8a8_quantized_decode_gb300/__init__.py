@@ -23,6 +23,7 @@ _lock = threading.Lock()
 _lib = None
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_BOUNDS, ERR_WORKSPACE, ERR_CUDA = 0, -1, -2, -3, -4, -5
+FLAG_PERSISTENT_STEP = 0x1
 DEVERR_SLOT, DEVERR_BLOCK, DEVERR_CTX, DEVERR_TOKEN, DEVERR_POS = 0x1, 0x2, 0x4, 0x8, 0x10
 
 
@@ -41,7 +42,7 @@ _sz = ctypes.c_size_t
 class Config(ctypes.Structure):
     _fields_ = [("hidden", _i), ("num_q_heads", _i), ("num_kv_heads", _i), ("head_dim", _i),
                 ("intermediate", _i), ("num_layers", _i), ("vocab", _i), ("page_size", _i),
-                ("down_k_splits", _i), ("rms_eps", _f)]
+                ("down_k_splits", _i), ("rms_eps", _f), ("flags", _i)]
 
 
 WEIGHT_FIELDS = ("input_norm_w", "w_qkv", "s_qkv", "q_norm_w", "k_norm_w", "w_o", "s_o",
@@ -155,7 +156,8 @@ def _stream(stream=None):
 def make_config(cfg: dict) -> Config:
     return Config(cfg["hidden"], cfg["num_q_heads"], cfg["num_kv_heads"], cfg["head_dim"],
                   cfg["intermediate"], cfg.get("num_layers", 1), cfg.get("vocab", 0),
-                  cfg["page_size"], cfg.get("down_k_splits", 2), cfg["rms_eps"])
+                  cfg["page_size"], cfg.get("down_k_splits", 2), cfg["rms_eps"],
+                  cfg.get("flags", 0))
 
 
 def layer_struct(w: dict) -> LayerWeights:

@@ -79,7 +79,7 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Workspace layout shared by the layer and the step.
 struct WsLayout {
-    size_t hid, qkv, attn, act, part, keys, ticket, total;
+    size_t hid, qkv, attn, act, part, keys, ticket, bar, total;
 };
 
 WsLayout ws_layout(const a8w8_config& c, int B, int max_blocks) {
@@ -100,6 +100,8 @@ WsLayout ws_layout(const a8w8_config& c, int B, int max_blocks) {
     w.keys = o;
     o = round_up(o + (size_t)B * 8, 256);
     w.ticket = o;
+    o = round_up(o + 16, 256);
+    w.bar = o;
     o = round_up(o + 16, 256);
     w.total = o;
     return w;
@@ -600,11 +602,76 @@ static a8w8_status enqueue_step(const a8w8_model* m, const a8w8_config& c, int B
                                 const int32_t* ctx_lens, a8w8_bf16* const* k_caches,
                                 a8w8_bf16* const* v_caches, const float* rope, int max_pos,
                                 int32_t* next_tokens, float* logits, a8w8_bf16* final_hidden,
-                                unsigned char* ws, const Launch& L) {
+                                unsigned char* ws, const Launch& L, bool device_loop) {
     const WsLayout lay = ws_layout(c, B, max_blocks);
     bf16* hidden = reinterpret_cast<bf16*>(ws + lay.hid);
     unsigned long long* keys = reinterpret_cast<unsigned long long*>(ws + lay.keys);
     unsigned* ticket = reinterpret_cast<unsigned*>(ws + lay.ticket);
+    if ((c.flags & A8W8_FLAG_PERSISTENT_STEP) &&
+        step_supported(B, c.head_dim, c.num_layers, c.hidden, c.intermediate, c.num_q_heads,
+                       c.num_kv_heads, max_blocks * c.page_size, L.num_sms) &&
+        c.down_k_splits == 2) {
+        StepParams P;
+        std::memset(&P, 0, sizeof P);
+        P.B = B;
+        P.H = c.hidden;
+        P.Hq = c.num_q_heads;
+        P.Hkv = c.num_kv_heads;
+        P.D = c.head_dim;
+        P.I = c.intermediate;
+        P.vocab = c.vocab;
+        P.page = c.page_size;
+        P.max_blocks = max_blocks;
+        P.num_blocks = num_blocks;
+        P.max_pos = max_pos;
+        P.L = c.num_layers;
+        P.down_splits = c.down_k_splits;
+        P.device_loop = device_loop ? 1 : 0;
+        P.eps = c.rms_eps;
+        P.embed = reinterpret_cast<const bf16*>(m->embed);
+        P.final_norm_w = reinterpret_cast<const bf16*>(m->final_norm_w);
+        P.lm_head = reinterpret_cast<const bf16*>(m->lm_head);
+        P.rope = rope;
+        P.token_ids = const_cast<int32_t*>(token_ids);
+        P.slot_mapping = const_cast<int32_t*>(slot_mapping);
+        P.block_table = const_cast<int32_t*>(block_table);
+        P.ctx_lens = const_cast<int32_t*>(ctx_lens);
+        P.next_tokens = next_tokens;
+        P.logits = logits;
+        P.final_hidden = reinterpret_cast<bf16*>(final_hidden);
+        P.hidden = hidden;
+        P.qkv = reinterpret_cast<bf16*>(ws + lay.qkv);
+        P.attn = reinterpret_cast<bf16*>(ws + lay.attn);
+        P.act = reinterpret_cast<bf16*>(ws + lay.act);
+        P.part = reinterpret_cast<float*>(ws + lay.part);
+        P.keys = keys;
+        P.ticket = ticket;
+        P.bar = reinterpret_cast<unsigned*>(ws + lay.bar);
+        P.err = device_error_word();
+        for (int l = 0; l < c.num_layers; ++l) {
+            const a8w8_layer_weights& w = m->layers[l];
+            StepLayer& d = P.layers[l];
+            d.input_norm_w = reinterpret_cast<const bf16*>(w.input_norm_w);
+            d.w_qkv = w.w_qkv;
+            d.s_qkv = w.s_qkv;
+            d.q_norm_w = reinterpret_cast<const bf16*>(w.q_norm_w);
+            d.k_norm_w = reinterpret_cast<const bf16*>(w.k_norm_w);
+            d.w_o = w.w_o;
+            d.s_o = w.s_o;
+            d.post_norm_w = reinterpret_cast<const bf16*>(w.post_norm_w);
+            d.w_gate_up = w.w_gate_up;
+            d.s_gate_up = w.s_gate_up;
+            d.w_down = w.w_down;
+            d.s_down = w.s_down;
+            P.k_cache[l] = reinterpret_cast<bf16*>(k_caches[l]);
+            P.v_cache[l] = reinterpret_cast<bf16*>(v_caches[l]);
+        }
+        cudaError_t e = cudaMemsetAsync(P.bar, 0, 16, L.stream);
+        if (e != cudaSuccess) return cuda_fail(e, "step barrier reset");
+        e = launch_step(P, L);
+        if (e != cudaSuccess) return cuda_fail(e, "persistent decode step");
+        return A8W8_OK;
+    }
     cudaError_t e = launch_embed(reinterpret_cast<const bf16*>(m->embed), c.vocab, c.hidden, token_ids,
                                  B, hidden, keys, ticket, device_error_word(), L);
     if (e != cudaSuccess) return cuda_fail(e, "embedding");
@@ -633,6 +700,12 @@ static a8w8_status enqueue_step(const a8w8_model* m, const a8w8_config& c, int B
         e = launch_lmhead_argmax(p, L);
         if (e != cudaSuccess) return cuda_fail(e, "LM head");
     }
+    if (device_loop) {
+        e = launch_advance(const_cast<int32_t*>(token_ids), const_cast<int32_t*>(slot_mapping),
+                           block_table, const_cast<int32_t*>(ctx_lens), next_tokens, B, max_blocks,
+                           c.page_size, L);
+        if (e != cudaSuccess) return cuda_fail(e, "advance kernel");
+    }
     return A8W8_OK;
 }
 
@@ -654,7 +727,7 @@ a8w8_status a8w8_decode_step(const a8w8_model* m, const a8w8_config* cfg, int B,
     if (L.num_sms <= 0) return fail(A8W8_ERR_CUDA, "no CUDA device");
     return enqueue_step(m, *cfg, B, token_ids, slot_mapping, block_table, max_blocks, num_blocks,
                         ctx_lens, k_caches, v_caches, rope, max_pos, next_tokens, logits,
-                        final_hidden, static_cast<unsigned char*>(ws), L);
+                        final_hidden, static_cast<unsigned char*>(ws), L, false);
 }
 
 // ---------------------------------------------------------------------------
@@ -707,12 +780,7 @@ a8w8_status a8w8_step_graph_create(a8w8_step_graph** out, const a8w8_model* m,
         Launch L = make_launch(cap, true);
         s = enqueue_step(m, *cfg, B, g->tok, g->slot, g->table, max_blocks, num_blocks, g->ctx,
                          k_caches, v_caches, rope, max_pos, g->next, logits, final_hidden,
-                         static_cast<unsigned char*>(ws), L);
-        if (s == A8W8_OK && device_loop) {
-            cudaError_t e3 = launch_advance(g->tok, g->slot, g->table, g->ctx, g->next, B, max_blocks,
-                                            cfg->page_size, L);
-            if (e3 != cudaSuccess) s = cuda_fail(e3, "advance kernel");
-        }
+                         static_cast<unsigned char*>(ws), L, device_loop != 0);
         cudaGraph_t graph = nullptr;
         cudaError_t e2 = cudaStreamEndCapture(cap, &graph);
         if (s == A8W8_OK && e2 != cudaSuccess) s = cuda_fail(e2, "end capture");

@@ -31,9 +31,26 @@ __device__ __forceinline__ int4 ld_stream_v4(const void* p) {
     return r;
 }
 
-// 16-byte load through the read-only path (inputs reused across CTAs).
+// 16-byte load through the read-only path, for data that no kernel writes
+// (weights, tables).
 __device__ __forceinline__ int4 ld_nc_v4(const void* p) {
     return __ldg(reinterpret_cast<const int4*>(p));
+}
+
+// 16-byte load from L2, bypassing L1, for data produced on the device
+// (activations, partials): inside one long-running kernel an SM's L1 may
+// still hold a line that another SM has since rewritten.
+__device__ __forceinline__ int4 ld_cg_v4(const void* p) {
+    return __ldcg(reinterpret_cast<const int4*>(p));
+}
+__device__ __forceinline__ bf16 ld_cg_bf16(const bf16* p) {
+    unsigned short u = __ldcg(reinterpret_cast<const unsigned short*>(p));
+    return __ushort_as_bfloat16(u);
+}
+
+// Hint: fetch the 128-byte line holding p into L2 (no register, no wait).
+__device__ __forceinline__ void prefetch_line_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 // Asynchronous 16-byte global -> shared copy (cp.async, L2 only).

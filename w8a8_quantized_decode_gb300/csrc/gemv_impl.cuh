@@ -1,0 +1,511 @@
+// gemv_impl.cuh -- device side of the A8W8 decode projections, shared by the
+// standalone projection kernels and the persistent decode-step kernel.
+//
+// What is computed ("perf(qwen3-a8w8): optimize decode scheduling and data
+// paths", pypto-lib PR #810, "Gate/Up INT8 path" and "Decode scheduling"):
+//   acc_j[m][n] = sum_{k in split j} x_q[m][k] * W[n][k]       (int32, exact)
+//   p_j         = (float(acc_j) * s_x[m]) * s_w[n]              (float32)
+//   y[m][n]     = bf16_rne( (p_0 [+ p_1]) [+ residual[m][n]] )
+// or, for the fused Gate/Up, act = bf16_rne( silu(g) * u ) from the gate and
+// up dequantised values. The two-way split-K of the down projection keeps two
+// independent INT32 accumulators over the two K halves, as the pages do; the
+// halves are consecutive pieces of the same row stream, so the partials never
+// leave the CTA.
+//
+// Streaming scheme (one CTA per SM, batch tiles of 1..8 rows):
+//   * CTA c owns output channels [c*N/G, (c+1)*N/G) (balanced to one row);
+//     for the fused Gate/Up it owns the same channels of both halves. Its
+//     weight rows are contiguous, so they form one byte stream (two for
+//     Gate/Up) cut into 512-byte units, one 16-byte load per lane. Every warp
+//     streams an equal contiguous run of units: the load pointer advances by
+//     512 bytes per unit, with L1-bypassing 128-bit loads, double-buffered
+//     (the next batch is in flight while the current one is multiplied).
+//   * Row (and split) boundaries inside a run flush the warp's INT32 partial
+//     sums into shared memory with an atomic add, which is exact, so how the
+//     rows are split across warps does not change the result.
+//   * The first batch of weight loads (and an L2 warm-up of the next units)
+//     is issued before waiting on the producer of the activations
+//     (griddepcontrol.wait or a grid barrier), since weights never depend on
+//     it.
+//   * A prologue then quantises the activation rows (redundantly in every
+//     CTA, from L2, staged once in shared memory when they fit): optional
+//     RMSNorm (float32, rounded to BF16), absmax, INT8 codes into shared
+//     memory; the stream multiplies with dp4a in two independent chains, and
+//     a float32 dequantisation epilogue finishes.
+#pragma once
+
+#include "kernels.cuh"
+
+namespace a8w8 {
+namespace gemv {
+
+constexpr int kUnit = 512;                // bytes per warp-wide load
+constexpr int kMaxWarps = 32;
+
+// Streaming kernel: 4 units per batch, two batches in flight; 32 warps for
+// batch tiles up to 4 rows (64 registers), 16 warps for 8-row tiles.
+__host__ __device__ constexpr int stream_threads(int BT) { return BT >= 8 ? 512 : 1024; }
+constexpr int kStreamUnroll = 4;
+
+__host__ __device__ __forceinline__ size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
+
+template <int BT>
+__device__ __forceinline__ void block_sum(float (&v)[BT], float* red) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+#pragma unroll
+    for (int b = 0; b < BT; ++b) {
+        float s = warp_sum(v[b]);
+        if (lane == 0) red[warp * BT + b] = s;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int b = 0; b < BT; ++b) {
+        float s = 0.0f;
+        for (int w = 0; w < nw; ++w) s += red[w * BT + b];
+        v[b] = s;
+    }
+    __syncthreads();
+}
+
+template <int BT>
+__device__ __forceinline__ void block_max(float (&v)[BT], float* red) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+#pragma unroll
+    for (int b = 0; b < BT; ++b) {
+        float s = warp_max(v[b]);
+        if (lane == 0) red[warp * BT + b] = s;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int b = 0; b < BT; ++b) {
+        float s = 0.0f;
+        for (int w = 0; w < nw; ++w) s = fmaxf(s, red[w * BT + b]);
+        v[b] = s;
+    }
+    __syncthreads();
+}
+
+// Per-thread slots of the normalisation weight held in registers (loaded
+// before the dependency wait): thread t holds 8-element vectors t, t + NT, ...
+// enough for K = 8192 with 1024 or 512 threads.
+__host__ __device__ constexpr int norm_pre_slots(int NT) { return NT >= 1024 ? 1 : 2; }
+
+// Quantised activation rows into act[BT][K] and their scales into xs[BT].
+// The BF16 rows are read from L2 once (each thread issues up to four 16-byte
+// loads before using any); when `stage` is given they are kept in shared
+// memory for the later passes (normalisation, quantisation). With `nw_pre`
+// the RMSNorm weight is taken from `nwr` (loaded before the wait).
+template <int BT, int PRO, int NP>
+__device__ __forceinline__ void prologue(const GemvParams& p, int8_t* act, float* xs, float* red,
+                                         bf16* stage, const int4 (&nwr)[NP], bool nw_pre) {
+    const int K = p.K, M = p.M;
+    const int nt = blockDim.x;
+    if (PRO == PRO_I8) {
+        const int vec = K / 16;
+        for (int i = threadIdx.x; i < BT * vec; i += nt) {
+            const int b = i / vec, j = i - b * vec;
+            int4 v = make_int4(0, 0, 0, 0);
+            if (b < M) v = ld_cg_v4(p.xq + (size_t)b * K + 16 * j);
+            *reinterpret_cast<int4*>(act + (size_t)b * K + 16 * j) = v;
+        }
+        if (threadIdx.x < BT) xs[threadIdx.x] = threadIdx.x < M ? __ldcg(p.x_scale + threadIdx.x) : 0.0f;
+        __syncthreads();
+        return;
+    }
+    const int vec = K / 8;
+    // pass 1 (L2): sum of squares (RMSNorm) or absmax (plain quantisation)
+    constexpr int C = BT == 1 ? 4 : (BT == 2 ? 2 : 1);   // loads in flight per row
+    float st[BT];
+#pragma unroll
+    for (int b = 0; b < BT; ++b) st[b] = 0.0f;
+    for (int j0 = threadIdx.x; j0 < vec; j0 += C * nt) {
+        int4 raw[C][BT];
+#pragma unroll
+        for (int c = 0; c < C; ++c) {
+            const int j = j0 + c * nt;
+#pragma unroll
+            for (int b = 0; b < BT; ++b)
+                raw[c][b] = (j < vec && b < M) ? ld_cg_v4(p.x + (size_t)b * p.ldx + 8 * j)
+                                               : make_int4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int c = 0; c < C; ++c) {
+            const int j = j0 + c * nt;
+            if (j < vec) {
+#pragma unroll
+                for (int b = 0; b < BT; ++b) {
+                    if (b < M) {
+                        if (stage) *reinterpret_cast<int4*>(stage + (size_t)b * K + 8 * j) = raw[c][b];
+                        float f[8];
+                        unpack8(raw[c][b], f);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            if (PRO == PRO_NORM_QUANT) st[b] += f[e] * f[e];
+                            else st[b] = fmaxf(st[b], fabsf(f[e]));
+                        }
+                    }
+                }
+            }
+        }
+    }
+    float sc[BT];
+    float inv[BT];
+    if (PRO == PRO_NORM_QUANT) {
+        block_sum<BT>(st, red);
+#pragma unroll
+        for (int b = 0; b < BT; ++b)
+            inv[b] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(st[b], (float)K), p.eps)));
+        // pass 2: normalised BF16 row (kept in the stage) and its absmax
+        const bool tapx = (blockIdx.x == 0) && p.tap_x != nullptr;
+        float am[BT];
+#pragma unroll
+        for (int b = 0; b < BT; ++b) am[b] = 0.0f;
+        auto pass2 = [&](int j, const int4 wraw) {
+            float w[8];
+            unpack8(wraw, w);
+#pragma unroll
+            for (int b = 0; b < BT; ++b) {
+                if (b < M) {
+                    const int4 raw = stage ? *reinterpret_cast<const int4*>(stage + (size_t)b * K + 8 * j)
+                                           : ld_cg_v4(p.x + (size_t)b * p.ldx + 8 * j);
+                    float f[8];
+                    unpack8(raw, f);
+                    __align__(16) bf16 y[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        y[e] = f2bf(__fmul_rn(__fmul_rn(f[e], inv[b]), w[e]));
+                        am[b] = fmaxf(am[b], fabsf(bf2f(y[e])));
+                    }
+                    if (stage) *reinterpret_cast<int4*>(stage + (size_t)b * K + 8 * j) = *reinterpret_cast<const int4*>(y);
+                    if (tapx) *reinterpret_cast<int4*>(p.tap_x + (size_t)b * K + 8 * j) = *reinterpret_cast<const int4*>(y);
+                }
+            }
+        };
+        if (nw_pre) {
+#pragma unroll
+            for (int i = 0; i < NP; ++i) {
+                const int j = threadIdx.x + i * nt;
+                if (j < vec) pass2(j, nwr[i]);
+            }
+        } else {
+            for (int j = threadIdx.x; j < vec; j += nt) pass2(j, ld_nc_v4(p.norm_w + 8 * j));
+        }
+        block_max<BT>(am, red);
+#pragma unroll
+        for (int b = 0; b < BT; ++b) sc[b] = __fdiv_rn(am[b], 127.0f);
+    } else {
+        block_max<BT>(st, red);
+#pragma unroll
+        for (int b = 0; b < BT; ++b) sc[b] = __fdiv_rn(st[b], 127.0f);
+    }
+    if (threadIdx.x < BT) {
+#pragma unroll
+        for (int b = 0; b < BT; ++b)
+            if (b == (int)threadIdx.x) xs[b] = sc[b];
+    }
+    const bool tap = (blockIdx.x == 0) && p.tap_q != nullptr;
+    if (tap && threadIdx.x < M && p.tap_s) {
+#pragma unroll
+        for (int b = 0; b < BT; ++b)
+            if (b == (int)threadIdx.x) p.tap_s[b] = sc[b];
+    }
+    // pass 3: INT8 codes of the BF16 row that is quantised
+    for (int j = threadIdx.x; j < vec; j += nt) {
+        float w[8];
+        if (PRO == PRO_NORM_QUANT && !stage) unpack8(ld_nc_v4(p.norm_w + 8 * j), w);
+#pragma unroll
+        for (int b = 0; b < BT; ++b) {
+            uint32_t lo = 0, hi = 0;
+            if (b < M) {
+                float f[8];
+                if (stage) {
+                    unpack8(*reinterpret_cast<const int4*>(stage + (size_t)b * K + 8 * j), f);
+                } else {
+                    unpack8(ld_cg_v4(p.x + (size_t)b * p.ldx + 8 * j), f);
+                    if (PRO == PRO_NORM_QUANT) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            f[e] = bf2f(f2bf(__fmul_rn(__fmul_rn(f[e], inv[b]), w[e])));
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint32_t c = (uint32_t)(quant_code(f[e], sc[b]) & 0xff);
+                    if (e < 4) lo |= c << (8 * e);
+                    else hi |= c << (8 * (e - 4));
+                }
+            }
+            *reinterpret_cast<uint2*>(act + (size_t)b * K + 8 * j) = make_uint2(lo, hi);
+            if (tap && b < M) *reinterpret_cast<uint2*>(p.tap_q + (size_t)b * K + 8 * j) = make_uint2(lo, hi);
+        }
+    }
+    __syncthreads();
+}
+
+// Dequantise in float32, add the residual or apply SwiGLU, narrow to BF16.
+// accs layout: [seg][rows_max][KS][BT].
+// With `pre` (one element per thread), element i's weight scales and residual
+// were loaded early into pre[0][i] (gate / row scale), pre[1][i] (up scale)
+// and pre[2][i] (residual as float).
+template <int BT, int EPI, int KS>
+__device__ __forceinline__ void epilogue(const GemvParams& p, const int32_t* accs, const float* xs,
+                                         int o0, int nrows, int rows_max, const float* pre,
+                                         bool use_pre) {
+    const int N = p.N, M = p.M;
+    const int total = nrows * M;
+    const int nt = blockDim.x;
+    for (int i = threadIdx.x; i < total; i += nt) {
+        const int b = i / nrows, r = i - b * nrows, o = o0 + r;
+        if (EPI == EPI_STORE) {
+            const float wsc = use_pre ? pre[i] : p.w_scale[o];
+            float sum = 0.0f;
+            long long full = 0;
+#pragma unroll
+            for (int s = 0; s < KS; ++s) {
+                const int a = accs[(r * KS + s) * BT + b];
+                const float pj = __fmul_rn(__fmul_rn(__int2float_rn(a), xs[b]), wsc);
+                sum = (s == 0) ? pj : __fadd_rn(sum, pj);
+                full += a;
+            }
+            if (p.residual)
+                sum = __fadd_rn(sum, use_pre ? pre[2 * nt + i]
+                                             : bf2f(ld_cg_bf16(p.residual + (size_t)b * p.ldy + o)));
+            p.y[(size_t)b * p.ldy + o] = f2bf(sum);
+            if (p.acc_out) p.acc_out[(size_t)b * N + o] = (int32_t)full;
+        } else {
+            const int ag = accs[(0 * rows_max + r) * BT + b];
+            const int au = accs[(1 * rows_max + r) * BT + b];
+            const float g = __fmul_rn(__fmul_rn(__int2float_rn(ag), xs[b]),
+                                      use_pre ? pre[i] : p.w_scale[o]);
+            const float u = __fmul_rn(__fmul_rn(__int2float_rn(au), xs[b]),
+                                      use_pre ? pre[nt + i] : p.w_scale[N + o]);
+            // silu(g) = g * sigmoid(g), with exp taken of -|g| so that it never overflows
+            const float e = expf(-fabsf(g));
+            const float sig = g >= 0.0f ? __fdiv_rn(1.0f, __fadd_rn(1.0f, e))
+                                        : __fdiv_rn(e, __fadd_rn(1.0f, e));
+            const float si = __fmul_rn(g, sig);
+            p.y[(size_t)b * p.ldy + o] = f2bf(__fmul_rn(si, u));
+            if (p.acc_out) {
+                p.acc_out[(size_t)b * 2 * N + o] = ag;
+                p.acc_out[(size_t)b * 2 * N + N + o] = au;
+            }
+        }
+    }
+}
+
+// Shared-memory layout common to both kernels. `stage` (BF16 copy of the
+// activation rows) is present when it fits in kStageBudget (stage == 0: none).
+constexpr size_t kStageBudget = 48 * 1024;
+struct SmemLayout {
+    size_t act, accs, xs, red, pre, stage, total;
+};
+__host__ __device__ __forceinline__ SmemLayout smem_layout(int BT, int nseg, int KS, int K, int N,
+                                                           int G, int nthreads) {
+    const int rows_max = (N + G - 1) / G;
+    SmemLayout s;
+    s.act = 0;
+    s.accs = align16((size_t)BT * K);
+    s.xs = s.accs + align16((size_t)nseg * rows_max * KS * BT * 4);
+    s.red = s.xs + align16((size_t)BT * 4);
+    s.pre = align16(s.red + (size_t)kMaxWarps * BT * 4);
+    s.total = s.pre + (size_t)3 * nthreads * 4;
+    s.stage = 0;
+    if ((size_t)BT * K * 2 <= kStageBudget) {
+        s.stage = s.total;
+        s.total += (size_t)BT * K * 2;
+    }
+    return s;
+}
+
+
+// One CTA's share of a projection, streamed by NT threads, UNR units per
+// batch. The first batch of weight loads and an L2 warm-up of the next
+// `l2_ahead` units per warp are issued before `wait()` (griddepcontrol.wait in
+// the standalone kernels, a grid barrier in the persistent step); `wait`
+// returns false to abandon the projection. All state lives in locals: the
+// whole function is inlined into the kernel.
+template <int BT, int PRO, int EPI, int KS, int NT, int UNR, class Wait>
+__device__ __forceinline__ bool stream_gemv(const GemvParams& p, unsigned char* smem, int l2_ahead,
+                                            Wait&& wait) {
+    constexpr int NSEG = (EPI == EPI_SWIGLU) ? 2 : 1;
+    constexpr int NW = NT / 32;
+    const int K = p.K, N = p.N;
+    const int G = gridDim.x;
+    const int o0 = (int)(((long long)N * blockIdx.x) / G);
+    const int o1 = (int)(((long long)N * (blockIdx.x + 1)) / G);
+    const int nrows = o1 - o0;
+    const int rows_max = (N + G - 1) / G;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int upr = K / kUnit;            // units per row
+    const int upp = upr / KS;             // units per piece (row split)
+    const int useg = nrows * upr;         // units per segment
+    const int U = NSEG * useg;
+    const int u0 = (int)(((long long)U * warp) / NW);
+    const int u1 = (int)(((long long)U * (warp + 1)) / NW);
+    const int n = u1 - u0;
+
+    // load stream: contiguous bytes inside a segment
+    int lseg = 0, lleft = 0;
+    const int8_t* lp = p.W;
+    if (n > 0) {
+        lseg = u0 / useg;
+        const int off = u0 - lseg * useg;
+        lleft = useg - off;
+        lp = p.W + ((size_t)(lseg * N + o0) * K + (size_t)off * kUnit + lane * 16);
+    }
+    auto load_batch = [&](int4 (&dst)[UNR], int count) {
+#pragma unroll
+        for (int i = 0; i < UNR; ++i) {
+            if (i < count) {
+                dst[i] = ld_stream_v4(lp);
+                lp += kUnit;
+                if (--lleft == 0) {
+                    ++lseg;
+                    lleft = useg;
+                    lp = p.W + ((size_t)(lseg * N + o0) * K + lane * 16);
+                }
+            }
+        }
+    };
+
+    int4 wa[UNR], wb[UNR];
+    load_batch(wa, n < UNR ? n : UNR);
+    {
+        // L2 warm-up of units [UNR, UNR + l2_ahead): 4 lanes per unit, one
+        // 128-byte line each; holds no registers across the wait
+        const int m = n < UNR + l2_ahead ? n : UNR + l2_ahead;
+        for (int base = UNR; base < m; base += 8) {
+            const int u = base + (lane >> 2);
+            if (u < m) {
+                const int gu = u0 + u;
+                const int seg = gu / useg, off = gu - seg * useg;
+                prefetch_line_l2(p.W + ((size_t)(seg * N + o0) * K + (size_t)off * kUnit +
+                                        (lane & 3) * 128));
+            }
+        }
+    }
+    // The other operands that no kernel writes: the RMSNorm weight (prologue)
+    // and this CTA's weight scales (epilogue), one epilogue element per thread.
+    constexpr int NP = norm_pre_slots(NT);
+    int4 nwr[NP];
+    const int vec = K / 8;
+    const bool nw_pre = PRO == PRO_NORM_QUANT && vec <= NP * NT;
+    if (PRO == PRO_NORM_QUANT && nw_pre) {
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+            const int j = threadIdx.x + i * NT;
+            nwr[i] = j < vec ? ld_nc_v4(p.norm_w + 8 * j) : make_int4(0, 0, 0, 0);
+        }
+    }
+    const int etotal = nrows * p.M;
+    const bool ep_pre = etotal <= NT;
+    const bool mine = ep_pre && (int)threadIdx.x < etotal;
+    float wsg = 0.0f, wsu = 0.0f;
+    if (mine) {
+        const int r = (int)threadIdx.x % nrows;
+        wsg = __ldg(p.w_scale + o0 + r);
+        if (EPI == EPI_SWIGLU) wsu = __ldg(p.w_scale + N + o0 + r);
+    }
+
+    if (!wait()) return false;
+
+    // the residual (written by an earlier kernel) is read right after the wait
+    float resv = 0.0f;
+    if (EPI == EPI_STORE && mine && p.residual) {
+        const int b = (int)threadIdx.x / nrows, r = (int)threadIdx.x - b * nrows;
+        resv = bf2f(ld_cg_bf16(p.residual + (size_t)b * p.ldy + o0 + r));
+    }
+    const SmemLayout L = smem_layout(BT, NSEG, KS, K, N, G, NT);
+    int8_t* act = reinterpret_cast<int8_t*>(smem + L.act);
+    int32_t* accs = reinterpret_cast<int32_t*>(smem + L.accs);
+    float* xs = reinterpret_cast<float*>(smem + L.xs);
+    float* red = reinterpret_cast<float*>(smem + L.red);
+    float* pre = reinterpret_cast<float*>(smem + L.pre);
+    const int acc_n = NSEG * rows_max * KS * BT;
+    for (int i = threadIdx.x; i < acc_n; i += blockDim.x) accs[i] = 0;
+    prologue<BT, PRO, NP>(p, act, xs, red,
+                          L.stage ? reinterpret_cast<bf16*>(smem + L.stage) : nullptr, nwr, nw_pre);
+    if (mine) {   // read by the epilogue, after the barrier that ends the stream
+        pre[threadIdx.x] = wsg;
+        pre[NT + threadIdx.x] = wsu;
+        pre[2 * NT + threadIdx.x] = resv;
+    }
+
+    // compute stream: piece = (segment, row, split)
+    int cpiece = 0, pleft = 0, rleft = 0, aoff = 0;
+    if (n > 0) {
+        cpiece = u0 / upp;
+        pleft = upp - (u0 - cpiece * upp);
+        const int ju = u0 % upr;                    // unit inside the row
+        rleft = upr - ju;
+        aoff = ju * kUnit + lane * 16;
+    }
+    int acc0[BT], acc1[BT];
+#pragma unroll
+    for (int b = 0; b < BT; ++b) acc0[b] = acc1[b] = 0;
+
+    auto flush = [&]() {
+        // piece index -> (segment, row, split) -> shared accumulator slot
+        const int split = cpiece % KS;
+        const int rowg = cpiece / KS;               // segment * nrows + row
+        const int seg = rowg / nrows;
+        const int r = rowg - seg * nrows;
+        int32_t* dst = accs + ((seg * rows_max + r) * KS + split) * BT;
+#pragma unroll
+        for (int b = 0; b < BT; ++b) {
+            const int v = warp_sum_i(acc0[b] + acc1[b]);
+            if (lane == 0) atomicAdd(&dst[b], v);
+            acc0[b] = acc1[b] = 0;
+        }
+    };
+    auto compute_batch = [&](const int4 (&w)[UNR], int count) {
+#pragma unroll
+        for (int i = 0; i < UNR; ++i) {
+            if (i < count) {
+#pragma unroll
+                for (int b = 0; b < BT; ++b) {
+                    const int4 a = *reinterpret_cast<const int4*>(act + (size_t)b * K + aoff);
+                    acc0[b] = __dp4a(w[i].x, a.x, acc0[b]);
+                    acc1[b] = __dp4a(w[i].y, a.y, acc1[b]);
+                    acc0[b] = __dp4a(w[i].z, a.z, acc0[b]);
+                    acc1[b] = __dp4a(w[i].w, a.w, acc1[b]);
+                }
+                aoff += kUnit;
+                if (--rleft == 0) {
+                    rleft = upr;
+                    aoff = lane * 16;
+                }
+                if (--pleft == 0) {
+                    flush();
+                    ++cpiece;
+                    pleft = upp;
+                }
+            }
+        }
+    };
+
+    // the next batch is always issued before the current one is multiplied
+    int done = 0;
+    while (done < n) {
+        const int ca = n - done < UNR ? n - done : UNR;
+        const int rest = n - done - ca;
+        const int cb = rest < UNR ? rest : UNR;
+        load_batch(wb, cb);
+        compute_batch(wa, ca);
+        done += ca;
+        if (done >= n) break;
+        const int rest2 = n - done - cb;
+        const int ca2 = rest2 < UNR ? rest2 : UNR;
+        load_batch(wa, ca2);
+        compute_batch(wb, cb);
+        done += cb;
+    }
+    if (n > 0 && pleft != upp) flush();
+    __syncthreads();
+    epilogue<BT, EPI, KS>(p, accs, xs, o0, nrows, rows_max, pre, ep_pre);
+    return true;
+}
+
+}  // namespace gemv
+}  // namespace a8w8

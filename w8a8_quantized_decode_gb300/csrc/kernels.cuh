@@ -127,4 +127,57 @@ cudaError_t launch_advance(int32_t* token_ids, int32_t* slot_mapping, const int3
                            int page, const Launch& L);
 cudaError_t launch_lmhead_argmax(const LmHeadParams& p, const Launch& L);
 
+// ---------------------------------------------------------------------------
+// Persistent decode step (one cooperative launch per step, batch <= 4)
+// ---------------------------------------------------------------------------
+constexpr int kMaxStepLayers = 64;
+
+struct StepLayer {
+    const bf16* input_norm_w;
+    const int8_t* w_qkv;
+    const float* s_qkv;
+    const bf16* q_norm_w;
+    const bf16* k_norm_w;
+    const int8_t* w_o;
+    const float* s_o;
+    const bf16* post_norm_w;
+    const int8_t* w_gate_up;
+    const float* s_gate_up;
+    const int8_t* w_down;
+    const float* s_down;
+};
+
+struct StepParams {
+    int B, H, Hq, Hkv, D, I, vocab, page, max_blocks, num_blocks, max_pos, L, down_splits;
+    int device_loop;
+    float eps;
+    const bf16* embed;
+    const bf16* final_norm_w;
+    const bf16* lm_head;
+    const float* rope;
+    int32_t* token_ids;
+    int32_t* slot_mapping;
+    int32_t* block_table;
+    int32_t* ctx_lens;
+    int32_t* next_tokens;
+    float* logits;
+    bf16* final_hidden;
+    bf16* hidden;
+    bf16* qkv;
+    bf16* attn;
+    bf16* act;
+    float* part;
+    unsigned long long* keys;
+    unsigned* ticket;
+    unsigned* bar;          // [0] arrivals, [1] abort flag; zero at launch
+    unsigned* err;
+    StepLayer layers[kMaxStepLayers];
+    bf16* k_cache[kMaxStepLayers];
+    bf16* v_cache[kMaxStepLayers];
+};
+
+// Whether the persistent step kernel can run this shape on the current device.
+bool step_supported(int B, int D, int L, int H, int I, int Hq, int Hkv, int max_ctx, int num_sms);
+cudaError_t launch_step(const StepParams& p, const Launch& L);
+
 }  // namespace a8w8
