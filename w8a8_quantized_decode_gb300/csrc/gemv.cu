@@ -23,12 +23,20 @@ namespace {
 
 using namespace gemv;
 
-constexpr size_t kSmemActBudget = 96 * 1024;
-// Units per warp fetched into L2 before the dependency wait.
-#ifndef A8W8_L2_AHEAD
-#define A8W8_L2_AHEAD 4
-#endif
-constexpr int kL2AheadUnits = A8W8_L2_AHEAD;
+// Shared memory: at most 227 KB per CTA; the INT8 activation tile of a launch
+// (batch tile x K bytes) gets up to 72 KB next to the weight ring.
+constexpr int kMaxDynSmem = 227 * 1024;
+constexpr size_t kSmemActBudget = 72 * 1024;
+// Ring geometry of the streaming kernel: units per batch, batches in the ring
+// (96 KB per CTA: 6 x 16 bytes per thread), batches requested before the
+// dependency wait.
+__host__ __device__ constexpr int ring_unr(int BT) { return BT >= 8 ? 2 : 1; }
+constexpr int kRingNB = 6;
+constexpr int kRingPre = 2;
+template <int BT>
+constexpr size_t stream_ring_bytes() {
+    return ring_bytes<stream_threads(BT), ring_unr(BT), kRingNB>();
+}
 // General kernel (any K multiple of 16).
 constexpr int kGenThreads = 512;
 constexpr int kGenUnroll = 8;
@@ -39,7 +47,7 @@ constexpr int kGenUnroll = 8;
 template <int BT, int PRO, int EPI, int KS>
 __global__ void __launch_bounds__(stream_threads(BT), 1) gemv_stream_kernel(const GemvParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
-    stream_gemv<BT, PRO, EPI, KS, stream_threads(BT), kStreamUnroll>(p, smem, kL2AheadUnits, [] {
+    stream_gemv<BT, PRO, EPI, KS, stream_threads(BT), ring_unr(BT), kRingNB, kRingPre>(p, smem, [] {
         pdl_wait();
         pdl_trigger();
         return true;
@@ -130,7 +138,7 @@ __global__ void __launch_bounds__(kGenThreads, 1) gemv_kernel(const GemvParams p
     for (int i = threadIdx.x; i < acc_n; i += blockDim.x) accs[i] = 0;
     int4 nwr[1];
     prologue<BT, PRO, 1>(p, act, xs, red, L.stage ? reinterpret_cast<bf16*>(smem + L.stage) : nullptr,
-                         nwr, false);
+                         nwr, false, [] {});
 
     int acc[KS][BT];
 #pragma unroll
@@ -192,20 +200,21 @@ cudaError_t launch_t(const GemvParams& p, const Launch& L) {
     const int G = L.num_sms;
     const int nseg = EPI == EPI_SWIGLU ? 2 : 1;
     const size_t smem =
-        smem_layout(BT, nseg, KS, p.K, p.N, G, stream ? stream_threads(BT) : kGenThreads).total;
+        stream ? smem_layout(BT, nseg, KS, p.K, p.N, G, stream_threads(BT), stream_ring_bytes<BT>()).total
+               : smem_layout(BT, nseg, KS, p.K, p.N, G, kGenThreads).total;
     static int configured_dev = -1;
     int dev = 0;
     cudaGetDevice(&dev);
     if (configured_dev != dev) {
         cudaError_t e = cudaFuncSetAttribute(gemv_kernel<BT, PRO, EPI, KS>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(gemv_stream_kernel<BT, PRO, EPI, KS>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
         if (e != cudaSuccess) return e;
         configured_dev = dev;
     }
-    if (smem > 200 * 1024) return cudaErrorInvalidValue;
+    if (smem > (size_t)kMaxDynSmem) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(G);
     cfg.blockDim = dim3(stream ? stream_threads(BT) : kGenThreads);

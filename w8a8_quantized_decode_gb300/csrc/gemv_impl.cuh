@@ -18,15 +18,15 @@
 //     weight rows are contiguous, so they form one byte stream (two for
 //     Gate/Up) cut into 512-byte units, one 16-byte load per lane. Every warp
 //     streams an equal contiguous run of units: the load pointer advances by
-//     512 bytes per unit, with L1-bypassing 128-bit loads, double-buffered
-//     (the next batch is in flight while the current one is multiplied).
+//     512 bytes per unit, each lane copying its 16 bytes into a private
+//     shared-memory ring with cp.async, several batches ahead of the one
+//     being multiplied.
 //   * Row (and split) boundaries inside a run flush the warp's INT32 partial
 //     sums into shared memory with an atomic add, which is exact, so how the
 //     rows are split across warps does not change the result.
-//   * The first batch of weight loads (and an L2 warm-up of the next units)
-//     is issued before waiting on the producer of the activations
-//     (griddepcontrol.wait or a grid barrier), since weights never depend on
-//     it.
+//   * The first weight batches are requested before waiting on the producer
+//     of the activations (griddepcontrol.wait or a grid barrier), since
+//     weights never depend on it.
 //   * A prologue then quantises the activation rows (redundantly in every
 //     CTA, from L2, staged once in shared memory when they fit): optional
 //     RMSNorm (float32, rounded to BF16), absmax, INT8 codes into shared
@@ -42,10 +42,9 @@ namespace gemv {
 constexpr int kUnit = 512;                // bytes per warp-wide load
 constexpr int kMaxWarps = 32;
 
-// Streaming kernel: 4 units per batch, two batches in flight; 32 warps for
-// batch tiles up to 4 rows (64 registers), 16 warps for 8-row tiles.
+// Streaming kernel: 32 warps for batch tiles up to 4 rows (64 registers),
+// 16 warps for 8-row tiles.
 __host__ __device__ constexpr int stream_threads(int BT) { return BT >= 8 ? 512 : 1024; }
-constexpr int kStreamUnroll = 4;
 
 __host__ __device__ __forceinline__ size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
@@ -95,12 +94,16 @@ __host__ __device__ constexpr int norm_pre_slots(int NT) { return NT >= 1024 ? 1
 // loads before using any); when `stage` is given they are kept in shared
 // memory for the later passes (normalisation, quantisation). With `nw_pre`
 // the RMSNorm weight is taken from `nwr` (loaded before the wait).
-template <int BT, int PRO, int NP>
+// `issued()` is called once, right after the first activation loads have been
+// issued (the caller can queue more weight loads behind them).
+template <int BT, int PRO, int NP, class Hook>
 __device__ __forceinline__ void prologue(const GemvParams& p, int8_t* act, float* xs, float* red,
-                                         bf16* stage, const int4 (&nwr)[NP], bool nw_pre) {
+                                         bf16* stage, const int4 (&nwr)[NP], bool nw_pre,
+                                         Hook&& issued) {
     const int K = p.K, M = p.M;
     const int nt = blockDim.x;
     if (PRO == PRO_I8) {
+        issued();
         const int vec = K / 16;
         for (int i = threadIdx.x; i < BT * vec; i += nt) {
             const int b = i / vec, j = i - b * vec;
@@ -118,6 +121,7 @@ __device__ __forceinline__ void prologue(const GemvParams& p, int8_t* act, float
     float st[BT];
 #pragma unroll
     for (int b = 0; b < BT; ++b) st[b] = 0.0f;
+    bool first = true;
     for (int j0 = threadIdx.x; j0 < vec; j0 += C * nt) {
         int4 raw[C][BT];
 #pragma unroll
@@ -127,6 +131,10 @@ __device__ __forceinline__ void prologue(const GemvParams& p, int8_t* act, float
             for (int b = 0; b < BT; ++b)
                 raw[c][b] = (j < vec && b < M) ? ld_cg_v4(p.x + (size_t)b * p.ldx + 8 * j)
                                                : make_int4(0, 0, 0, 0);
+        }
+        if (first) {
+            issued();
+            first = false;
         }
 #pragma unroll
         for (int c = 0; c < C; ++c) {
@@ -148,6 +156,7 @@ __device__ __forceinline__ void prologue(const GemvParams& p, int8_t* act, float
             }
         }
     }
+    if (first) issued();
     float sc[BT];
     float inv[BT];
     if (PRO == PRO_NORM_QUANT) {
@@ -297,10 +306,11 @@ __device__ __forceinline__ void epilogue(const GemvParams& p, const int32_t* acc
 // activation rows) is present when it fits in kStageBudget (stage == 0: none).
 constexpr size_t kStageBudget = 48 * 1024;
 struct SmemLayout {
-    size_t act, accs, xs, red, pre, stage, total;
+    size_t act, accs, xs, red, pre, stage, ring, total;
 };
 __host__ __device__ __forceinline__ SmemLayout smem_layout(int BT, int nseg, int KS, int K, int N,
-                                                           int G, int nthreads) {
+                                                           int G, int nthreads,
+                                                           size_t ring_bytes = 0) {
     const int rows_max = (N + G - 1) / G;
     SmemLayout s;
     s.act = 0;
@@ -314,19 +324,28 @@ __host__ __device__ __forceinline__ SmemLayout smem_layout(int BT, int nseg, int
         s.stage = s.total;
         s.total += (size_t)BT * K * 2;
     }
+    s.ring = (s.total + 127) & ~size_t(127);
+    s.total = s.ring + ring_bytes;
     return s;
 }
 
 
-// One CTA's share of a projection, streamed by NT threads, UNR units per
-// batch. The first batch of weight loads and an L2 warm-up of the next
-// `l2_ahead` units per warp are issued before `wait()` (griddepcontrol.wait in
-// the standalone kernels, a grid barrier in the persistent step); `wait`
-// returns false to abandon the projection. All state lives in locals: the
-// whole function is inlined into the kernel.
-template <int BT, int PRO, int EPI, int KS, int NT, int UNR, class Wait>
-__device__ __forceinline__ bool stream_gemv(const GemvParams& p, unsigned char* smem, int l2_ahead,
-                                            Wait&& wait) {
+// One CTA's share of a projection, streamed by NT threads. The weight units
+// travel HBM -> shared memory with cp.async (no registers held while in
+// flight), into a ring of NB batches of UNR units that is private to each
+// lane: lane t of the CTA copies, and later reads back, only its own 16-byte
+// slots, so the only synchronisation is the thread's own cp.async.wait_group.
+// NBPRE batches are requested before `wait()` (griddepcontrol.wait in the
+// standalone kernels, a grid barrier in the persistent step; false abandons
+// the projection), the rest right behind the prologue's activation loads, so
+// HBM stays busy through the dependency wait and the prologue; afterwards
+// NB - 1 batches are always in flight while one is multiplied. All state
+// lives in locals: the whole function is inlined into the kernel.
+template <int NT, int UNR, int NB>
+__host__ __device__ constexpr size_t ring_bytes() { return (size_t)NB * UNR * NT * 16; }
+
+template <int BT, int PRO, int EPI, int KS, int NT, int UNR, int NB, int NBPRE, class Wait>
+__device__ __forceinline__ bool stream_gemv(const GemvParams& p, unsigned char* smem, Wait&& wait) {
     constexpr int NSEG = (EPI == EPI_SWIGLU) ? 2 : 1;
     constexpr int NW = NT / 32;
     const int K = p.K, N = p.N;
@@ -345,6 +364,9 @@ __device__ __forceinline__ bool stream_gemv(const GemvParams& p, unsigned char* 
     const int u1 = (int)(((long long)U * (warp + 1)) / NW);
     const int n = u1 - u0;
 
+    const SmemLayout L = smem_layout(BT, NSEG, KS, K, N, G, NT, ring_bytes<NT, UNR, NB>());
+    const uint32_t ring = (uint32_t)__cvta_generic_to_shared(smem + L.ring) + threadIdx.x * 16u;
+
     // load stream: contiguous bytes inside a segment
     int lseg = 0, lleft = 0;
     const int8_t* lp = p.W;
@@ -354,11 +376,14 @@ __device__ __forceinline__ bool stream_gemv(const GemvParams& p, unsigned char* 
         lleft = useg - off;
         lp = p.W + ((size_t)(lseg * N + o0) * K + (size_t)off * kUnit + lane * 16);
     }
-    auto load_batch = [&](int4 (&dst)[UNR], int count) {
+    int issued = 0;   // units requested so far
+    // one copy group per batch (empty when the stream is exhausted)
+    auto issue_batch = [&](int slot) {
 #pragma unroll
         for (int i = 0; i < UNR; ++i) {
-            if (i < count) {
-                dst[i] = ld_stream_v4(lp);
+            if (issued < n) {
+                cp_async16_s(ring + (uint32_t)((slot * UNR + i) * NT * 16), lp);
+                ++issued;
                 lp += kUnit;
                 if (--lleft == 0) {
                     ++lseg;
@@ -367,26 +392,12 @@ __device__ __forceinline__ bool stream_gemv(const GemvParams& p, unsigned char* 
                 }
             }
         }
+        cp_async_commit();
     };
 
-    int4 wa[UNR], wb[UNR];
-    load_batch(wa, n < UNR ? n : UNR);
-    {
-        // L2 warm-up of units [UNR, UNR + l2_ahead): 4 lanes per unit, one
-        // 128-byte line each; holds no registers across the wait
-        const int m = n < UNR + l2_ahead ? n : UNR + l2_ahead;
-        for (int base = UNR; base < m; base += 8) {
-            const int u = base + (lane >> 2);
-            if (u < m) {
-                const int gu = u0 + u;
-                const int seg = gu / useg, off = gu - seg * useg;
-                prefetch_line_l2(p.W + ((size_t)(seg * N + o0) * K + (size_t)off * kUnit +
-                                        (lane & 3) * 128));
-            }
-        }
-    }
-    // The other operands that no kernel writes: the RMSNorm weight (prologue)
-    // and this CTA's weight scales (epilogue), one epilogue element per thread.
+    // First the small operands that no kernel writes: the RMSNorm weight
+    // (prologue) and this CTA's weight scales (epilogue), one epilogue element
+    // per thread, so that they are not queued behind the weight stream.
     constexpr int NP = norm_pre_slots(NT);
     int4 nwr[NP];
     const int vec = K / 8;
@@ -408,7 +419,15 @@ __device__ __forceinline__ bool stream_gemv(const GemvParams& p, unsigned char* 
         if (EPI == EPI_SWIGLU) wsu = __ldg(p.w_scale + N + o0 + r);
     }
 
-    if (!wait()) return false;
+    // then the first NBPRE batches of the ring; the others are queued behind
+    // the activation loads of the prologue
+#pragma unroll
+    for (int b = 0; b < NBPRE; ++b) issue_batch(b);
+
+    if (!wait()) {
+        cp_async_wait_all();
+        return false;
+    }
 
     // the residual (written by an earlier kernel) is read right after the wait
     float resv = 0.0f;
@@ -416,7 +435,6 @@ __device__ __forceinline__ bool stream_gemv(const GemvParams& p, unsigned char* 
         const int b = (int)threadIdx.x / nrows, r = (int)threadIdx.x - b * nrows;
         resv = bf2f(ld_cg_bf16(p.residual + (size_t)b * p.ldy + o0 + r));
     }
-    const SmemLayout L = smem_layout(BT, NSEG, KS, K, N, G, NT);
     int8_t* act = reinterpret_cast<int8_t*>(smem + L.act);
     int32_t* accs = reinterpret_cast<int32_t*>(smem + L.accs);
     float* xs = reinterpret_cast<float*>(smem + L.xs);
@@ -425,7 +443,11 @@ __device__ __forceinline__ bool stream_gemv(const GemvParams& p, unsigned char* 
     const int acc_n = NSEG * rows_max * KS * BT;
     for (int i = threadIdx.x; i < acc_n; i += blockDim.x) accs[i] = 0;
     prologue<BT, PRO, NP>(p, act, xs, red,
-                          L.stage ? reinterpret_cast<bf16*>(smem + L.stage) : nullptr, nwr, nw_pre);
+                          L.stage ? reinterpret_cast<bf16*>(smem + L.stage) : nullptr, nwr, nw_pre,
+                          [&] {
+#pragma unroll
+                              for (int b = NBPRE; b < NB; ++b) issue_batch(b);
+                          });
     if (mine) {   // read by the epilogue, after the barrier that ends the stream
         pre[threadIdx.x] = wsg;
         pre[NT + threadIdx.x] = wsu;
@@ -459,10 +481,16 @@ __device__ __forceinline__ bool stream_gemv(const GemvParams& p, unsigned char* 
             acc0[b] = acc1[b] = 0;
         }
     };
-    auto compute_batch = [&](const int4 (&w)[UNR], int count) {
+
+    int slot = 0;
+    for (int done = 0; done < n; done += UNR) {
+        cp_async_wait_group<NB - 1>();          // this thread's oldest batch has landed
+        int4 w[UNR];
+#pragma unroll
+        for (int i = 0; i < UNR; ++i) w[i] = lds_v4(ring + (uint32_t)((slot * UNR + i) * NT * 16));
 #pragma unroll
         for (int i = 0; i < UNR; ++i) {
-            if (i < count) {
+            if (done + i < n) {
 #pragma unroll
                 for (int b = 0; b < BT; ++b) {
                     const int4 a = *reinterpret_cast<const int4*>(act + (size_t)b * K + aoff);
@@ -483,24 +511,10 @@ __device__ __forceinline__ bool stream_gemv(const GemvParams& p, unsigned char* 
                 }
             }
         }
-    };
-
-    // the next batch is always issued before the current one is multiplied
-    int done = 0;
-    while (done < n) {
-        const int ca = n - done < UNR ? n - done : UNR;
-        const int rest = n - done - ca;
-        const int cb = rest < UNR ? rest : UNR;
-        load_batch(wb, cb);
-        compute_batch(wa, ca);
-        done += ca;
-        if (done >= n) break;
-        const int rest2 = n - done - cb;
-        const int ca2 = rest2 < UNR ? rest2 : UNR;
-        load_batch(wa, ca2);
-        compute_batch(wb, cb);
-        done += cb;
+        issue_batch(slot);                       // refill the slot just consumed
+        slot = slot + 1 == NB ? 0 : slot + 1;
     }
+    cp_async_wait_all();
     if (n > 0 && pleft != upp) flush();
     __syncthreads();
     epilogue<BT, EPI, KS>(p, accs, xs, o0, nrows, rows_max, pre, ep_pre);

@@ -80,15 +80,21 @@ __device__ __forceinline__ void gemv_params(const StepParams& P, GemvParams& g) 
     g.err = P.err;
 }
 
-constexpr int kL2PrefetchUnits = 16;   // per warp: 8 KB, 128 KB per SM
+constexpr int kL2PrefetchUnits = 16;   // LM head: per warp 8 KB, 128 KB per SM
+// Weight ring of the projection phases: 2 units per batch, 6 batches (96 KB),
+// 2 requested before the barrier.
+constexpr int kStepRingUnr = 2;
+constexpr int kStepRingNB = 6;
+constexpr int kStepRingPre = 2;
+constexpr size_t kStepRingBytes = gemv::ring_bytes<kStepThreads, kStepRingUnr, kStepRingNB>();
 
 // One projection phase: issue the first weight loads of this CTA's share,
 // wait for the producer of the activations (grid barrier), then stream.
 template <int BT, int PRO, int EPI, int KS>
 __device__ __forceinline__ bool gemv_phase(const GemvParams& g, unsigned char* smem, unsigned* bar,
                                            unsigned* k, unsigned* err, int* s_ok) {
-    return gemv::stream_gemv<BT, PRO, EPI, KS, kStepThreads, kStepUnroll>(
-        g, smem, kL2PrefetchUnits, [&] { return grid_sync(bar, k, err, s_ok); });
+    return gemv::stream_gemv<BT, PRO, EPI, KS, kStepThreads, kStepRingUnr, kStepRingNB, kStepRingPre>(
+        g, smem, [&] { return grid_sync(bar, k, err, s_ok); });
 }
 
 template <int D>
@@ -278,10 +284,11 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
 
 size_t step_smem_bytes(int BT, int D, int G, int H, int I, int Hq, int Hkv, int max_ctx, int ksd) {
     const int NQ = Hq * D, NQKV = NQ + 2 * Hkv * D;
-    size_t m = gemv::smem_layout(BT, 1, 1, H, NQKV, G, kStepThreads).total;
-    m = std::max(m, gemv::smem_layout(BT, 1, 1, NQ, H, G, kStepThreads).total);
-    m = std::max(m, gemv::smem_layout(BT, 2, 1, H, I, G, kStepThreads).total);
-    m = std::max(m, gemv::smem_layout(BT, 1, ksd, I, H, G, kStepThreads).total);
+    const size_t r = kStepRingBytes;
+    size_t m = gemv::smem_layout(BT, 1, 1, H, NQKV, G, kStepThreads, r).total;
+    m = std::max(m, gemv::smem_layout(BT, 1, 1, NQ, H, G, kStepThreads, r).total);
+    m = std::max(m, gemv::smem_layout(BT, 2, 1, H, I, G, kStepThreads, r).total);
+    m = std::max(m, gemv::smem_layout(BT, 1, ksd, I, H, G, kStepThreads, r).total);
     m = std::max(m, attn_item_smem_bytes(max_ctx <= 256 ? 256 : 128, D));
     m = std::max(m, lm::smem_bytes(BT, H, kStepThreads));
     return m;
@@ -326,7 +333,7 @@ bool step_supported(int B, int D, int L, int H, int I, int Hq, int Hkv, int max_
     // every projection must take the streaming path (K a multiple of 512 per split)
     if (H % 512 || NQ % 512 || I % 1024) return false;
     const int BT = B <= 1 ? 1 : B <= 2 ? 2 : 4;
-    return step_smem_bytes(BT, D, num_sms, H, I, Hq, Hkv, max_ctx, 2) <= 200 * 1024;
+    return step_smem_bytes(BT, D, num_sms, H, I, Hq, Hkv, max_ctx, 2) <= 227 * 1024;
 }
 
 cudaError_t launch_step(const StepParams& p, const Launch& L) {
