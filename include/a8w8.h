@@ -245,11 +245,14 @@ a8w8_status paged_decode_attention_bf16_noalloc(const a8w8_bf16* q, const a8w8_b
                                                 int num_blocks, float softmax_scale,
                                                 a8w8_bf16* out, void* stream);
 
-/* Fills the RoPE table used by the layer: rope[p][i] = cos(p * theta^(-2i/D))
- * and rope[p][D/2 + i] = sin(p * theta^(-2i/D)) for i < D/2, p < max_pos,
- * computed in double and rounded to float ([SRV-52] "Current behavior": Q/K
+/* Fills the RoPE table used by the layer ([SRV-52] "Current behavior": Q/K
  * RoPE of the fused QK-norm path; reading: Qwen3 rotate-half, theta from the
- * model). rope: device [max_pos, D] float. */
+ * model). With c = cos(p * theta^(-2i/D)) and s = sin(p * theta^(-2i/D))
+ * computed in double for i < D/2, p < max_pos, each split into float
+ * hi + lo parts (hi = float(x), lo = float(x - hi)):
+ *   rope[p][i] = c_hi, rope[p][D/2 + i] = s_hi,
+ *   rope[p][D + i] = c_lo, rope[p][3D/2 + i] = s_lo.
+ * rope: device [max_pos, 2 * D] float. */
 a8w8_status a8w8_rope_table(float* rope, int max_pos, int D, double theta, void* stream);
 
 /* Bytes of workspace a8w8_decode_layer / a8w8_decode_step need for batches of

@@ -244,5 +244,13 @@ def test_rope_table(a8w8):
         pos = np.arange(4200, dtype=np.float64)[:, None]
         inv = 1e6 ** (-2.0 * np.arange(D // 2) / D)
         ang = pos * inv[None, :]
+        c = t[:, : D // 2].astype(np.float64) + t[:, D: 3 * D // 2]
+        s = t[:, D // 2: D].astype(np.float64) + t[:, 3 * D // 2:]
         np.testing.assert_allclose(t[:, : D // 2], np.cos(ang), atol=1e-7, rtol=0)
-        np.testing.assert_allclose(t[:, D // 2:], np.sin(ang), atol=1e-7, rtol=0)
+        np.testing.assert_allclose(t[:, D // 2: D], np.sin(ang), atol=1e-7, rtol=0)
+        # hi + lo carries the device's double value to about 2^-48; that value
+        # differs from numpy's by the few-ulp differences of pow/cos/sin at
+        # angles up to ~4200 rad (~4200 * 2^-52 absolute)
+        np.testing.assert_allclose(c, np.cos(ang), atol=1e-12, rtol=0)
+        np.testing.assert_allclose(s, np.sin(ang), atol=1e-12, rtol=0)
+        assert t.shape == (4200, 2 * D)

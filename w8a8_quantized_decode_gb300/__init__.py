@@ -268,7 +268,7 @@ def paged_decode_attention_bf16_noalloc(q, k_cache, v_cache, block_table, ctx_le
 
 def a8w8_rope_table(max_pos, D, theta, device="cuda", stream=None):
     torch = _torch()
-    t = torch.empty((max_pos, D), dtype=torch.float32, device=device)
+    t = torch.empty((max_pos, 2 * D), dtype=torch.float32, device=device)
     _check(lib().a8w8_rope_table(_ptr(t), max_pos, D, float(theta), _stream(stream)))
     return t
 

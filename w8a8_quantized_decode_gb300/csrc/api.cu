@@ -2,6 +2,7 @@
 // orchestration of the decode layer and step, and the replayable step graph.
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -224,7 +225,12 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     a.page = c.page_size;
     a.max_blocks = max_blocks;
     a.num_blocks = num_blocks;
-    a.scale = 1.0f / sqrtf((float)D);
+    {
+        // 1 / sqrt(D) of the layer, as a float pair
+        const double sd = 1.0 / std::sqrt((double)D);
+        a.scale = (float)sd;
+        a.scale_lo = (float)(sd - (double)a.scale);
+    }
     a.out = attn;
     a.part = part;
     a.err = device_error_word();
@@ -628,6 +634,11 @@ static a8w8_status enqueue_step(const a8w8_model* m, const a8w8_config& c, int B
         P.down_splits = c.down_k_splits;
         P.device_loop = device_loop ? 1 : 0;
         P.eps = c.rms_eps;
+        {
+            const double sd = 1.0 / std::sqrt((double)c.head_dim);
+            P.attn_scale = (float)sd;
+            P.attn_scale_lo = (float)(sd - (double)P.attn_scale);
+        }
         P.embed = reinterpret_cast<const bf16*>(m->embed);
         P.final_norm_w = reinterpret_cast<const bf16*>(m->final_norm_w);
         P.lm_head = reinterpret_cast<const bf16*>(m->lm_head);

@@ -119,7 +119,7 @@ int attn_splits(int max_ctx) {
 size_t attn_part_bytes(int B, int Hq, int D, int max_ctx) {
     const int s = attn_splits(max_ctx);
     if (s <= 1) return 0;
-    return (size_t)B * Hq * s * (D + 2) * sizeof(float);
+    return (size_t)B * Hq * s * (2 * D + 4) * sizeof(float);
 }
 
 cudaError_t launch_attention(const AttnParams& p, const Launch& L) {

@@ -37,9 +37,12 @@ constexpr int kAttnThreads = 256;
 constexpr int kAttnWarps = kAttnThreads / 32;
 constexpr int kGMax = 8;
 
+// Shared memory of one item: K and V tiles (BF16), the G query rows (float),
+// scores / probabilities (two-float: hi and lo planes), per-head (m, l) as
+// two-float pairs. The P.V cross-group reduction reuses the K/V tiles.
 __host__ __device__ inline size_t attn_item_smem_bytes(int chunk, int D) {
-    return (size_t)2 * chunk * D * 2 + (size_t)kGMax * D * 4 + (size_t)kGMax * chunk * 4 +
-           (size_t)kGMax * 2 * 4 + 16;
+    return (size_t)2 * chunk * D * 2 + (size_t)kGMax * D * 4 + (size_t)2 * kGMax * chunk * 4 +
+           (size_t)kGMax * 4 * 4 + 16;
 }
 
 __device__ __forceinline__ void attn_sync() {
@@ -57,23 +60,29 @@ __device__ __forceinline__ void norm_rope_head(const bf16* src, const bf16* norm
     float x[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) x[e] = bf2f(ld_cg_bf16(src + lane * E + e));
-    float ss = 0.0f;
+    // per-head RMSNorm, correctly rounded to BF16 (see norm_bf16); the
+    // float64 scalar is evaluated by lane 0 and broadcast
+    f2 ss = {0.0f, 0.0f};
 #pragma unroll
-    for (int e = 0; e < E; ++e) ss += x[e] * x[e];
-    ss = warp_sum(ss);
-    const float inv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, (float)D), eps)));
+    for (int e = 0; e < E; ++e) f2_acc(ss, __fmul_rn(x[e], x[e]));
+    ss = warp_sum_f2(ss);
+    f2 inv = {0.0f, 0.0f};
+    if (lane == 0) inv = rms_inv(ss, D, eps);
+    inv.hi = __shfl_sync(0xffffffffu, inv.hi, 0);
+    inv.lo = __shfl_sync(0xffffffffu, inv.lo, 0);
 #pragma unroll
-    for (int e = 0; e < E; ++e)
-        x[e] = bf2f(f2bf(__fmul_rn(__fmul_rn(x[e], inv), bf2f(norm_w[lane * E + e]))));
+    for (int e = 0; e < E; ++e) x[e] = bf2f(norm_bf16(x[e], bf2f(norm_w[lane * E + e]), inv));
+    // rotate-half RoPE, each output correctly rounded to BF16: x and its
+    // partner are exact floats, cos / sin are hi + lo pairs from the table
 #pragma unroll
     for (int e = 0; e < E; ++e) {
         const float partner = __shfl_xor_sync(0xffffffffu, x[e], 16);
         const int i = (lane * E + e) % (D / 2);
-        const float c = rope_row[i], s = rope_row[D / 2 + i];
-        float r;
-        if (lane < 16) r = __fsub_rn(__fmul_rn(x[e], c), __fmul_rn(partner, s));
-        else r = __fadd_rn(__fmul_rn(x[e], c), __fmul_rn(partner, s));
-        y[e] = bf2f(f2bf(r));
+        const f2 c = {rope_row[i], rope_row[D + i]};
+        const f2 sn = {rope_row[D / 2 + i], rope_row[3 * D / 2 + i]};
+        const f2 a = f2_mulf(c, x[e]);
+        const f2 b2 = f2_mulf(sn, partner);
+        y[e] = bf2f(f2_to_bf16(lane < 16 ? f2_sub(a, b2) : f2_add(a, b2)));
     }
 }
 
@@ -86,10 +95,11 @@ __device__ __forceinline__ void attn_item(const AttnParams& p, int chunk, int sp
     bf16* Ks = reinterpret_cast<bf16*>(smem);
     bf16* Vs = Ks + (size_t)chunk * D;
     float* qs = reinterpret_cast<float*>(Vs + (size_t)chunk * D);
-    float* sc = qs + kGMax * D;
-    float* stat = sc + (size_t)kGMax * chunk;
-    int* s_bad_block = reinterpret_cast<int*>(stat + kGMax * 2);
-    float* red = reinterpret_cast<float*>(smem);   // aliases Ks once the scores are done
+    float* sc = qs + kGMax * D;                    // [G][chunk] hi
+    float* sl = sc + (size_t)kGMax * chunk;        // [G][chunk] lo
+    float* stat = sl + (size_t)kGMax * chunk;      // [G][4]: m hi, m lo, l hi, l lo
+    int* s_bad_block = reinterpret_cast<int*>(stat + kGMax * 4);
+    float* red = reinterpret_cast<float*>(smem);   // aliases the K/V tiles after P.V
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -144,7 +154,7 @@ __device__ __forceinline__ void attn_item(const AttnParams& p, int chunk, int sp
                 const bf16* src = p.q + (size_t)b * p.q_stride + (size_t)h * D;
                 float y[E];
                 if (p.fused) {
-                    norm_rope_head<D>(src, p.q_norm_w, p.rope + (size_t)pos * D, p.eps, lane, y);
+                    norm_rope_head<D>(src, p.q_norm_w, p.rope + (size_t)pos * 2 * D, p.eps, lane, y);
                     if (p.tap_q_rot && split == 0) {
 #pragma unroll
                         for (int e = 0; e < E; ++e)
@@ -161,7 +171,7 @@ __device__ __forceinline__ void attn_item(const AttnParams& p, int chunk, int sp
                 const bf16* ksrc = p.q + (size_t)b * p.q_stride + NQ + (size_t)kvh * D;
                 const bf16* vsrc = p.q + (size_t)b * p.q_stride + NQ + NK + (size_t)kvh * D;
                 float y[E];
-                norm_rope_head<D>(ksrc, p.k_norm_w, p.rope + (size_t)pos * D, p.eps, lane, y);
+                norm_rope_head<D>(ksrc, p.k_norm_w, p.rope + (size_t)pos * 2 * D, p.eps, lane, y);
                 const int tr = pos - t0;
                 const long slot = p.slot_mapping[b];
                 const long num_slots = (long)p.num_blocks * p.page;
@@ -187,10 +197,16 @@ __device__ __forceinline__ void attn_item(const AttnParams& p, int chunk, int sp
     attn_sync();
     if (tid == 0 && *s_bad_block) set_error(p.err, 0x2u);
 
-    // scores: q read from shared memory (keeps the item within 64 registers)
+    // Scores, softmax and P.V in two-float arithmetic (see f2): q and k are
+    // BF16 values, so each product q_d k_d is exact in float32 and the dot
+    // product is summed as a pair; the probabilities and the weighted sum of
+    // V are pairs too, so the BF16 output rounds as an evaluation in float64
+    // would.
+    // scores: LPT lanes per token, 8 columns each, q read from shared memory
     constexpr int LPT = D / 8;
     constexpr int TPW = 32 / LPT;
     const int j = lane % LPT, tw = lane / LPT;
+    const f2 scale = {p.scale, p.scale_lo};
     if (n > 0) {
         const int step = kAttnWarps * TPW;
         const int n_pad = ((n + step - 1) / step) * step;
@@ -205,38 +221,49 @@ __device__ __forceinline__ void attn_item(const AttnParams& p, int chunk, int sp
             for (int g = 0; g < G; ++g) {
                 const float4 qa = *reinterpret_cast<const float4*>(qs + g * D + 8 * j);
                 const float4 qb = *reinterpret_cast<const float4*>(qs + g * D + 8 * j + 4);
-                float d = 0.0f;
-                d = fmaf(qa.x, kf[0], d);
-                d = fmaf(qa.y, kf[1], d);
-                d = fmaf(qa.z, kf[2], d);
-                d = fmaf(qa.w, kf[3], d);
-                d = fmaf(qb.x, kf[4], d);
-                d = fmaf(qb.y, kf[5], d);
-                d = fmaf(qb.z, kf[6], d);
-                d = fmaf(qb.w, kf[7], d);
+                f2 d = f2_make(__fmul_rn(qa.x, kf[0]));
+                f2_acc(d, __fmul_rn(qa.y, kf[1]));
+                f2_acc(d, __fmul_rn(qa.z, kf[2]));
+                f2_acc(d, __fmul_rn(qa.w, kf[3]));
+                f2_acc(d, __fmul_rn(qb.x, kf[4]));
+                f2_acc(d, __fmul_rn(qb.y, kf[5]));
+                f2_acc(d, __fmul_rn(qb.z, kf[6]));
+                f2_acc(d, __fmul_rn(qb.w, kf[7]));
 #pragma unroll
-                for (int o = LPT / 2; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-                if (j == 0 && t < n) sc[g * chunk + t] = d * p.scale;
+                for (int o = LPT / 2; o > 0; o >>= 1) {
+                    f2 r;
+                    r.hi = __shfl_xor_sync(0xffffffffu, d.hi, o);
+                    r.lo = __shfl_xor_sync(0xffffffffu, d.lo, o);
+                    d = f2_add(d, r);
+                }
+                if (j == 0 && t < n) {
+                    const f2 sv = f2_mul(d, scale);
+                    sc[g * chunk + t] = sv.hi;
+                    sl[g * chunk + t] = sv.lo;
+                }
             }
         }
     }
     attn_sync();
 
-    // softmax over the chunk, per head
+    // softmax over the chunk, per head: p_t = exp(s_t - m), l = sum p_t
     for (int g = warp; g < G; g += kAttnWarps) {
-        float m = -INFINITY;
-        for (int t = lane; t < n; t += 32) m = fmaxf(m, sc[g * chunk + t]);
-        m = warp_max(m);
-        float l = 0.0f;
+        f2 m = {-INFINITY, 0.0f};
+        for (int t = lane; t < n; t += 32) m = f2_max(m, f2{sc[g * chunk + t], sl[g * chunk + t]});
+        m = warp_max_f2(m);
+        f2 l = {0.0f, 0.0f};
         for (int t = lane; t < n; t += 32) {
-            const float e = expf(sc[g * chunk + t] - m);
-            sc[g * chunk + t] = e;
-            l += e;
+            const f2 e = f2_exp(f2_sub(f2{sc[g * chunk + t], sl[g * chunk + t]}, m));
+            sc[g * chunk + t] = e.hi;
+            sl[g * chunk + t] = e.lo;
+            l = f2_add(l, e);
         }
-        l = warp_sum(l);
+        l = warp_sum_f2(l);
         if (lane == 0) {
-            stat[2 * g] = m;
-            stat[2 * g + 1] = l;
+            stat[4 * g] = m.hi;
+            stat[4 * g + 1] = m.lo;
+            stat[4 * g + 2] = l.hi;
+            stat[4 * g + 3] = l.lo;
         }
     }
     attn_sync();
@@ -245,69 +272,86 @@ __device__ __forceinline__ void attn_item(const AttnParams& p, int chunk, int sp
     constexpr int CP = D / 2;
     constexpr int NTG = kAttnThreads / CP;
     const int cp = tid % CP, tg = tid / CP;
-    float o[kGMax][2];
+    f2 o[kGMax][2];
 #pragma unroll
-    for (int g = 0; g < kGMax; ++g) o[g][0] = o[g][1] = 0.0f;
+    for (int g = 0; g < kGMax; ++g) o[g][0] = o[g][1] = f2{0.0f, 0.0f};
     for (int t = tg; t < n; t += NTG) {
         const float2 v = __bfloat1622float2(
             *reinterpret_cast<const __nv_bfloat162*>(Vs + (size_t)t * D + 2 * cp));
 #pragma unroll
         for (int g = 0; g < kGMax; ++g) {
             if (g < G) {
-                const float pr = sc[g * chunk + t];
-                o[g][0] = fmaf(pr, v.x, o[g][0]);
-                o[g][1] = fmaf(pr, v.y, o[g][1]);
+                const f2 pr = {sc[g * chunk + t], sl[g * chunk + t]};
+                o[g][0] = f2_add(o[g][0], f2_mulf(pr, v.x));
+                o[g][1] = f2_add(o[g][1], f2_mulf(pr, v.y));
             }
         }
     }
-    // Ks is no longer read: reuse it for the cross-group reduction
+    attn_sync();   // every thread is done with V: the tiles become the reduction buffer
+    // red: [NTG][kGMax][2][D] (hi plane, lo plane)
 #pragma unroll
     for (int g = 0; g < kGMax; ++g) {
         if (g < G) {
-            red[((size_t)tg * kGMax + g) * D + 2 * cp] = o[g][0];
-            red[((size_t)tg * kGMax + g) * D + 2 * cp + 1] = o[g][1];
+            float* r = red + ((size_t)tg * kGMax + g) * 2 * D;
+            r[2 * cp] = o[g][0].hi;
+            r[2 * cp + 1] = o[g][1].hi;
+            r[D + 2 * cp] = o[g][0].lo;
+            r[D + 2 * cp + 1] = o[g][1].lo;
         }
     }
     attn_sync();
     for (int i = tid; i < G * D; i += kAttnThreads) {
         const int g = i / D, d = i - g * D;
-        float acc = 0.0f;
+        f2 acc = {0.0f, 0.0f};
 #pragma unroll
-        for (int q = 0; q < NTG; ++q) acc += red[((size_t)q * kGMax + g) * D + d];
+        for (int q = 0; q < NTG; ++q) {
+            const float* r = red + ((size_t)q * kGMax + g) * 2 * D;
+            acc = f2_add(acc, f2{r[d], r[D + d]});
+        }
         const int h = kvh * G + g;
+        const f2 l = {stat[4 * g + 2], stat[4 * g + 3]};
         if (splits == 1) {
-            const float val = n > 0 ? __fdiv_rn(acc, stat[2 * g + 1]) : 0.0f;
-            p.out[((size_t)b * p.Hq + h) * D + d] = f2bf(val);
+            p.out[((size_t)b * p.Hq + h) * D + d] =
+                n > 0 ? f2_to_bf16(f2_div(acc, l)) : __float2bfloat16_rn(0.0f);
         } else {
-            float* pp = p.part + (((size_t)b * p.Hq + h) * splits + split) * (D + 2);
-            pp[d] = n > 0 ? acc : 0.0f;
+            // partial: o (hi, lo planes), then m and l pairs
+            float* pp = p.part + (((size_t)b * p.Hq + h) * splits + split) * (2 * D + 4);
+            pp[d] = n > 0 ? acc.hi : 0.0f;
+            pp[D + d] = n > 0 ? acc.lo : 0.0f;
             if (d == 0) {
-                pp[D] = n > 0 ? stat[2 * g] : -INFINITY;
-                pp[D + 1] = n > 0 ? stat[2 * g + 1] : 0.0f;
+                pp[2 * D] = n > 0 ? stat[4 * g] : -INFINITY;
+                pp[2 * D + 1] = n > 0 ? stat[4 * g + 1] : 0.0f;
+                pp[2 * D + 2] = n > 0 ? l.hi : 0.0f;
+                pp[2 * D + 3] = n > 0 ? l.lo : 0.0f;
             }
         }
     }
     attn_sync();   // the shared tiles may be reused by the caller afterwards
 }
 
-// Combine of split-KV partials for (request b, query head h, element d).
+// Combine of split-KV partials for (request b, query head h, element d), in
+// two-float arithmetic: O = sum_s o_s e^{m_s - M} / sum_s l_s e^{m_s - M}.
 template <int D>
 __device__ __forceinline__ void attn_combine_elem(const float* part, int splits, int Hq, int b,
                                                   int h, int d, bf16* out) {
-    const float* pp = part + ((size_t)b * Hq + h) * splits * (D + 2);
-    float M = -INFINITY;
-    for (int s = 0; s < splits; ++s) M = fmaxf(M, __ldcg(pp + (size_t)s * (D + 2) + D));
-    float L = 0.0f, acc = 0.0f;
-    if (M != -INFINITY) {
+    constexpr int S = 2 * D + 4;
+    const float* pp = part + ((size_t)b * Hq + h) * splits * S;
+    f2 M = {-INFINITY, 0.0f};
+    for (int s = 0; s < splits; ++s)
+        M = f2_max(M, f2{__ldcg(pp + (size_t)s * S + 2 * D), __ldcg(pp + (size_t)s * S + 2 * D + 1)});
+    f2 L = {0.0f, 0.0f}, acc = {0.0f, 0.0f};
+    if (M.hi != -INFINITY) {
         for (int s = 0; s < splits; ++s) {
-            const float m = __ldcg(pp + (size_t)s * (D + 2) + D);
-            if (m == -INFINITY) continue;
-            const float w = expf(m - M);
-            L = fmaf(__ldcg(pp + (size_t)s * (D + 2) + D + 1), w, L);
-            acc = fmaf(__ldcg(pp + (size_t)s * (D + 2) + d), w, acc);
+            const float* q = pp + (size_t)s * S;
+            const f2 m = {__ldcg(q + 2 * D), __ldcg(q + 2 * D + 1)};
+            if (m.hi == -INFINITY) continue;
+            const f2 w = f2_exp(f2_sub(m, M));
+            L = f2_add(L, f2_mul(f2{__ldcg(q + 2 * D + 2), __ldcg(q + 2 * D + 3)}, w));
+            acc = f2_add(acc, f2_mul(f2{__ldcg(q + d), __ldcg(q + D + d)}, w));
         }
     }
-    out[((size_t)b * Hq + h) * D + d] = f2bf(L > 0.0f ? __fdiv_rn(acc, L) : 0.0f);
+    out[((size_t)b * Hq + h) * D + d] =
+        L.hi > 0.0f ? f2_to_bf16(f2_div(acc, L)) : __float2bfloat16_rn(0.0f);
 }
 
 }  // namespace a8w8

@@ -48,11 +48,6 @@ __device__ __forceinline__ bf16 ld_cg_bf16(const bf16* p) {
     return __ushort_as_bfloat16(u);
 }
 
-// Hint: fetch the 128-byte line holding p into L2 (no register, no wait).
-__device__ __forceinline__ void prefetch_line_l2(const void* p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
-
 // Asynchronous 16-byte global -> shared copy (cp.async, L2 only).
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
     unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem));
@@ -60,9 +55,13 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-// Same copy with a 32-bit shared-space destination address.
-__device__ __forceinline__ void cp_async16_s(uint32_t s, const void* gmem) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+// Same copy with a 32-bit shared-space destination address and an L2 cache
+// policy (weights streamed once: evict-first, so that the small operands
+// read by every step stay resident in L2).
+__device__ __forceinline__ void cp_async16_s(uint32_t s, const void* gmem, uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem),
+                 "l"(policy)
+                 : "memory");
 }
 // Wait until at most N of this thread's most recent copy groups are pending.
 template <int N>
@@ -77,63 +76,11 @@ __device__ __forceinline__ int4 lds_v4(uint32_t s) {
     return r;
 }
 
-// ---------------------------------------------------------------------------
-// mbarrier + bulk asynchronous copy (TMA engine, 1-D). Every wait is bounded:
-// after kWaitLimit polls it gives up and reports failure, so no kernel can
-// hang on a barrier that is never completed.
-// ---------------------------------------------------------------------------
-constexpr unsigned kWaitLimit = 1u << 20;
-
-__device__ __forceinline__ unsigned smem_addr(const void* p) {
-    return static_cast<unsigned>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void fence_barrier_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_addr(bar))
-                 : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, unsigned bytes) {
-    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
-                     smem_addr(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
-    unsigned ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-// Bounded wait for the phase with the given parity; false if it never completed.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity) {
-    for (unsigned i = 0; i < kWaitLimit; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
-}
-// L2 policy for data read once (weights): evict first.
+// L2 policy for data read once per step (weights): evict first.
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
     return pol;
-}
-// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
-// global to shared memory, completing on `bar` as transaction bytes.
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned bytes, uint64_t* bar,
-                                         uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
-            smem_addr(dst)),
-        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
-        : "memory");
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -167,11 +114,173 @@ __device__ __forceinline__ void unpack8(const int4& v, float (&f)[8]) {
 }
 
 // Per-row INT8 code of x with row scale s: clamp(rne(x / s), -127, 127) with
-// an IEEE float32 division; s == 0 gives 0.
-__device__ __forceinline__ int quant_code(float x, float s) {
+// x / s the IEEE float32 quotient; s == 0 gives 0. The quotient is formed
+// without a division instruction, from R = RN(1 / s) (quant_recip, once per
+// row): q0 = RN(x R), then one correction by the exact remainder x - q0 s
+// (an FMA), q = RN(q0 + (x - q0 s) R), which equals RN(x / s) (Markstein's
+// theorem, e.g. Muller et al., Handbook of Floating-Point Arithmetic, 2nd
+// ed., section 4.7). Where R overflows (s below 2^-126) the division is
+// used as is.
+__device__ __forceinline__ float quant_recip(float s) { return s == 0.0f ? 0.0f : __frcp_rn(s); }
+__device__ __forceinline__ int quant_code(float x, float s, float R) {
     if (s == 0.0f) return 0;
-    int q = __float2int_rn(__fdiv_rn(x, s));
-    return max(-127, min(127, q));
+    float q;
+    if (isfinite(R)) {
+        const float q0 = __fmul_rn(x, R);
+        q = __fmaf_rn(__fmaf_rn(-q0, s, x), R, q0);
+    } else {
+        q = __fdiv_rn(x, s);
+    }
+    return max(-127, min(127, __float2int_rn(q)));
+}
+
+// ---------------------------------------------------------------------------
+// Two-float ("double-float") arithmetic. Every floating-point stage whose
+// result is rounded to BF16 (the norms, RoPE, SiLU, attention) is evaluated
+// as an unevaluated pair hi + lo carrying about 44-48 significant bits, so
+// that its BF16 rounding agrees with an evaluation in float64 (and with the
+// exact real value) except when that value lies within ~2^-40 (relative) of
+// a rounding boundary. Building blocks (Dekker 1971; Knuth, TAOCP vol. 2):
+// TwoSum and FastTwoSum give the exact rounding error of a sum, an FMA the
+// exact rounding error of a product.
+// ---------------------------------------------------------------------------
+struct f2 {
+    float hi, lo;
+};
+
+__device__ __forceinline__ f2 f2_make(float a) { return f2{a, 0.0f}; }
+// Knuth's TwoSum: s + e == a + b exactly, s = fl(a + b).
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+// Dekker's FastTwoSum (|a| >= |b| or a == 0): the renormalised pair. A zero
+// b leaves a untouched, so that a signed zero keeps its sign.
+__device__ __forceinline__ f2 fast_two_sum(float a, float b) {
+    f2 r;
+    r.hi = b == 0.0f ? a : __fadd_rn(a, b);
+    r.lo = __fsub_rn(b, __fsub_rn(r.hi, a));
+    return r;
+}
+// a += v (v a float), without renormalisation (a few terms at a time).
+__device__ __forceinline__ void f2_acc(f2& a, float v) {
+    float s, e;
+    two_sum(a.hi, v, s, e);
+    a.hi = s;
+    a.lo = __fadd_rn(a.lo, e);
+}
+__device__ __forceinline__ f2 f2_add(f2 a, f2 b) {
+    float s, e;
+    two_sum(a.hi, b.hi, s, e);
+    e = __fadd_rn(e, __fadd_rn(a.lo, b.lo));
+    return fast_two_sum(s, e);
+}
+__device__ __forceinline__ f2 f2_addf(f2 a, float b) {
+    float s, e;
+    two_sum(a.hi, b, s, e);
+    return fast_two_sum(s, __fadd_rn(e, a.lo));
+}
+__device__ __forceinline__ f2 f2_neg(f2 a) { return f2{-a.hi, -a.lo}; }
+__device__ __forceinline__ f2 f2_sub(f2 a, f2 b) { return f2_add(a, f2_neg(b)); }
+// Exact product of two floats as a pair.
+__device__ __forceinline__ f2 two_prod(float a, float b) {
+    f2 r;
+    r.hi = __fmul_rn(a, b);
+    r.lo = __fmaf_rn(a, b, -r.hi);
+    return r;
+}
+__device__ __forceinline__ f2 f2_mulf(f2 a, float b) {
+    f2 p = two_prod(a.hi, b);
+    return fast_two_sum(p.hi, __fmaf_rn(a.lo, b, p.lo));
+}
+__device__ __forceinline__ f2 f2_mul(f2 a, f2 b) {
+    f2 p = two_prod(a.hi, b.hi);
+    float e = __fmaf_rn(a.hi, b.lo, p.lo);
+    e = __fmaf_rn(a.lo, b.hi, e);
+    return fast_two_sum(p.hi, e);
+}
+// a / b: one correction of the float quotient by the exact remainder.
+__device__ __forceinline__ f2 f2_div(f2 a, f2 b) {
+    const float q1 = __fdiv_rn(a.hi, b.hi);
+    const f2 r = f2_sub(a, f2_mulf(b, q1));
+    const float q2 = __fdiv_rn(r.hi, b.hi);
+    return fast_two_sum(q1, q2);
+}
+// Ordering of pairs (both renormalised).
+__device__ __forceinline__ bool f2_gt(f2 a, f2 b) { return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo); }
+__device__ __forceinline__ f2 f2_max(f2 a, f2 b) { return f2_gt(b, a) ? b : a; }
+__device__ __forceinline__ f2 warp_sum_f2(f2 v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        f2 t;
+        t.hi = __shfl_xor_sync(0xffffffffu, v.hi, o);
+        t.lo = __shfl_xor_sync(0xffffffffu, v.lo, o);
+        v = f2_add(v, t);
+    }
+    return v;
+}
+__device__ __forceinline__ f2 warp_max_f2(f2 v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        f2 t;
+        t.hi = __shfl_xor_sync(0xffffffffu, v.hi, o);
+        t.lo = __shfl_xor_sync(0xffffffffu, v.lo, o);
+        v = f2_max(v, t);
+    }
+    return v;
+}
+// 1 / sqrt(s), s > 0: the float estimate refined by one Newton step
+// y' = y + y (1 - s y^2) / 2 with the residual formed exactly.
+__device__ __forceinline__ f2 f2_rsqrt(f2 s) {
+    const float y = rsqrtf(s.hi);
+    const f2 t = f2_mul(s, two_prod(y, y));
+    const float e = __fsub_rn(__fsub_rn(1.0f, t.hi), t.lo);   // 1 - t.hi is exact
+    return fast_two_sum(y, __fmul_rn(__fmul_rn(y, e), 0.5f));
+}
+// exp(x) for x.hi <= 88 (underflows to 0 below about -103): x = k ln2 + r,
+// exp(r) = (1 + p)^(2^8) with p = expm1(r / 2^8) from its Taylor series to
+// the fourth power, squared eight times in expm1 form (1 + p)^2 = 1 + (2p +
+// p^2); then scaled by 2^k.
+__device__ __forceinline__ f2 f2_exp(f2 x) {
+    if (x.hi < -104.0f) return f2{0.0f, 0.0f};
+    if (x.hi > 88.5f) return f2{INFINITY, 0.0f};
+    const float k = rintf(__fmul_rn(x.hi, 1.44269504088896341f));
+    const f2 ln2 = {0.693147182464599609375f, -1.904654323148236e-09f};   // ln 2 = hi + lo
+    const f2 r = f2_sub(x, f2_mulf(ln2, k));
+    const f2 t = f2{__fmul_rn(r.hi, 0.00390625f), __fmul_rn(r.lo, 0.00390625f)};   // r / 2^8
+    const f2 t2 = f2_mul(t, t);
+    const float t3 = __fmul_rn(t2.hi, t.hi);
+    const float tail = __fmaf_rn(__fmul_rn(t3, t.hi), 1.0f / 24.0f, __fmul_rn(t3, 1.0f / 6.0f));
+    f2 p = f2_addf(f2_add(t, f2{__fmul_rn(t2.hi, 0.5f), __fmul_rn(t2.lo, 0.5f)}), tail);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) p = f2_add(f2{__fmul_rn(p.hi, 2.0f), __fmul_rn(p.lo, 2.0f)}, f2_mul(p, p));
+    const f2 e = f2_addf(p, 1.0f);
+    const int ki = (int)k;
+    return f2{ldexpf(e.hi, ki), ldexpf(e.lo, ki)};
+}
+// BF16 nearest-even rounding of the value hi + lo.
+__device__ __forceinline__ bf16 f2_to_bf16(f2 v) {
+    const f2 n = fast_two_sum(v.hi, v.lo);       // |n.lo| <= ulp(n.hi) / 2
+    const unsigned u = __float_as_uint(n.hi);
+    if ((u & 0xFFFFu) == 0x8000u && n.lo != 0.0f && isfinite(n.hi)) {
+        // n.hi is a midpoint between two BF16 values: n.lo decides
+        const bool away = (n.lo > 0.0f) == (n.hi > 0.0f);
+        return __ushort_as_bfloat16((unsigned short)((u >> 16) + (away ? 1u : 0u)));
+    }
+    return __float2bfloat16_rn(n.hi);
+}
+
+// RMSNorm pieces. Every x*x of a BF16 x is exact in float32, so a row's sum
+// of squares is accumulated exactly enough with f2_acc; the scale
+// 1 / sqrt(ss / n + eps) is formed in two-float arithmetic; and x * w (two
+// 8-bit significands) is exact in float32, so the normalised value
+// x * w * scale needs one two-float product.
+__device__ __forceinline__ f2 rms_inv(f2 ss, int n, float eps) {
+    return f2_rsqrt(f2_addf(f2_div(ss, f2_make((float)n)), eps));
+}
+__device__ __forceinline__ bf16 norm_bf16(float x, float w, f2 inv) {
+    return f2_to_bf16(f2_mulf(inv, __fmul_rn(x, w)));
 }
 
 __device__ __forceinline__ void set_error(unsigned* err, unsigned bit) {

@@ -48,40 +48,47 @@ __host__ __device__ constexpr int stream_threads(int BT) { return BT >= 8 ? 512 
 
 __host__ __device__ __forceinline__ size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
-template <int BT>
-__device__ __forceinline__ void block_sum(float (&v)[BT], float* red) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-#pragma unroll
-    for (int b = 0; b < BT; ++b) {
-        float s = warp_sum(v[b]);
-        if (lane == 0) red[warp * BT + b] = s;
-    }
-    __syncthreads();
-#pragma unroll
-    for (int b = 0; b < BT; ++b) {
-        float s = 0.0f;
-        for (int w = 0; w < nw; ++w) s += red[w * BT + b];
-        v[b] = s;
-    }
-    __syncthreads();
-}
-
+// Block reductions with one barrier each: every warp writes its partials,
+// then every warp reads all of them (one per lane) and reduces them with
+// shuffles, so each thread ends with the block result. Each call site uses
+// its own region of `red`, which therefore needs no second barrier.
 template <int BT>
 __device__ __forceinline__ void block_max(float (&v)[BT], float* red) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
 #pragma unroll
     for (int b = 0; b < BT; ++b) {
-        float s = warp_max(v[b]);
-        if (lane == 0) red[warp * BT + b] = s;
+        const float s = warp_max(v[b]);
+        if (lane == 0) red[b * kMaxWarps + warp] = s;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int b = 0; b < BT; ++b) v[b] = warp_max(lane < nw ? red[b * kMaxWarps + lane] : 0.0f);
+}
+
+// Row sums of squares (float pairs) -> per-row RMSNorm scale 1/sqrt(ss/K+eps)
+// as a float pair (see norm_bf16). red: 2 * kMaxWarps * BT floats.
+template <int BT>
+__device__ __forceinline__ void block_rms_inv(f2 (&ss)[BT], float* red, int K, float eps,
+                                              f2 (&inv)[BT]) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+#pragma unroll
+    for (int b = 0; b < BT; ++b) {
+        const f2 t = warp_sum_f2(ss[b]);
+        if (lane == 0) {
+            red[2 * (b * kMaxWarps + warp)] = t.hi;
+            red[2 * (b * kMaxWarps + warp) + 1] = t.lo;
+        }
     }
     __syncthreads();
 #pragma unroll
     for (int b = 0; b < BT; ++b) {
-        float s = 0.0f;
-        for (int w = 0; w < nw; ++w) s = fmaxf(s, red[w * BT + b]);
-        v[b] = s;
+        f2 t = {0.0f, 0.0f};
+        if (lane < nw) {
+            t.hi = red[2 * (b * kMaxWarps + lane)];
+            t.lo = red[2 * (b * kMaxWarps + lane) + 1];
+        }
+        inv[b] = rms_inv(warp_sum_f2(t), K, eps);
     }
-    __syncthreads();
 }
 
 // Per-thread slots of the normalisation weight held in registers (loaded
@@ -118,9 +125,13 @@ __device__ __forceinline__ void prologue(const GemvParams& p, int8_t* act, float
     const int vec = K / 8;
     // pass 1 (L2): sum of squares (RMSNorm) or absmax (plain quantisation)
     constexpr int C = BT == 1 ? 4 : (BT == 2 ? 2 : 1);   // loads in flight per row
-    float st[BT];
+    float st[BT];    // absmax (plain quantisation)
+    f2 ss[BT];       // sum of squares (RMSNorm)
 #pragma unroll
-    for (int b = 0; b < BT; ++b) st[b] = 0.0f;
+    for (int b = 0; b < BT; ++b) {
+        st[b] = 0.0f;
+        ss[b].hi = ss[b].lo = 0.0f;
+    }
     bool first = true;
     for (int j0 = threadIdx.x; j0 < vec; j0 += C * nt) {
         int4 raw[C][BT];
@@ -148,7 +159,7 @@ __device__ __forceinline__ void prologue(const GemvParams& p, int8_t* act, float
                         unpack8(raw[c][b], f);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
-                            if (PRO == PRO_NORM_QUANT) st[b] += f[e] * f[e];
+                            if (PRO == PRO_NORM_QUANT) f2_acc(ss[b], __fmul_rn(f[e], f[e]));
                             else st[b] = fmaxf(st[b], fabsf(f[e]));
                         }
                     }
@@ -158,12 +169,9 @@ __device__ __forceinline__ void prologue(const GemvParams& p, int8_t* act, float
     }
     if (first) issued();
     float sc[BT];
-    float inv[BT];
+    f2 inv[BT];
     if (PRO == PRO_NORM_QUANT) {
-        block_sum<BT>(st, red);
-#pragma unroll
-        for (int b = 0; b < BT; ++b)
-            inv[b] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(st[b], (float)K), p.eps)));
+        block_rms_inv<BT>(ss, red, K, p.eps, inv);            // red[0, 2 W BT)
         // pass 2: normalised BF16 row (kept in the stage) and its absmax
         const bool tapx = (blockIdx.x == 0) && p.tap_x != nullptr;
         float am[BT];
@@ -182,7 +190,7 @@ __device__ __forceinline__ void prologue(const GemvParams& p, int8_t* act, float
                     __align__(16) bf16 y[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        y[e] = f2bf(__fmul_rn(__fmul_rn(f[e], inv[b]), w[e]));
+                        y[e] = norm_bf16(f[e], w[e], inv[b]);
                         am[b] = fmaxf(am[b], fabsf(bf2f(y[e])));
                     }
                     if (stage) *reinterpret_cast<int4*>(stage + (size_t)b * K + 8 * j) = *reinterpret_cast<const int4*>(y);
@@ -199,7 +207,7 @@ __device__ __forceinline__ void prologue(const GemvParams& p, int8_t* act, float
         } else {
             for (int j = threadIdx.x; j < vec; j += nt) pass2(j, ld_nc_v4(p.norm_w + 8 * j));
         }
-        block_max<BT>(am, red);
+        block_max<BT>(am, red + 2 * kMaxWarps * BT);          // red[2 W BT, 3 W BT)
 #pragma unroll
         for (int b = 0; b < BT; ++b) sc[b] = __fdiv_rn(am[b], 127.0f);
     } else {
@@ -219,6 +227,9 @@ __device__ __forceinline__ void prologue(const GemvParams& p, int8_t* act, float
             if (b == (int)threadIdx.x) p.tap_s[b] = sc[b];
     }
     // pass 3: INT8 codes of the BF16 row that is quantised
+    float rc[BT];
+#pragma unroll
+    for (int b = 0; b < BT; ++b) rc[b] = quant_recip(sc[b]);
     for (int j = threadIdx.x; j < vec; j += nt) {
         float w[8];
         if (PRO == PRO_NORM_QUANT && !stage) unpack8(ld_nc_v4(p.norm_w + 8 * j), w);
@@ -233,13 +244,12 @@ __device__ __forceinline__ void prologue(const GemvParams& p, int8_t* act, float
                     unpack8(ld_cg_v4(p.x + (size_t)b * p.ldx + 8 * j), f);
                     if (PRO == PRO_NORM_QUANT) {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            f[e] = bf2f(f2bf(__fmul_rn(__fmul_rn(f[e], inv[b]), w[e])));
+                        for (int e = 0; e < 8; ++e) f[e] = bf2f(norm_bf16(f[e], w[e], inv[b]));
                     }
                 }
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const uint32_t c = (uint32_t)(quant_code(f[e], sc[b]) & 0xff);
+                    const uint32_t c = (uint32_t)(quant_code(f[e], sc[b], rc[b]) & 0xff);
                     if (e < 4) lo |= c << (8 * e);
                     else hi |= c << (8 * (e - 4));
                 }
@@ -288,12 +298,13 @@ __device__ __forceinline__ void epilogue(const GemvParams& p, const int32_t* acc
                                       use_pre ? pre[i] : p.w_scale[o]);
             const float u = __fmul_rn(__fmul_rn(__int2float_rn(au), xs[b]),
                                       use_pre ? pre[nt + i] : p.w_scale[N + o]);
-            // silu(g) = g * sigmoid(g), with exp taken of -|g| so that it never overflows
-            const float e = expf(-fabsf(g));
-            const float sig = g >= 0.0f ? __fdiv_rn(1.0f, __fadd_rn(1.0f, e))
-                                        : __fdiv_rn(e, __fadd_rn(1.0f, e));
-            const float si = __fmul_rn(g, sig);
-            p.y[(size_t)b * p.ldy + o] = f2bf(__fmul_rn(si, u));
+            // silu(g) * u = g u sigmoid(g) in two-float arithmetic (see f2),
+            // with the exponential taken of -|g|: g u / (1 + e) for g >= 0,
+            // g u e / (1 + e) for g < 0, e = exp(-|g|)
+            const f2 e = f2_exp(f2_make(-fabsf(g)));
+            f2 num = two_prod(g, u);
+            if (g < 0.0f) num = f2_mul(num, e);
+            p.y[(size_t)b * p.ldy + o] = f2_to_bf16(f2_div(num, f2_addf(e, 1.0f)));
             if (p.acc_out) {
                 p.acc_out[(size_t)b * 2 * N + o] = ag;
                 p.acc_out[(size_t)b * 2 * N + N + o] = au;
@@ -317,7 +328,7 @@ __host__ __device__ __forceinline__ SmemLayout smem_layout(int BT, int nseg, int
     s.accs = align16((size_t)BT * K);
     s.xs = s.accs + align16((size_t)nseg * rows_max * KS * BT * 4);
     s.red = s.xs + align16((size_t)BT * 4);
-    s.pre = align16(s.red + (size_t)kMaxWarps * BT * 4);
+    s.pre = align16(s.red + (size_t)3 * kMaxWarps * BT * 4);
     s.total = s.pre + (size_t)3 * nthreads * 4;
     s.stage = 0;
     if ((size_t)BT * K * 2 <= kStageBudget) {
@@ -377,12 +388,13 @@ __device__ __forceinline__ bool stream_gemv(const GemvParams& p, unsigned char* 
         lp = p.W + ((size_t)(lseg * N + o0) * K + (size_t)off * kUnit + lane * 16);
     }
     int issued = 0;   // units requested so far
+    const uint64_t pol = l2_evict_first_policy();
     // one copy group per batch (empty when the stream is exhausted)
     auto issue_batch = [&](int slot) {
 #pragma unroll
         for (int i = 0; i < UNR; ++i) {
             if (issued < n) {
-                cp_async16_s(ring + (uint32_t)((slot * UNR + i) * NT * 16), lp);
+                cp_async16_s(ring + (uint32_t)((slot * UNR + i) * NT * 16), lp, pol);
                 ++issued;
                 lp += kUnit;
                 if (--lleft == 0) {

@@ -83,9 +83,10 @@ struct AttnParams {
     const int32_t* block_table;   // [B, max_blocks]
     const int32_t* ctx_lens;      // [B]
     int B, Hq, Hkv, D, page, max_blocks, num_blocks;
-    float scale;
+    float scale;            // softmax scale as a float pair scale + scale_lo
+    float scale_lo;
     bf16* out;              // [B, Hq*D]
-    float* part;            // split partials, [B, Hq, splits, D + 2]
+    float* part;            // split partials, [B, Hq, splits, 2 D + 4]
     unsigned* err;
     bf16* tap_q_rot;        // [B, Hq, D] or null
     bf16* tap_k_rot;        // [B, Hkv, D] or null
@@ -151,6 +152,7 @@ struct StepParams {
     int B, H, Hq, Hkv, D, I, vocab, page, max_blocks, num_blocks, max_pos, L, down_splits;
     int device_loop;
     float eps;
+    float attn_scale, attn_scale_lo;   // 1 / sqrt(D) as a float pair
     const bf16* embed;
     const bf16* final_norm_w;
     const bf16* lm_head;

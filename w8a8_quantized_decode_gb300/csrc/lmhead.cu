@@ -1,17 +1,26 @@
 // lmhead.cu -- standalone kernels of the decode step's ends (embedding
 // gather, final RMSNorm + LM head + greedy argmax, device-side decode-loop
 // advance) and the RoPE table; their device bodies live in lmhead_impl.cuh.
+#include <algorithm>
+
 #include "lmhead_impl.cuh"
 
 namespace a8w8 {
 
 namespace {
 
-// 32 warps for one row; 16 warps (more registers each) for 2-4 rows.
-__host__ __device__ constexpr int lm_threads(int BT) { return BT >= 2 ? 512 : 1024; }
-constexpr int kLmMaxTile = 4;
-// Units per warp fetched into L2 before the dependency wait.
-constexpr int kLmL2Ahead = 4;
+// 16 warps; weight ring of 8 batches of 2 steps (128 KB), 2 batches requested
+// before the dependency wait; up to 8 batch rows per launch. The shared
+// memory (at least kLmMinSmem) admits one CTA per SM: two CTAs sharing an SM
+// would halve its share of the stream and leave the kernel waiting on that
+// SM.
+constexpr int kLmThreads = 512;
+constexpr int kLmRingUnr = 2;
+constexpr int kLmRingNB = 8;
+constexpr size_t kLmMinSmem = 120 * 1024;
+constexpr int kLmRingPre = 2;
+constexpr int kLmMaxTile = 8;
+constexpr size_t kLmRingBytes = lm::ring_bytes(kLmThreads, kLmRingUnr, kLmRingNB);
 
 __global__ void embed_kernel(const bf16* __restrict__ embed, int vocab, int H,
                              const int32_t* __restrict__ ids, bf16* __restrict__ hidden,
@@ -33,20 +42,24 @@ __global__ void rope_table_kernel(float* rope, int D, double theta) {
     const int pos = blockIdx.x, i = threadIdx.x;
     const double inv_freq = pow(theta, -2.0 * (double)i / (double)D);
     const double ang = (double)pos * inv_freq;
-    rope[(size_t)pos * D + i] = (float)cos(ang);
-    rope[(size_t)pos * D + D / 2 + i] = (float)sin(ang);
+    const double c = cos(ang), sn = sin(ang);
+    const float ch = (float)c, sh = (float)sn;
+    float* row = rope + (size_t)pos * 2 * D;
+    row[i] = ch;
+    row[D / 2 + i] = sh;
+    row[D + i] = (float)(c - (double)ch);
+    row[3 * D / 2 + i] = (float)(sn - (double)sh);
 }
 
 template <int BT>
-__global__ void __launch_bounds__(lm_threads(BT), 1) lmhead_kernel(const LmHeadParams p) {
+__global__ void __launch_bounds__(kLmThreads, 1) lmhead_kernel(const LmHeadParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
-    lm::stream_lm<BT, lm_threads(BT), 4>(p, smem, kLmL2Ahead, [] {
+    lm::stream_lm<BT, kLmThreads, kLmRingUnr, kLmRingNB, kLmRingPre>(p, smem, [] {
         pdl_wait();
         pdl_trigger();
         return true;
     });
 }
-
 
 template <int BT>
 cudaError_t launch_lm_t(const LmHeadParams& p, const Launch& L) {
@@ -56,14 +69,15 @@ cudaError_t launch_lm_t(const LmHeadParams& p, const Launch& L) {
     cudaGetDevice(&dev);
     if (configured_dev != dev) {
         cudaError_t e =
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
         if (e != cudaSuccess) return e;
         configured_dev = dev;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(L.num_sms);
-    cfg.blockDim = dim3(lm_threads(BT));
-    cfg.dynamicSmemBytes = lm::smem_bytes(BT, p.H, lm_threads(BT));
+    cfg.blockDim = dim3(kLmThreads);
+    cfg.dynamicSmemBytes = std::max(lm::smem_bytes(BT, p.H, kLmThreads, kLmRingBytes), kLmMinSmem);
+    if (cfg.dynamicSmemBytes > 227 * 1024) return cudaErrorInvalidValue;
     cfg.stream = L.stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -82,6 +96,7 @@ cudaError_t launch_lmhead_argmax(const LmHeadParams& p, const Launch& L) {
     if (p.M == 1) return launch_lm_t<1>(p, L);
     if (p.M == 2) return launch_lm_t<2>(p, L);
     if (p.M <= 4) return launch_lm_t<4>(p, L);
+    if (p.M <= 8) return launch_lm_t<8>(p, L);
     return cudaErrorInvalidValue;
 }
 

@@ -7,23 +7,27 @@
 // serving path" (pypto-serving PR #48), "Performance" settings: temperature
 // 0 and top_p 1, i.e. greedy decoding.
 //
-// LM head: CTA c owns vocabulary rows [cV/G, (c+1)V/G); each warp owns whole
-// rows (so every logit is reduced in one fixed order and is reproducible) and
-// streams them with double-buffered 128-bit L1-bypassing loads, 4 units of
-// 512 bytes per batch; the first batch (and an L2 warm-up of the next units)
-// is issued before the dependency wait. The hidden rows are read from L2
-// once, staged in shared memory and normalised there. FP32 logits; the argmax is reduced inside the CTA, merged across CTAs
-// with a 64-bit atomic max on (order-preserving logit bits, inverted index) so
-// ties go to the lowest index, and the last CTA to finish (atomic ticket, no
-// waiting) writes the token ids and clears the keys.
+// LM head on the tensor cores (mma.sync m16n8k16, BF16 x BF16 -> FP32): the
+// weight rows are the B operand (8 vocabulary rows per instruction), the
+// normalised hidden rows the A operand (batch rows 0..7 of M = 16). CTA c
+// owns 8-row groups [c*NG/G, (c+1)*NG/G); each warp owns whole groups and
+// runs over all of K, so every logit is accumulated in one fixed order and is
+// reproducible. Step s of a group: lane (g, c) = (lane / 4, lane % 4) copies
+// the 16 bytes W[row0 + g][32 s + 8 c .. + 8) into its private slot of a
+// cp.async shared-memory ring; its four BF16 pairs are the B fragments of
+// two instructions, whose A fragments are the same eight columns of the
+// hidden rows (the k order inside the 32 columns of a step is permuted
+// identically on both sides, which leaves the dot products unchanged).
+// FP32 logits; the argmax is reduced inside the CTA, merged across CTAs
+// with a 64-bit atomic max on (order-preserving logit bits, inverted index)
+// so ties go to the lowest index, and the last CTA to finish (atomic ticket,
+// no waiting) writes the token ids and clears the keys.
 #pragma once
 
-#include "kernels.cuh"
+#include "gemv_impl.cuh"
 
 namespace a8w8 {
 namespace lm {
-
-constexpr int kUnit = 512;
 
 __device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
     const unsigned u = __float_as_uint(v);
@@ -31,194 +35,217 @@ __device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
     return ((unsigned long long)ord << 32) | (unsigned long long)(0xFFFFFFFFu - (unsigned)idx);
 }
 
-__host__ __device__ inline size_t smem_bytes(int BT, int H, int nthreads) {
+// Shared memory: hidden rows [BT][H + 32] BF16 (32 zero columns of padding
+// keep the rows on different banks and cover a ragged last step), warp
+// reductions, the weight ring.
+__host__ __device__ constexpr size_t ring_bytes(int NT, int UNR, int NB) {
+    return (size_t)NB * UNR * NT * 16;
+}
+__host__ __device__ inline size_t hn_stride(int H) { return (size_t)H + 32; }
+__host__ __device__ inline size_t smem_bytes(int BT, int H, int nthreads, size_t ring) {
     const int nw = nthreads / 32;
-    return (size_t)BT * H * 4 + (size_t)nw * BT * 4 + (size_t)nw * BT * 8 + 16;
+    const size_t hn = ((size_t)BT * hn_stride(H) * 2 + 15) & ~size_t(15);
+    const size_t red = (size_t)2 * gemv::kMaxWarps * BT * 4 + (size_t)nw * BT * 8 + 16;
+    return ((hn + red + 127) & ~size_t(127)) + ring;
 }
 
-// One CTA's share of the LM head: NT threads, UNR units per batch. The first
-// batch of weight loads and an L2 warm-up of the next `l2_ahead` units per
-// warp are issued before `wait()`; returns -1 if `wait` returned false, else 1
-// in the CTA that finished last (it wrote next_tokens) and 0 elsewhere.
-template <int BT, int NT, int UNR, class Wait>
-__device__ __forceinline__ int stream_lm(const LmHeadParams& p, unsigned char* smem, int l2_ahead,
-                                         Wait&& wait) {
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// 16-byte cp.async that copies src_bytes (16 or 0) and zero-fills the rest,
+// with an L2 cache policy.
+__device__ __forceinline__ void cp_async16_zfill(uint32_t s, const void* g, int src_bytes,
+                                                 uint64_t policy) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(s), "l"(g),
+                 "r"(src_bytes), "l"(policy)
+                 : "memory");
+}
+
+// One CTA's share of the LM head (BT <= 8 batch rows): NT threads, a weight
+// ring of NB batches of UNR steps, NBPRE of them requested before `wait()`.
+// Returns -1 if `wait` returned false, else 1 in the CTA that finished last
+// (it wrote next_tokens) and 0 elsewhere.
+template <int BT, int NT, int UNR, int NB, int NBPRE, class Wait>
+__device__ __forceinline__ int stream_lm(const LmHeadParams& p, unsigned char* smem, Wait&& wait) {
+    static_assert(BT <= 8, "the A operand holds batch rows 0..7");
     constexpr int NW = NT / 32;
-    const int H = p.H, V = p.V;
-    const int row_bytes = H * 2;
-    const int upr = (row_bytes + kUnit - 1) / kUnit;
+    const int H = p.H, V = p.V, M = p.M;
+    const int spr = (H + 31) / 32;          // steps per 8-row group
+    const int NG = (V + 7) / 8;
     const int G = gridDim.x;
-    const int r0 = (int)(((long long)V * blockIdx.x) / G);
-    const int r1 = (int)(((long long)V * (blockIdx.x + 1)) / G);
-    const int nrows = r1 - r0;
+    const int cg0 = (int)(((long long)NG * blockIdx.x) / G);
+    const int cg1 = (int)(((long long)NG * (blockIdx.x + 1)) / G);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int wr0 = r0 + (int)((long long)nrows * warp / NW);
-    const int wr1 = r0 + (int)((long long)nrows * (warp + 1) / NW);
-    const int n = (wr1 - wr0) * upr;   // units of this warp
-    const unsigned char* W = reinterpret_cast<const unsigned char*>(p.W);
+    const int gr = lane >> 2, gc = lane & 3;
+    const int wg0 = cg0 + (int)((long long)(cg1 - cg0) * warp / NW);
+    const int wg1 = cg0 + (int)((long long)(cg1 - cg0) * (warp + 1) / NW);
+    const int n = (wg1 - wg0) * spr;        // steps of this warp
+    const bf16* W = p.W;
 
-    int lrow = 0, lch = 0;
-    const unsigned char* lp = W + (size_t)wr0 * row_bytes + lane * 16;
-    auto load_batch = [&](int4 (&dst)[UNR], int count) {
-#pragma unroll
-        for (int i = 0; i < UNR; ++i) {
-            if (i < count) {
-                dst[i] = make_int4(0, 0, 0, 0);
-                if (lch * kUnit + lane * 16 < row_bytes) dst[i] = ld_stream_v4(lp);
-                lp += kUnit;
-                if (++lch == upr) {
-                    lch = 0;
-                    ++lrow;
-                    lp = W + (size_t)(wr0 + lrow) * row_bytes + lane * 16;
-                }
-            }
-        }
-    };
-    int4 wa[UNR], wb[UNR];
-    load_batch(wa, n < UNR ? n : UNR);
-    {
-        const int m = n < UNR + l2_ahead ? n : UNR + l2_ahead;
-        for (int base = UNR; base < m; base += 8) {
-            const int u = base + (lane >> 2);
-            if (u < m) {
-                const int row = u / upr, ch = u - row * upr;
-                const int off = ch * kUnit + (lane & 3) * 128;
-                if (off < row_bytes) prefetch_line_l2(W + (size_t)(wr0 + row) * row_bytes + off);
-            }
-        }
-    }
-
-    if (!wait()) return -1;
-
-    const int M = p.M;
-    float* hn = reinterpret_cast<float*>(smem);                  // [BT][H]
-    float* red = hn + (size_t)BT * H;                            // [NW][BT]
-    unsigned long long* best = reinterpret_cast<unsigned long long*>(red + NW * BT);
+    const size_t hs = hn_stride(H);
+    const size_t hn_bytes = ((size_t)BT * hs * 2 + 15) & ~size_t(15);
+    bf16* hn = reinterpret_cast<bf16*>(smem);
+    float* red = reinterpret_cast<float*>(smem + hn_bytes);          // [2 * kMaxWarps * BT]
+    unsigned long long* best =
+        reinterpret_cast<unsigned long long*>(red + 2 * gemv::kMaxWarps * BT);
     int* s_last = reinterpret_cast<int*>(best + NW * BT);
+    const size_t ring_off =
+        (hn_bytes + (size_t)2 * gemv::kMaxWarps * BT * 4 + (size_t)NW * BT * 8 + 16 + 127) & ~size_t(127);
+    const uint32_t ring = (uint32_t)__cvta_generic_to_shared(smem + ring_off) + threadIdx.x * 16u;
 
-    // final RMSNorm of the hidden rows (float32, rounded to BF16)
-    const int vec = H / 8;
-    {
-        float ss[BT];
-#pragma unroll
-        for (int b = 0; b < BT; ++b) ss[b] = 0.0f;
-        for (int j = threadIdx.x; j < vec; j += NT) {
-#pragma unroll
-            for (int b = 0; b < BT; ++b) {
-                if (b < M) {
-                    const int4 raw = ld_cg_v4(p.hidden + (size_t)b * H + 8 * j);
-                    float f[8];
-                    unpack8(raw, f);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        ss[b] += f[e] * f[e];
-                        hn[(size_t)b * H + 8 * j + e] = f[e];   // staged raw row
-                    }
-                }
-            }
-        }
-#pragma unroll
-        for (int b = 0; b < BT; ++b) {
-            const float t = warp_sum(ss[b]);
-            if (lane == 0) red[warp * BT + b] = t;
-        }
-        __syncthreads();
-        float inv[BT];
-#pragma unroll
-        for (int b = 0; b < BT; ++b) {
-            float t = 0.0f;
-            for (int w = 0; w < NW; ++w) t += red[w * BT + b];
-            inv[b] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(t, (float)H), p.eps)));
-        }
-        for (int j = threadIdx.x; j < vec; j += NT) {
-            float w[8];
-            unpack8(ld_nc_v4(p.norm_w + 8 * j), w);
-#pragma unroll
-            for (int b = 0; b < BT; ++b) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float f = b < M ? hn[(size_t)b * H + 8 * j + e] : 0.0f;
-                    const bf16 y = f2bf(__fmul_rn(__fmul_rn(f, inv[b]), w[e]));
-                    hn[(size_t)b * H + 8 * j + e] = bf2f(y);
-                    if (blockIdx.x == 0 && p.final_hidden && b < M)
-                        p.final_hidden[(size_t)b * H + 8 * j + e] = y;
-                }
-            }
-        }
-        __syncthreads();
-    }
-
-    float acc[BT];
-    unsigned long long wbest[BT];
-#pragma unroll
-    for (int b = 0; b < BT; ++b) {
-        wbest[b] = 0ull;
-        acc[b] = 0.0f;
-    }
-    int cr = 0, cch = 0;
-    auto compute_batch = [&](const int4 (&w)[UNR], int count) {
+    int lg = wg0, ls = 0, issued = 0;
+    const uint64_t pol = l2_evict_first_policy();   // the LM head is streamed once per step
+    auto issue_batch = [&](int slot) {
 #pragma unroll
         for (int i = 0; i < UNR; ++i) {
-            if (i < count) {
-                const int off = cch * kUnit + lane * 16;
-                if (off < row_bytes) {
-                    float wf[8];
-                    unpack8(w[i], wf);
-                    const int k = off / 2;
-#pragma unroll
-                    for (int b = 0; b < BT; ++b) {
-                        const float4 h0 = *reinterpret_cast<const float4*>(hn + (size_t)b * H + k);
-                        const float4 h1 = *reinterpret_cast<const float4*>(hn + (size_t)b * H + k + 4);
-                        float a = acc[b];
-                        a = fmaf(wf[0], h0.x, a);
-                        a = fmaf(wf[1], h0.y, a);
-                        a = fmaf(wf[2], h0.z, a);
-                        a = fmaf(wf[3], h0.w, a);
-                        a = fmaf(wf[4], h1.x, a);
-                        a = fmaf(wf[5], h1.y, a);
-                        a = fmaf(wf[6], h1.z, a);
-                        a = fmaf(wf[7], h1.w, a);
-                        acc[b] = a;
-                    }
+            if (issued < n) {
+                const int row = lg * 8 + gr, k = ls * 32 + 8 * gc;
+                const bool ok = row < V && k < H;
+                cp_async16_zfill(ring + (uint32_t)((slot * UNR + i) * NT * 16),
+                                 ok ? (const void*)(W + (size_t)row * H + k) : (const void*)W,
+                                 ok ? 16 : 0, pol);
+                ++issued;
+                if (++ls == spr) {
+                    ls = 0;
+                    ++lg;
                 }
-                if (++cch == upr) {
-                    const int row = wr0 + cr;
+            }
+        }
+        cp_async_commit();
+    };
 #pragma unroll
-                    for (int b = 0; b < BT; ++b) {
-                        const float logit = warp_sum(acc[b]);
-                        acc[b] = 0.0f;
-                        if (lane == 0 && b < M) {
-                            if (p.logits) p.logits[(size_t)b * V + row] = logit;
-                            const unsigned long long key = argmax_key(logit, row);
-                            wbest[b] = key > wbest[b] ? key : wbest[b];
+    for (int b = 0; b < NBPRE; ++b) issue_batch(b);
+    constexpr int NP = (8192 / 8 + NT - 1) / NT;   // RMSNorm weight (H <= 8192) in registers,
+    int4 nwr[NP];                                   // loaded before the wait
+    const int vec = H / 8;
+    const bool nw_pre = vec <= NP * NT;
+    if (nw_pre) {
+#pragma unroll
+        for (int i = 0; i < NP; ++i) {
+            const int j = threadIdx.x + i * NT;
+            nwr[i] = j < vec ? ld_nc_v4(p.norm_w + 8 * j) : make_int4(0, 0, 0, 0);
+        }
+    }
+
+    if (!wait()) {
+        cp_async_wait_all();
+        return -1;
+    }
+
+    // final RMSNorm of the hidden rows (correctly rounded to BF16, see
+    // norm_bf16): the raw rows are staged in hn, then normalised in place
+    {
+        f2 ss[BT];
+#pragma unroll
+        for (int b = 0; b < BT; ++b) ss[b].hi = ss[b].lo = 0.0f;
+        for (int j = threadIdx.x; j < vec; j += NT) {
+            int4 raw[BT];
+#pragma unroll
+            for (int b = 0; b < BT; ++b)
+                raw[b] = b < M ? ld_cg_v4(p.hidden + (size_t)b * H + 8 * j) : make_int4(0, 0, 0, 0);
+#pragma unroll
+            for (int b = 0; b < BT; ++b) {
+                *reinterpret_cast<int4*>(hn + (size_t)b * hs + 8 * j) = raw[b];
+                float f[8];
+                unpack8(raw[b], f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f2_acc(ss[b], __fmul_rn(f[e], f[e]));
+            }
+        }
+        // zero padding (a ragged last step multiplies it by zero weights)
+        for (int i = threadIdx.x; i < BT * 32; i += NT)
+            hn[(size_t)(i / 32) * hs + H + (i % 32)] = __float2bfloat16_rn(0.0f);
+        // the rest of the ring, queued behind the hidden-row loads
+#pragma unroll
+        for (int b = NBPRE; b < NB; ++b) issue_batch(b);
+        f2 inv[BT];
+        gemv::block_rms_inv<BT>(ss, red, H, p.eps, inv);
+        auto norm_vec = [&](int j, const int4 wraw) {
+            float w[8];
+            unpack8(wraw, w);
+#pragma unroll
+            for (int b = 0; b < BT; ++b) {
+                float f[8];
+                unpack8(*reinterpret_cast<const int4*>(hn + (size_t)b * hs + 8 * j), f);
+                __align__(16) bf16 y[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) y[e] = norm_bf16(f[e], w[e], inv[b]);
+                *reinterpret_cast<int4*>(hn + (size_t)b * hs + 8 * j) = *reinterpret_cast<const int4*>(y);
+                if (blockIdx.x == 0 && p.final_hidden && b < M)
+                    *reinterpret_cast<int4*>(p.final_hidden + (size_t)b * H + 8 * j) =
+                        *reinterpret_cast<const int4*>(y);
+            }
+        };
+        if (nw_pre) {
+#pragma unroll
+            for (int i = 0; i < NP; ++i) {
+                const int j = threadIdx.x + i * NT;
+                if (j < vec) norm_vec(j, nwr[i]);
+            }
+        } else {
+            for (int j = threadIdx.x; j < vec; j += NT) norm_vec(j, ld_nc_v4(p.norm_w + 8 * j));
+        }
+        __syncthreads();
+    }
+
+    // A fragments come from hidden row gr (zero for rows >= M and for the
+    // upper eight rows of the 16-row operand)
+    const uint32_t hrow = (uint32_t)__cvta_generic_to_shared(hn) + (uint32_t)(gr * hs * 2) + 16u * gc;
+    const bool arow = gr < M;
+    float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    unsigned long long wbest = 0ull;          // this lane's best key for batch row gr
+    int cgp = wg0, cs = 0, slot = 0;
+    for (int done = 0; done < n; done += UNR) {
+        cp_async_wait_group<NB - 1>();
+        int4 w[UNR];
+#pragma unroll
+        for (int i = 0; i < UNR; ++i) w[i] = lds_v4(ring + (uint32_t)((slot * UNR + i) * NT * 16));
+#pragma unroll
+        for (int i = 0; i < UNR; ++i) {
+            if (done + i < n) {
+                int4 a = make_int4(0, 0, 0, 0);
+                if (arow) a = lds_v4(hrow + (uint32_t)(cs * 64));
+                mma_bf16_16816(d, (uint32_t)a.x, 0u, (uint32_t)a.y, 0u, (uint32_t)w[i].x, (uint32_t)w[i].y);
+                mma_bf16_16816(d, (uint32_t)a.z, 0u, (uint32_t)a.w, 0u, (uint32_t)w[i].z, (uint32_t)w[i].w);
+                if (++cs == spr) {
+                    // d[0], d[1]: logits of batch row gr, vocabulary rows
+                    // 8*cgp + 2*gc and + 1
+                    const int row = cgp * 8 + 2 * gc;
+                    if (arow) {
+                        if (row < V) {
+                            if (p.logits) p.logits[(size_t)gr * V + row] = d[0];
+                            const unsigned long long k0 = argmax_key(d[0], row);
+                            wbest = k0 > wbest ? k0 : wbest;
+                        }
+                        if (row + 1 < V) {
+                            if (p.logits) p.logits[(size_t)gr * V + row + 1] = d[1];
+                            const unsigned long long k1 = argmax_key(d[1], row + 1);
+                            wbest = k1 > wbest ? k1 : wbest;
                         }
                     }
-                    cch = 0;
-                    ++cr;
+                    d[0] = d[1] = d[2] = d[3] = 0.0f;
+                    cs = 0;
+                    ++cgp;
                 }
             }
         }
-    };
-    int done = 0;
-    while (done < n) {
-        const int ca = n - done < UNR ? n - done : UNR;
-        const int rest = n - done - ca;
-        const int cb = rest < UNR ? rest : UNR;
-        load_batch(wb, cb);
-        compute_batch(wa, ca);
-        done += ca;
-        if (done >= n) break;
-        const int rest2 = n - done - cb;
-        const int ca2 = rest2 < UNR ? rest2 : UNR;
-        load_batch(wa, ca2);
-        compute_batch(wb, cb);
-        done += cb;
+        issue_batch(slot);
+        slot = slot + 1 == NB ? 0 : slot + 1;
     }
-
-    if (lane == 0) {
+    cp_async_wait_all();
+    // best key per batch row: over the four lanes of the row, then the warps
 #pragma unroll
-        for (int b = 0; b < BT; ++b) best[warp * BT + b] = wbest[b];
+    for (int o = 1; o <= 2; o <<= 1) {
+        const unsigned long long v = __shfl_xor_sync(0xffffffffu, wbest, o);
+        wbest = v > wbest ? v : wbest;
     }
+    if (gc == 0 && gr < BT) best[warp * BT + gr] = arow ? wbest : 0ull;
     __syncthreads();
     if ((int)threadIdx.x < M) {
         unsigned long long k = 0ull;

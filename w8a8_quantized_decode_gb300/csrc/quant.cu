@@ -41,6 +41,7 @@ __global__ void __launch_bounds__(kQuantThreads) quant_rows_kernel(const bf16* _
     }
     __syncthreads();
     const float sc = __fdiv_rn(red[0], 127.0f);
+    const float rc = quant_recip(sc);
     if (threadIdx.x == 0) s[row] = sc;
     int8_t* qr = q + (size_t)row * cols;
     for (int i = threadIdx.x; i < nvec; i += kQuantThreads) {
@@ -48,9 +49,9 @@ __global__ void __launch_bounds__(kQuantThreads) quant_rows_kernel(const bf16* _
         unpack8(ld_nc_v4(xr + 8 * i), f);
         uint32_t lo = 0, hi = 0;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) lo |= (uint32_t)(quant_code(f[j], sc) & 0xff) << (8 * j);
+        for (int j = 0; j < 4; ++j) lo |= (uint32_t)(quant_code(f[j], sc, rc) & 0xff) << (8 * j);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) hi |= (uint32_t)(quant_code(f[4 + j], sc) & 0xff) << (8 * j);
+        for (int j = 0; j < 4; ++j) hi |= (uint32_t)(quant_code(f[4 + j], sc, rc) & 0xff) << (8 * j);
         *reinterpret_cast<uint2*>(qr + 8 * i) = make_uint2(lo, hi);
     }
 }

@@ -27,7 +27,6 @@ namespace {
 // 16 warps with a 128-register budget (64 registers per thread would spill
 // inside the streaming loops of this much larger kernel), 4 units per batch.
 constexpr int kStepThreads = 512;
-constexpr int kStepUnroll = 4;
 constexpr unsigned long long kBarrierTimeoutNs = 2000000000ull;
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
@@ -80,7 +79,6 @@ __device__ __forceinline__ void gemv_params(const StepParams& P, GemvParams& g) 
     g.err = P.err;
 }
 
-constexpr int kL2PrefetchUnits = 16;   // LM head: per warp 8 KB, 128 KB per SM
 // Weight ring of the projection phases: 2 units per batch, 6 batches (96 KB),
 // 2 requested before the barrier.
 constexpr int kStepRingUnr = 2;
@@ -114,8 +112,8 @@ __device__ __forceinline__ void attn_phase(const AttnParams& a, int chunk, int s
 template <int BT>
 __device__ __forceinline__ bool lm_phase(const LmHeadParams& lp, unsigned char* smem, unsigned* bar,
                                       unsigned* k, unsigned* err, int* s_ok, bool* last) {
-    const int r = lm::stream_lm<BT, kStepThreads, kStepUnroll>(
-        lp, smem, kL2PrefetchUnits, [&] { return grid_sync(bar, k, err, s_ok); });
+    const int r = lm::stream_lm<BT, kStepThreads, kStepRingUnr, kStepRingNB, kStepRingPre>(
+        lp, smem, [&] { return grid_sync(bar, k, err, s_ok); });
     *last = r == 1;
     return r >= 0;
 }
@@ -170,7 +168,8 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
                 a.page = P.page;
                 a.max_blocks = P.max_blocks;
                 a.num_blocks = P.num_blocks;
-                a.scale = rsqrtf((float)D);
+                a.scale = P.attn_scale;
+                a.scale_lo = P.attn_scale_lo;
                 a.out = P.attn;
                 a.part = P.part;
                 a.err = P.err;
@@ -290,7 +289,7 @@ size_t step_smem_bytes(int BT, int D, int G, int H, int I, int Hq, int Hkv, int 
     m = std::max(m, gemv::smem_layout(BT, 2, 1, H, I, G, kStepThreads, r).total);
     m = std::max(m, gemv::smem_layout(BT, 1, ksd, I, H, G, kStepThreads, r).total);
     m = std::max(m, attn_item_smem_bytes(max_ctx <= 256 ? 256 : 128, D));
-    m = std::max(m, lm::smem_bytes(BT, H, kStepThreads));
+    m = std::max(m, lm::smem_bytes(BT, H, kStepThreads, lm::ring_bytes(kStepThreads, kStepRingUnr, kStepRingNB)));
     return m;
 }
 
