@@ -2,6 +2,7 @@
 // orchestration of the decode layer and step, and the replayable step graph.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -80,7 +81,7 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Workspace layout shared by the layer and the step.
 struct WsLayout {
-    size_t hid, qkv, attn, act, part, keys, ticket, bar, total;
+    size_t hid, qkv, attn, act, part, att_tk, keys, ticket, bar, total;
 };
 
 WsLayout ws_layout(const a8w8_config& c, int B, int max_blocks) {
@@ -97,7 +98,12 @@ WsLayout ws_layout(const a8w8_config& c, int B, int max_blocks) {
     w.act = o;
     o = round_up(o + (size_t)B * c.intermediate * 2, 256);
     w.part = o;
-    o = round_up(o + attn_part_bytes(B, c.num_q_heads, D, max_blocks * c.page_size), 256);
+    const int max_ctx = max_blocks * c.page_size;
+    o = round_up(o + std::max(attn_part_bytes(B, c.num_q_heads, D, max_ctx, true),
+                              attn_part_bytes(B, c.num_q_heads, D, max_ctx, false)),
+                 256);
+    w.att_tk = o;   // attention split tickets [B, Hq]
+    o = round_up(o + (size_t)B * c.num_q_heads * 4, 256);
     w.keys = o;
     o = round_up(o + (size_t)B * 8, 256);
     w.ticket = o;
@@ -178,6 +184,7 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     bf16* attn = reinterpret_cast<bf16*>(ws + lay.attn);
     bf16* act = reinterpret_cast<bf16*>(ws + lay.act);
     float* part = reinterpret_cast<float*>(ws + lay.part);
+    unsigned* att_tk = reinterpret_cast<unsigned*>(ws + lay.att_tk);
     const a8w8_layer_taps none = {};
     const a8w8_layer_taps& T = taps ? *taps : none;
 
@@ -196,6 +203,8 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     g.tap_x = reinterpret_cast<bf16*>(T.xn);
     g.tap_q = T.xq;
     g.tap_s = T.xs;
+    g.clear = att_tk;   // the attention that follows counts its splits there
+    g.clear_n = B * Hq;
     cudaError_t e = run_gemv(PRO_NORM_QUANT, EPI_STORE, 1, g, B, L);
     if (e != cudaSuccess) return cuda_fail(e, "QKV projection");
     if (T.qkv) {
@@ -233,6 +242,7 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     }
     a.out = attn;
     a.part = part;
+    a.tickets = att_tk;
     a.err = device_error_word();
     a.tap_q_rot = reinterpret_cast<bf16*>(T.q_rot);
     a.tap_k_rot = reinterpret_cast<bf16*>(T.k_rot);
@@ -415,7 +425,7 @@ a8w8_status paged_kv_write(const a8w8_bf16* k, const a8w8_bf16* v, int T, int Hk
 
 size_t a8w8_attention_workspace_bytes(int B, int Hq, int D, int max_ctx) {
     if (B <= 0 || Hq <= 0 || D <= 0 || max_ctx <= 0) return 0;
-    return attn_part_bytes(B, Hq, D, max_ctx);
+    return attn_part_bytes(B, Hq, D, max_ctx, false);
 }
 
 a8w8_status paged_decode_attention_bf16(const a8w8_bf16* q, const a8w8_bf16* k_cache,
@@ -433,7 +443,7 @@ a8w8_status paged_decode_attention_bf16(const a8w8_bf16* q, const a8w8_bf16* k_c
         return fail(A8W8_ERR_UNSUPPORTED_SHAPE, "context longer than 2^24 tokens");
     a8w8_status s = check_ptrs({q, k_cache, v_cache, block_table, ctx_lens, out}, "paged_decode_attention_bf16");
     if (s != A8W8_OK) return s;
-    const size_t need = attn_part_bytes(B, Hq, D, max_blocks * page_size);
+    const size_t need = attn_part_bytes(B, Hq, D, max_blocks * page_size, false);
     if (need > 0 && (!ws || ws_bytes < need || !aligned16(ws)))
         return fail(A8W8_ERR_WORKSPACE, "attention workspace needs %zu bytes", need);
     AttnParams a = {};
@@ -508,7 +518,7 @@ a8w8_status paged_decode_attention_bf16_noalloc(const a8w8_bf16* q, const a8w8_b
     a8w8_status s = check_ptrs({q, k_cache, v_cache, block_table, ctx_lens, out},
                                "paged_decode_attention_bf16_noalloc");
     if (s != A8W8_OK) return s;
-    const size_t need = attn_part_bytes(B, Hq, D, max_blocks * page_size);
+    const size_t need = attn_part_bytes(B, Hq, D, max_blocks * page_size, false);
     if (need > A8W8_NOALLOC_SCRATCH_BYTES)
         return fail(A8W8_ERR_WORKSPACE,
                     "paged_decode_attention_bf16_noalloc: split-KV partials need %zu bytes, more than "

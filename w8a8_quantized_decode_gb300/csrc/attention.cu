@@ -30,21 +30,33 @@
 
 namespace a8w8 {
 
+// Contexts up to this length use the in-kernel combine in the decode layer.
+constexpr int kInKernelMaxCtx = 64 * 256;
+bool in_kernel_combine(int max_ctx, bool tickets) { return tickets && max_ctx <= kInKernelMaxCtx; }
+
 namespace {
 
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnParams p, int chunk,
                                                             int splits) {
     extern __shared__ __align__(16) unsigned char smem[];
-    attn_item<D>(p, chunk, splits, blockIdx.x, blockIdx.y, blockIdx.z, smem, true);
+    attn_item<D, kAttnThreads>(p, chunk, splits, blockIdx.x, blockIdx.y, blockIdx.z, smem, true);
 }
 
+// One CTA per (query head, request): split weights by warp 0 into shared
+// memory, then one element per thread.
 template <int D>
 __global__ void __launch_bounds__(D) attn_combine_kernel(const float* __restrict__ part, int splits,
                                                          int Hq, bf16* __restrict__ out) {
+    extern __shared__ float cws[];   // [splits][2] weights, then L[2]
     pdl_wait();
     pdl_trigger();
-    attn_combine_elem<D>(part, splits, Hq, blockIdx.y, blockIdx.x, threadIdx.x, out);
+    const int h = blockIdx.x, b = blockIdx.y;
+    const float* pp = part + ((size_t)b * Hq + h) * splits * (2 * D + 4);
+    if (threadIdx.x < 32) combine_weights<D>(pp, splits, cws, cws + 2 * splits, threadIdx.x);
+    __syncthreads();
+    out[((size_t)b * Hq + h) * D + threadIdx.x] =
+        combine_elem<D>(pp, splits, cws, cws + 2 * splits, threadIdx.x);
 }
 
 __global__ void kv_write_kernel(const bf16* __restrict__ k, const bf16* __restrict__ v, int T,
@@ -87,8 +99,9 @@ cudaError_t launch_ex(Kern kern, dim3 grid, dim3 block, size_t smem, const Launc
 template <int D>
 cudaError_t launch_attn_d(const AttnParams& p, const Launch& L) {
     const int max_ctx = p.max_blocks * p.page;
-    const int chunk = attn_chunk(max_ctx);
-    const int splits = attn_splits(max_ctx);
+    const bool in_kernel = in_kernel_combine(max_ctx, p.tickets != nullptr);
+    const int chunk = attn_chunk(max_ctx, in_kernel);
+    const int splits = attn_splits(max_ctx, in_kernel);
     const size_t smem = attn_item_smem_bytes(chunk, D);
     static int configured_dev = -1;
     int dev = 0;
@@ -100,24 +113,39 @@ cudaError_t launch_attn_d(const AttnParams& p, const Launch& L) {
         if (e != cudaSuccess) return e;
         configured_dev = dev;
     }
-    cudaError_t e = launch_ex(attn_kernel<D>, dim3(splits, p.Hkv, p.B), dim3(kAttnThreads), smem,
-                              L, p, chunk, splits);
-    if (e != cudaSuccess || splits == 1) return e;
-    return launch_ex(attn_combine_kernel<D>, dim3(p.Hq, p.B), dim3(D), 0, L,
-                     (const float*)p.part, splits, p.Hq, p.out);
+    AttnParams q = p;
+    if (!in_kernel) q.tickets = nullptr;   // partials go to the combine kernel
+    cudaError_t e = launch_ex(attn_kernel<D>, dim3(splits, p.Hq, p.B), dim3(kAttnThreads), smem,
+                              L, q, chunk, splits);
+    if (e != cudaSuccess || splits == 1 || in_kernel) return e;
+    if ((size_t)(2 * splits + 2) * sizeof(float) > 48 * 1024) return cudaErrorInvalidValue;
+    return launch_ex(attn_combine_kernel<D>, dim3(p.Hq, p.B), dim3(D),
+                     (size_t)(2 * splits + 2) * sizeof(float), L, (const float*)p.part, splits, p.Hq,
+                     p.out);
 }
 
 }  // namespace
 
-int attn_chunk(int max_ctx) { return max_ctx <= 256 ? 256 : 128; }
+// Standalone: one or two large chunks per CTA. In-kernel combine (decode
+// layer, contexts up to kInKernelMaxCtx): chunks of 64 tokens, at most 64
+// chunks per request (longer contexts get longer chunks, at most 256
+// tokens); only the chunks that hold tokens run, and a context of one chunk
+// needs no combine. Longer contexts use the standalone form.
 
-int attn_splits(int max_ctx) {
-    const int c = attn_chunk(max_ctx);
+int attn_chunk(int max_ctx, bool combine_in_kernel) {
+    if (!in_kernel_combine(max_ctx, combine_in_kernel)) return max_ctx <= 256 ? 256 : 128;
+    int c = (max_ctx + 63) / 64;
+    c = (c + 15) / 16 * 16;
+    return c < 64 ? 64 : (c > 256 ? 256 : c);
+}
+
+int attn_splits(int max_ctx, bool combine_in_kernel) {
+    const int c = attn_chunk(max_ctx, combine_in_kernel);
     return max_ctx <= 0 ? 1 : (max_ctx + c - 1) / c;
 }
 
-size_t attn_part_bytes(int B, int Hq, int D, int max_ctx) {
-    const int s = attn_splits(max_ctx);
+size_t attn_part_bytes(int B, int Hq, int D, int max_ctx, bool combine_in_kernel) {
+    const int s = attn_splits(max_ctx, combine_in_kernel);
     if (s <= 1) return 0;
     return (size_t)B * Hq * s * (2 * D + 4) * sizeof(float);
 }

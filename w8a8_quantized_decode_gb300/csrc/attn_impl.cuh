@@ -33,77 +33,192 @@
 
 namespace a8w8 {
 
-constexpr int kAttnThreads = 256;
-constexpr int kAttnWarps = kAttnThreads / 32;
-constexpr int kGMax = 8;
+constexpr int kAttnThreads = 256;    // the standalone / decode-layer kernel
+constexpr int kTilePad = 8;          // K/V tile rows of D + 8 BF16 (16-byte aligned, fewer bank conflicts)
 
-// Shared memory of one item: K and V tiles (BF16), the G query rows (float),
-// scores / probabilities (two-float: hi and lo planes), per-head (m, l) as
-// two-float pairs. The P.V cross-group reduction reuses the K/V tiles.
+// Shared memory of one item (one query head): K and V tiles (BF16, padded
+// rows; after P.V the region holds the in-kernel combine's scratch), the
+// query row (float), scores / probabilities (two-float: hi and lo planes)
+// and (m, l) as two-float pairs.
+constexpr int kMaxInKernelSplits = 64;
+__host__ __device__ inline size_t attn_tiles_bytes(int chunk, int D) {
+    const size_t kv = (size_t)2 * chunk * (D + kTilePad) * 2;
+    const size_t comb = (size_t)(2 * kMaxInKernelSplits + 2) * 4 + (size_t)(kMaxInKernelSplits + 1) * 4;
+    return kv > comb ? kv : comb;
+}
 __host__ __device__ inline size_t attn_item_smem_bytes(int chunk, int D) {
-    return (size_t)2 * chunk * D * 2 + (size_t)kGMax * D * 4 + (size_t)2 * kGMax * chunk * 4 +
-           (size_t)kGMax * 4 * 4 + 16;
+    return attn_tiles_bytes(chunk, D) + (size_t)D * 4 + (size_t)2 * chunk * 4 + 4 * 4 + 16;
 }
 
+template <int NT>
 __device__ __forceinline__ void attn_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kAttnThreads) : "memory");
+    asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
 }
 
-// Per-head RMSNorm + RoPE of one head vector held as E = D/32 elements per
-// lane (elements [lane*E, lane*E + E)); the rotate-half partner of lane l is
-// lane l ^ 16. Returns BF16-rounded results in y.
 template <int D>
-__device__ __forceinline__ void norm_rope_head(const bf16* src, const bf16* norm_w,
-                                               const float* rope_row, float eps, int lane,
+struct HeadPre {
+    static constexpr int E = D / 32;
+    float qw[E], kw[E];                  // q / k norm weights
+    float ch[E], sh[E], cl[E], sl[E];    // cos / sin, hi and lo parts
+};
+
+template <int D>
+__device__ __forceinline__ void load_bf16_lane(const bf16* src, float (&x)[D / 32]) {
+    if constexpr (D == 128) {
+        const uint2 v = __ldcg(reinterpret_cast<const uint2*>(src));
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+        const float2 a = __bfloat1622float2(h[0]), c = __bfloat1622float2(h[1]);
+        x[0] = a.x;
+        x[1] = a.y;
+        x[2] = c.x;
+        x[3] = c.y;
+    } else {
+        const unsigned v = __ldcg(reinterpret_cast<const unsigned*>(src));
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
+        x[0] = a.x;
+        x[1] = a.y;
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void load_head_pre(const AttnParams& p, int pos, int lane,
+                                              HeadPre<D>& hp) {
+    constexpr int E = D / 32;
+    load_bf16_lane<D>(p.q_norm_w + lane * E, hp.qw);
+    load_bf16_lane<D>(p.k_norm_w + lane * E, hp.kw);
+    const float* row = p.rope + (size_t)pos * 2 * D;
+    const int i0 = (lane * E) % (D / 2);
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        hp.ch[e] = __ldg(row + i0 + e);
+        hp.sh[e] = __ldg(row + D / 2 + i0 + e);
+        hp.cl[e] = __ldg(row + D + i0 + e);
+        hp.sl[e] = __ldg(row + 3 * D / 2 + i0 + e);
+    }
+}
+
+// Per-head RMSNorm then rotate-half RoPE of the lane's elements x, each
+// output correctly rounded to BF16 (see f2): x and its partner are exact
+// floats, cos / sin hi + lo pairs.
+template <int D>
+__device__ __noinline__ void norm_rope_head(float (&x)[D / 32], const float (&w)[D / 32],
+                                               const HeadPre<D>& hp, float eps, int lane,
                                                float (&y)[D / 32]) {
     constexpr int E = D / 32;
-    float x[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) x[e] = bf2f(ld_cg_bf16(src + lane * E + e));
-    // per-head RMSNorm, correctly rounded to BF16 (see norm_bf16); the
-    // float64 scalar is evaluated by lane 0 and broadcast
     f2 ss = {0.0f, 0.0f};
 #pragma unroll
     for (int e = 0; e < E; ++e) f2_acc(ss, __fmul_rn(x[e], x[e]));
-    ss = warp_sum_f2(ss);
-    f2 inv = {0.0f, 0.0f};
-    if (lane == 0) inv = rms_inv(ss, D, eps);
-    inv.hi = __shfl_sync(0xffffffffu, inv.hi, 0);
-    inv.lo = __shfl_sync(0xffffffffu, inv.lo, 0);
+    const f2 inv = rms_inv(warp_sum_f2(ss), D, eps);
 #pragma unroll
-    for (int e = 0; e < E; ++e) x[e] = bf2f(norm_bf16(x[e], bf2f(norm_w[lane * E + e]), inv));
-    // rotate-half RoPE, each output correctly rounded to BF16: x and its
-    // partner are exact floats, cos / sin are hi + lo pairs from the table
+    for (int e = 0; e < E; ++e) x[e] = bf2f(norm_bf16(x[e], w[e], inv));
 #pragma unroll
     for (int e = 0; e < E; ++e) {
         const float partner = __shfl_xor_sync(0xffffffffu, x[e], 16);
-        const int i = (lane * E + e) % (D / 2);
-        const f2 c = {rope_row[i], rope_row[D + i]};
-        const f2 sn = {rope_row[D / 2 + i], rope_row[3 * D / 2 + i]};
-        const f2 a = f2_mulf(c, x[e]);
-        const f2 b2 = f2_mulf(sn, partner);
+        const f2 a = f2_mulf(f2{hp.ch[e], hp.cl[e]}, x[e]);
+        const f2 b2 = f2_mulf(f2{hp.sh[e], hp.sl[e]}, partner);
         y[e] = bf2f(f2_to_bf16(lane < 16 ? f2_sub(a, b2) : f2_add(a, b2)));
     }
 }
 
-// One attention work item. Threads with threadIdx.x >= kAttnThreads must not
-// call it. With `pdl` the cached-KV copies are issued before
-// griddepcontrol.wait.
+// Combine of the split-KV partials of one (request b, query head h), in
+// two-float arithmetic: O = sum_s o_s e^{m_s - M} / sum_s l_s e^{m_s - M}
+// with M = max_s m_s. Partial layout per split: o hi plane [D], o lo plane
+// [D], m (hi, lo), l (hi, lo).
+// Step 1 (one warp): the split weights w_s = e^{m_s - M} into w[2s], w[2s+1]
+// and L = sum_s l_s w_s into L[0], L[1].
 template <int D>
+__device__ __forceinline__ void combine_weights(const float* pp, int splits, float* w, float* L,
+                                                int lane, int* active = nullptr,
+                                                int* n_active = nullptr) {
+    constexpr int S = 2 * D + 4;
+    f2 M = {-INFINITY, 0.0f};
+    for (int s = lane; s < splits; s += 32)
+        M = f2_max(M, f2{__ldcg(pp + (size_t)s * S + 2 * D), __ldcg(pp + (size_t)s * S + 2 * D + 1)});
+    M = warp_max_f2(M);
+    f2 l = {0.0f, 0.0f};
+    int base = 0;
+    for (int s0 = 0; s0 < splits; s0 += 32) {
+        const int s = s0 + lane;
+        f2 ws = {0.0f, 0.0f};
+        if (s < splits) {
+            const float* q = pp + (size_t)s * S;
+            const f2 m = {__ldcg(q + 2 * D), __ldcg(q + 2 * D + 1)};
+            if (m.hi != -INFINITY) {
+                ws = f2_exp(f2_sub(m, M));
+                l = f2_add(l, f2_mul(f2{__ldcg(q + 2 * D + 2), __ldcg(q + 2 * D + 3)}, ws));
+            }
+            w[2 * s] = ws.hi;
+            w[2 * s + 1] = ws.lo;
+        }
+        if (active) {
+            // compact list of the splits with a non-zero weight
+            const unsigned nz = __ballot_sync(0xffffffffu, ws.hi != 0.0f);
+            if (ws.hi != 0.0f) active[base + __popc(nz & ((1u << lane) - 1u))] = s;
+            base += __popc(nz);
+        }
+    }
+    l = warp_sum_f2(l);
+    if (lane == 0) {
+        L[0] = l.hi;
+        L[1] = l.lo;
+        if (n_active) *n_active = base;
+    }
+}
+template <int D>
+__device__ __forceinline__ bf16 combine_elem(const float* pp, int splits, const float* w,
+                                             const float* L, int d) {
+    constexpr int S = 2 * D + 4;
+    constexpr int U = 8;   // partials loaded together
+    const f2 l = {L[0], L[1]};
+    if (!(l.hi > 0.0f)) return __float2bfloat16_rn(0.0f);
+    f2 acc = {0.0f, 0.0f};
+    for (int s0 = 0; s0 < splits; s0 += U) {
+        float oh[U], ol[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            oh[u] = ol[u] = 0.0f;
+            if (s0 + u < splits) {
+                const float* q = pp + (size_t)(s0 + u) * S;
+                oh[u] = __ldcg(q + d);
+                ol[u] = __ldcg(q + D + d);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (s0 + u < splits) {
+                const f2 ws = {w[2 * (s0 + u)], w[2 * (s0 + u) + 1]};
+                if (ws.hi != 0.0f) acc = f2_add(acc, f2_mul(f2{oh[u], ol[u]}, ws));
+            }
+        }
+    }
+    return f2_to_bf16(f2_div(acc, l));
+}
+
+// One attention work item, (request b, query head h, token chunk `split`),
+// on the first NT threads of the CTA (the others must not call it; they are
+// not synchronised with). The G query heads of a KV head are separate items
+// (their K/V tiles are read once per item, from L2 after the first), so a
+// batch-1 step spreads over Hq x chunks CTAs. With `pdl` the cached-KV copies
+// and the other immutable operands are requested before
+// griddepcontrol.wait.
+template <int D, int NT>
 __device__ __forceinline__ void attn_item(const AttnParams& p, int chunk, int splits, int split,
-                                          int kvh, int b, unsigned char* smem, bool pdl) {
+                                          int h, int b, unsigned char* smem, bool pdl) {
+    constexpr int NW = NT / 32;
+    constexpr int DP = D + kTilePad;
     bf16* Ks = reinterpret_cast<bf16*>(smem);
-    bf16* Vs = Ks + (size_t)chunk * D;
-    float* qs = reinterpret_cast<float*>(Vs + (size_t)chunk * D);
-    float* sc = qs + kGMax * D;                    // [G][chunk] hi
-    float* sl = sc + (size_t)kGMax * chunk;        // [G][chunk] lo
-    float* stat = sl + (size_t)kGMax * chunk;      // [G][4]: m hi, m lo, l hi, l lo
-    int* s_bad_block = reinterpret_cast<int*>(stat + kGMax * 4);
-    float* red = reinterpret_cast<float*>(smem);   // aliases the K/V tiles after P.V
+    bf16* Vs = Ks + (size_t)chunk * DP;
+    float* qs = reinterpret_cast<float*>(smem + attn_tiles_bytes(chunk, D));   // [D]
+    float* sc = qs + D;                            // [chunk] hi
+    float* sl = sc + chunk;                        // [chunk] lo
+    float* stat = sl + chunk;                      // m hi, m lo, l hi, l lo
+    int* s_flag = reinterpret_cast<int*>(stat + 4);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int G = p.Hq / p.Hkv;
+    const int kvh = h / G;
+    const bool lead = h - kvh * G == 0;            // the head that writes the new K/V
     const int t0 = split * chunk;
     const int max_ctx = p.max_blocks * p.page;
     const int ctx_raw = p.ctx_lens[b];
@@ -115,25 +230,32 @@ __device__ __forceinline__ void attn_item(const AttnParams& p, int chunk, int sp
     const int n = max(t1 - t0, 0);
     const bool covers_new = p.fused && ctx > 0 && pos >= t0 && pos < t0 + chunk;
     const int n_old = covers_new ? n - 1 : n;
+    // In-kernel combine: only the chunks that hold tokens take part; a lone
+    // chunk writes the output itself.
+    const int active = p.tickets ? max(1, (ctx + chunk - 1) / chunk) : splits;
+    if (split >= active) return;   // the whole CTA, before any barrier
+    const bool single = active == 1;
 
-    if (tid == 0) *s_bad_block = 0;
-    attn_sync();
+    if (tid == 0) *s_flag = 0;
+    attn_sync<NT>();
     constexpr int RV = D / 8;   // 16-byte vectors per row
-    for (int i = tid; i < n_old * RV; i += kAttnThreads) {
+    for (int i = tid; i < n_old * RV; i += NT) {
         const int t = i / RV, c = i - t * RV;
         const int tok = t0 + t;
         const int blk = p.block_table[(size_t)b * p.max_blocks + tok / p.page];
         if (blk < 0 || blk >= p.num_blocks) {
-            *reinterpret_cast<int4*>(Ks + (size_t)t * D + 8 * c) = make_int4(0, 0, 0, 0);
-            *reinterpret_cast<int4*>(Vs + (size_t)t * D + 8 * c) = make_int4(0, 0, 0, 0);
-            *s_bad_block = 1;
+            *reinterpret_cast<int4*>(Ks + (size_t)t * DP + 8 * c) = make_int4(0, 0, 0, 0);
+            *reinterpret_cast<int4*>(Vs + (size_t)t * DP + 8 * c) = make_int4(0, 0, 0, 0);
+            *s_flag = 1;
             continue;
         }
         const size_t off = (((size_t)blk * p.page + tok % p.page) * p.Hkv + kvh) * D + 8 * c;
-        cp_async16(Ks + (size_t)t * D + 8 * c, p.k_cache + off);
-        cp_async16(Vs + (size_t)t * D + 8 * c, p.v_cache + off);
+        cp_async16(Ks + (size_t)t * DP + 8 * c, p.k_cache + off);
+        cp_async16(Vs + (size_t)t * DP + 8 * c, p.v_cache + off);
     }
     cp_async_commit();
+    HeadPre<D> hp;
+    if (p.fused && n > 0 && warp < 2) load_head_pre<D>(p, pos < p.max_pos ? pos : 0, lane, hp);
 
     if (pdl) {
         pdl_wait();
@@ -145,213 +267,219 @@ __device__ __forceinline__ void attn_item(const AttnParams& p, int chunk, int sp
         if (bad_pos) set_error(p.err, 0x10u);
     }
 
-    // query heads (and, for the item holding the new token, its K and V)
-    if (n > 0) {
-        for (int task = warp; task <= G; task += kAttnWarps) {
-            constexpr int E = D / 32;
-            if (task < G) {
-                const int h = kvh * G + task;
-                const bf16* src = p.q + (size_t)b * p.q_stride + (size_t)h * D;
-                float y[E];
-                if (p.fused) {
-                    norm_rope_head<D>(src, p.q_norm_w, p.rope + (size_t)pos * 2 * D, p.eps, lane, y);
-                    if (p.tap_q_rot && split == 0) {
+    // warp 0: the query head; warp 1: the new token's K (norm + RoPE) and V
+    constexpr int E = D / 32;
+    if (n > 0 && warp == 0) {
+        const bf16* src = p.q + (size_t)b * p.q_stride + (size_t)h * D;
+        float x[E], y[E];
+        load_bf16_lane<D>(src + lane * E, x);
+        if (p.fused) {
+            norm_rope_head<D>(x, hp.qw, hp, p.eps, lane, y);
+            if (p.tap_q_rot && split == 0) {
 #pragma unroll
-                        for (int e = 0; e < E; ++e)
-                            p.tap_q_rot[((size_t)b * p.Hq + h) * D + lane * E + e] = f2bf(y[e]);
-                    }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < E; ++e) y[e] = bf2f(ld_cg_bf16(src + lane * E + e));
-                }
-#pragma unroll
-                for (int e = 0; e < E; ++e) qs[task * D + lane * E + e] = y[e];
-            } else if (covers_new) {
-                const int NQ = p.Hq * D, NK = p.Hkv * D;
-                const bf16* ksrc = p.q + (size_t)b * p.q_stride + NQ + (size_t)kvh * D;
-                const bf16* vsrc = p.q + (size_t)b * p.q_stride + NQ + NK + (size_t)kvh * D;
-                float y[E];
-                norm_rope_head<D>(ksrc, p.k_norm_w, p.rope + (size_t)pos * 2 * D, p.eps, lane, y);
-                const int tr = pos - t0;
-                const long slot = p.slot_mapping[b];
-                const long num_slots = (long)p.num_blocks * p.page;
-                const bool slot_ok = slot >= 0 && slot < num_slots;
-                if (lane == 0 && slot >= num_slots) set_error(p.err, 0x1u);
-#pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    const int d = lane * E + e;
-                    const bf16 kb = f2bf(y[e]);
-                    const bf16 vb = ld_cg_bf16(vsrc + d);
-                    Ks[(size_t)tr * D + d] = kb;
-                    Vs[(size_t)tr * D + d] = vb;
-                    if (slot_ok) {
-                        p.k_cache[((size_t)slot * p.Hkv + kvh) * D + d] = kb;
-                        p.v_cache[((size_t)slot * p.Hkv + kvh) * D + d] = vb;
-                    }
-                    if (p.tap_k_rot) p.tap_k_rot[((size_t)b * p.Hkv + kvh) * D + d] = kb;
-                }
+                for (int e = 0; e < E; ++e)
+                    p.tap_q_rot[((size_t)b * p.Hq + h) * D + lane * E + e] = f2bf(y[e]);
             }
+        } else {
+#pragma unroll
+            for (int e = 0; e < E; ++e) y[e] = x[e];
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) qs[lane * E + e] = y[e];
+    } else if (n > 0 && warp == 1 && covers_new) {
+        const int NQ = p.Hq * D, NK = p.Hkv * D;
+        const bf16* ksrc = p.q + (size_t)b * p.q_stride + NQ + (size_t)kvh * D;
+        const bf16* vsrc = p.q + (size_t)b * p.q_stride + NQ + NK + (size_t)kvh * D;
+        float x[E], vv[E], y[E];
+        load_bf16_lane<D>(ksrc + lane * E, x);
+        load_bf16_lane<D>(vsrc + lane * E, vv);
+        norm_rope_head<D>(x, hp.kw, hp, p.eps, lane, y);
+        const int tr = pos - t0;
+        const long slot = p.slot_mapping[b];
+        const long num_slots = (long)p.num_blocks * p.page;
+        const bool slot_ok = lead && slot >= 0 && slot < num_slots;
+        if (lead && lane == 0 && slot >= num_slots) set_error(p.err, 0x1u);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const int d = lane * E + e;
+            const bf16 kb = f2bf(y[e]);
+            const bf16 vb = f2bf(vv[e]);
+            Ks[(size_t)tr * DP + d] = kb;
+            Vs[(size_t)tr * DP + d] = vb;
+            if (slot_ok) {
+                p.k_cache[((size_t)slot * p.Hkv + kvh) * D + d] = kb;
+                p.v_cache[((size_t)slot * p.Hkv + kvh) * D + d] = vb;
+            }
+            if (lead && p.tap_k_rot) p.tap_k_rot[((size_t)b * p.Hkv + kvh) * D + d] = kb;
         }
     }
     cp_async_wait_all();
-    attn_sync();
-    if (tid == 0 && *s_bad_block) set_error(p.err, 0x2u);
+    attn_sync<NT>();
+    if (tid == 0 && *s_flag) set_error(p.err, 0x2u);
 
     // Scores, softmax and P.V in two-float arithmetic (see f2): q and k are
     // BF16 values, so each product q_d k_d is exact in float32 and the dot
     // product is summed as a pair; the probabilities and the weighted sum of
     // V are pairs too, so the BF16 output rounds as an evaluation in float64
     // would.
-    // scores: LPT lanes per token, 8 columns each, q read from shared memory
+    // scores: one token per LPT lanes, 8 columns per lane
     constexpr int LPT = D / 8;
-    constexpr int TPW = 32 / LPT;
-    const int j = lane % LPT, tw = lane / LPT;
+    constexpr int PPW = 32 / LPT;
     const f2 scale = {p.scale, p.scale_lo};
-    if (n > 0) {
-        const int step = kAttnWarps * TPW;
-        const int n_pad = ((n + step - 1) / step) * step;
-        for (int t = warp * TPW + tw; t < n_pad; t += step) {
+    {
+        const int j = lane % LPT, pw = lane / LPT;
+        const float4 qa = *reinterpret_cast<const float4*>(qs + 8 * j);
+        const float4 qb = *reinterpret_cast<const float4*>(qs + 8 * j + 4);
+        const int step = NW * PPW;
+        const int n_pad = (n + step - 1) / step * step;
+        for (int t = warp * PPW + pw; t < n_pad; t += step) {
+            const bool ok = t < n;
             float kf[8];
-            if (t < n) {
-                unpack8(*reinterpret_cast<const int4*>(Ks + (size_t)t * D + 8 * j), kf);
-            } else {
+            unpack8(*reinterpret_cast<const int4*>(Ks + (size_t)(ok ? t : 0) * DP + 8 * j), kf);
+            f2 d = f2_make(__fmul_rn(qa.x, kf[0]));
+            f2_acc(d, __fmul_rn(qa.y, kf[1]));
+            f2_acc(d, __fmul_rn(qa.z, kf[2]));
+            f2_acc(d, __fmul_rn(qa.w, kf[3]));
+            f2_acc(d, __fmul_rn(qb.x, kf[4]));
+            f2_acc(d, __fmul_rn(qb.y, kf[5]));
+            f2_acc(d, __fmul_rn(qb.z, kf[6]));
+            f2_acc(d, __fmul_rn(qb.w, kf[7]));
 #pragma unroll
-                for (int e = 0; e < 8; ++e) kf[e] = 0.0f;
+            for (int o = LPT / 2; o > 0; o >>= 1) {
+                f2 r;
+                r.hi = __shfl_xor_sync(0xffffffffu, d.hi, o);
+                r.lo = __shfl_xor_sync(0xffffffffu, d.lo, o);
+                d = f2_add(d, r);
             }
-            for (int g = 0; g < G; ++g) {
-                const float4 qa = *reinterpret_cast<const float4*>(qs + g * D + 8 * j);
-                const float4 qb = *reinterpret_cast<const float4*>(qs + g * D + 8 * j + 4);
-                f2 d = f2_make(__fmul_rn(qa.x, kf[0]));
-                f2_acc(d, __fmul_rn(qa.y, kf[1]));
-                f2_acc(d, __fmul_rn(qa.z, kf[2]));
-                f2_acc(d, __fmul_rn(qa.w, kf[3]));
-                f2_acc(d, __fmul_rn(qb.x, kf[4]));
-                f2_acc(d, __fmul_rn(qb.y, kf[5]));
-                f2_acc(d, __fmul_rn(qb.z, kf[6]));
-                f2_acc(d, __fmul_rn(qb.w, kf[7]));
-#pragma unroll
-                for (int o = LPT / 2; o > 0; o >>= 1) {
-                    f2 r;
-                    r.hi = __shfl_xor_sync(0xffffffffu, d.hi, o);
-                    r.lo = __shfl_xor_sync(0xffffffffu, d.lo, o);
-                    d = f2_add(d, r);
-                }
-                if (j == 0 && t < n) {
-                    const f2 sv = f2_mul(d, scale);
-                    sc[g * chunk + t] = sv.hi;
-                    sl[g * chunk + t] = sv.lo;
-                }
+            if (j == 0 && ok) {
+                const f2 sv = f2_mul(d, scale);
+                sc[t] = sv.hi;
+                sl[t] = sv.lo;
             }
         }
     }
-    attn_sync();
+    attn_sync<NT>();
 
-    // softmax over the chunk, per head: p_t = exp(s_t - m), l = sum p_t
-    for (int g = warp; g < G; g += kAttnWarps) {
+    // softmax over the chunk: p_t = exp(s_t - m), l = sum p_t (warp 0)
+    if (warp == 0) {
         f2 m = {-INFINITY, 0.0f};
-        for (int t = lane; t < n; t += 32) m = f2_max(m, f2{sc[g * chunk + t], sl[g * chunk + t]});
+        for (int t = lane; t < n; t += 32) m = f2_max(m, f2{sc[t], sl[t]});
         m = warp_max_f2(m);
         f2 l = {0.0f, 0.0f};
         for (int t = lane; t < n; t += 32) {
-            const f2 e = f2_exp(f2_sub(f2{sc[g * chunk + t], sl[g * chunk + t]}, m));
-            sc[g * chunk + t] = e.hi;
-            sl[g * chunk + t] = e.lo;
+            const f2 e = f2_exp(f2_sub(f2{sc[t], sl[t]}, m));
+            sc[t] = e.hi;
+            sl[t] = e.lo;
             l = f2_add(l, e);
         }
         l = warp_sum_f2(l);
         if (lane == 0) {
-            stat[4 * g] = m.hi;
-            stat[4 * g + 1] = m.lo;
-            stat[4 * g + 2] = l.hi;
-            stat[4 * g + 3] = l.lo;
+            stat[0] = m.hi;
+            stat[1] = m.lo;
+            stat[2] = l.hi;
+            stat[3] = l.lo;
         }
     }
-    attn_sync();
+    attn_sync<NT>();
 
-    // P.V: thread = (column pair, token group)
-    constexpr int CP = D / 2;
-    constexpr int NTG = kAttnThreads / CP;
-    const int cp = tid % CP, tg = tid / CP;
-    f2 o[kGMax][2];
+    // P.V: TG consecutive lanes share a column pair and split the tokens;
+    // their sums are combined with shuffles
+    {
+        constexpr int CP = D / 2;
+        constexpr int TG = NT / CP;
+        static_assert(TG >= 1 && TG <= 32 && (TG & (TG - 1)) == 0, "token groups");
+        const int cp = tid / TG, tg = tid % TG;
+        f2 o0 = {0.0f, 0.0f}, o1 = {0.0f, 0.0f};
+        for (int t = tg; t < n; t += TG) {
+            const float2 v = __bfloat1622float2(
+                *reinterpret_cast<const __nv_bfloat162*>(Vs + (size_t)t * DP + 2 * cp));
+            const f2 pr = {sc[t], sl[t]};
+            o0 = f2_add(o0, f2_mulf(pr, v.x));
+            o1 = f2_add(o1, f2_mulf(pr, v.y));
+        }
 #pragma unroll
-    for (int g = 0; g < kGMax; ++g) o[g][0] = o[g][1] = f2{0.0f, 0.0f};
-    for (int t = tg; t < n; t += NTG) {
-        const float2 v = __bfloat1622float2(
-            *reinterpret_cast<const __nv_bfloat162*>(Vs + (size_t)t * D + 2 * cp));
-#pragma unroll
-        for (int g = 0; g < kGMax; ++g) {
-            if (g < G) {
-                const f2 pr = {sc[g * chunk + t], sl[g * chunk + t]};
-                o[g][0] = f2_add(o[g][0], f2_mulf(pr, v.x));
-                o[g][1] = f2_add(o[g][1], f2_mulf(pr, v.y));
+        for (int o = TG / 2; o > 0; o >>= 1) {
+            f2 r;
+            r.hi = __shfl_xor_sync(0xffffffffu, o0.hi, o);
+            r.lo = __shfl_xor_sync(0xffffffffu, o0.lo, o);
+            o0 = f2_add(o0, r);
+            r.hi = __shfl_xor_sync(0xffffffffu, o1.hi, o);
+            r.lo = __shfl_xor_sync(0xffffffffu, o1.lo, o);
+            o1 = f2_add(o1, r);
+        }
+        if (tg == 0) {
+            const f2 l = {stat[2], stat[3]};
+            if (single) {
+                bf16* out = p.out + ((size_t)b * p.Hq + h) * D + 2 * cp;
+                out[0] = n > 0 ? f2_to_bf16(f2_div(o0, l)) : __float2bfloat16_rn(0.0f);
+                out[1] = n > 0 ? f2_to_bf16(f2_div(o1, l)) : __float2bfloat16_rn(0.0f);
+            } else {
+                // partial: o (hi, lo planes), then m and l pairs
+                float* pp = p.part + (((size_t)b * p.Hq + h) * splits + split) * (2 * D + 4);
+                pp[2 * cp] = n > 0 ? o0.hi : 0.0f;
+                pp[2 * cp + 1] = n > 0 ? o1.hi : 0.0f;
+                pp[D + 2 * cp] = n > 0 ? o0.lo : 0.0f;
+                pp[D + 2 * cp + 1] = n > 0 ? o1.lo : 0.0f;
+                if (cp == 0) {
+                    pp[2 * D] = n > 0 ? stat[0] : -INFINITY;
+                    pp[2 * D + 1] = n > 0 ? stat[1] : 0.0f;
+                    pp[2 * D + 2] = n > 0 ? l.hi : 0.0f;
+                    pp[2 * D + 3] = n > 0 ? l.lo : 0.0f;
+                }
             }
         }
     }
-    attn_sync();   // every thread is done with V: the tiles become the reduction buffer
-    // red: [NTG][kGMax][2][D] (hi plane, lo plane)
-#pragma unroll
-    for (int g = 0; g < kGMax; ++g) {
-        if (g < G) {
-            float* r = red + ((size_t)tg * kGMax + g) * 2 * D;
-            r[2 * cp] = o[g][0].hi;
-            r[2 * cp + 1] = o[g][1].hi;
-            r[D + 2 * cp] = o[g][0].lo;
-            r[D + 2 * cp + 1] = o[g][1].lo;
+    if (!single && p.tickets) {
+        // the last CTA of this (request, query head) to finish combines the
+        // partials (no CTA waits for another)
+        __threadfence();
+        attn_sync<NT>();
+        if (tid == 0) {
+            unsigned* tk = p.tickets + (size_t)b * p.Hq + h;
+            const unsigned prev = atomicAdd(tk, 1u);
+            *s_flag = prev == (unsigned)(active - 1);
+            if (*s_flag) *tk = 0u;   // ready for the next launch
         }
-    }
-    attn_sync();
-    for (int i = tid; i < G * D; i += kAttnThreads) {
-        const int g = i / D, d = i - g * D;
-        f2 acc = {0.0f, 0.0f};
+        attn_sync<NT>();
+        if (*s_flag) {
+            __threadfence();
+            // split weights and the active splits (warp 0), in the tile region
+            float* cw = reinterpret_cast<float*>(smem);            // [splits][2]
+            float* cl = cw + 2 * kMaxInKernelSplits;               // [2]
+            int* act = reinterpret_cast<int*>(cl + 2);             // [splits]
+            int* nact = act + kMaxInKernelSplits;                  // [1]
+            const float* pb = p.part + ((size_t)b * p.Hq + h) * splits * (2 * D + 4);
+            if (warp == 0) combine_weights<D>(pb, active, cw, cl, lane, act, nact);
+            attn_sync<NT>();
+            constexpr int KA = 4;   // active splits per round of loads
+            for (int d = tid; d < D; d += NT) {
+                f2 acc = {0.0f, 0.0f};
+                for (int k0 = 0; k0 < *nact; k0 += KA) {
+                    float oh[KA], ol[KA];
 #pragma unroll
-        for (int q = 0; q < NTG; ++q) {
-            const float* r = red + ((size_t)q * kGMax + g) * 2 * D;
-            acc = f2_add(acc, f2{r[d], r[D + d]});
-        }
-        const int h = kvh * G + g;
-        const f2 l = {stat[4 * g + 2], stat[4 * g + 3]};
-        if (splits == 1) {
-            p.out[((size_t)b * p.Hq + h) * D + d] =
-                n > 0 ? f2_to_bf16(f2_div(acc, l)) : __float2bfloat16_rn(0.0f);
-        } else {
-            // partial: o (hi, lo planes), then m and l pairs
-            float* pp = p.part + (((size_t)b * p.Hq + h) * splits + split) * (2 * D + 4);
-            pp[d] = n > 0 ? acc.hi : 0.0f;
-            pp[D + d] = n > 0 ? acc.lo : 0.0f;
-            if (d == 0) {
-                pp[2 * D] = n > 0 ? stat[4 * g] : -INFINITY;
-                pp[2 * D + 1] = n > 0 ? stat[4 * g + 1] : 0.0f;
-                pp[2 * D + 2] = n > 0 ? l.hi : 0.0f;
-                pp[2 * D + 3] = n > 0 ? l.lo : 0.0f;
+                    for (int k = 0; k < KA; ++k) {
+                        oh[k] = ol[k] = 0.0f;
+                        if (k0 + k < *nact) {
+                            const float* q = pb + (size_t)act[k0 + k] * (2 * D + 4);
+                            oh[k] = __ldcg(q + d);
+                            ol[k] = __ldcg(q + D + d);
+                        }
+                    }
+#pragma unroll
+                    for (int k = 0; k < KA; ++k) {
+                        if (k0 + k < *nact) {
+                            const int sp = act[k0 + k];
+                            acc = f2_add(acc, f2_mul(f2{oh[k], ol[k]}, f2{cw[2 * sp], cw[2 * sp + 1]}));
+                        }
+                    }
+                }
+                const f2 l = {cl[0], cl[1]};
+                p.out[((size_t)b * p.Hq + h) * D + d] =
+                    l.hi > 0.0f ? f2_to_bf16(f2_div(acc, l)) : __float2bfloat16_rn(0.0f);
             }
         }
     }
-    attn_sync();   // the shared tiles may be reused by the caller afterwards
-}
-
-// Combine of split-KV partials for (request b, query head h, element d), in
-// two-float arithmetic: O = sum_s o_s e^{m_s - M} / sum_s l_s e^{m_s - M}.
-template <int D>
-__device__ __forceinline__ void attn_combine_elem(const float* part, int splits, int Hq, int b,
-                                                  int h, int d, bf16* out) {
-    constexpr int S = 2 * D + 4;
-    const float* pp = part + ((size_t)b * Hq + h) * splits * S;
-    f2 M = {-INFINITY, 0.0f};
-    for (int s = 0; s < splits; ++s)
-        M = f2_max(M, f2{__ldcg(pp + (size_t)s * S + 2 * D), __ldcg(pp + (size_t)s * S + 2 * D + 1)});
-    f2 L = {0.0f, 0.0f}, acc = {0.0f, 0.0f};
-    if (M.hi != -INFINITY) {
-        for (int s = 0; s < splits; ++s) {
-            const float* q = pp + (size_t)s * S;
-            const f2 m = {__ldcg(q + 2 * D), __ldcg(q + 2 * D + 1)};
-            if (m.hi == -INFINITY) continue;
-            const f2 w = f2_exp(f2_sub(m, M));
-            L = f2_add(L, f2_mul(f2{__ldcg(q + 2 * D + 2), __ldcg(q + 2 * D + 3)}, w));
-            acc = f2_add(acc, f2_mul(f2{__ldcg(q + d), __ldcg(q + D + d)}, w));
-        }
-    }
-    out[((size_t)b * Hq + h) * D + d] =
-        L.hi > 0.0f ? f2_to_bf16(f2_div(acc, L)) : __float2bfloat16_rn(0.0f);
+    attn_sync<NT>();   // the shared tiles may be reused by the caller afterwards
 }
 
 }  // namespace a8w8

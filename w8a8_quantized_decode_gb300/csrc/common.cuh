@@ -242,7 +242,7 @@ __device__ __forceinline__ f2 f2_rsqrt(f2 s) {
 // exp(r) = (1 + p)^(2^8) with p = expm1(r / 2^8) from its Taylor series to
 // the fourth power, squared eight times in expm1 form (1 + p)^2 = 1 + (2p +
 // p^2); then scaled by 2^k.
-__device__ __forceinline__ f2 f2_exp(f2 x) {
+static __device__ __noinline__ f2 f2_exp(f2 x) {
     if (x.hi < -104.0f) return f2{0.0f, 0.0f};
     if (x.hi > 88.5f) return f2{INFINITY, 0.0f};
     const float k = rintf(__fmul_rn(x.hi, 1.44269504088896341f));
@@ -253,7 +253,7 @@ __device__ __forceinline__ f2 f2_exp(f2 x) {
     const float t3 = __fmul_rn(t2.hi, t.hi);
     const float tail = __fmaf_rn(__fmul_rn(t3, t.hi), 1.0f / 24.0f, __fmul_rn(t3, 1.0f / 6.0f));
     f2 p = f2_addf(f2_add(t, f2{__fmul_rn(t2.hi, 0.5f), __fmul_rn(t2.lo, 0.5f)}), tail);
-#pragma unroll
+#pragma unroll 1
     for (int i = 0; i < 8; ++i) p = f2_add(f2{__fmul_rn(p.hi, 2.0f), __fmul_rn(p.lo, 2.0f)}, f2_mul(p, p));
     const f2 e = f2_addf(p, 1.0f);
     const int ki = (int)k;

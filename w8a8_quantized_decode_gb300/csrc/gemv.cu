@@ -135,6 +135,8 @@ __global__ void __launch_bounds__(kGenThreads, 1) gemv_kernel(const GemvParams p
     pdl_wait();
     pdl_trigger();
 
+    if (p.clear && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < p.clear_n; i += blockDim.x) p.clear[i] = 0u;
     for (int i = threadIdx.x; i < acc_n; i += blockDim.x) accs[i] = 0;
     int4 nwr[1];
     prologue<BT, PRO, 1>(p, act, xs, red, L.stage ? reinterpret_cast<bf16*>(smem + L.stage) : nullptr,

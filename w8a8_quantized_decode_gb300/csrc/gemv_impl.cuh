@@ -441,6 +441,8 @@ __device__ __forceinline__ bool stream_gemv(const GemvParams& p, unsigned char* 
         return false;
     }
 
+    if (p.clear && blockIdx.x == 0)
+        for (int i = threadIdx.x; i < p.clear_n; i += NT) p.clear[i] = 0u;
     // the residual (written by an earlier kernel) is read right after the wait
     float resv = 0.0f;
     if (EPI == EPI_STORE && mine && p.residual) {

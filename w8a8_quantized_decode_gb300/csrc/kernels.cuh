@@ -52,6 +52,8 @@ struct GemvParams {
     int8_t* tap_q;          // [M, K]
     float* tap_s;           // [M]
     unsigned* err;          // device error word (timeouts)
+    unsigned* clear;        // CTA 0 zeroes clear[0, clear_n) after the wait (or null)
+    int clear_n;
 };
 
 // Largest batch tile one launch handles; bigger batches are tiled by the host.
@@ -87,15 +89,20 @@ struct AttnParams {
     float scale_lo;
     bf16* out;              // [B, Hq*D]
     float* part;            // split partials, [B, Hq, splits, 2 D + 4]
+    unsigned* tickets;      // [B, Hq] zero on entry, or null (separate combine kernel)
     unsigned* err;
     bf16* tap_q_rot;        // [B, Hq, D] or null
     bf16* tap_k_rot;        // [B, Hkv, D] or null
 };
 
 // Tokens per attention CTA and the number of CTAs per (request, KV head).
-int attn_chunk(int max_ctx);
-int attn_splits(int max_ctx);
-size_t attn_part_bytes(int B, int Hq, int D, int max_ctx);
+// Token chunk per attention CTA and chunks per request. `combine_in_kernel`:
+// the decode-layer form (small chunks; the last CTA of each (request, KV
+// head) combines the partials, counted on AttnParams::tickets); otherwise
+// the standalone form (large chunks, separate combine kernel).
+int attn_chunk(int max_ctx, bool combine_in_kernel);
+int attn_splits(int max_ctx, bool combine_in_kernel);
+size_t attn_part_bytes(int B, int Hq, int D, int max_ctx, bool combine_in_kernel);
 cudaError_t launch_attention(const AttnParams& p, const Launch& L);
 
 // ---------------------------------------------------------------------------

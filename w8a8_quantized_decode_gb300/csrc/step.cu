@@ -98,14 +98,12 @@ __device__ __forceinline__ bool gemv_phase(const GemvParams& g, unsigned char* s
 template <int D>
 __device__ __forceinline__ void attn_phase(const AttnParams& a, int chunk, int splits,
                                         unsigned char* smem) {
-    const int items = a.B * a.Hkv * splits;
-    if (threadIdx.x < kAttnThreads) {
-        for (int it = blockIdx.x; it < items; it += gridDim.x) {
-            const int split = it % splits;
-            const int kvh = (it / splits) % a.Hkv;
-            const int b = it / (splits * a.Hkv);
-            attn_item<D>(a, chunk, splits, split, kvh, b, smem, false);
-        }
+    const int items = a.B * a.Hq * splits;
+    for (int it = blockIdx.x; it < items; it += gridDim.x) {
+        const int split = it % splits;
+        const int h = (it / splits) % a.Hq;
+        const int b = it / (splits * a.Hq);
+        attn_item<D, kStepThreads>(a, chunk, splits, split, h, b, smem, false);
     }
 }
 
@@ -231,10 +229,18 @@ __global__ void __launch_bounds__(kStepThreads, 1) step_kernel(const __grid_cons
                 if (ok && splits > 1) {
                     ok = grid_sync(P.bar, &k, P.err, &s_ok);
                     if (ok) {
-                        const int total = P.B * P.Hq * D;
-                        for (int i = cta * kStepThreads + threadIdx.x; i < total; i += G * kStepThreads) {
-                            const int d = i % D, h = (i / D) % P.Hq, b = i / (D * P.Hq);
-                            attn_combine_elem<D>(P.part, splits, P.Hq, b, h, d, P.attn);
+                        // one (request, query head) per CTA at a time: split
+                        // weights by warp 0 (shared memory), then D elements
+                        float* cw = reinterpret_cast<float*>(smem);
+                        const int lane = threadIdx.x & 31;
+                        for (int r = cta; r < P.B * P.Hq; r += G) {
+                            const float* pp = P.part + (size_t)r * splits * (2 * D + 4);
+                            __syncthreads();
+                            if (threadIdx.x < 32) combine_weights<D>(pp, splits, cw, cw + 2 * splits, lane);
+                            __syncthreads();
+                            if ((int)threadIdx.x < D)
+                                P.attn[(size_t)r * D + threadIdx.x] =
+                                    combine_elem<D>(pp, splits, cw, cw + 2 * splits, threadIdx.x);
                         }
                     }
                 }
