@@ -101,7 +101,7 @@ __device__ __forceinline__ void load_head_pre(const AttnParams& p, int pos, int 
 // output correctly rounded to BF16 (see f2): x and its partner are exact
 // floats, cos / sin hi + lo pairs.
 template <int D>
-__device__ __noinline__ void norm_rope_head(float (&x)[D / 32], const float (&w)[D / 32],
+__device__ __forceinline__ void norm_rope_head(float (&x)[D / 32], const float (&w)[D / 32],
                                                const HeadPre<D>& hp, float eps, int lane,
                                                float (&y)[D / 32]) {
     constexpr int E = D / 32;
