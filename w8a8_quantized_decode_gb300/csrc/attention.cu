@@ -8,24 +8,13 @@
 // issue #52), "Current behavior": the decode layer normalises Q and K per head
 // and applies RoPE before attention ("fused QK norm path").
 //
-// One CTA handles one (request, KV head, token chunk). It serves the whole GQA
-// group of Hq/Hkv query heads, so every cached K/V byte is read once.
-//   1. Before griddepcontrol.wait: the chunk's cached K and V rows (earlier
-//      tokens, immutable during this kernel's predecessors) are copied into
-//      shared memory with cp.async, so the KV read overlaps the tail of the
-//      QKV projection.
-//   2. Fused prologue (decode layer): per-head RMSNorm of the G query heads
-//      and of the new K head (float32, rounded to BF16), rotate-half RoPE at
-//      position ctx_len - 1 from a cos/sin table (rounded to BF16); the CTA
-//      whose chunk holds the new token writes K/V into the cache slot and
-//      into its shared tiles.
-//   3. Scores: D/8 lanes per token, 8 BF16 of K per lane, the G query heads
-//      in registers, reduced over the lane group with shuffles.
-//   4. Softmax per head over the chunk (max-subtracted, float32).
-//   5. P.V with column pairs per thread, reduced over token groups.
-//   6. One chunk: normalise and write BF16. Several chunks: write float32
-//      partials (unnormalised o, running max m, sum l) and combine them in a
-//      second kernel: O = sum_s o_s e^{m_s - M} / sum_s l_s e^{m_s - M}.
+// One CTA (256 threads) handles one (request, query head, token chunk); the
+// device body and its arithmetic are described in attn_impl.cuh. Grid:
+// (chunks, Hq, B). Decode layer: 64-token chunks (longer for contexts beyond
+// 4096 tokens), only the chunks holding tokens run, and the last CTA of a
+// (request, head) combines the partials (tickets in the workspace). The
+// standalone entry uses 256/128-token chunks and a separate combine kernel
+// (one CTA per query head and request).
 #include "attn_impl.cuh"
 
 namespace a8w8 {

@@ -1,5 +1,5 @@
 // attn_impl.cuh -- body of the paged GQA decode attention for one work item
-// (request b, KV head kvh, token chunk `split`), shared by the standalone
+// (request b, query head h, token chunk `split`), shared by the standalone
 // attention kernel and the persistent decode-step kernel.
 //
 // "perf(qwen3-a8w8): optimize decode scheduling and data paths" (pypto-lib PR
@@ -10,22 +10,24 @@
 // issue #52), "Current behavior": Q and K are normalised per head and rotated
 // (RoPE) before attention.
 //
-// The item runs on the first kAttnThreads threads of the CTA and synchronises
-// with named barrier 1, so that the rest of a larger CTA may skip it. It
-// serves the whole GQA group of Hq/Hkv query heads, so every cached K/V byte is
-// read once:
-//   1. the chunk's cached K and V rows (earlier tokens) are copied into shared
-//      memory with cp.async (in the standalone kernel before
-//      griddepcontrol.wait, so the KV read overlaps the previous kernel);
-//   2. fused prologue: per-head RMSNorm of the query heads and of the new K
-//      head (float32, rounded to BF16), rotate-half RoPE at position
-//      ctx_len - 1 from a cos/sin table (rounded to BF16); the item whose chunk
-//      holds the new token writes K/V into the cache slot and its tiles;
-//   3. scores: D/8 lanes per token, 8 BF16 of K per lane, reduced over the
-//      lane group with shuffles; 4. float32 max-subtracted softmax per head;
-//   5. P.V with column pairs per thread, reduced over token groups;
-//   6. one chunk: normalise and write BF16; several chunks: write float32
-//      partials (unnormalised o, running max m, sum l) for the combine pass:
+// The item runs on the first NT threads of the CTA and synchronises with
+// named barrier 1, so that the rest of a larger CTA may skip it:
+//   1. the chunk's cached K and V rows of KV head h / (Hq/Hkv) (earlier
+//      tokens) are copied into shared memory with cp.async, together with the
+//      norm weights and the RoPE row, before griddepcontrol.wait in the
+//      standalone kernel, so these reads overlap the previous kernel;
+//   2. fused prologue: per-head RMSNorm of the query head (warp 0) and of the
+//      new K head (warp 1), rotate-half RoPE at position ctx_len - 1, each
+//      result correctly rounded to BF16; the group's first head writes the
+//      new K/V into the cache slot, every item into its own tiles;
+//   3. scores: D/8 lanes per token, products of BF16 values exact in float32,
+//      summed as two-float pairs and reduced over the lane group with
+//      shuffles; 4. max-subtracted softmax with a two-float exp;
+//   5. P.V: lanes of a column pair split the tokens, two-float sums combined
+//      with shuffles;
+//   6. one chunk: normalise and write BF16; several chunks: write two-float
+//      partials (unnormalised o, running max m, sum l) that the last chunk's
+//      CTA (or a combine kernel) merges:
 //      O = sum_s o_s e^{m_s - M} / sum_s l_s e^{m_s - M}.
 #pragma once
 
