@@ -29,9 +29,9 @@
 //     weights never depend on it.
 //   * A prologue then quantises the activation rows (redundantly in every
 //     CTA, from L2, staged once in shared memory when they fit): optional
-//     RMSNorm (float32, rounded to BF16), absmax, INT8 codes into shared
-//     memory; the stream multiplies with dp4a in two independent chains, and
-//     a float32 dequantisation epilogue finishes.
+//     RMSNorm (two-float, correctly rounded to BF16), absmax, INT8 codes into
+//     shared memory; the stream multiplies with dp4a in two independent
+//     chains, and a float32 dequantisation epilogue finishes.
 #pragma once
 
 #include "kernels.cuh"

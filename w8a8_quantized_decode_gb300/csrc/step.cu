@@ -1,6 +1,6 @@
 // step.cu -- the whole decode step as one persistent cooperative kernel.
 //
-// One CTA per SM (1024 threads) runs, in order: the embedding gather, for
+// One CTA per SM (512 threads) runs, in order: the embedding gather, for
 // every layer the QKV projection (input RMSNorm + quantisation prologue), the
 // fused QK-norm / RoPE / KV-write / paged attention, the O projection +
 // residual, the Gate/Up projection + SwiGLU and the split-K down projection +
