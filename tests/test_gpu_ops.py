@@ -77,6 +77,11 @@ LINEAR_CASES = [
     (8, 5120, 1000, 1, True),
     (16, 17408, 300, 2, True),     # batch tiles of 4
     (11, 4128, 97, 2, False),      # K not a multiple of 512
+    # tensor-core form (3..16 rows per launch)
+    (16, 5120, 7168, 1, False),    # QKV at batch 16
+    (13, 17408, 5120, 2, True),    # down at batch 13: split halves of 136 steps
+    (17, 5120, 5120, 1, True),     # two launches (16 + 1 rows)
+    (4, 64, 9, 1, True),           # one K step, fewer rows than one 8-row group
 ]
 
 
@@ -108,19 +113,24 @@ def test_linear_residual_in_place(a8w8):
     assert np.array_equal(to_host(hd), oy)
 
 
-def test_linear_extreme_values_no_overflow(a8w8):
+@pytest.mark.parametrize("M,xv,wv", [(1, 127, 127), (16, 127, 127), (16, -128, -128)])
+def test_linear_extreme_values_no_overflow(a8w8, M, xv, wv):
+    # the largest products; with M >= 3 the tensor-core form sums up to 1024 of
+    # them in float32 (|sum| <= 2^24, still exact) before converting to INT32
     K, N = 17408, 160
-    xq = np.full((1, K), 127, np.int8)
-    W = np.full((N, K), -127, np.int8)
-    W[::2] = 127
-    y, acc = a8w8.a8w8_linear(to_dev(xq), to_dev(np.ones(1, np.float32)), to_dev(W),
+    xq = np.full((M, K), xv, np.int8)
+    W = np.full((N, K), -wv, np.int8) if wv == 127 else np.full((N, K), wv, np.int8)
+    W[::2] = wv
+    xs = np.ones(M, np.float32)
+    y, acc = a8w8.a8w8_linear(to_dev(xq), to_dev(xs), to_dev(W),
                               to_dev(np.full(N, 1e-6, np.float32)), 2, acc_out=True)
-    oy, oacc = oracle.linear(xq, np.ones(1, np.float32), W, np.full(N, 1e-6, np.float32), 2)
+    oy, oacc = oracle.linear(xq, xs, W, np.full(N, 1e-6, np.float32), 2)
     assert np.array_equal(to_host(acc), oacc)
     assert np.array_equal(to_host(y), oy)
 
 
-@pytest.mark.parametrize("M,K,I", [(1, 5120, 17408), (4, 256, 512), (9, 5120, 700)])
+@pytest.mark.parametrize("M,K,I", [(1, 5120, 17408), (4, 256, 512), (9, 5120, 700),
+                                   (16, 256, 17408), (16, 5120, 2000)])
 def test_gate_up_swiglu(a8w8, M, K, I):
     seed = M + K + I
     xq = synth.int8_uniform(seed, (M, K))

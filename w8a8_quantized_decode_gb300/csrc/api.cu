@@ -81,7 +81,7 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Workspace layout shared by the layer and the step.
 struct WsLayout {
-    size_t hid, qkv, attn, act, part, att_tk, keys, ticket, bar, total;
+    size_t hid, qkv, attn, act, qx, qs, part, att_tk, keys, ticket, bar, total;
 };
 
 WsLayout ws_layout(const a8w8_config& c, int B, int max_blocks) {
@@ -97,6 +97,11 @@ WsLayout ws_layout(const a8w8_config& c, int B, int max_blocks) {
     o = round_up(o + (size_t)B * c.num_q_heads * D * 2, 256);
     w.act = o;
     o = round_up(o + (size_t)B * c.intermediate * 2, 256);
+    // INT8 activation rows quantised once for the tensor-core projections
+    w.qx = o;
+    o = round_up(o + (size_t)B * std::max({c.hidden, c.num_q_heads * D, c.intermediate}), 256);
+    w.qs = o;
+    o = round_up(o + (size_t)B * 4, 256);
     w.part = o;
     const int max_ctx = max_blocks * c.page_size;
     o = round_up(o + std::max(attn_part_bytes(B, c.num_q_heads, D, max_ctx, true),
@@ -149,10 +154,44 @@ a8w8_status check_layer_weights(const a8w8_layer_weights* w) {
                       "layer weights");
 }
 
-// Runs a projection over batch tiles.
-cudaError_t run_gemv(int pro, int epi, int ks, GemvParams p, int M, const Launch& L) {
-    const int tile = gemv_max_batch_tile(p.K, ks);
+// Batches of at least this many rows use the tensor-core projection (their
+// activation rows quantised once by a separate kernel); smaller ones the dp4a
+// stream with the quantisation in each CTA's prologue.
+constexpr int kMmaMinBatch = 3;
+
+bool use_mma(int M, int K, int ks) { return M >= kMmaMinBatch && gemv_mma_supported(K, ks); }
+
+// Runs a projection over batch tiles. `qx` / `qs` (room for M rows of K
+// codes and M scales) receive the quantised rows on the tensor-core path.
+cudaError_t run_gemv(int pro, int epi, int ks, GemvParams p, int M, const Launch& L,
+                     int8_t* qx = nullptr, float* qs = nullptr) {
     const int Ntot = (epi == EPI_SWIGLU) ? 2 * p.N : p.N;
+    if (use_mma(M, p.K, ks) && (pro == PRO_I8 || (qx && qs))) {
+        p.err = device_error_word();
+        if (pro != PRO_I8) {
+            GemvParams q = p;
+            q.M = M;
+            cudaError_t e = launch_quant_prep(pro, q, qx, qs, L);
+            if (e != cudaSuccess) return e;
+            p.xq = qx;
+            p.x_scale = qs;
+        }
+        constexpr int tile = 16;
+        for (int b0 = 0; b0 < M; b0 += tile) {
+            GemvParams q = p;
+            q.M = M - b0 < tile ? M - b0 : tile;
+            q.xq = p.xq + (size_t)b0 * p.K;
+            q.x_scale = p.x_scale + b0;
+            if (p.residual) q.residual = p.residual + (size_t)b0 * p.ldy;
+            q.y = p.y + (size_t)b0 * p.ldy;
+            if (p.acc_out) q.acc_out = p.acc_out + (size_t)b0 * Ntot;
+            if (b0) q.clear = nullptr;
+            cudaError_t e = launch_gemv_mma(epi, ks, q, L);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }
+    const int tile = gemv_max_batch_tile(p.K, ks);
     for (int b0 = 0; b0 < M; b0 += tile) {
         GemvParams q = p;
         q.M = M - b0 < tile ? M - b0 : tile;
@@ -185,6 +224,8 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     bf16* act = reinterpret_cast<bf16*>(ws + lay.act);
     float* part = reinterpret_cast<float*>(ws + lay.part);
     unsigned* att_tk = reinterpret_cast<unsigned*>(ws + lay.att_tk);
+    int8_t* qx = reinterpret_cast<int8_t*>(ws + lay.qx);
+    float* qs = reinterpret_cast<float*>(ws + lay.qs);
     const a8w8_layer_taps none = {};
     const a8w8_layer_taps& T = taps ? *taps : none;
 
@@ -205,7 +246,7 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     g.tap_s = T.xs;
     g.clear = att_tk;   // the attention that follows counts its splits there
     g.clear_n = B * Hq;
-    cudaError_t e = run_gemv(PRO_NORM_QUANT, EPI_STORE, 1, g, B, L);
+    cudaError_t e = run_gemv(PRO_NORM_QUANT, EPI_STORE, 1, g, B, L, qx, qs);
     if (e != cudaSuccess) return cuda_fail(e, "QKV projection");
     if (T.qkv) {
         e = cudaMemcpyAsync(T.qkv, qkv, (size_t)B * NQKV * 2, cudaMemcpyDeviceToDevice, L.stream);
@@ -266,7 +307,7 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     g.ldy = H;
     g.tap_q = T.aq;
     g.tap_s = T.as;
-    e = run_gemv(PRO_QUANT, EPI_STORE, 1, g, B, L);
+    e = run_gemv(PRO_QUANT, EPI_STORE, 1, g, B, L, qx, qs);
     if (e != cudaSuccess) return cuda_fail(e, "O projection");
     if (T.h1) {
         e = cudaMemcpyAsync(T.h1, hidden, (size_t)B * H * 2, cudaMemcpyDeviceToDevice, L.stream);
@@ -288,7 +329,7 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     g.tap_x = reinterpret_cast<bf16*>(T.hn);
     g.tap_q = T.hq;
     g.tap_s = T.hs;
-    e = run_gemv(PRO_NORM_QUANT, EPI_SWIGLU, 1, g, B, L);
+    e = run_gemv(PRO_NORM_QUANT, EPI_SWIGLU, 1, g, B, L, qx, qs);
     if (e != cudaSuccess) return cuda_fail(e, "Gate/Up projection");
     if (T.act) {
         e = cudaMemcpyAsync(T.act, act, (size_t)B * I * 2, cudaMemcpyDeviceToDevice, L.stream);
@@ -308,7 +349,7 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     g.ldy = H;
     g.tap_q = T.actq;
     g.tap_s = T.acts;
-    e = run_gemv(PRO_QUANT, EPI_STORE, c.down_k_splits, g, B, L);
+    e = run_gemv(PRO_QUANT, EPI_STORE, c.down_k_splits, g, B, L, qx, qs);
     if (e != cudaSuccess) return cuda_fail(e, "down projection");
     return A8W8_OK;
 }

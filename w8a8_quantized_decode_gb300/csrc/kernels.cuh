@@ -61,6 +61,15 @@ int gemv_max_batch_tile(int K, int k_splits);
 cudaError_t launch_gemv(int prologue, int epilogue, int k_splits, const GemvParams& p,
                         const Launch& L);
 
+// Tensor-core form for batches of up to 16 rows (PRO_I8 input: p.xq and
+// p.x_scale), K a multiple of 64 * k_splits; and the once-per-row
+// quantisation (PRO_QUANT or PRO_NORM_QUANT of p.x, p.M rows) into xq [M, K]
+// and xs [M] that feeds it (taps of p written per row).
+bool gemv_mma_supported(int K, int k_splits);
+cudaError_t launch_gemv_mma(int epilogue, int k_splits, const GemvParams& p, const Launch& L);
+cudaError_t launch_quant_prep(int prologue, const GemvParams& p, int8_t* xq, float* xs,
+                              const Launch& L);
+
 // ---------------------------------------------------------------------------
 // KV write and paged decode attention
 // ---------------------------------------------------------------------------
