@@ -189,3 +189,20 @@ def test_qwen3_14b_layer_b16_long_ctx(a8w8):
     ctx = synth.batched_ctx_lens(106, 16)
     case = synth.decode_layer_case(cfg, 16, list(ctx), seed_base=106)
     _layer_parity(a8w8, cfg, case, max_abs_bar=0.15)
+
+
+def test_tiny_layer_grouped_attention_long_ctx(a8w8):
+    # batch x context above the grouped-attention threshold: one CTA per (row,
+    # KV head, 128-token chunk); contexts of one token, exactly one chunk, one
+    # chunk and a token, and nine chunks, and a padded row
+    cfg = synth.TINY
+    ctx = [1, 17, 128, 129, 500, 1024, 1025, 1100]
+    case = synth.decode_layer_case(cfg, 8, ctx, seed_base=107, padded_rows=(2,))
+    _layer_parity(a8w8, cfg, case)
+
+
+def test_qwen3_14b_layer_grouped_attention_b2(a8w8):
+    # two rows, 4096 and 2049 tokens: 33 and 17 chunks merged in the kernel
+    cfg = dict(synth.QWEN3_14B, num_layers=1)
+    case = synth.decode_layer_case(cfg, 2, [4096, 2049], seed_base=108)
+    _layer_parity(a8w8, cfg, case)

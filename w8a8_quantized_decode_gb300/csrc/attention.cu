@@ -139,8 +139,14 @@ size_t attn_part_bytes(int B, int Hq, int D, int max_ctx, bool combine_in_kernel
     return (size_t)B * Hq * s * (2 * D + 4) * sizeof(float);
 }
 
+// Decode-layer attention over at least this many (request, cached token)
+// slots of the launch shape uses the grouped form (attn_group.cu).
+constexpr long kGroupMinWork = 8192;
+
 cudaError_t launch_attention(const AttnParams& p, const Launch& L) {
     if (p.B == 0) return cudaSuccess;
+    if ((long)p.B * p.max_blocks * p.page >= kGroupMinWork && attn_group_supported(p))
+        return launch_attn_group(p, L);
     if (p.D == 128) return launch_attn_d<128>(p, L);
     if (p.D == 64) return launch_attn_d<64>(p, L);
     return cudaErrorInvalidValue;

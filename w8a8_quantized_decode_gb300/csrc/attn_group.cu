@@ -1,0 +1,405 @@
+// attn_group.cu -- paged GQA decode attention for large batches and long
+// contexts: one CTA per (request, KV head, 128-token chunk) serving every
+// query head of the group.
+//
+// Same method and arithmetic as attn_impl.cuh ("perf(qwen3-a8w8): optimize
+// decode scheduling and data paths", pypto-lib PR #810, "BF16 KV cache";
+// "[Feature] Add native Qwen3-14B A8W8 serving path", pypto-serving issue #52,
+// "Current behavior": per-head QK RMSNorm and RoPE before attention): scores
+// q.k / sqrt(D) of BF16 operands, max-subtracted softmax, P.V, all evaluated
+// in two-float arithmetic so that the BF16 output is the correctly rounded
+// value of the real-valued result.
+//
+// Why a second form: with two-float arithmetic attention is ALU bound. The
+// per-query-head form (attn_impl.cuh) suits batch-1 decode (many small CTAs,
+// short latency); at batch 16 and contexts of thousands of tokens it spends
+// most of its instructions on shuffle reductions, a one-warp softmax and
+// staging every K/V tile once per query head. Here:
+//   * the K/V tile of the chunk is staged once for the G = Hq / Hkv query
+//     heads of the KV head (cp.async, before the dependency wait);
+//   * scores: one lane per token, the lane's K row read from shared memory
+//     8 columns at a time and multiplied with the query rows (broadcast
+//     reads) of the warp's heads; products of BF16 values are exact in
+//     float32 and summed as (hi, lo) pairs (TwoSum), with no reduction;
+//   * softmax: one warp per head;
+//   * P.V: thread (column pair, token group) accumulates all heads of the
+//     group, each term p * v as an exact product pair added by TwoSum with
+//     the low parts summed separately (Ogita, Rump and Oishi's Dot2), then
+//     the token groups are combined with shuffles;
+//   * more than one chunk: two-float partials (o, m, l) per head, merged by
+//     the last CTA of the (request, KV head) to finish (atomic ticket).
+#include "attn_impl.cuh"
+
+namespace a8w8 {
+
+namespace {
+
+constexpr int kGrpThreads = 256;
+constexpr int kGrpChunk = 128;
+constexpr int kGrpMaxG = 7;          // query heads per KV head served here
+constexpr int kGrpMaxSplits = 64;    // chunks per request (in-kernel combine)
+
+struct GrpSmem {
+    size_t tiles, q, sc, sl, stat, blk, flag, total;
+};
+__host__ __device__ inline GrpSmem grp_smem(int D) {
+    GrpSmem s;
+    s.tiles = 0;
+    const size_t kv = (size_t)2 * kGrpChunk * (D + kTilePad) * 2;
+    // combine scratch reuses the tiles: per head 2*splits weights, 2 for L,
+    // splits active indices and their count
+    const size_t comb = (size_t)kGrpMaxG * (2 * kGrpMaxSplits + 2 + kGrpMaxSplits + 1) * 4;
+    s.q = kv > comb ? kv : comb;                         // [G][D] float
+    s.sc = s.q + (size_t)kGrpMaxG * D * 4;               // [G][chunk] hi
+    s.sl = s.sc + (size_t)kGrpMaxG * kGrpChunk * 4;      // [G][chunk] lo
+    s.stat = s.sl + (size_t)kGrpMaxG * kGrpChunk * 4;    // [G][4]: m hi, m lo, l hi, l lo
+    s.blk = s.stat + (size_t)kGrpMaxG * 4 * 4;           // [chunk] physical block per token
+    s.flag = s.blk + (size_t)kGrpChunk * 4;
+    s.total = s.flag + 16;
+    return s;
+}
+
+// acc += p * v with p a pair and v a float: the product's high part is added
+// by TwoSum, its rounding error, p.lo * v and the TwoSum error go to acc.lo
+// (no renormalisation per term).
+__device__ __forceinline__ void dot2_acc(f2& acc, const f2 p, float v) {
+    const float h = __fmul_rn(p.hi, v);
+    const float e = __fmaf_rn(p.hi, v, -h);
+    float s, err;
+    two_sum(acc.hi, h, s, err);
+    acc.hi = s;
+    acc.lo = __fadd_rn(acc.lo, __fadd_rn(err, __fmaf_rn(p.lo, v, e)));
+}
+
+template <int D>
+__global__ void __launch_bounds__(kGrpThreads) attn_group_kernel(const AttnParams p, int splits) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    constexpr int NT = kGrpThreads, NW = NT / 32, C = kGrpChunk;
+    constexpr int DP = D + kTilePad;
+    constexpr int RV = D / 8;         // 16-byte vectors per row
+    constexpr int E = D / 32;
+    const GrpSmem L = grp_smem(D);
+    bf16* Ks = reinterpret_cast<bf16*>(smem + L.tiles);
+    bf16* Vs = Ks + (size_t)C * DP;
+    float* qs = reinterpret_cast<float*>(smem + L.q);
+    float* sc = reinterpret_cast<float*>(smem + L.sc);
+    float* sl = reinterpret_cast<float*>(smem + L.sl);
+    float* stat = reinterpret_cast<float*>(smem + L.stat);
+    int* blk = reinterpret_cast<int*>(smem + L.blk);
+    int* s_flag = reinterpret_cast<int*>(smem + L.flag);
+
+    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int G = p.Hq / p.Hkv;
+    const int h0 = kvh * G;
+    const int t0 = split * C;
+    const int max_ctx = p.max_blocks * p.page;
+    const int ctx_raw = p.ctx_lens[b];
+    const bool bad_ctx = ctx_raw < 0 || ctx_raw > max_ctx;
+    const int pos = ctx_raw - 1;
+    const bool bad_pos = !bad_ctx && ctx_raw > 0 && pos >= p.max_pos;
+    const int ctx = (bad_ctx || bad_pos) ? 0 : ctx_raw;
+    const int n = max(min(t0 + C, ctx) - t0, 0);
+    const bool covers_new = ctx > 0 && pos >= t0 && pos < t0 + C;
+    const int n_old = covers_new ? n - 1 : n;
+    const int active = max(1, (ctx + C - 1) / C);
+    if (split >= active) return;   // the whole CTA, before any barrier
+    const bool single = active == 1;
+
+    // physical block of every cached token of the chunk
+    if (tid == 0) *s_flag = 0;
+    for (int t = tid; t < n_old; t += NT) {
+        const int tok = t0 + t;
+        const int bk = p.block_table[(size_t)b * p.max_blocks + tok / p.page];
+        blk[t] = (bk < 0 || bk >= p.num_blocks) ? -1 : bk;
+    }
+    __syncthreads();
+    for (int i = tid; i < n_old * RV; i += NT) {
+        const int t = i / RV, c = i - t * RV;
+        const int bk = blk[t];
+        if (bk < 0) {
+            *reinterpret_cast<int4*>(Ks + (size_t)t * DP + 8 * c) = make_int4(0, 0, 0, 0);
+            *reinterpret_cast<int4*>(Vs + (size_t)t * DP + 8 * c) = make_int4(0, 0, 0, 0);
+            *s_flag = 1;
+            continue;
+        }
+        const int tok = t0 + t;
+        const size_t off = (((size_t)bk * p.page + tok % p.page) * p.Hkv + kvh) * D + 8 * c;
+        cp_async16(Ks + (size_t)t * DP + 8 * c, p.k_cache + off);
+        cp_async16(Vs + (size_t)t * DP + 8 * c, p.v_cache + off);
+    }
+    cp_async_commit();
+    // warps 0..G-1: query heads; warp G: the new token's K and V
+    const bool qwarp = warp < G;
+    const bool kwarp = warp == G && covers_new;
+    HeadPre<D> hp;
+    if (n > 0 && (qwarp || kwarp)) load_head_pre<D>(p, pos < p.max_pos ? pos : 0, lane, hp);
+
+    pdl_wait();
+    pdl_trigger();
+
+    if (tid == 0) {
+        if (bad_ctx) set_error(p.err, 0x4u);
+        if (bad_pos) set_error(p.err, 0x10u);
+    }
+    if (n > 0 && qwarp) {
+        const int h = h0 + warp;
+        float x[E], y[E];
+        load_bf16_lane<D>(p.q + (size_t)b * p.q_stride + (size_t)h * D + lane * E, x);
+        norm_rope_head<D>(x, hp.qw, hp, p.eps, lane, y);
+#pragma unroll
+        for (int e = 0; e < E; ++e) qs[warp * D + lane * E + e] = y[e];
+        if (p.tap_q_rot && split == 0) {
+#pragma unroll
+            for (int e = 0; e < E; ++e)
+                p.tap_q_rot[((size_t)b * p.Hq + h) * D + lane * E + e] = f2bf(y[e]);
+        }
+    } else if (n > 0 && kwarp) {
+        const int NQ = p.Hq * D, NK = p.Hkv * D;
+        const bf16* row = p.q + (size_t)b * p.q_stride;
+        float x[E], vv[E], y[E];
+        load_bf16_lane<D>(row + NQ + (size_t)kvh * D + lane * E, x);
+        load_bf16_lane<D>(row + NQ + NK + (size_t)kvh * D + lane * E, vv);
+        norm_rope_head<D>(x, hp.kw, hp, p.eps, lane, y);
+        const int tr = pos - t0;
+        const long slot = p.slot_mapping[b];
+        const long num_slots = (long)p.num_blocks * p.page;
+        const bool slot_ok = slot >= 0 && slot < num_slots;
+        if (lane == 0 && slot >= num_slots) set_error(p.err, 0x1u);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const int d = lane * E + e;
+            const bf16 kb = f2bf(y[e]);
+            const bf16 vb = f2bf(vv[e]);
+            Ks[(size_t)tr * DP + d] = kb;
+            Vs[(size_t)tr * DP + d] = vb;
+            if (slot_ok) {
+                p.k_cache[((size_t)slot * p.Hkv + kvh) * D + d] = kb;
+                p.v_cache[((size_t)slot * p.Hkv + kvh) * D + d] = vb;
+            }
+            if (p.tap_k_rot) p.tap_k_rot[((size_t)b * p.Hkv + kvh) * D + d] = kb;
+        }
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    if (tid == 0 && *s_flag) set_error(p.err, 0x2u);
+
+    // scores: warp w takes tokens 32 (w % 4) + lane and heads w / 4, +2, +4, +6
+    const f2 scale = {p.scale, p.scale_lo};
+    {
+        const int t = (warp & 3) * 32 + lane;
+        const int hb = warp >> 2;
+        constexpr int HW = (kGrpMaxG + 1) / 2;    // heads per warp, at most
+        if (t < n) {
+            f2 acc[HW];
+#pragma unroll
+            for (int i = 0; i < HW; ++i) acc[i] = f2{0.0f, 0.0f};
+            const bf16* krow = Ks + (size_t)t * DP;
+#pragma unroll 2
+            for (int dv = 0; dv < RV; ++dv) {
+                float kf[8];
+                unpack8(*reinterpret_cast<const int4*>(krow + 8 * dv), kf);
+#pragma unroll
+                for (int i = 0; i < HW; ++i) {
+                    const int hh = hb + 2 * i;
+                    if (hh < G) {
+                        const float4 qa = *reinterpret_cast<const float4*>(qs + hh * D + 8 * dv);
+                        const float4 qb = *reinterpret_cast<const float4*>(qs + hh * D + 8 * dv + 4);
+                        f2_acc(acc[i], __fmul_rn(qa.x, kf[0]));
+                        f2_acc(acc[i], __fmul_rn(qa.y, kf[1]));
+                        f2_acc(acc[i], __fmul_rn(qa.z, kf[2]));
+                        f2_acc(acc[i], __fmul_rn(qa.w, kf[3]));
+                        f2_acc(acc[i], __fmul_rn(qb.x, kf[4]));
+                        f2_acc(acc[i], __fmul_rn(qb.y, kf[5]));
+                        f2_acc(acc[i], __fmul_rn(qb.z, kf[6]));
+                        f2_acc(acc[i], __fmul_rn(qb.w, kf[7]));
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < HW; ++i) {
+                const int hh = hb + 2 * i;
+                if (hh < G) {
+                    const f2 s = f2_mul(fast_two_sum(acc[i].hi, acc[i].lo), scale);
+                    sc[hh * C + t] = s.hi;
+                    sl[hh * C + t] = s.lo;
+                }
+            }
+        }
+    }
+    __syncthreads();
+
+    // softmax of head w over the chunk: p = exp(s - m), l = sum p
+    if (warp < G) {
+        float* shi = sc + warp * C;
+        float* slo = sl + warp * C;
+        f2 m = {-INFINITY, 0.0f};
+        for (int t = lane; t < n; t += 32) m = f2_max(m, f2{shi[t], slo[t]});
+        m = warp_max_f2(m);
+        f2 l = {0.0f, 0.0f};
+        for (int t = lane; t < n; t += 32) {
+            const f2 e = f2_exp(f2_sub(f2{shi[t], slo[t]}, m));
+            shi[t] = e.hi;
+            slo[t] = e.lo;
+            l = f2_add(l, e);
+        }
+        l = warp_sum_f2(l);
+        if (lane == 0) {
+            stat[warp * 4 + 0] = m.hi;
+            stat[warp * 4 + 1] = m.lo;
+            stat[warp * 4 + 2] = l.hi;
+            stat[warp * 4 + 3] = l.lo;
+        }
+    }
+    __syncthreads();
+
+    // P.V: TG consecutive threads share a column pair and split the tokens
+    {
+        constexpr int CP = D / 2;
+        constexpr int TG = NT / CP;
+        static_assert(TG >= 1 && TG <= 32 && (TG & (TG - 1)) == 0, "token groups");
+        const int cp = tid / TG, tg = tid % TG;
+        f2 o[kGrpMaxG][2];
+#pragma unroll
+        for (int h = 0; h < kGrpMaxG; ++h) o[h][0] = o[h][1] = f2{0.0f, 0.0f};
+        for (int t = tg; t < n; t += TG) {
+            const float2 v = __bfloat1622float2(
+                *reinterpret_cast<const __nv_bfloat162*>(Vs + (size_t)t * DP + 2 * cp));
+#pragma unroll
+            for (int h = 0; h < kGrpMaxG; ++h) {
+                if (h < G) {
+                    const f2 pr = {sc[h * C + t], sl[h * C + t]};
+                    dot2_acc(o[h][0], pr, v.x);
+                    dot2_acc(o[h][1], pr, v.y);
+                }
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < kGrpMaxG; ++h) {
+            if (h < G) {
+                o[h][0] = fast_two_sum(o[h][0].hi, o[h][0].lo);
+                o[h][1] = fast_two_sum(o[h][1].hi, o[h][1].lo);
+#pragma unroll
+                for (int s = TG / 2; s > 0; s >>= 1) {
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        f2 r;
+                        r.hi = __shfl_xor_sync(0xffffffffu, o[h][c].hi, s);
+                        r.lo = __shfl_xor_sync(0xffffffffu, o[h][c].lo, s);
+                        o[h][c] = f2_add(o[h][c], r);
+                    }
+                }
+            }
+        }
+        if (tg == 0) {
+#pragma unroll
+            for (int h = 0; h < kGrpMaxG; ++h) {
+                if (h < G) {
+                    const int hq = h0 + h;
+                    const f2 l = {stat[h * 4 + 2], stat[h * 4 + 3]};
+                    if (single) {
+                        bf16* out = p.out + ((size_t)b * p.Hq + hq) * D + 2 * cp;
+                        out[0] = n > 0 ? f2_to_bf16(f2_div(o[h][0], l)) : __float2bfloat16_rn(0.0f);
+                        out[1] = n > 0 ? f2_to_bf16(f2_div(o[h][1], l)) : __float2bfloat16_rn(0.0f);
+                    } else {
+                        float* pp = p.part + (((size_t)b * p.Hq + hq) * splits + split) * (2 * D + 4);
+                        pp[2 * cp] = n > 0 ? o[h][0].hi : 0.0f;
+                        pp[2 * cp + 1] = n > 0 ? o[h][1].hi : 0.0f;
+                        pp[D + 2 * cp] = n > 0 ? o[h][0].lo : 0.0f;
+                        pp[D + 2 * cp + 1] = n > 0 ? o[h][1].lo : 0.0f;
+                        if (cp == 0) {
+                            pp[2 * D] = n > 0 ? stat[h * 4 + 0] : -INFINITY;
+                            pp[2 * D + 1] = n > 0 ? stat[h * 4 + 1] : 0.0f;
+                            pp[2 * D + 2] = n > 0 ? l.hi : 0.0f;
+                            pp[2 * D + 3] = n > 0 ? l.lo : 0.0f;
+                        }
+                    }
+                }
+            }
+        }
+    }
+    if (single) return;   // no barrier follows on this path
+
+    // the last CTA of this (request, KV head) merges the chunks' partials
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        unsigned* tk = p.tickets + (size_t)b * p.Hq + kvh;
+        const unsigned prev = atomicAdd(tk, 1u);
+        *s_flag = prev == (unsigned)(active - 1);
+        if (*s_flag) *tk = 0u;   // ready for the next launch
+    }
+    __syncthreads();
+    if (!*s_flag) return;
+    __threadfence();
+    constexpr int CS = 2 * kGrpMaxSplits + 2 + kGrpMaxSplits + 1;   // floats per head
+    float* scratch = reinterpret_cast<float*>(smem + L.tiles);
+    if (warp < G) {
+        float* cw = scratch + warp * CS;
+        int* act = reinterpret_cast<int*>(cw + 2 * kGrpMaxSplits + 2);
+        const float* pb = p.part + ((size_t)b * p.Hq + h0 + warp) * splits * (2 * D + 4);
+        combine_weights<D>(pb, active, cw, cw + 2 * kGrpMaxSplits, lane, act, act + kGrpMaxSplits);
+    }
+    __syncthreads();
+    for (int i = tid; i < G * D; i += NT) {
+        const int h = i / D, d = i - h * D;
+        const float* cw = scratch + h * CS;
+        const float* cl = cw + 2 * kGrpMaxSplits;
+        const int* act = reinterpret_cast<const int*>(cw + 2 * kGrpMaxSplits + 2);
+        const int nact = act[kGrpMaxSplits];
+        const float* pb = p.part + ((size_t)b * p.Hq + h0 + h) * splits * (2 * D + 4);
+        f2 acc = {0.0f, 0.0f};
+        for (int k = 0; k < nact; ++k) {
+            const int sp = act[k];
+            const float* q = pb + (size_t)sp * (2 * D + 4);
+            acc = f2_add(acc, f2_mul(f2{__ldcg(q + d), __ldcg(q + D + d)}, f2{cw[2 * sp], cw[2 * sp + 1]}));
+        }
+        const f2 l = {cl[0], cl[1]};
+        p.out[((size_t)b * p.Hq + h0 + h) * D + d] =
+            l.hi > 0.0f ? f2_to_bf16(f2_div(acc, l)) : __float2bfloat16_rn(0.0f);
+    }
+}
+
+}  // namespace
+
+bool attn_group_supported(const AttnParams& p) {
+    const int max_ctx = p.max_blocks * p.page;
+    return p.fused && p.tickets && p.Hq % p.Hkv == 0 && p.Hq / p.Hkv <= kGrpMaxG &&
+           (p.D == 128 || p.D == 64) && (max_ctx + kGrpChunk - 1) / kGrpChunk <= kGrpMaxSplits;
+}
+
+int attn_group_splits(int max_ctx) { return max_ctx <= 0 ? 1 : (max_ctx + kGrpChunk - 1) / kGrpChunk; }
+
+cudaError_t launch_attn_group(const AttnParams& p, const Launch& L) {
+    if (p.B == 0) return cudaSuccess;
+    if (!attn_group_supported(p)) return cudaErrorInvalidValue;
+    const int splits = attn_group_splits(p.max_blocks * p.page);
+    const size_t smem = grp_smem(p.D).total;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(splits, p.Hkv, p.B);
+    cfg.blockDim = dim3(kGrpThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = L.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = L.pdl ? 1 : 0;
+    static int configured_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_dev != dev) {
+        cudaError_t e = cudaFuncSetAttribute(attn_group_kernel<128>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)grp_smem(128).total);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(attn_group_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)grp_smem(64).total);
+        if (e != cudaSuccess) return e;
+        configured_dev = dev;
+    }
+    if (p.D == 128) return cudaLaunchKernelEx(&cfg, attn_group_kernel<128>, p, splits);
+    return cudaLaunchKernelEx(&cfg, attn_group_kernel<64>, p, splits);
+}
+
+}  // namespace a8w8
