@@ -15,8 +15,10 @@
 // short latency); at batch 16 and contexts of thousands of tokens it spends
 // most of its instructions on shuffle reductions, a one-warp softmax and
 // staging every K/V tile once per query head. Here:
-//   * the K/V tile of the chunk is staged once for the G = Hq / Hkv query
-//     heads of the KV head (cp.async, before the dependency wait);
+//   * the K tile of the chunk is staged once for the G = Hq / Hkv query
+//     heads of the KV head (cp.async, before the dependency wait), and the V
+//     tile replaces it in the same buffer while the softmax runs, so that
+//     five CTAs fit on an SM;
 //   * scores: one lane per token, the lane's K row read from shared memory
 //     8 columns at a time and multiplied with the query rows (broadcast
 //     reads) of the warp's heads; products of BF16 values are exact in
@@ -40,20 +42,20 @@ constexpr int kGrpMaxG = 7;          // query heads per KV head served here
 constexpr int kGrpMaxSplits = 64;    // chunks per request (in-kernel combine)
 
 struct GrpSmem {
-    size_t tiles, q, sc, sl, stat, blk, flag, total;
+    size_t tile, vnew, q, pr, stat, blk, flag, total;
 };
-__host__ __device__ inline GrpSmem grp_smem(int D) {
+__host__ __device__ inline GrpSmem grp_smem(int D, int G) {
     GrpSmem s;
-    s.tiles = 0;
-    const size_t kv = (size_t)2 * kGrpChunk * (D + kTilePad) * 2;
-    // combine scratch reuses the tiles: per head 2*splits weights, 2 for L,
+    s.tile = 0;
+    const size_t kv = (size_t)kGrpChunk * (D + kTilePad) * 2;
+    // combine scratch reuses the tile: per head 2*splits weights, 2 for L,
     // splits active indices and their count
-    const size_t comb = (size_t)kGrpMaxG * (2 * kGrpMaxSplits + 2 + kGrpMaxSplits + 1) * 4;
-    s.q = kv > comb ? kv : comb;                         // [G][D] float
-    s.sc = s.q + (size_t)kGrpMaxG * D * 4;               // [G][chunk] hi
-    s.sl = s.sc + (size_t)kGrpMaxG * kGrpChunk * 4;      // [G][chunk] lo
-    s.stat = s.sl + (size_t)kGrpMaxG * kGrpChunk * 4;    // [G][4]: m hi, m lo, l hi, l lo
-    s.blk = s.stat + (size_t)kGrpMaxG * 4 * 4;           // [chunk] physical block per token
+    const size_t comb = (size_t)G * (2 * kGrpMaxSplits + 2 + kGrpMaxSplits + 1) * 4;
+    s.vnew = (kv > comb ? kv : comb);                    // [D] bf16: the new token's V
+    s.q = s.vnew + (size_t)D * 2;                        // [G][D] float
+    s.pr = s.q + (size_t)G * D * 4;                      // [G][chunk] (hi, lo) pairs
+    s.stat = s.pr + (size_t)G * kGrpChunk * 8;           // [G][4]: m hi, m lo, l hi, l lo
+    s.blk = s.stat + (size_t)G * 4 * 4;                  // [chunk] physical block per token
     s.flag = s.blk + (size_t)kGrpChunk * 4;
     s.total = s.flag + 16;
     return s;
@@ -71,26 +73,25 @@ __device__ __forceinline__ void dot2_acc(f2& acc, const f2 p, float v) {
     acc.lo = __fadd_rn(acc.lo, __fadd_rn(err, __fmaf_rn(p.lo, v, e)));
 }
 
-template <int D>
+template <int D, int G>
 __global__ void __launch_bounds__(kGrpThreads) attn_group_kernel(const AttnParams p, int splits) {
+    static_assert(G >= 1 && G <= kGrpMaxG, "query heads per KV head");
     extern __shared__ __align__(16) unsigned char smem[];
-    constexpr int NT = kGrpThreads, NW = NT / 32, C = kGrpChunk;
+    constexpr int NT = kGrpThreads, C = kGrpChunk;
     constexpr int DP = D + kTilePad;
     constexpr int RV = D / 8;         // 16-byte vectors per row
     constexpr int E = D / 32;
-    const GrpSmem L = grp_smem(D);
-    bf16* Ks = reinterpret_cast<bf16*>(smem + L.tiles);
-    bf16* Vs = Ks + (size_t)C * DP;
+    const GrpSmem L = grp_smem(D, G);
+    bf16* Ts = reinterpret_cast<bf16*>(smem + L.tile);   // K tile, then V tile
+    bf16* vnew = reinterpret_cast<bf16*>(smem + L.vnew);
     float* qs = reinterpret_cast<float*>(smem + L.q);
-    float* sc = reinterpret_cast<float*>(smem + L.sc);
-    float* sl = reinterpret_cast<float*>(smem + L.sl);
+    float2* pr = reinterpret_cast<float2*>(smem + L.pr);
     float* stat = reinterpret_cast<float*>(smem + L.stat);
     int* blk = reinterpret_cast<int*>(smem + L.blk);
     int* s_flag = reinterpret_cast<int*>(smem + L.flag);
 
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int G = p.Hq / p.Hkv;
     const int h0 = kvh * G;
     const int t0 = split * C;
     const int max_ctx = p.max_blocks * p.page;
@@ -114,21 +115,23 @@ __global__ void __launch_bounds__(kGrpThreads) attn_group_kernel(const AttnParam
         blk[t] = (bk < 0 || bk >= p.num_blocks) ? -1 : bk;
     }
     __syncthreads();
-    for (int i = tid; i < n_old * RV; i += NT) {
-        const int t = i / RV, c = i - t * RV;
-        const int bk = blk[t];
-        if (bk < 0) {
-            *reinterpret_cast<int4*>(Ks + (size_t)t * DP + 8 * c) = make_int4(0, 0, 0, 0);
-            *reinterpret_cast<int4*>(Vs + (size_t)t * DP + 8 * c) = make_int4(0, 0, 0, 0);
-            *s_flag = 1;
-            continue;
+    // rows of the cached tokens of `cache` into the tile (zeros for a bad block)
+    auto load_tile = [&](const bf16* cache) {
+        for (int i = tid; i < n_old * RV; i += NT) {
+            const int t = i / RV, c = i - t * RV;
+            const int bk = blk[t];
+            if (bk < 0) {
+                *reinterpret_cast<int4*>(Ts + (size_t)t * DP + 8 * c) = make_int4(0, 0, 0, 0);
+                *s_flag = 1;
+                continue;
+            }
+            const int tok = t0 + t;
+            const size_t off = (((size_t)bk * p.page + tok % p.page) * p.Hkv + kvh) * D + 8 * c;
+            cp_async16(Ts + (size_t)t * DP + 8 * c, cache + off);
         }
-        const int tok = t0 + t;
-        const size_t off = (((size_t)bk * p.page + tok % p.page) * p.Hkv + kvh) * D + 8 * c;
-        cp_async16(Ks + (size_t)t * DP + 8 * c, p.k_cache + off);
-        cp_async16(Vs + (size_t)t * DP + 8 * c, p.v_cache + off);
-    }
-    cp_async_commit();
+        cp_async_commit();
+    };
+    load_tile(p.k_cache);
     // warps 0..G-1: query heads; warp G: the new token's K and V
     const bool qwarp = warp < G;
     const bool kwarp = warp == G && covers_new;
@@ -171,8 +174,8 @@ __global__ void __launch_bounds__(kGrpThreads) attn_group_kernel(const AttnParam
             const int d = lane * E + e;
             const bf16 kb = f2bf(y[e]);
             const bf16 vb = f2bf(vv[e]);
-            Ks[(size_t)tr * DP + d] = kb;
-            Vs[(size_t)tr * DP + d] = vb;
+            Ts[(size_t)tr * DP + d] = kb;
+            vnew[d] = vb;
             if (slot_ok) {
                 p.k_cache[((size_t)slot * p.Hkv + kvh) * D + d] = kb;
                 p.v_cache[((size_t)slot * p.Hkv + kvh) * D + d] = vb;
@@ -189,12 +192,12 @@ __global__ void __launch_bounds__(kGrpThreads) attn_group_kernel(const AttnParam
     {
         const int t = (warp & 3) * 32 + lane;
         const int hb = warp >> 2;
-        constexpr int HW = (kGrpMaxG + 1) / 2;    // heads per warp, at most
+        constexpr int HW = (G + 1) / 2;    // heads per warp, at most
         if (t < n) {
             f2 acc[HW];
 #pragma unroll
             for (int i = 0; i < HW; ++i) acc[i] = f2{0.0f, 0.0f};
-            const bf16* krow = Ks + (size_t)t * DP;
+            const bf16* krow = Ts + (size_t)t * DP;
 #pragma unroll 2
             for (int dv = 0; dv < RV; ++dv) {
                 float kf[8];
@@ -220,27 +223,30 @@ __global__ void __launch_bounds__(kGrpThreads) attn_group_kernel(const AttnParam
             for (int i = 0; i < HW; ++i) {
                 const int hh = hb + 2 * i;
                 if (hh < G) {
-                    const f2 s = f2_mul(fast_two_sum(acc[i].hi, acc[i].lo), scale);
-                    sc[hh * C + t] = s.hi;
-                    sl[hh * C + t] = s.lo;
+                    const f2 sv = f2_mul(fast_two_sum(acc[i].hi, acc[i].lo), scale);
+                    pr[hh * C + t] = make_float2(sv.hi, sv.lo);
                 }
             }
         }
     }
-    __syncthreads();
+    __syncthreads();   // the K tile is no longer read
+
+    // the V tile into the same buffer, behind the softmax
+    load_tile(p.v_cache);
+    if (n > 0 && warp == G && covers_new) {
+        for (int d = lane; d < D; d += 32) Ts[(size_t)(pos - t0) * DP + d] = vnew[d];
+    }
 
     // softmax of head w over the chunk: p = exp(s - m), l = sum p
     if (warp < G) {
-        float* shi = sc + warp * C;
-        float* slo = sl + warp * C;
+        float2* ph = pr + warp * C;
         f2 m = {-INFINITY, 0.0f};
-        for (int t = lane; t < n; t += 32) m = f2_max(m, f2{shi[t], slo[t]});
+        for (int t = lane; t < n; t += 32) m = f2_max(m, f2{ph[t].x, ph[t].y});
         m = warp_max_f2(m);
         f2 l = {0.0f, 0.0f};
         for (int t = lane; t < n; t += 32) {
-            const f2 e = f2_exp(f2_sub(f2{shi[t], slo[t]}, m));
-            shi[t] = e.hi;
-            slo[t] = e.lo;
+            const f2 e = f2_exp(f2_sub(f2{ph[t].x, ph[t].y}, m));
+            ph[t] = make_float2(e.hi, e.lo);
             l = f2_add(l, e);
         }
         l = warp_sum_f2(l);
@@ -251,6 +257,7 @@ __global__ void __launch_bounds__(kGrpThreads) attn_group_kernel(const AttnParam
             stat[warp * 4 + 3] = l.lo;
         }
     }
+    cp_async_wait_all();
     __syncthreads();
 
     // P.V: TG consecutive threads share a column pair and split the tokens
@@ -259,24 +266,22 @@ __global__ void __launch_bounds__(kGrpThreads) attn_group_kernel(const AttnParam
         constexpr int TG = NT / CP;
         static_assert(TG >= 1 && TG <= 32 && (TG & (TG - 1)) == 0, "token groups");
         const int cp = tid / TG, tg = tid % TG;
-        f2 o[kGrpMaxG][2];
+        f2 o[G][2];
 #pragma unroll
-        for (int h = 0; h < kGrpMaxG; ++h) o[h][0] = o[h][1] = f2{0.0f, 0.0f};
+        for (int h = 0; h < G; ++h) o[h][0] = o[h][1] = f2{0.0f, 0.0f};
         for (int t = tg; t < n; t += TG) {
             const float2 v = __bfloat1622float2(
-                *reinterpret_cast<const __nv_bfloat162*>(Vs + (size_t)t * DP + 2 * cp));
+                *reinterpret_cast<const __nv_bfloat162*>(Ts + (size_t)t * DP + 2 * cp));
 #pragma unroll
-            for (int h = 0; h < kGrpMaxG; ++h) {
-                if (h < G) {
-                    const f2 pr = {sc[h * C + t], sl[h * C + t]};
-                    dot2_acc(o[h][0], pr, v.x);
-                    dot2_acc(o[h][1], pr, v.y);
-                }
+            for (int h = 0; h < G; ++h) {
+                const float2 q = pr[h * C + t];
+                dot2_acc(o[h][0], f2{q.x, q.y}, v.x);
+                dot2_acc(o[h][1], f2{q.x, q.y}, v.y);
             }
         }
 #pragma unroll
-        for (int h = 0; h < kGrpMaxG; ++h) {
-            if (h < G) {
+        for (int h = 0; h < G; ++h) {
+            {
                 o[h][0] = fast_two_sum(o[h][0].hi, o[h][0].lo);
                 o[h][1] = fast_two_sum(o[h][1].hi, o[h][1].lo);
 #pragma unroll
@@ -293,8 +298,8 @@ __global__ void __launch_bounds__(kGrpThreads) attn_group_kernel(const AttnParam
         }
         if (tg == 0) {
 #pragma unroll
-            for (int h = 0; h < kGrpMaxG; ++h) {
-                if (h < G) {
+            for (int h = 0; h < G; ++h) {
+                {
                     const int hq = h0 + h;
                     const f2 l = {stat[h * 4 + 2], stat[h * 4 + 3]};
                     if (single) {
@@ -333,7 +338,7 @@ __global__ void __launch_bounds__(kGrpThreads) attn_group_kernel(const AttnParam
     if (!*s_flag) return;
     __threadfence();
     constexpr int CS = 2 * kGrpMaxSplits + 2 + kGrpMaxSplits + 1;   // floats per head
-    float* scratch = reinterpret_cast<float*>(smem + L.tiles);
+    float* scratch = reinterpret_cast<float*>(smem + L.tile);
     if (warp < G) {
         float* cw = scratch + warp * CS;
         int* act = reinterpret_cast<int*>(cw + 2 * kGrpMaxSplits + 2);
@@ -370,11 +375,18 @@ bool attn_group_supported(const AttnParams& p) {
 
 int attn_group_splits(int max_ctx) { return max_ctx <= 0 ? 1 : (max_ctx + kGrpChunk - 1) / kGrpChunk; }
 
-cudaError_t launch_attn_group(const AttnParams& p, const Launch& L) {
-    if (p.B == 0) return cudaSuccess;
-    if (!attn_group_supported(p)) return cudaErrorInvalidValue;
-    const int splits = attn_group_splits(p.max_blocks * p.page);
-    const size_t smem = grp_smem(p.D).total;
+template <int D, int G>
+cudaError_t launch_grp_t(const AttnParams& p, int splits, const Launch& L) {
+    const size_t smem = grp_smem(D, G).total;
+    static int configured_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_dev != dev) {
+        cudaError_t e = cudaFuncSetAttribute(attn_group_kernel<D, G>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        configured_dev = dev;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(splits, p.Hkv, p.B);
     cfg.blockDim = dim3(kGrpThreads);
@@ -385,21 +397,29 @@ cudaError_t launch_attn_group(const AttnParams& p, const Launch& L) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = L.pdl ? 1 : 0;
-    static int configured_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(attn_group_kernel<128>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)grp_smem(128).total);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(attn_group_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)grp_smem(64).total);
-        if (e != cudaSuccess) return e;
-        configured_dev = dev;
+    return cudaLaunchKernelEx(&cfg, attn_group_kernel<D, G>, p, splits);
+}
+
+template <int D>
+cudaError_t launch_grp_d(const AttnParams& p, int splits, const Launch& L) {
+    switch (p.Hq / p.Hkv) {
+        case 1: return launch_grp_t<D, 1>(p, splits, L);
+        case 2: return launch_grp_t<D, 2>(p, splits, L);
+        case 3: return launch_grp_t<D, 3>(p, splits, L);
+        case 4: return launch_grp_t<D, 4>(p, splits, L);
+        case 5: return launch_grp_t<D, 5>(p, splits, L);
+        case 6: return launch_grp_t<D, 6>(p, splits, L);
+        case 7: return launch_grp_t<D, 7>(p, splits, L);
+        default: return cudaErrorInvalidValue;
     }
-    if (p.D == 128) return cudaLaunchKernelEx(&cfg, attn_group_kernel<128>, p, splits);
-    return cudaLaunchKernelEx(&cfg, attn_group_kernel<64>, p, splits);
+}
+
+cudaError_t launch_attn_group(const AttnParams& p, const Launch& L) {
+    if (p.B == 0) return cudaSuccess;
+    if (!attn_group_supported(p)) return cudaErrorInvalidValue;
+    const int splits = attn_group_splits(p.max_blocks * p.page);
+    if (p.D == 128) return launch_grp_d<128>(p, splits, L);
+    return launch_grp_d<64>(p, splits, L);
 }
 
 }  // namespace a8w8
