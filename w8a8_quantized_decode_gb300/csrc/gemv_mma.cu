@@ -7,18 +7,13 @@
 // (acc * s_x) * s_w, residual or SwiGLU, one BF16 narrowing.
 //
 // Why tensor cores here: with a batch of 16 the dp4a GEMV reads every
-// activation byte from shared memory once per batch row and weight byte, and
-// dp4a issues at a quarter of the FP16 MMA rate, so the projection becomes
-// ALU bound well below the HBM roofline. mma.sync m16n8k16 multiplies the 16
-// batch rows (A) by 8 weight rows (B) per instruction.
-//
-// Exactness: INT8 codes are integers in [-128, 127], exact in FP16; every
-// product is an integer below 2^15 in magnitude, exact in float32, and a
-// float32 sum of at most 1024 of them stays below 2^24, where every integer
-// is a float32 value. The tensor-core float32 accumulation of such sums is
-// therefore exact, and each warp converts its float32 tile to INT32 (exact)
-// at least every 1024 K columns, adding it into the CTA's INT32 accumulators
-// in shared memory. The INT32 result equals the dp4a path bit for bit.
+// activation byte from shared memory once per batch row and weight byte and
+// becomes ALU bound well below the HBM roofline. mma.sync m16n8k32 (INT8 x
+// INT8 -> INT32, exact) multiplies the 16 batch rows (A) by 8 weight rows (B)
+// per instruction, straight from the INT8 bytes. (tcgen05 has no INT8 kind
+// on this architecture; an FP16 mma.sync on exact FP16 images of the codes
+// measured the same time, so the INT8 form, which needs no conversion and no
+// float chunking, is the one kept.)
 //
 // Layout and schedule (one CTA of 512 threads per SM):
 //   * CTA c owns output channels [c*N/G, (c+1)*N/G) (both halves for
@@ -29,10 +24,11 @@
 //     INT8 codes, from L2) once and reuses it for up to 8 weight groups.
 //   * Weight unit = 8 rows x 64 columns (512 bytes): lane (g, t) copies the
 //     16 bytes of row g at column 16 t into a private shared-memory ring with
-//     cp.async, 16 units ahead (one commit group per unit); the 16 bytes
-//     become the B fragments of four m16n8k16 instructions. The K columns are
+//     cp.async, 16 units ahead (one commit group per unit); its four words
+//     are the B fragments of two m16n8k32 instructions. The K columns are
 //     permuted inside a step (the same permutation for A), which a sum does
-//     not see. The cursors divide only when the group batch changes.
+//     not see. Each warp's INT32 tiles are added into the CTA's accumulators
+//     in shared memory (atomics, exact) at batch and split boundaries.
 //   * The activation rows are quantised once, by quant_prep_kernel (one CTA
 //     per row, RMSNorm optional, the same code as the dp4a prologue), not
 //     once per CTA.
@@ -48,32 +44,18 @@ constexpr int kMmaThreads = 512;
 constexpr int kMmaRows = 16;      // batch rows per launch (the MMA's M)
 constexpr int kMmaStep = 64;      // K columns per step
 constexpr int kMmaGroupsMax = 8;  // weight groups per batch
-constexpr int kMmaChunkSteps = 16;  // steps per float32 chunk: 1024 columns
 constexpr int kMmaNB = 16;        // ring depth, units per lane (16 copies in flight)
 constexpr int kMmaNBPre = 8;      // units requested before the dependency wait
 constexpr size_t kMmaRingBytes = (size_t)kMmaNB * kMmaThreads * 16;
 constexpr int kMaxDynSmem = 227 * 1024;
 constexpr int kPrepThreads = 256;
 
-// 4 INT8 -> 2 x f16x2 (exact): byte v becomes the f16 1024 + (v + 128),
-// then 1152 is subtracted.
-__device__ __forceinline__ void i8x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
-    const uint32_t u = w ^ 0x80808080u;
-    const uint32_t l = __byte_perm(u, 0x64646464u, 0x4140);
-    const uint32_t h = __byte_perm(u, 0x64646464u, 0x4342);
-    const __half2 off = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
-    const __half2 lf = __hsub2(*reinterpret_cast<const __half2*>(&l), off);
-    const __half2 hf = __hsub2(*reinterpret_cast<const __half2*>(&h), off);
-    lo = *reinterpret_cast<const uint32_t*>(&lf);
-    hi = *reinterpret_cast<const uint32_t*>(&hf);
-}
-
-__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+__device__ __forceinline__ void mma_s8_16832(int (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                             uint32_t a3, uint32_t b0, uint32_t b1) {
     asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
         "{%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
@@ -184,9 +166,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const GemvPara
         b = rb ? ld_cg_v4(xb + (size_t)step * kMmaStep) : make_int4(0, 0, 0, 0);
     };
 
-    float c[GM][4];
+    int c[GM][4];
 #pragma unroll
-    for (int j = 0; j < GM; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.0f;
+    for (int j = 0; j < GM; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0;
 
     // consumer cursor: batch bt (groups [ga, ga + ng)), step st
     int bt = 0, st = 0, ga = 0, ng = 0;
@@ -199,22 +181,14 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const GemvPara
     int rslot = 0;
     int4 na = make_int4(0, 0, 0, 0), nb = na;
     if (s0 < s1) load_a(st, na, nb);
-    int cnt = 0, split = KS == 1 ? 0 : st / kps;
+    int split = KS == 1 ? 0 : st / kps;
 #pragma unroll 1
     for (int sl = s0; sl < s1; ++sl) {
-        // A fragments of this step, the next step's loads in flight
-        uint32_t af[4][4];
-        {
-            const uint32_t wa[4] = {(uint32_t)na.x, (uint32_t)na.y, (uint32_t)na.z, (uint32_t)na.w};
-            const uint32_t wb[4] = {(uint32_t)nb.x, (uint32_t)nb.y, (uint32_t)nb.z, (uint32_t)nb.w};
-#pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                // MMA m: logical columns (2t, 2t+1) <- bytes 4m, 4m+1 of the
-                // lane's 16; (2t+8, 2t+9) <- bytes 4m+2, 4m+3
-                i8x4_to_f16x2(wa[m], af[m][0], af[m][2]);
-                i8x4_to_f16x2(wb[m], af[m][1], af[m][3]);
-            }
-        }
+        // A fragments of this step (rows g and g + 8), the next step's loads
+        // in flight. MMA m of the step: logical columns 4t..4t+3 <- the
+        // lane's word 2m, 16+4t..16+4t+3 <- word 2m + 1 (A and B alike).
+        const uint32_t wa[4] = {(uint32_t)na.x, (uint32_t)na.y, (uint32_t)na.z, (uint32_t)na.w};
+        const uint32_t wb[4] = {(uint32_t)nb.x, (uint32_t)nb.y, (uint32_t)nb.z, (uint32_t)nb.w};
         const int nst = st + 1 == KST ? 0 : st + 1;
         if (sl + 1 < s1) load_a(nst, na, nb);
 #pragma unroll
@@ -223,23 +197,16 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const GemvPara
                 cp_async_wait_group<kMmaNB - 1>();
                 const int4 w = lds_v4(ring + (uint32_t)(rslot * kMmaThreads * 16));
                 rslot = rslot + 1 == kMmaNB ? 0 : rslot + 1;
-                uint32_t bf[4][2];
-                i8x4_to_f16x2((uint32_t)w.x, bf[0][0], bf[0][1]);
-                i8x4_to_f16x2((uint32_t)w.y, bf[1][0], bf[1][1]);
-                i8x4_to_f16x2((uint32_t)w.z, bf[2][0], bf[2][1]);
-                i8x4_to_f16x2((uint32_t)w.w, bf[3][0], bf[3][1]);
                 issue();   // refill the slot just read
-#pragma unroll
-                for (int m = 0; m < 4; ++m)
-                    mma_f16_16816(c[j], af[m][0], af[m][1], af[m][2], af[m][3], bf[m][0], bf[m][1]);
+                mma_s8_16832(c[j], wa[0], wb[0], wa[1], wb[1], (uint32_t)w.x, (uint32_t)w.y);
+                mma_s8_16832(c[j], wa[2], wb[2], wa[3], wb[3], (uint32_t)w.z, (uint32_t)w.w);
             }
         }
-        ++cnt;
         const bool last = sl + 1 == s1;
         const bool batch_end = nst == 0;
         const bool split_end = KS == 2 && st + 1 == kps;
-        if (last || batch_end || split_end || cnt == kMmaChunkSteps) {
-            // exact float32 tiles -> INT32 shared accumulators
+        if (last || batch_end || split_end) {
+            // INT32 tiles -> shared accumulators
 #pragma unroll
             for (int j = 0; j < GM; ++j) {
                 if (j < ng) {
@@ -251,13 +218,11 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const GemvPara
                         const int r = r0 + (e & 1);
                         const int b = g + ((e >> 1) << 3);
                         if (r < nrows && b < M)
-                            atomicAdd(&accs[((seg * rows_max + r) * KS + split) * kMmaRows + b],
-                                      __float2int_rn(c[j][e]));
-                        c[j][e] = 0.0f;
+                            atomicAdd(&accs[((seg * rows_max + r) * KS + split) * kMmaRows + b], c[j][e]);
+                        c[j][e] = 0;
                     }
                 }
             }
-            cnt = 0;
         }
         if (split_end) split = 1;
         if (batch_end) {
