@@ -115,8 +115,8 @@ def test_linear_residual_in_place(a8w8):
 
 @pytest.mark.parametrize("M,xv,wv", [(1, 127, 127), (16, 127, 127), (16, -128, -128)])
 def test_linear_extreme_values_no_overflow(a8w8, M, xv, wv):
-    # the largest products; with M >= 3 the tensor-core form sums up to 1024 of
-    # them in float32 (|sum| <= 2^24, still exact) before converting to INT32
+    # the largest products over K = 17408 (|sum| < 2^31); with M >= 3 the
+    # tensor-core form (INT8 MMA, INT32 accumulators) runs
     K, N = 17408, 160
     xq = np.full((M, K), xv, np.int8)
     W = np.full((N, K), -wv, np.int8) if wv == 127 else np.full((N, K), wv, np.int8)
