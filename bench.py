@@ -14,7 +14,14 @@ roofline : the Gate/Up projection kernel (54% of the step's bytes), timed live
            with CUDA events over the 40 layers' Gate/Up weights.
 cpu_baseline / --impl reference : the CPU oracle, timed on one decode step.
 
+--workload batched16: the batched paged decode step instead (batch 16, contexts
+drawn uniformly from [64, 4096], pages of 128 tokens in a seeded shuffled
+permutation, synthetic N(0,1) context K/V, each new token written into its
+request's last page), K replays of the device-loop step graph (default 32
+steps); one JSON line with the step time, tokens/s and the step's HBM bytes.
+
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--workload decode_b1|batched16]
 """
 from __future__ import annotations
 
@@ -391,6 +398,109 @@ def run_ours(args, cfg):
         torch.distributed.destroy_process_group()
 
 
+BATCHED_B = 16
+BATCHED_WORKLOAD = "qwen3_14b_a8w8_batched_decode_b16"
+BATCHED_METRIC = "A8W8 batched decode step (ms/step, 40 layers, bs=16, contexts 64..4096)"
+
+
+def run_batched(args, cfg):
+    """Batch-16 paged decode with long mixed contexts (one GPU per rank)."""
+    import torch
+    import w8a8_quantized_decode_gb300 as a8w8
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    a8w8.build()
+    B, page = BATCHED_B, cfg["page_size"]
+    Hkv, D, L = cfg["num_kv_heads"], cfg["head_dim"], cfg["num_layers"]
+    ctx0 = synth.batched_ctx_lens(SEED + 20, B)
+    grow = args.warmup + args.steps
+    bt, nblk = synth.paged_layout(SEED + 21, ctx0, page, extra_tokens=grow)
+    max_blocks = bt.shape[1]
+    model = build_model(cfg, device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(SEED + 22)
+    kc, vc = [], []
+    for _ in range(L):
+        kc.append(torch.randn((nblk * page, Hkv, D), generator=gen, device=device).to(torch.bfloat16))
+        vc.append(torch.randn((nblk * page, Hkv, D), generator=gen, device=device).to(torch.bfloat16))
+    rope = a8w8.a8w8_rope_table(max_blocks * page, D, cfg["rope_theta"], device=device)
+    ws = a8w8.alloc_workspace(cfg, B, max_blocks, device=device)
+    stream = torch.cuda.Stream(device)
+    with torch.cuda.stream(stream):
+        g = a8w8.StepGraph(model, cfg, B, max_blocks, kc, vc, rope, ws, device_loop=True,
+                           stream=stream)
+        tok = synth.prompt_ids(SEED + 23, B, cfg["vocab"])
+        slots = synth.slots_for(bt, ctx0 - 1, page)
+        g.set_inputs(torch.from_numpy(tok).to(device), torch.from_numpy(slots).to(device),
+                     torch.from_numpy(bt).to(device),
+                     torch.from_numpy(ctx0.astype(np.int32)).to(device))
+        for _ in range(args.warmup):
+            g.launch(stream)
+        stream.synchronize()
+        gpu_uuid = None
+        try:
+            gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+        except Exception:
+            pass
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        with ClockSampler(gpu_uuid) as clocks:
+            ev0.record(stream)
+            for _ in range(args.steps):
+                g.launch(stream)
+            ev1.record(stream)
+            ev1.synchronize()
+        torch.cuda.synchronize()
+        ms = ev0.elapsed_time(ev1)
+        if world > 1:
+            t = torch.tensor([ms], device=device)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ms = float(t.item())
+        errs = a8w8.read_device_errors(stream)
+        g.close()
+    per_step = ms / args.steps
+    # contexts of the timed steps: ctx0 + warmup + i + 1 tokens, summed over rows
+    ctx_sum = sum(int(c) + args.warmup + i for c in ctx0 for i in range(args.steps))
+    sb = step_bytes(cfg, [ctx_sum])
+    per_step_bytes = sb["layers"] + sb["lm_head"] + sb["kv"] / args.steps
+    peaks = measured_peaks()
+    # embed; per layer 4 row quantisations + 4 projections + attention; the LM
+    # head in tiles of 8 rows; the device-loop advance
+    n_launch = 1 + L * 9 + (B + 7) // 8 + 1
+    if rank == 0:
+        line = {
+            "metric": BATCHED_METRIC, "value": per_step, "unit": "ms/step", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int8 x int8 -> int32, f32 dequant, bf16 activations",
+            "data": "synthetic (seeded random-init weights and N(0,1) context K/V on the device)",
+            "config": {"workload": BATCHED_WORKLOAD, "batch": B, "layers": L,
+                       "ctx_range": [64, 4096], "mean_ctx_start": float(ctx0.mean()),
+                       "page_size": page, "max_blocks": int(max_blocks),
+                       "parallelism": "replicas" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2 (14.8 GB of weights + KV per step)"},
+            "tokens_per_s": B * 1000.0 / per_step * world,
+            "step_bytes": per_step_bytes,
+            "step_hbm_gbs": per_step_bytes / (per_step * 1e-3) / 1e9,
+            "step_frac_of_peak": per_step_bytes / (per_step * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "e2e": None,
+            "gpu_launches": n_launch * args.steps,
+            "clocks": clocks.summary(),
+            "device_errors": errs,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def cpu_baseline(model, cfg):
     """The oracle on a bounded sample: decode steps until about 20 s of CPU time."""
     import torch
@@ -408,17 +518,23 @@ def cpu_baseline(model, cfg):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=48)
+    ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--layers", type=int, default=40, help=argparse.SUPPRESS)
+    ap.add_argument("--workload", choices=["decode_b1", "batched16"], default="decode_b1")
+    ap.add_argument("--layers", type=int, default=40,
+                    help="layers of the model (fewer only for profiling captures)")
     args = ap.parse_args()
+    if args.steps is None:
+        args.steps = 32 if args.workload == "batched16" else 48
     if args.warmup < 3:
         raise SystemExit("warmup must be >= 3")
     cfg = dict(synth.QWEN3_14B, num_layers=args.layers)
     if args.impl == "reference":
         run_reference(args, cfg)
+    elif args.workload == "batched16":
+        run_batched(args, cfg)
     else:
         run_ours(args, cfg)
 

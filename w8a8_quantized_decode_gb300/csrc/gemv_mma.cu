@@ -48,7 +48,7 @@ constexpr int kMmaNB = 16;        // ring depth, units per lane (16 copies in fl
 constexpr int kMmaNBPre = 8;      // units requested before the dependency wait
 constexpr size_t kMmaRingBytes = (size_t)kMmaNB * kMmaThreads * 16;
 constexpr int kMaxDynSmem = 227 * 1024;
-constexpr int kPrepThreads = 256;
+constexpr int kPrepThreads = 1024;  // one CTA per row, the batch-1 prologue's width
 
 __device__ __forceinline__ void mma_s8_16832(int (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                              uint32_t a3, uint32_t b0, uint32_t b1) {
