@@ -278,6 +278,26 @@ a8w8_status a8w8_decode_layer(const a8w8_layer_weights* w, const a8w8_config* cf
                               const float* rope, int max_pos, void* ws, size_t ws_bytes,
                               const a8w8_layer_taps* taps, void* stream);
 
+/* One A8W8 prefill chunk through one layer: M token rows (of one or more
+ * sequences) with the decode layer's arguments, where row r is the token at
+ * position ctx_lens[r] - 1 of its sequence, whose block table row
+ * block_table[r] it shares with the sequence's other rows ([SRV-52]
+ * "Current behavior": the A8W8 prefill path; configuration of the pages'
+ * prefill-chunk workload). Every row's rotated K and its V are written to its
+ * slot first, then each row attends over its own ctx_lens[r] tokens, so the
+ * chunk is causal: row r sees the cache's earlier tokens and the chunk's rows
+ * of its sequence up to its own position. Results equal those of decoding the
+ * rows one at a time in position order. Projections run on the tensor cores
+ * in tiles of 16 rows. 1 <= M <= 16384; attention supports Hq / Hkv <= 7 and
+ * contexts of at most 64 chunks of 128 tokens (A8W8_ERR_UNSUPPORTED_SHAPE
+ * otherwise). ws / ws_bytes: a8w8_workspace_bytes(cfg, M, max_blocks). */
+a8w8_status a8w8_prefill_layer(const a8w8_layer_weights* w, const a8w8_config* cfg, int M,
+                               a8w8_bf16* hidden, const int32_t* slot_mapping,
+                               const int32_t* block_table, int max_blocks, int num_blocks,
+                               const int32_t* ctx_lens, a8w8_bf16* k_cache, a8w8_bf16* v_cache,
+                               const float* rope, int max_pos, void* ws, size_t ws_bytes,
+                               const a8w8_layer_taps* taps, void* stream);
+
 /* One decode step: embedding gather of token_ids [B], the num_layers layers,
  * final RMSNorm, BF16 LM head with FP32 logits and greedy argmax (lowest index
  * on ties) into next_tokens [B] int32 ([SRV-48] "Performance": temperature 0,

@@ -324,6 +324,21 @@ def decode_layer(w: dict, cfg: dict, hidden, slot_mapping, block_table, ctx_lens
     return h, tap_arrays, rc
 
 
+def prefill_layer(w: dict, cfg: dict, hidden, slot_mapping, block_table, ctx_lens,
+                  k_cache, v_cache, taps: bool = False):
+    """One layer over a prefill chunk: M token rows, row r the token at position
+    ctx_lens[r] - 1 of the sequence whose block table row it carries.
+
+    The layer runs stage by stage over all rows (decode_layer): every row's K/V
+    is written (a7) before any row attends (a8), each over its own ctx_lens[r]
+    tokens, so the chunk is causal; quantisation and projections are per row.
+    Hence the result equals decoding the rows one at a time in position order
+    (reading of "A8W8-compatible prefill chunk": the prompt decoded as a
+    chunk), which tests/test_oracle_pins.py checks."""
+    return decode_layer(w, cfg, hidden, slot_mapping, block_table, ctx_lens, k_cache, v_cache,
+                        taps)
+
+
 def lm_head(hn, W_lm) -> np.ndarray:
     hn = _c(hn, U16)
     W_lm = _c(W_lm, U16)

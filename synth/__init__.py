@@ -183,6 +183,40 @@ def decode_layer_case(cfg: dict, B: int, ctx_lens, seed_base: int = 1234,
         k_cache=kc, v_cache=vc)
 
 
+def prefill_case(cfg: dict, seq_lens, prior_ctx=None, seed_base: int = 4321,
+                 spare_blocks: int = 1):
+    """Inputs of one layer over a prefill chunk: sequences s = 0.. with
+    seq_lens[s] new tokens after prior_ctx[s] cached ones (N(0,1) K/V).
+
+    Rows are sequence-major; row (s, i) is the token at position
+    prior_ctx[s] + i, carries its sequence's block table row, ctx_len
+    prior_ctx[s] + i + 1 and the slot of that position."""
+    seq_lens = [int(n) for n in seq_lens]
+    prior = [0] * len(seq_lens) if prior_ctx is None else [int(c) for c in prior_ctx]
+    page = cfg["page_size"]
+    bt_seq, nblk = paged_layout(seed_base + 7, [p + n for p, n in zip(prior, seq_lens)], page,
+                                spare_blocks=spare_blocks)
+    rows_bt, ctx, slots = [], [], []
+    for s, (p, n) in enumerate(zip(prior, seq_lens)):
+        for i in range(n):
+            pos = p + i
+            rows_bt.append(bt_seq[s])
+            ctx.append(pos + 1)
+            slots.append(int(bt_seq[s, pos // page]) * page + pos % page)
+    bt = np.stack(rows_bt).astype(np.int32)
+    Hkv, D = cfg["num_kv_heads"], cfg["head_dim"]
+    kc = kv_cache(seed_base + 8, nblk, page, Hkv, D, bt_seq, prior)
+    vc = kv_cache(seed_base + 9, nblk, page, Hkv, D, bt_seq, prior)
+    M = len(ctx)
+    return dict(
+        weights=layer_weights(cfg, seed_base),
+        hidden=hidden_states(seed_base + 5, M, cfg["hidden"]),
+        ctx_lens=np.asarray(ctx, np.int32), slot_mapping=np.asarray(slots, np.int32),
+        block_table=bt, num_blocks=nblk, k_cache=kc, v_cache=vc,
+        seq_block_table=bt_seq, prior_ctx=np.asarray(prior, np.int32),
+        seq_lens=np.asarray(seq_lens, np.int32))
+
+
 def model_weights_host(cfg: dict, seed_base: int) -> dict:
     """A whole model on the host (small configs only)."""
     H, V = cfg["hidden"], cfg["vocab"]

@@ -24,7 +24,7 @@ def a8w8():
     return m
 
 
-def _run_gpu_layer(a8w8, cfg, case, with_taps=True):
+def _run_gpu_layer(a8w8, cfg, case, with_taps=True, prefill=False):
     import torch
     w = {k: to_dev(v) for k, v in case["weights"].items()}
     hidden = to_dev(case["hidden"])
@@ -35,8 +35,9 @@ def _run_gpu_layer(a8w8, cfg, case, with_taps=True):
     ws = a8w8.alloc_workspace(cfg, hidden.shape[0], bt.shape[1])
     taps = a8w8.make_taps(cfg, hidden.shape[0]) if with_taps else None
     a8w8.read_device_errors()
-    a8w8.a8w8_decode_layer(w, cfg, hidden, to_dev(case["slot_mapping"]), bt,
-                           to_dev(case["ctx_lens"]), kc, vc, rope, ws, taps=taps)
+    layer = a8w8.a8w8_prefill_layer if prefill else a8w8.a8w8_decode_layer
+    layer(w, cfg, hidden, to_dev(case["slot_mapping"]), bt, to_dev(case["ctx_lens"]), kc, vc,
+          rope, ws, taps=taps)
     torch.cuda.synchronize()
     assert a8w8.read_device_errors() == 0
     t = {k: to_host(v) for k, v in taps.items()} if taps else None
@@ -124,8 +125,8 @@ def _stage_report(t, ot, out, ref):
     return rep
 
 
-def _layer_parity(a8w8, cfg, case, max_abs_bar=None):
-    out, t, kc, vc = _run_gpu_layer(a8w8, cfg, case)
+def _layer_parity(a8w8, cfg, case, max_abs_bar=None, prefill=False):
+    out, t, kc, vc = _run_gpu_layer(a8w8, cfg, case, prefill=prefill)
     _check_stages(cfg, case, out, t, kc, vc)
     # whole layer against the oracle's own layer from the same inputs
     okc, ovc = case["k_cache"].copy(), case["v_cache"].copy()
@@ -205,3 +206,60 @@ def test_qwen3_14b_layer_grouped_attention_b2(a8w8):
     cfg = dict(synth.QWEN3_14B, num_layers=1)
     case = synth.decode_layer_case(cfg, 2, [4096, 2049], seed_base=108)
     _layer_parity(a8w8, cfg, case)
+
+
+# ---------------------------------------------------------------------------
+# Prefill chunk: M token rows through the layer at once (causal by ctx_lens)
+# ---------------------------------------------------------------------------
+
+def test_tiny_prefill_chunk(a8w8):
+    # three sequences of 21 new tokens after 0, 5 and 17 cached ones
+    cfg = synth.TINY
+    case = synth.prefill_case(cfg, [21, 21, 21], prior_ctx=[0, 5, 17], seed_base=201)
+    _layer_parity(a8w8, cfg, case, prefill=True)
+
+
+def test_qwen3_14b_prefill_chunk(a8w8):
+    cfg = dict(synth.QWEN3_14B, num_layers=1)
+    case = synth.prefill_case(cfg, [24, 24], prior_ctx=[0, 130], seed_base=202)
+    _layer_parity(a8w8, cfg, case, prefill=True)
+
+
+def test_qwen3_14b_prefill_4x512_equals_sequential_decode(a8w8):
+    # the pages' prefill-chunk workload (4 sequences x 512 tokens, M = 2048):
+    # the chunk through the prefill entry against the same rows decoded one
+    # position at a time (4 rows per call) on the GPU; both write the caches
+    import torch
+    cfg = dict(synth.QWEN3_14B, num_layers=1)
+    case = synth.prefill_case(cfg, [512] * 4, seed_base=203)
+    w = {k: to_dev(v) for k, v in case["weights"].items()}
+    bt_rows = to_dev(case["block_table"])
+    nb = case["block_table"].shape[1]
+    rope = a8w8.a8w8_rope_table(nb * cfg["page_size"], cfg["head_dim"], cfg["rope_theta"])
+    h1 = to_dev(case["hidden"])
+    kc1, vc1 = to_dev(case["k_cache"]), to_dev(case["v_cache"])
+    ws = a8w8.alloc_workspace(cfg, 2048, nb)
+    a8w8.read_device_errors()
+    a8w8.a8w8_prefill_layer(w, cfg, h1, to_dev(case["slot_mapping"]), bt_rows,
+                            to_dev(case["ctx_lens"]), kc1, vc1, rope, ws)
+    torch.cuda.synchronize()
+    assert a8w8.read_device_errors() == 0
+    h2 = to_dev(case["hidden"])
+    kc2, vc2 = to_dev(case["k_cache"]), to_dev(case["v_cache"])
+    ws4 = a8w8.alloc_workspace(cfg, 4, nb)
+    slots, ctx = to_dev(case["slot_mapping"]), to_dev(case["ctx_lens"])
+    for i in range(512):
+        rows = torch.arange(4, device=h2.device) * 512 + i
+        hb = h2[rows].contiguous()
+        a8w8.a8w8_decode_layer(w, cfg, hb, slots[rows].contiguous(), bt_rows[rows].contiguous(),
+                               ctx[rows].contiguous(), kc2, vc2, rope, ws4)
+        h2[rows] = hb
+    torch.cuda.synchronize()
+    assert a8w8.read_device_errors() == 0
+    a, b = to_host(h1), to_host(h2)
+    same = (a == b).mean()
+    print("prefill vs sequential decode: identical fraction", same)
+    assert same >= 0.999, same
+    assert rel_l2(bf16_to_f64(a), bf16_to_f64(b)) <= 5e-3
+    assert (to_host(kc1) == to_host(kc2)).mean() >= 0.9999
+    assert (to_host(vc1) == to_host(vc2)).mean() == 1.0

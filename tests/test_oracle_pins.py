@@ -621,3 +621,33 @@ def test_step_composes_embed_layers_norm_head():
     _, _, _, rc = oracle.decode_step(model, cfg, np.array([5, 97], np.int32), slots, bt, ctx,
                                      [c.copy() for c in kcs], [c.copy() for c in vcs])
     assert rc == -3
+
+
+def test_prefill_chunk_equals_sequential_decode():
+    # a prefill chunk (all rows through the layer at once, each at its own
+    # position) must equal decoding the rows one position at a time: same
+    # outputs, same caches -- the causal reading of the prefill chunk
+    cfg = synth.TINY
+    case = synth.prefill_case(cfg, seq_lens=[5, 7], prior_ctx=[3, 0], seed_base=31)
+    w = case["weights"]
+    kc1, vc1 = case["k_cache"].copy(), case["v_cache"].copy()
+    out, _, rc = oracle.prefill_layer(w, cfg, case["hidden"], case["slot_mapping"],
+                                      case["block_table"], case["ctx_lens"], kc1, vc1)
+    assert rc == 0
+    kc2, vc2 = case["k_cache"].copy(), case["v_cache"].copy()
+    seq_of = np.repeat(np.arange(2), case["seq_lens"])
+    idx = np.arange(len(seq_of)) - np.concatenate([[0], np.cumsum(case["seq_lens"])[:-1]])[seq_of]
+    seq_out = np.empty_like(case["hidden"])
+    for i in range(int(case["seq_lens"].max())):
+        rows = np.nonzero(idx == i)[0]
+        h, _, rc = oracle.decode_layer(w, cfg, case["hidden"][rows], case["slot_mapping"][rows],
+                                       case["block_table"][rows], case["ctx_lens"][rows], kc2, vc2)
+        assert rc == 0
+        seq_out[rows] = h
+    assert np.array_equal(out, seq_out)
+    assert np.array_equal(kc1, kc2) and np.array_equal(vc1, vc2)
+    # and a row's output does depend on the earlier rows of its sequence
+    h_alone, _, _ = oracle.decode_layer(w, cfg, case["hidden"][4:5], case["slot_mapping"][4:5],
+                                        case["block_table"][4:5], case["ctx_lens"][4:5],
+                                        case["k_cache"].copy(), case["v_cache"].copy())
+    assert not np.array_equal(h_alone[0], out[4])

@@ -82,6 +82,8 @@ _SIGNATURES = {
     "a8w8_workspace_bytes": (_sz, [_p, _i, _i]),
     "a8w8_decode_layer": (_i, [_p, _p, _i, _p, _p, _p, _i, _i, _p, _p, _p, _p, _i, _p, _sz, _p,
                                _p]),
+    "a8w8_prefill_layer": (_i, [_p, _p, _i, _p, _p, _p, _i, _i, _p, _p, _p, _p, _i, _p, _sz, _p,
+                                _p]),
     "a8w8_decode_step": (_i, [_p, _p, _i, _p, _p, _p, _i, _i, _p, _p, _p, _p, _i, _p, _p, _p, _p,
                               _sz, _p]),
     "a8w8_step_graph_create": (_i, [ctypes.POINTER(_p), _p, _p, _i, _i, _i, _p, _p, _p, _i, _p,
@@ -311,6 +313,29 @@ def a8w8_decode_layer(weights: dict, cfg: dict, hidden, slot_mapping, block_tabl
             setattr(t, n, _ptr(taps.get(n)))
     _check(lib().a8w8_decode_layer(
         ctypes.byref(w), ctypes.byref(c), B, _ptr(hidden), _ptr(slot_mapping), _ptr(block_table),
+        block_table.shape[1], num_blocks, _ptr(ctx_lens), _ptr(k_cache), _ptr(v_cache),
+        _ptr(rope), rope.shape[0], _ptr(ws), ws.numel(),
+        None if t is None else ctypes.byref(t), _stream(stream)))
+
+
+def a8w8_prefill_layer(weights: dict, cfg: dict, hidden, slot_mapping, block_table, ctx_lens,
+                       k_cache, v_cache, rope, ws, taps: dict | None = None, stream=None):
+    """One layer over a prefill chunk of M token rows; `hidden` [M, H] bf16 is
+    updated in place. Row r is the token at position ctx_lens[r] - 1 of the
+    sequence whose block table row it carries; all rows' K/V are written
+    before attention, so the chunk is causal."""
+    M = hidden.shape[0]
+    Hkv, D, page = cfg["num_kv_heads"], cfg["head_dim"], cfg["page_size"]
+    num_blocks = k_cache.numel() // (Hkv * D * page)
+    c = make_config(cfg)
+    w = layer_struct(weights)
+    t = None
+    if taps is not None:
+        t = LayerTaps()
+        for n in TAP_FIELDS:
+            setattr(t, n, _ptr(taps.get(n)))
+    _check(lib().a8w8_prefill_layer(
+        ctypes.byref(w), ctypes.byref(c), M, _ptr(hidden), _ptr(slot_mapping), _ptr(block_table),
         block_table.shape[1], num_blocks, _ptr(ctx_lens), _ptr(k_cache), _ptr(v_cache),
         _ptr(rope), rope.shape[0], _ptr(ws), ws.numel(),
         None if t is None else ctypes.byref(t), _stream(stream)))

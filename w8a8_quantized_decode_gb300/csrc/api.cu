@@ -216,7 +216,7 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
                           const int32_t* slot_mapping, const int32_t* block_table, int max_blocks,
                           int num_blocks, const int32_t* ctx_lens, bf16* k_cache, bf16* v_cache,
                           const float* rope, int max_pos, unsigned char* ws, const WsLayout& lay,
-                          const a8w8_layer_taps* taps, const Launch& L) {
+                          const a8w8_layer_taps* taps, const Launch& L, bool prefill = false) {
     const int H = c.hidden, D = c.head_dim, Hq = c.num_q_heads, Hkv = c.num_kv_heads;
     const int I = c.intermediate, NQ = Hq * D, NQKV = NQ + 2 * Hkv * D;
     bf16* qkv = reinterpret_cast<bf16*>(ws + lay.qkv);
@@ -287,7 +287,16 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     a.err = device_error_word();
     a.tap_q_rot = reinterpret_cast<bf16*>(T.q_rot);
     a.tap_k_rot = reinterpret_cast<bf16*>(T.k_rot);
-    e = launch_attention(a, L);
+    if (prefill) {
+        // every token's K/V into the cache first: the chunk's rows attend to
+        // each other's earlier tokens (causal by their context lengths)
+        e = launch_kv_prep(a, L);
+        if (e != cudaSuccess) return cuda_fail(e, "prefill KV write");
+        a.kv_in_cache = true;
+        e = launch_attn_group(a, L);
+    } else {
+        e = launch_attention(a, L);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "attention");
     if (T.attn) {
         e = cudaMemcpyAsync(T.attn, attn, (size_t)B * NQ * 2, cudaMemcpyDeviceToDevice, L.stream);
@@ -631,6 +640,43 @@ a8w8_status a8w8_decode_layer(const a8w8_layer_weights* w, const a8w8_config* cf
                          max_blocks, num_blocks, ctx_lens, reinterpret_cast<bf16*>(k_cache),
                          reinterpret_cast<bf16*>(v_cache), rope, max_pos,
                          static_cast<unsigned char*>(ws), lay, taps, L);
+}
+
+a8w8_status a8w8_prefill_layer(const a8w8_layer_weights* w, const a8w8_config* cfg, int M,
+                               a8w8_bf16* hidden, const int32_t* slot_mapping,
+                               const int32_t* block_table, int max_blocks, int num_blocks,
+                               const int32_t* ctx_lens, a8w8_bf16* k_cache, a8w8_bf16* v_cache,
+                               const float* rope, int max_pos, void* ws, size_t ws_bytes,
+                               const a8w8_layer_taps* taps, void* stream) {
+    if (M < 1 || M > 16384) return fail(A8W8_ERR_UNSUPPORTED_SHAPE, "M=%d outside [1, 16384]", M);
+    a8w8_status s = check_layer_common(cfg, 1, max_blocks, num_blocks, rope, max_pos);
+    if (s != A8W8_OK) return s;
+    if ((s = check_layer_weights(w)) != A8W8_OK) return s;
+    if ((s = check_ptrs({hidden, slot_mapping, block_table, ctx_lens, k_cache, v_cache, rope},
+                        "a8w8_prefill_layer")) != A8W8_OK)
+        return s;
+    {
+        AttnParams probe = {};
+        probe.fused = true;
+        probe.tickets = reinterpret_cast<unsigned*>(16);   // shape check only
+        probe.Hq = cfg->num_q_heads;
+        probe.Hkv = cfg->num_kv_heads;
+        probe.D = cfg->head_dim;
+        probe.page = cfg->page_size;
+        probe.max_blocks = max_blocks;
+        if (!attn_group_supported(probe))
+            return fail(A8W8_ERR_UNSUPPORTED_SHAPE,
+                        "prefill attention needs Hq/Hkv <= 7 and at most 64 chunks of 128 tokens");
+    }
+    const WsLayout lay = ws_layout(*cfg, M, max_blocks);
+    if (!ws || ws_bytes < lay.total || !aligned16(ws))
+        return fail(A8W8_ERR_WORKSPACE, "prefill layer workspace needs %zu bytes", lay.total);
+    Launch L = make_launch(stream, true);
+    if (L.num_sms <= 0) return fail(A8W8_ERR_CUDA, "no CUDA device");
+    return enqueue_layer(w, *cfg, M, reinterpret_cast<bf16*>(hidden), slot_mapping, block_table,
+                         max_blocks, num_blocks, ctx_lens, reinterpret_cast<bf16*>(k_cache),
+                         reinterpret_cast<bf16*>(v_cache), rope, max_pos,
+                         static_cast<unsigned char*>(ws), lay, taps, L, true);
 }
 
 static a8w8_status check_step(const a8w8_model* m, const a8w8_config* cfg, int B, int max_blocks,

@@ -114,6 +114,9 @@ __global__ void __launch_bounds__(kGrpThreads) attn_group_kernel(const AttnParam
         const int bk = p.block_table[(size_t)b * p.max_blocks + tok / p.page];
         blk[t] = (bk < 0 || bk >= p.num_blocks) ? -1 : bk;
     }
+    // prefill: the cache rows of this launch's tokens are written by the
+    // kernel before, so they are read only after the dependency wait
+    if (p.kv_in_cache) pdl_wait();
     __syncthreads();
     // rows of the cached tokens of `cache` into the tile (zeros for a bad block)
     auto load_tile = [&](const bf16* cache) {
@@ -168,7 +171,7 @@ __global__ void __launch_bounds__(kGrpThreads) attn_group_kernel(const AttnParam
         const long slot = p.slot_mapping[b];
         const long num_slots = (long)p.num_blocks * p.page;
         const bool slot_ok = slot >= 0 && slot < num_slots;
-        if (lane == 0 && slot >= num_slots) set_error(p.err, 0x1u);
+        if (lane == 0 && slot >= num_slots && !p.kv_in_cache) set_error(p.err, 0x1u);
 #pragma unroll
         for (int e = 0; e < E; ++e) {
             const int d = lane * E + e;
@@ -176,11 +179,11 @@ __global__ void __launch_bounds__(kGrpThreads) attn_group_kernel(const AttnParam
             const bf16 vb = f2bf(vv[e]);
             Ts[(size_t)tr * DP + d] = kb;
             vnew[d] = vb;
-            if (slot_ok) {
+            if (slot_ok && !p.kv_in_cache) {
                 p.k_cache[((size_t)slot * p.Hkv + kvh) * D + d] = kb;
                 p.v_cache[((size_t)slot * p.Hkv + kvh) * D + d] = vb;
             }
-            if (p.tap_k_rot) p.tap_k_rot[((size_t)b * p.Hkv + kvh) * D + d] = kb;
+            if (p.tap_k_rot && !p.kv_in_cache) p.tap_k_rot[((size_t)b * p.Hkv + kvh) * D + d] = kb;
         }
     }
     cp_async_wait_all();
@@ -365,7 +368,67 @@ __global__ void __launch_bounds__(kGrpThreads) attn_group_kernel(const AttnParam
     }
 }
 
+// Prefill pre-pass: one CTA per row, warp w handles KV heads w, w + 8, ...:
+// per-head RMSNorm and RoPE of the row's new K (the attention's own code),
+// then K and V into the row's cache slot.
+constexpr int kPrepKvThreads = 256;
+template <int D>
+__global__ void __launch_bounds__(kPrepKvThreads) kv_prep_kernel(const AttnParams p) {
+    constexpr int E = D / 32;
+    const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int max_ctx = p.max_blocks * p.page;
+    const int ctx_raw = p.ctx_lens[b];
+    const bool bad_ctx = ctx_raw < 0 || ctx_raw > max_ctx;
+    const int pos = ctx_raw - 1;
+    const bool bad_pos = !bad_ctx && ctx_raw > 0 && pos >= p.max_pos;
+    const bool live = !bad_ctx && !bad_pos && ctx_raw > 0;
+    HeadPre<D> hp;
+    if (live) load_head_pre<D>(p, pos, lane, hp);
+    pdl_wait();
+    pdl_trigger();
+    if (!live) return;   // the attention kernel flags bad contexts and positions
+    const long slot = p.slot_mapping[b];
+    const long num_slots = (long)p.num_blocks * p.page;
+    if (threadIdx.x == 0 && slot >= num_slots) set_error(p.err, 0x1u);
+    const bool slot_ok = slot >= 0 && slot < num_slots;
+    const int NQ = p.Hq * D, NK = p.Hkv * D;
+    const bf16* row = p.q + (size_t)b * p.q_stride;
+    for (int kvh = warp; kvh < p.Hkv; kvh += kPrepKvThreads / 32) {
+        float x[E], vv[E], y[E];
+        load_bf16_lane<D>(row + NQ + (size_t)kvh * D + lane * E, x);
+        load_bf16_lane<D>(row + NQ + NK + (size_t)kvh * D + lane * E, vv);
+        norm_rope_head<D>(x, hp.kw, hp, p.eps, lane, y);
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const int d = lane * E + e;
+            const bf16 kb = f2bf(y[e]);
+            if (slot_ok) {
+                p.k_cache[((size_t)slot * p.Hkv + kvh) * D + d] = kb;
+                p.v_cache[((size_t)slot * p.Hkv + kvh) * D + d] = f2bf(vv[e]);
+            }
+            if (p.tap_k_rot) p.tap_k_rot[((size_t)b * p.Hkv + kvh) * D + d] = kb;
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_kv_prep(const AttnParams& p, const Launch& L) {
+    if (p.B == 0) return cudaSuccess;
+    if (!p.fused || (p.D != 128 && p.D != 64)) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.B);
+    cfg.blockDim = dim3(kPrepKvThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = L.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = L.pdl ? 1 : 0;
+    if (p.D == 128) return cudaLaunchKernelEx(&cfg, kv_prep_kernel<128>, p);
+    return cudaLaunchKernelEx(&cfg, kv_prep_kernel<64>, p);
+}
 
 bool attn_group_supported(const AttnParams& p) {
     const int max_ctx = p.max_blocks * p.page;

@@ -102,6 +102,8 @@ struct AttnParams {
     unsigned* err;
     bf16* tap_q_rot;        // [B, Hq, D] or null
     bf16* tap_k_rot;        // [B, Hkv, D] or null
+    bool kv_in_cache;       // every row's new K/V was written by launch_kv_prep
+                            // (prefill: rows attend to each other's tokens)
 };
 
 // Tokens per attention CTA and the number of CTAs per (request, KV head).
@@ -118,6 +120,9 @@ cudaError_t launch_attention(const AttnParams& p, const Launch& L);
 bool attn_group_supported(const AttnParams& p);
 int attn_group_splits(int max_ctx);
 cudaError_t launch_attn_group(const AttnParams& p, const Launch& L);
+// Prefill: per-head K RMSNorm + RoPE of every row's new token and the K/V
+// write into the cache, before the attention (fused QKV rows in p.q).
+cudaError_t launch_kv_prep(const AttnParams& p, const Launch& L);
 
 // ---------------------------------------------------------------------------
 // Embedding, RoPE table, LM head + argmax
