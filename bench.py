@@ -501,6 +501,116 @@ def run_batched(args, cfg):
         torch.distributed.destroy_process_group()
 
 
+PREFILL_SEQS, PREFILL_LEN = 4, 512
+PREFILL_WORKLOAD = "qwen3_14b_a8w8_prefill_chunk_4x512"
+PREFILL_METRIC = "A8W8 prefill chunk through one layer (ms, 4 x 512 tokens)"
+# mma.sync m16n8k32 INT8 rate measured on this GPU with a register-only loop
+# (8 independent accumulators per warp, 32 warps per SM)
+MMA_S8_TOPS_MEASURED = 150.2
+
+
+def run_prefill(args, cfg):
+    """One layer over the pages' prefill chunk: 4 sequences x 512 tokens."""
+    import torch
+    import w8a8_quantized_decode_gb300 as a8w8
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    a8w8.build()
+    cfg = dict(cfg, num_layers=1)
+    page = cfg["page_size"]
+    Hkv, D, H = cfg["num_kv_heads"], cfg["head_dim"], cfg["hidden"]
+    M = PREFILL_SEQS * PREFILL_LEN
+    bt_seq, nblk = synth.paged_layout(SEED + 31, [PREFILL_LEN] * PREFILL_SEQS, page,
+                                      spare_blocks=1)
+    rows = np.repeat(np.arange(PREFILL_SEQS), PREFILL_LEN)
+    pos = np.tile(np.arange(PREFILL_LEN), PREFILL_SEQS)
+    bt = bt_seq[rows].astype(np.int32)
+    ctx = (pos + 1).astype(np.int32)
+    slots = (bt_seq[rows, pos // page] * page + pos % page).astype(np.int32)
+    w = synth.t_layer_weights(cfg, SEED, 0, device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(SEED + 32)
+    hidden = torch.randn((M, H), generator=gen, device=device).to(torch.bfloat16)
+    kc = torch.zeros((nblk * page, Hkv, D), dtype=torch.bfloat16, device=device)
+    vc = torch.zeros_like(kc)
+    rope = a8w8.a8w8_rope_table(bt.shape[1] * page, D, cfg["rope_theta"], device=device)
+    ws = a8w8.alloc_workspace(cfg, M, bt.shape[1], device=device)
+    d_bt, d_ctx, d_slot = (torch.from_numpy(x).to(device) for x in (bt, ctx, slots))
+    h0 = hidden.clone()
+    stream = torch.cuda.Stream(device)
+    times = []
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            hidden.copy_(h0)
+            a8w8.a8w8_prefill_layer(w, cfg, hidden, d_slot, d_bt, d_ctx, kc, vc, rope, ws,
+                                    stream=stream)
+        stream.synchronize()
+        gpu_uuid = None
+        try:
+            gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+        except Exception:
+            pass
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        with ClockSampler(gpu_uuid) as clocks:
+            for _ in range(args.steps):
+                hidden.copy_(h0)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                a8w8.a8w8_prefill_layer(w, cfg, hidden, d_slot, d_bt, d_ctx, kc, vc, rope, ws,
+                                        stream=stream)
+                e1.record(stream)
+                e1.synchronize()
+                times.append(e0.elapsed_time(e1))
+        errs = a8w8.read_device_errors(stream)
+    ms = sum(times) / len(times)
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    ops = 2.0 * M * (cfg["hidden"] * ((cfg["num_q_heads"] + 2 * Hkv) * D) +
+                      cfg["num_q_heads"] * D * cfg["hidden"] + 2 * cfg["intermediate"] * cfg["hidden"]
+                      + cfg["intermediate"] * cfg["hidden"])
+    attn_flops = 4.0 * PREFILL_SEQS * (PREFILL_LEN * (PREFILL_LEN + 1) / 2) * cfg["num_q_heads"] * D
+    tops = ops / (ms * 1e-3) / 1e12
+    # INT8 projections (4 per layer, 16-row tensor-core tiles) + quantisation, KV
+    # pre-pass, attention
+    n_launch = 4 * ((M + 15) // 16) + 4 + 1 + 1
+    if rank == 0:
+        line = {
+            "metric": PREFILL_METRIC, "value": ms, "unit": "ms/chunk-layer", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int8 x int8 -> int32, f32 dequant, bf16 activations",
+            "data": "synthetic (seeded random-init weights and hidden states on the device)",
+            "config": {"workload": PREFILL_WORKLOAD, "sequences": PREFILL_SEQS,
+                       "tokens_per_sequence": PREFILL_LEN, "M": M, "layers": 1,
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "tokens_per_s": M * 1000.0 / ms * world,
+            "int8_tops": tops,
+            "attention_flop": attn_flops,
+            "roofline": {"bound": "tensor", "kernel": "INT8 mma.sync projections",
+                         "achieved": tops, "peak": MMA_S8_TOPS_MEASURED, "unit": "TOP/s",
+                         "frac": tops / MMA_S8_TOPS_MEASURED, "traffic": None,
+                         "peak_source": "measured mma.sync s8 rate on this GPU (register-only "
+                                        "microbenchmark); no INT8 figure in MEASURED_PEAKS.json"},
+            "e2e": None,
+            "gpu_launches": n_launch * args.steps,
+            "clocks": clocks.summary(),
+            "device_errors": errs,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def cpu_baseline(model, cfg):
     """The oracle on a bounded sample: decode steps until about 20 s of CPU time."""
     import torch
@@ -522,12 +632,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["decode_b1", "batched16"], default="decode_b1")
+    ap.add_argument("--workload", choices=["decode_b1", "batched16", "prefill"],
+                    default="decode_b1")
     ap.add_argument("--layers", type=int, default=40,
                     help="layers of the model (fewer only for profiling captures)")
     args = ap.parse_args()
     if args.steps is None:
-        args.steps = 32 if args.workload == "batched16" else 48
+        args.steps = {"batched16": 32, "prefill": 5}.get(args.workload, 48)
     if args.warmup < 3:
         raise SystemExit("warmup must be >= 3")
     cfg = dict(synth.QWEN3_14B, num_layers=args.layers)
@@ -535,6 +646,8 @@ def main():
         run_reference(args, cfg)
     elif args.workload == "batched16":
         run_batched(args, cfg)
+    elif args.workload == "prefill":
+        run_prefill(args, cfg)
     else:
         run_ours(args, cfg)
 
