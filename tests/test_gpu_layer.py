@@ -212,16 +212,26 @@ def test_qwen3_14b_layer_grouped_attention_b2(a8w8):
 # Prefill chunk: M token rows through the layer at once (causal by ctx_lens)
 # ---------------------------------------------------------------------------
 
-def test_tiny_prefill_chunk(a8w8):
-    # three sequences of 21 new tokens after 0, 5 and 17 cached ones
+def test_tiny_prefill_chunk_small(a8w8):
+    # three sequences of 7 new tokens after 0, 5 and 17 cached ones (21 rows:
+    # the 16-row tensor-core projections)
     cfg = synth.TINY
-    case = synth.prefill_case(cfg, [21, 21, 21], prior_ctx=[0, 5, 17], seed_base=201)
+    case = synth.prefill_case(cfg, [7, 7, 7], prior_ctx=[0, 5, 17], seed_base=200)
+    _layer_parity(a8w8, cfg, case, prefill=True)
+
+
+def test_tiny_prefill_chunk(a8w8):
+    # three sequences of 40 new tokens after 0, 5 and 17 cached ones (120 rows:
+    # the tiled GEMM, a partial 128-row tile)
+    cfg = synth.TINY
+    case = synth.prefill_case(cfg, [40, 40, 40], prior_ctx=[0, 5, 17], seed_base=201)
     _layer_parity(a8w8, cfg, case, prefill=True)
 
 
 def test_qwen3_14b_prefill_chunk(a8w8):
+    # 80 rows through the tiled GEMM at the Qwen3-14B shapes
     cfg = dict(synth.QWEN3_14B, num_layers=1)
-    case = synth.prefill_case(cfg, [24, 24], prior_ctx=[0, 130], seed_base=202)
+    case = synth.prefill_case(cfg, [40, 40], prior_ctx=[0, 130], seed_base=202)
     _layer_parity(a8w8, cfg, case, prefill=True)
 
 

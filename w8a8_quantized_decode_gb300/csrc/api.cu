@@ -81,8 +81,11 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Workspace layout shared by the layer and the step.
 struct WsLayout {
-    size_t hid, qkv, attn, act, qx, qs, part, att_tk, keys, ticket, bar, total;
+    size_t hid, qkv, attn, act, qx, qs, gacc, part, att_tk, keys, ticket, bar, total;
 };
+
+// Row counts above this use the tiled GEMM (prefill chunks).
+constexpr int kGemmMinRows = 64;
 
 WsLayout ws_layout(const a8w8_config& c, int B, int max_blocks) {
     const int D = c.head_dim;
@@ -102,6 +105,11 @@ WsLayout ws_layout(const a8w8_config& c, int B, int max_blocks) {
     o = round_up(o + (size_t)B * std::max({c.hidden, c.num_q_heads * D, c.intermediate}), 256);
     w.qs = o;
     o = round_up(o + (size_t)B * 4, 256);
+    // INT32 results of the tiled GEMM (prefill-sized batches only)
+    w.gacc = o;
+    if (B > kGemmMinRows)
+        o = round_up(o + (size_t)B * std::max({nqkv, (size_t)2 * c.intermediate,
+                                               (size_t)2 * c.hidden}) * 4, 256);
     w.part = o;
     const int max_ctx = max_blocks * c.page_size;
     o = round_up(o + std::max(attn_part_bytes(B, c.num_q_heads, D, max_ctx, true),
@@ -164,8 +172,20 @@ bool use_mma(int M, int K, int ks) { return M >= kMmaMinBatch && gemv_mma_suppor
 // Runs a projection over batch tiles. `qx` / `qs` (room for M rows of K
 // codes and M scales) receive the quantised rows on the tensor-core path.
 cudaError_t run_gemv(int pro, int epi, int ks, GemvParams p, int M, const Launch& L,
-                     int8_t* qx = nullptr, float* qs = nullptr) {
+                     int8_t* qx = nullptr, float* qs = nullptr, int32_t* gacc = nullptr) {
     const int Ntot = (epi == EPI_SWIGLU) ? 2 * p.N : p.N;
+    if (M > kGemmMinRows && gacc && gemm_supported(p.K, ks) && (pro == PRO_I8 || (qx && qs)) &&
+        !p.acc_out) {
+        p.err = device_error_word();
+        p.M = M;
+        if (pro != PRO_I8) {
+            cudaError_t e = launch_quant_prep(pro, p, qx, qs, L);
+            if (e != cudaSuccess) return e;
+            p.xq = qx;
+            p.x_scale = qs;
+        }
+        return launch_gemm_projection(epi, ks, p, gacc, L);
+    }
     if (use_mma(M, p.K, ks) && (pro == PRO_I8 || (qx && qs))) {
         p.err = device_error_word();
         if (pro != PRO_I8) {
@@ -226,6 +246,7 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     unsigned* att_tk = reinterpret_cast<unsigned*>(ws + lay.att_tk);
     int8_t* qx = reinterpret_cast<int8_t*>(ws + lay.qx);
     float* qs = reinterpret_cast<float*>(ws + lay.qs);
+    int32_t* gacc = B > kGemmMinRows ? reinterpret_cast<int32_t*>(ws + lay.gacc) : nullptr;
     const a8w8_layer_taps none = {};
     const a8w8_layer_taps& T = taps ? *taps : none;
 
@@ -246,7 +267,7 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     g.tap_s = T.xs;
     g.clear = att_tk;   // the attention that follows counts its splits there
     g.clear_n = B * Hq;
-    cudaError_t e = run_gemv(PRO_NORM_QUANT, EPI_STORE, 1, g, B, L, qx, qs);
+    cudaError_t e = run_gemv(PRO_NORM_QUANT, EPI_STORE, 1, g, B, L, qx, qs, gacc);
     if (e != cudaSuccess) return cuda_fail(e, "QKV projection");
     if (T.qkv) {
         e = cudaMemcpyAsync(T.qkv, qkv, (size_t)B * NQKV * 2, cudaMemcpyDeviceToDevice, L.stream);
@@ -316,7 +337,7 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     g.ldy = H;
     g.tap_q = T.aq;
     g.tap_s = T.as;
-    e = run_gemv(PRO_QUANT, EPI_STORE, 1, g, B, L, qx, qs);
+    e = run_gemv(PRO_QUANT, EPI_STORE, 1, g, B, L, qx, qs, gacc);
     if (e != cudaSuccess) return cuda_fail(e, "O projection");
     if (T.h1) {
         e = cudaMemcpyAsync(T.h1, hidden, (size_t)B * H * 2, cudaMemcpyDeviceToDevice, L.stream);
@@ -338,7 +359,7 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     g.tap_x = reinterpret_cast<bf16*>(T.hn);
     g.tap_q = T.hq;
     g.tap_s = T.hs;
-    e = run_gemv(PRO_NORM_QUANT, EPI_SWIGLU, 1, g, B, L, qx, qs);
+    e = run_gemv(PRO_NORM_QUANT, EPI_SWIGLU, 1, g, B, L, qx, qs, gacc);
     if (e != cudaSuccess) return cuda_fail(e, "Gate/Up projection");
     if (T.act) {
         e = cudaMemcpyAsync(T.act, act, (size_t)B * I * 2, cudaMemcpyDeviceToDevice, L.stream);
@@ -358,7 +379,7 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     g.ldy = H;
     g.tap_q = T.actq;
     g.tap_s = T.acts;
-    e = run_gemv(PRO_QUANT, EPI_STORE, c.down_k_splits, g, B, L, qx, qs);
+    e = run_gemv(PRO_QUANT, EPI_STORE, c.down_k_splits, g, B, L, qx, qs, gacc);
     if (e != cudaSuccess) return cuda_fail(e, "down projection");
     return A8W8_OK;
 }

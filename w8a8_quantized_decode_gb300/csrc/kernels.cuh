@@ -70,6 +70,14 @@ cudaError_t launch_gemv_mma(int epilogue, int k_splits, const GemvParams& p, con
 cudaError_t launch_quant_prep(int prologue, const GemvParams& p, int8_t* xq, float* xs,
                               const Launch& L);
 
+// Prefill-sized projections (many rows): tiled tensor-core GEMM with an exact
+// INT32 result in acc (gemm_acc_bytes), then the dequantisation epilogue.
+// PRO_I8 input (p.xq, p.x_scale); K a multiple of 64 * k_splits.
+bool gemm_supported(int K, int k_splits);
+size_t gemm_acc_bytes(int M, int N, int epilogue, int k_splits);
+cudaError_t launch_gemm_projection(int epilogue, int k_splits, const GemvParams& p, int32_t* acc,
+                                   const Launch& L);
+
 // ---------------------------------------------------------------------------
 // KV write and paged decode attention
 // ---------------------------------------------------------------------------
