@@ -30,6 +30,8 @@ constexpr int kBM = 128, kBN = 128, kBK = 64;
 constexpr int kGemmThreads = 256;
 constexpr int kChunkSteps = 16;          // steps per exact float32 chunk
 constexpr int kHP = kBK + 8;             // FP16 tile row pitch (halves)
+constexpr int kCP = kBN + 4;             // INT32 tile row pitch (words): the 8 rows
+                                         // a flush instruction touches fall in 8 bank groups
 
 struct GemmSmem {
     size_t a8, b8, ah, bh, c, total;
@@ -40,8 +42,8 @@ __host__ __device__ inline GemmSmem gemm_smem() {
     s.b8 = s.a8 + (size_t)2 * kBM * kBK;             // [2][BN][BK] int8
     s.ah = s.b8 + (size_t)2 * kBN * kBK;             // [BM][kHP] f16
     s.bh = s.ah + (size_t)kBM * kHP * 2;             // [BN][kHP] f16
-    s.c = s.bh + (size_t)kBN * kHP * 2;              // [BM][BN] int32
-    s.total = s.c + (size_t)kBM * kBN * 4;
+    s.c = s.bh + (size_t)kBN * kHP * 2;              // [BM][kCP] int32
+    s.total = s.c + (size_t)kBM * kCP * 4;
     return s;
 }
 
@@ -92,14 +94,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t = lane & 3;
-    const int n0 = blockIdx.x * kBN, m0 = blockIdx.y * kBM;
+    // M tiles vary fastest: the CTAs that share a weight tile run together and
+    // read it from L2 after the first
+    const int m0 = blockIdx.x * kBM, n0 = blockIdx.y * kBN;
     const int wm = warp >> 2, wn = warp & 3;     // warp tile rows wm*64, cols wn*32
     const int steps = (k1 - k0) / kBK;
 
     pdl_wait();
     pdl_trigger();
 
-    for (int i = tid; i < kBM * kBN; i += kGemmThreads) sc[i] = 0;
+    for (int i = tid; i < kBM * kCP; i += kGemmThreads) sc[i] = 0;
 
     // copies of step s into stage s & 1: 512 16-byte pieces per operand, 2 per thread
     auto issue = [&](int s) {
@@ -193,7 +197,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     for (int e = 0; e < 4; ++e) {
                         const int r = wm * 64 + i * 16 + g + ((e >> 1) << 3);
                         const int c = wn * 32 + j * 8 + 2 * t + (e & 1);
-                        sc[r * kBN + c] += __float2int_rn(acc[i][j][e]);
+                        sc[r * kCP + c] += __float2int_rn(acc[i][j][e]);
                         acc[i][j][e] = 0.0f;
                     }
         }
@@ -202,7 +206,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     for (int i = tid; i < kBM * kBN / 4; i += kGemmThreads) {
         const int r = (i * 4) / kBN, c = (i * 4) % kBN;
         if (m0 + r >= M) continue;
-        const int4 v = *reinterpret_cast<const int4*>(sc + r * kBN + c);
+        const int4 v = *reinterpret_cast<const int4*>(sc + r * kCP + c);
         int32_t* dst = C + (size_t)(m0 + r) * ldc + n0 + c;
         if (n0 + c + 3 < N && (ldc & 3) == 0) {
             *reinterpret_cast<int4*>(dst) = v;
@@ -294,7 +298,7 @@ cudaError_t launch_gemm_projection(int epilogue, int k_splits, const GemvParams&
         if (e != cudaSuccess) return e;
         configured_dev = dev;
     }
-    const dim3 grid((Nc + kBN - 1) / kBN, (p.M + kBM - 1) / kBM);
+    const dim3 grid((p.M + kBM - 1) / kBM, (Nc + kBN - 1) / kBN);
     const int Ks = p.K / k_splits;
     for (int s = 0; s < k_splits; ++s) {
         cudaError_t e = launch_pdl(gemm_i8_kernel, grid, dim3(kGemmThreads), smem, L, p.xq, p.K, p.W,
