@@ -141,3 +141,25 @@ def test_rope_table_validation(lib):
     assert lib.a8w8_rope_table(FAKE, 16, 64, 0.0, None) == a8w8.ERR_INVALID_ARG
     assert lib.a8w8_rope_table(None, 16, 64, 1e6, None) == a8w8.ERR_INVALID_ARG
     assert lib.a8w8_rope_table(None, 0, 64, 1e6, None) == a8w8.OK
+
+
+def test_prefill_layer_validation(lib):
+    L = lib
+    q = synth.QWEN3_14B
+    w = a8w8.LayerWeights(*([FAKE] * len(a8w8.WEIGHT_FIELDS)))
+
+    def call(cfg, M=64, max_blocks=4, wsb=1 << 34, wptr=w):
+        return L.a8w8_prefill_layer(ctypes.byref(wptr), _cfg(cfg), M, FAKE, FAKE, FAKE, max_blocks,
+                                    8, FAKE, FAKE, FAKE, FAKE, 512, FAKE, wsb, None, None)
+    assert call(q, M=0) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert call(q, M=16385) == a8w8.ERR_UNSUPPORTED_SHAPE
+    # grouped attention: at most 7 query heads per KV head, 64 chunks of 128 tokens
+    assert call(dict(q, num_kv_heads=5)) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert call(q, max_blocks=65) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert b"prefill attention" in L.a8w8_last_error()
+    # the workspace grows with M (the GEMM's INT32 results for M > 64 rows)
+    need = L.a8w8_workspace_bytes(_cfg(q), 2048, 4)
+    assert need > L.a8w8_workspace_bytes(_cfg(q), 64, 4) * 8
+    assert call(q, M=2048, wsb=need - 1) == a8w8.ERR_WORKSPACE
+    nullw = a8w8.LayerWeights(*([None] * len(a8w8.WEIGHT_FIELDS)))
+    assert call(q, wptr=nullw) == a8w8.ERR_INVALID_ARG
