@@ -651,3 +651,88 @@ def test_prefill_chunk_equals_sequential_decode():
                                         case["block_table"][4:5], case["ctx_lens"][4:5],
                                         case["k_cache"].copy(), case["v_cache"].copy())
     assert not np.array_equal(h_alone[0], out[4])
+
+
+# ---------------------------------------------------------------------------
+# Sampling beyond greedy (oracle/sampling.py)
+# ---------------------------------------------------------------------------
+
+from oracle import sampling  # noqa: E402
+
+
+def test_philox_is_a_deterministic_bijection_with_uniform_words():
+    n = 1 << 16
+    i = np.arange(n, dtype=np.uint64)
+    z = np.zeros(n, np.uint64)
+    w = sampling.philox4x32_10(i, z, z, z, 7, 9)
+    w2 = sampling.philox4x32_10(i, z, z, z, 7, 9)
+    assert all(np.array_equal(a, b) for a, b in zip(w, w2))
+    # a bijection of the 128-bit counter for a fixed key: distinct counters,
+    # distinct outputs (checked on the full 128-bit words)
+    packed = set(zip(*(x.tolist() for x in w)))
+    assert len(packed) == n
+    # another key changes every output word
+    v = sampling.philox4x32_10(i, z, z, z, 8, 9)
+    assert (w[0] != v[0]).mean() > 0.99
+    # each word uniform over 32 bits: 16-bin chi-square and bit balance
+    for x in w:
+        counts = np.bincount((x >> np.uint64(28)).astype(np.int64), minlength=16)
+        chi2 = ((counts - n / 16) ** 2 / (n / 16)).sum()
+        assert chi2 < 60, chi2           # 15 degrees of freedom: p ~ 1e-7 at 60
+        bits = np.unpackbits(x.astype(np.uint32).view(np.uint8)).mean()
+        assert abs(bits - 0.5) < 0.005
+
+
+def test_uniforms_open_interval_and_stream_independence():
+    u = sampling.uniforms(100_000, 3, seed=12345, step=7)
+    assert u.min() > 0.0 and u.max() < 1.0
+    assert abs(u.mean() - 0.5) < 0.005
+    u2 = sampling.uniforms(100_000, 4, seed=12345, step=7)
+    u3 = sampling.uniforms(100_000, 3, seed=12345, step=8)
+    assert abs(np.corrcoef(u, u2)[0, 1]) < 0.01 and abs(np.corrcoef(u, u3)[0, 1]) < 0.01
+
+
+def test_sampling_greedy_limits():
+    rng = np.random.default_rng(5)
+    logits = rng.normal(size=(3, 1000)).astype(np.float32)
+    logits[1, 17] = logits[1].max()          # a tie: lowest index wins
+    am = np.array([np.argmax(r) for r in logits])
+    assert am[1] == 17
+    assert np.array_equal(sampling.sample_rows(logits, 0.0, 1.0, 1, 0), am)
+    tied = set(np.nonzero(logits[1] == logits[1].max())[0].tolist())
+    assert len(tied) == 2
+    seen = set()
+    for s in range(40):
+        # a tiny nucleus holds the maximum alone (both tied maxima in row 1,
+        # each drawn with probability 1/2); a tiny temperature likewise
+        for x in (sampling.sample_rows(logits, 1.0, 1e-9, s, s),
+                  sampling.sample_rows(logits, 1e-6, 1.0, s, s)):
+            assert x[0] == am[0] and x[2] == am[2] and x[1] in tied
+            seen.add(int(x[1]))
+    assert seen == tied
+
+
+def test_sampling_distribution_is_the_softmax():
+    logits = np.array([[1.0, 0.0, -1.0, 2.0, 0.5, -3.0]], np.float32)
+    T = 0.8
+    p = np.exp(logits[0] / T) / np.exp(logits[0] / T).sum()
+    n = 30_000
+    draws = np.array([sampling.sample_rows(logits, T, 1.0, 99, s)[0] for s in range(n)])
+    freq = np.bincount(draws, minlength=6) / n
+    sigma = np.sqrt(p * (1 - p) / n)
+    assert (np.abs(freq - p) < 5 * sigma + 1e-4).all(), (freq, p)
+
+
+def test_sampling_nucleus_renormalises():
+    # probabilities 0.5, 0.3, 0.1, 0.05, 0.05: top_p 0.75 keeps {0, 1}
+    p = np.array([0.5, 0.3, 0.1, 0.05, 0.05])
+    logits = np.log(p)[None, :].astype(np.float32)
+    keep = sampling.nucleus(np.log(p) - np.log(p).max(), 0.75)
+    assert keep.tolist() == [True, True, False, False, False]
+    # the boundary tie is kept whole: top_p 0.92 reaches into the 0.05 pair
+    assert sampling.nucleus(np.log(p) - np.log(p).max(), 0.92).tolist() == [True] * 5
+    n = 20_000
+    draws = np.array([sampling.sample_rows(logits, 1.0, 0.75, 3, s)[0] for s in range(n)])
+    freq = np.bincount(draws, minlength=5) / n
+    assert freq[2:].sum() == 0
+    assert abs(freq[0] - 0.625) < 5 * np.sqrt(0.625 * 0.375 / n)
