@@ -621,6 +621,48 @@ def run_prefill(args, cfg):
         torch.distributed.destroy_process_group()
 
 
+def run_sample(args, cfg):
+    """Device-side sampling over the 151936-token vocabulary (rank 0 only):
+    microseconds per call at batch 1 and 16, greedy, temperature and top-p."""
+    import torch
+    import w8a8_quantized_decode_gb300 as a8w8
+
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    a8w8.build()
+    V = cfg["vocab"]
+    gen = torch.Generator(device=device)
+    gen.manual_seed(SEED + 41)
+    res = {}
+    for B in (1, 16):
+        logits = torch.randn((B, V), generator=gen, device=device) * 2.0
+        out = torch.empty(B, dtype=torch.int32, device=device)
+        ws = torch.empty(a8w8.lib().a8w8_sample_workspace_bytes(B, V), dtype=torch.uint8,
+                         device=device)
+        for name, T, p in (("greedy", 0.0, 1.0), ("temperature", 0.7, 1.0), ("top_p", 0.7, 0.9)):
+            for s in range(args.warmup):
+                a8w8.a8w8_sample(logits, T, p, 1, s, out=out, ws=ws)
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for s in range(args.steps):
+                a8w8.a8w8_sample(logits, T, p, 1, s, out=out, ws=ws)
+            e1.record()
+            e1.synchronize()
+            res[f"b{B}_{name}_us"] = e0.elapsed_time(e1) * 1000.0 / args.steps
+    line = {"metric": "device sampling over 151936 logits (us per call)",
+            "value": res["b1_top_p_us"], "unit": "us/call", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": False, "vs_baseline": None,
+            "dtype": "f32 logits, two-float softmax masses, f32 Gumbel keys",
+            "data": "synthetic N(0, 2^2) logits", "config": {"workload": "sample", "vocab": V},
+            "detail": res}
+    print(json.dumps(line), flush=True)
+
+
 def cpu_baseline(model, cfg):
     """The oracle on a bounded sample: decode steps until about 20 s of CPU time."""
     import torch
@@ -642,13 +684,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["decode_b1", "batched16", "prefill"],
+    ap.add_argument("--workload", choices=["decode_b1", "batched16", "prefill", "sample"],
                     default="decode_b1")
     ap.add_argument("--layers", type=int, default=40,
                     help="layers of the model (fewer only for profiling captures)")
     args = ap.parse_args()
     if args.steps is None:
-        args.steps = {"batched16": 32, "prefill": 5}.get(args.workload, 48)
+        args.steps = {"batched16": 32, "prefill": 5, "sample": 20}.get(args.workload, 48)
     if args.warmup < 3:
         raise SystemExit("warmup must be >= 3")
     cfg = dict(synth.QWEN3_14B, num_layers=args.layers)
@@ -658,6 +700,8 @@ def main():
         run_batched(args, cfg)
     elif args.workload == "prefill":
         run_prefill(args, cfg)
+    elif args.workload == "sample":
+        run_sample(args, cfg)
     else:
         run_ours(args, cfg)
 

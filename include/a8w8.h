@@ -255,6 +255,28 @@ a8w8_status paged_decode_attention_bf16_noalloc(const a8w8_bf16* q, const a8w8_b
  * rope: device [max_pos, 2 * D] float. */
 a8w8_status a8w8_rope_table(float* rope, int max_pos, int D, double theta, void* stream);
 
+/* Sampling beyond greedy, on the device ([SRV-48] "Performance": the greedy
+ * step is temperature 0, top_p 1; [SRV-61] "Related": device-side sampling).
+ * logits: device [B, ld] float32 (e.g. the logits output of a8w8_decode_step);
+ * next_tokens: device [B] int32. Per row: temperature <= 0 gives the argmax
+ * (lowest index on ties). Otherwise z = (l - max l) / temperature and
+ * p = exp(z); for top_p < 1 the nucleus is {float(p) >= tau} with tau the
+ * largest such value whose tokens carry at least top_p of the mass (ties at
+ * tau kept); the token is the argmax over the nucleus of z_i + g_i with
+ * g_i = -log(-log(u_i)), a draw from softmax(z) on the nucleus (Gumbel-max
+ * rule). u_i = (floor(x / 2^8) + 1/2) / 2^24 with x the first word of
+ * Philox4x32-10, key (seed low 32 bits, seed high 32 bits), counter
+ * (i, row, step low 32 bits, step high 32 bits): the same (seed, step) gives
+ * the same tokens. ws / ws_bytes: a8w8_sample_workspace_bytes(B, V), device
+ * memory owned by the caller (its contents need no initialisation). Calls
+ * that share a workspace must not overlap on the GPU. Errors: top_p outside
+ * (0, 1], a non-finite temperature, ld < V, NULL pointers, a small
+ * workspace. */
+size_t a8w8_sample_workspace_bytes(int B, int V);
+a8w8_status a8w8_sample(const float* logits, int B, int V, int ld, float temperature, float top_p,
+                        uint64_t seed, uint64_t step, int32_t* next_tokens, void* ws,
+                        size_t ws_bytes, void* stream);
+
 /* Bytes of workspace a8w8_decode_layer / a8w8_decode_step need for batches of
  * up to max_B rows and block tables of max_blocks entries. */
 size_t a8w8_workspace_bytes(const a8w8_config* cfg, int max_B, int max_blocks);

@@ -79,6 +79,9 @@ def sample_rows(logits, temperature: float, top_p: float, seed: int, step: int) 
     """Next token of each logits row [B, V] (float32) -> int32 [B]."""
     logits = np.asarray(logits, dtype=np.float32)
     B, V = logits.shape
+    # the device receives both parameters as float32
+    temperature = float(np.float32(temperature))
+    top_p = float(np.float32(top_p))
     out = np.empty(B, dtype=np.int32)
     for b in range(B):
         row = logits[b].astype(np.float64)

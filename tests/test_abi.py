@@ -163,3 +163,23 @@ def test_prefill_layer_validation(lib):
     assert call(q, M=2048, wsb=need - 1) == a8w8.ERR_WORKSPACE
     nullw = a8w8.LayerWeights(*([None] * len(a8w8.WEIGHT_FIELDS)))
     assert call(q, wptr=nullw) == a8w8.ERR_INVALID_ARG
+
+
+def test_sample_validation(lib):
+    L = lib
+    ok = dict(B=2, V=10, ld=10, T=1.0, p=0.9, ws=FAKE, wsb=1 << 20)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return L.a8w8_sample(FAKE, a["B"], a["V"], a["ld"], a["T"], a["p"], 1, 2, FAKE, a["ws"],
+                             a["wsb"], None)
+    assert call(p=0.0) == a8w8.ERR_INVALID_ARG
+    assert call(p=1.5) == a8w8.ERR_INVALID_ARG
+    assert call(T=float("nan")) == a8w8.ERR_INVALID_ARG
+    assert call(ld=5) == a8w8.ERR_INVALID_ARG
+    assert call(B=0) == a8w8.OK
+    assert call(ws=None, wsb=0) == a8w8.ERR_WORKSPACE
+    assert call(T=0.0, ws=None, wsb=0) == a8w8.ERR_WORKSPACE
+    need = L.a8w8_sample_workspace_bytes(2, 10)
+    assert need >= 2 * 10 * 8 and L.a8w8_sample_workspace_bytes(2, 20) - need == 2 * 10 * 8
+    assert call(wsb=need - 1) == a8w8.ERR_WORKSPACE

@@ -80,6 +80,9 @@ _SIGNATURES = {
                                                  _f, _p, _p]),
     "a8w8_rope_table": (_i, [_p, _i, _i, ctypes.c_double, _p]),
     "a8w8_workspace_bytes": (_sz, [_p, _i, _i]),
+    "a8w8_sample_workspace_bytes": (_sz, [_i, _i]),
+    "a8w8_sample": (_i, [_p, _i, _i, _i, _f, _f, ctypes.c_uint64, ctypes.c_uint64, _p, _p, _sz,
+                         _p]),
     "a8w8_decode_layer": (_i, [_p, _p, _i, _p, _p, _p, _i, _i, _p, _p, _p, _p, _i, _p, _sz, _p,
                                _p]),
     "a8w8_prefill_layer": (_i, [_p, _p, _i, _p, _p, _p, _i, _i, _p, _p, _p, _p, _i, _p, _sz, _p,
@@ -273,6 +276,23 @@ def a8w8_rope_table(max_pos, D, theta, device="cuda", stream=None):
     t = torch.empty((max_pos, 2 * D), dtype=torch.float32, device=device)
     _check(lib().a8w8_rope_table(_ptr(t), max_pos, D, float(theta), _stream(stream)))
     return t
+
+
+def a8w8_sample(logits, temperature: float, top_p: float, seed: int, step: int, out=None,
+                ws=None, stream=None):
+    """Next tokens [B] int32 from logits [B, V] float32 on the device:
+    temperature <= 0 is greedy; otherwise a top-p nucleus draw by the
+    Gumbel-max rule with Philox4x32-10 noise keyed by (seed, step)."""
+    torch = _torch()
+    B, V = logits.shape
+    o = out if out is not None else torch.empty(B, dtype=torch.int32, device=logits.device)
+    need = lib().a8w8_sample_workspace_bytes(B, V)
+    if ws is None:
+        ws = torch.empty(need, dtype=torch.uint8, device=logits.device)
+    _check(lib().a8w8_sample(_ptr(logits), B, V, logits.stride(0), float(temperature), float(top_p),
+                             int(seed) & (2 ** 64 - 1), int(step) & (2 ** 64 - 1), _ptr(o), _ptr(ws),
+                             0 if ws is None else ws.numel(), _stream(stream)))
+    return o
 
 
 def workspace_bytes(cfg: dict, max_B: int, max_blocks: int) -> int:

@@ -635,6 +635,30 @@ a8w8_status a8w8_rope_table(float* rope, int max_pos, int D, double theta, void*
     return e == cudaSuccess ? A8W8_OK : cuda_fail(e, "a8w8_rope_table");
 }
 
+size_t a8w8_sample_workspace_bytes(int B, int V) {
+    if (B <= 0 || V <= 0) return 0;
+    return sample_workspace_bytes(B, V);
+}
+
+a8w8_status a8w8_sample(const float* logits, int B, int V, int ld, float temperature, float top_p,
+                        uint64_t seed, uint64_t step, int32_t* next_tokens, void* ws,
+                        size_t ws_bytes, void* stream) {
+    if (B < 0 || V < 1 || ld < V) return fail(A8W8_ERR_INVALID_ARG, "sample: need B >= 0, V >= 1, ld >= V");
+    if (!(top_p > 0.0f && top_p <= 1.0f)) return fail(A8W8_ERR_INVALID_ARG, "sample: top_p must be in (0, 1]");
+    if (temperature != temperature || temperature > 3.0e38f)
+        return fail(A8W8_ERR_INVALID_ARG, "sample: temperature must be finite");
+    if (B == 0) return A8W8_OK;
+    if (!logits || !next_tokens) return fail(A8W8_ERR_INVALID_ARG, "sample: NULL pointer");
+    if (!ws || ws_bytes < sample_workspace_bytes(B, V) || !aligned16(ws))
+        return fail(A8W8_ERR_WORKSPACE, "sample: needs %zu bytes of workspace",
+                    sample_workspace_bytes(B, V));
+    Launch L = make_launch(stream, true);
+    CUDA_TRY(launch_sample(logits, B, V, ld, temperature, top_p, seed, step,
+                           static_cast<float*>(ws), next_tokens, L),
+             "sample");
+    return A8W8_OK;
+}
+
 size_t a8w8_workspace_bytes(const a8w8_config* cfg, int max_B, int max_blocks) {
     if (!cfg || max_B <= 0 || max_blocks <= 0) return 0;
     return ws_layout(*cfg, max_B, max_blocks).total;
