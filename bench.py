@@ -136,6 +136,26 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
+def max_over_ranks(value: float, device=None) -> float:
+    """The maximum of a per-rank timing over all ranks (the job ends with its
+    slowest replica); the value itself when the run is not distributed. NCCL
+    reduces a tensor on the rank's GPU, gloo one on the CPU."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64,
+                     device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: float, ms_max: float, world: int) -> float:
+    """Whole-job throughput per second: every rank (a replica) processes the
+    same units, and the job takes the slowest rank's time."""
+    return units_per_rank * world * 1000.0 / ms_max
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -291,10 +311,7 @@ def run_ours(args, cfg):
         torch.cuda.synchronize()
         ms = ev0.elapsed_time(ev1)
         ctx_timed = [PROMPT_LEN + args.warmup + i + 1 for i in range(args.steps)]
-        if world > 1:
-            t = torch.tensor([ms], device=device)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ms = float(t.item())
+        ms = max_over_ranks(ms, device)
         tpot = ms / args.steps
         errs = a8w8.read_device_errors(stream)
 
@@ -376,7 +393,7 @@ def run_ours(args, cfg):
                        "prompt_len": PROMPT_LEN, "max_seq_len": MAX_SEQ, "page_size": page,
                        "parallelism": "replicas" if world > 1 else "single GPU",
                        "l2": "inputs larger than L2 (14.8 GB of weights per step)"},
-            "tokens_per_s": 1000.0 / tpot * world,
+            "tokens_per_s": job_rate(1, tpot, world),
             "step_bytes": per_step_bytes,
             "step_hbm_gbs": per_step_bytes / (tpot * 1e-3) / 1e9,
             "step_frac_of_peak": per_step_bytes / (tpot * 1e-3) / 1e9 / peaks["hbm_gbs"],
@@ -460,10 +477,7 @@ def run_batched(args, cfg):
             ev1.synchronize()
         torch.cuda.synchronize()
         ms = ev0.elapsed_time(ev1)
-        if world > 1:
-            t = torch.tensor([ms], device=device)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ms = float(t.item())
+        ms = max_over_ranks(ms, device)
         errs = a8w8.read_device_errors(stream)
         g.close()
     per_step = ms / args.steps
@@ -487,7 +501,7 @@ def run_batched(args, cfg):
                        "page_size": page, "max_blocks": int(max_blocks),
                        "parallelism": "replicas" if world > 1 else "single GPU",
                        "l2": "inputs larger than L2 (14.8 GB of weights + KV per step)"},
-            "tokens_per_s": B * 1000.0 / per_step * world,
+            "tokens_per_s": job_rate(B, per_step, world),
             "step_bytes": per_step_bytes,
             "step_hbm_gbs": per_step_bytes / (per_step * 1e-3) / 1e9,
             "step_frac_of_peak": per_step_bytes / (per_step * 1e-3) / 1e9 / peaks["hbm_gbs"],
@@ -578,10 +592,7 @@ def run_prefill(args, cfg):
                 times.append(e0.elapsed_time(e1))
         errs = a8w8.read_device_errors(stream)
     ms = sum(times) / len(times)
-    if world > 1:
-        t = torch.tensor([ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, device)
     ops = 2.0 * M * (cfg["hidden"] * ((cfg["num_q_heads"] + 2 * Hkv) * D) +
                       cfg["num_q_heads"] * D * cfg["hidden"] + 2 * cfg["intermediate"] * cfg["hidden"]
                       + cfg["intermediate"] * cfg["hidden"])
@@ -602,7 +613,7 @@ def run_prefill(args, cfg):
             "config": {"workload": PREFILL_WORKLOAD, "sequences": PREFILL_SEQS,
                        "tokens_per_sequence": PREFILL_LEN, "M": M, "layers": 1,
                        "parallelism": "replicas" if world > 1 else "single GPU"},
-            "tokens_per_s": M * 1000.0 / ms * world,
+            "tokens_per_s": job_rate(M, ms, world),
             "int8_ops_per_s_e12": tops,
             "attention_flop": attn_flops,
             "roofline": {"bound": "tensor",
