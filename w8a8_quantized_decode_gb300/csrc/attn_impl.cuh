@@ -22,9 +22,11 @@
 //      new K/V into the cache slot, every item into its own tiles;
 //   3. scores: D/8 lanes per token, products of BF16 values exact in float32,
 //      summed as two-float pairs and reduced over the lane group with
-//      shuffles; 4. max-subtracted softmax with a two-float exp;
-//   5. P.V: lanes of a column pair split the tokens, two-float sums combined
-//      with shuffles;
+//      shuffles; the chunk maximum by a shared-memory atomic maximum on an
+//      order-preserving 64-bit key of the pair;
+//   4. softmax numerators exp(s - m), one token per thread (two-float exp);
+//   5. P.V: lanes of a column pair split the tokens, two-float sums (and the
+//      denominator, the sum of the numerators) combined with shuffles;
 //   6. one chunk: normalise and write BF16; several chunks: write two-float
 //      partials (unnormalised o, running max m, sum l) that the last chunk's
 //      CTA (or a combine kernel) merges:
@@ -49,6 +51,7 @@ __host__ __device__ inline size_t attn_tiles_bytes(int chunk, int D) {
     return kv > comb ? kv : comb;
 }
 __host__ __device__ inline size_t attn_item_smem_bytes(int chunk, int D) {
+    // ... + (m, l) pairs, then the flag (4 bytes, 4 padding) and the maximum's key (8)
     return attn_tiles_bytes(chunk, D) + (size_t)D * 4 + (size_t)2 * chunk * 4 + 4 * 4 + 16;
 }
 
@@ -196,6 +199,19 @@ __device__ __forceinline__ bf16 combine_elem(const float* pp, int splits, const 
     return f2_to_bf16(f2_div(acc, l));
 }
 
+// Order-preserving 64-bit key of a renormalised float pair (hi, lo): the
+// numeric order of the pairs is the order of the keys.
+__device__ __forceinline__ unsigned ord32(float x) {
+    const unsigned u = __float_as_uint(x);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float unord32(unsigned k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+__device__ __forceinline__ unsigned long long f2_key(f2 v) {
+    return ((unsigned long long)ord32(v.hi) << 32) | ord32(v.lo);
+}
+
 // One attention work item, (request b, query head h, token chunk `split`),
 // on the first NT threads of the CTA (the others must not call it; they are
 // not synchronised with). The G query heads of a KV head are separate items
@@ -215,6 +231,7 @@ __device__ __forceinline__ void attn_item(const AttnParams& p, int chunk, int sp
     float* sl = sc + chunk;                        // [chunk] lo
     float* stat = sl + chunk;                      // m hi, m lo, l hi, l lo
     int* s_flag = reinterpret_cast<int*>(stat + 4);
+    unsigned long long* s_mkey = reinterpret_cast<unsigned long long*>(stat + 6);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -238,7 +255,10 @@ __device__ __forceinline__ void attn_item(const AttnParams& p, int chunk, int sp
     if (split >= active) return;   // the whole CTA, before any barrier
     const bool single = active == 1;
 
-    if (tid == 0) *s_flag = 0;
+    if (tid == 0) {
+        *s_flag = 0;
+        *s_mkey = 0ull;   // below every score's key
+    }
     attn_sync<NT>();
     constexpr int RV = D / 8;   // 16-byte vectors per row
     for (int i = tid; i < n_old * RV; i += NT) {
@@ -357,29 +377,25 @@ __device__ __forceinline__ void attn_item(const AttnParams& p, int chunk, int sp
                 const f2 sv = f2_mul(d, scale);
                 sc[t] = sv.hi;
                 sl[t] = sv.lo;
+                atomicMax(s_mkey, f2_key(sv));   // the chunk maximum m
             }
         }
     }
     attn_sync<NT>();
 
-    // softmax over the chunk: p_t = exp(s_t - m), l = sum p_t (warp 0)
-    if (warp == 0) {
-        f2 m = {-INFINITY, 0.0f};
-        for (int t = lane; t < n; t += 32) m = f2_max(m, f2{sc[t], sl[t]});
-        m = warp_max_f2(m);
-        f2 l = {0.0f, 0.0f};
-        for (int t = lane; t < n; t += 32) {
+    // softmax numerators p_t = exp(s_t - m), one token per thread; their sum
+    // l is formed in the P.V reduction below
+    {
+        const unsigned long long mk = *s_mkey;
+        const f2 m = {unord32((unsigned)(mk >> 32)), unord32((unsigned)mk)};
+        if (tid == 0) {
+            stat[0] = m.hi;
+            stat[1] = m.lo;
+        }
+        for (int t = tid; t < n; t += NT) {
             const f2 e = f2_exp(f2_sub(f2{sc[t], sl[t]}, m));
             sc[t] = e.hi;
             sl[t] = e.lo;
-            l = f2_add(l, e);
-        }
-        l = warp_sum_f2(l);
-        if (lane == 0) {
-            stat[0] = m.hi;
-            stat[1] = m.lo;
-            stat[2] = l.hi;
-            stat[3] = l.lo;
         }
     }
     attn_sync<NT>();
@@ -391,13 +407,14 @@ __device__ __forceinline__ void attn_item(const AttnParams& p, int chunk, int sp
         constexpr int TG = NT / CP;
         static_assert(TG >= 1 && TG <= 32 && (TG & (TG - 1)) == 0, "token groups");
         const int cp = tid / TG, tg = tid % TG;
-        f2 o0 = {0.0f, 0.0f}, o1 = {0.0f, 0.0f};
+        f2 o0 = {0.0f, 0.0f}, o1 = {0.0f, 0.0f}, l = {0.0f, 0.0f};
         for (int t = tg; t < n; t += TG) {
             const float2 v = __bfloat1622float2(
                 *reinterpret_cast<const __nv_bfloat162*>(Vs + (size_t)t * DP + 2 * cp));
             const f2 pr = {sc[t], sl[t]};
             o0 = f2_add(o0, f2_mulf(pr, v.x));
             o1 = f2_add(o1, f2_mulf(pr, v.y));
+            l = f2_add(l, pr);
         }
 #pragma unroll
         for (int o = TG / 2; o > 0; o >>= 1) {
@@ -408,9 +425,11 @@ __device__ __forceinline__ void attn_item(const AttnParams& p, int chunk, int sp
             r.hi = __shfl_xor_sync(0xffffffffu, o1.hi, o);
             r.lo = __shfl_xor_sync(0xffffffffu, o1.lo, o);
             o1 = f2_add(o1, r);
+            r.hi = __shfl_xor_sync(0xffffffffu, l.hi, o);
+            r.lo = __shfl_xor_sync(0xffffffffu, l.lo, o);
+            l = f2_add(l, r);
         }
         if (tg == 0) {
-            const f2 l = {stat[2], stat[3]};
             if (single) {
                 bf16* out = p.out + ((size_t)b * p.Hq + h) * D + 2 * cp;
                 out[0] = n > 0 ? f2_to_bf16(f2_div(o0, l)) : __float2bfloat16_rn(0.0f);
