@@ -632,6 +632,86 @@ def run_prefill(args, cfg):
         torch.distributed.destroy_process_group()
 
 
+def run_layer_b1(args, cfg):
+    """One decode layer, batch 1, 255 cached tokens + the decoded one (context
+    256, pages of 128), the layer's weights rotated over 4 copies so that L2
+    (129 MB) cannot serve a repeat (rank 0 only)."""
+    import torch
+    import w8a8_quantized_decode_gb300 as a8w8
+
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    a8w8.build()
+    cfg = dict(cfg, num_layers=1)
+    page, ctx = cfg["page_size"], 256
+    Hkv, D, H = cfg["num_kv_heads"], cfg["head_dim"], cfg["hidden"]
+    copies = [synth.t_layer_weights(cfg, SEED + 50 + c, 0, device) for c in range(4)]
+    bt_np, nblk = synth.paged_layout(SEED + 51, [ctx], page, spare_blocks=1)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(SEED + 52)
+    kc = torch.randn((nblk * page, Hkv, D), generator=gen, device=device).to(torch.bfloat16)
+    vc = torch.randn((nblk * page, Hkv, D), generator=gen, device=device).to(torch.bfloat16)
+    hidden = torch.randn((1, H), generator=gen, device=device).to(torch.bfloat16)
+    h0 = hidden.clone()
+    bt = torch.from_numpy(bt_np).to(device)
+    cl = torch.tensor([ctx], dtype=torch.int32, device=device)
+    sl = torch.from_numpy(synth.slots_for(bt_np, [ctx - 1], page)).to(device)
+    rope = a8w8.a8w8_rope_table(bt_np.shape[1] * page, D, cfg["rope_theta"], device=device)
+    ws = a8w8.alloc_workspace(cfg, 1, bt_np.shape[1], device=device)
+    stream = torch.cuda.Stream(device)
+    n = max(args.steps, 8)
+    with torch.cuda.stream(stream):
+        g = torch.cuda.CUDAGraph()
+        # one graph replay = n layer calls over the 4 rotating copies
+        for _ in range(2):
+            for i in range(4):
+                a8w8.a8w8_decode_layer(copies[i], cfg, hidden, sl, bt, cl, kc, vc, rope, ws,
+                                       stream=stream)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n):
+                a8w8.a8w8_decode_layer(copies[i % 4], cfg, hidden, sl, bt, cl, kc, vc, rope, ws,
+                                       stream=stream)
+        for _ in range(args.warmup):
+            hidden.copy_(h0)
+            g.replay()
+        stream.synchronize()
+        gpu_uuid = None
+        try:
+            gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+        except Exception:
+            pass
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        reps = 10    # ~35 ms timed, so that the clock sampler sees the run
+        with ClockSampler(gpu_uuid) as clocks:
+            hidden.copy_(h0)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+            e1.synchronize()
+        errs = a8w8.read_device_errors(stream)
+    us = e0.elapsed_time(e1) * 1000.0 / (n * reps)
+    layer_bytes = synth.layer_weight_bytes(cfg) + ctx * 2 * Hkv * D * 2
+    peaks = measured_peaks()
+    line = {"metric": "A8W8 decode layer, batch 1, context 256 (us per layer)", "value": us,
+            "unit": "us/layer", "n_gpus": 1, "steps": n * reps, "warmup": args.warmup,
+            "higher_is_better": False, "vs_baseline": None,
+            "dtype": "int8 x int8 -> int32, f32 dequant, bf16 activations",
+            "data": "synthetic (seeded random-init weights, 4 rotating copies; N(0,1) context K/V)",
+            "config": {"workload": "qwen3_14b_a8w8_layer_b1_ctx256", "batch": 1, "context": ctx,
+                       "weight_copies": 4,
+                       "l2": "weights rotated over 4 copies (1.32 GB), larger than L2"},
+            "layer_bytes": layer_bytes, "hbm_gbs": layer_bytes / (us * 1e-6) / 1e9,
+            "frac_of_peak": layer_bytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
+            "clocks": clocks.summary(), "device_errors": errs}
+    print(json.dumps(line), flush=True)
+
+
 def run_sample(args, cfg):
     """Device-side sampling over the 151936-token vocabulary (rank 0 only):
     microseconds per call at batch 1 and 16, greedy, temperature and top-p."""
@@ -695,13 +775,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["decode_b1", "batched16", "prefill", "sample"],
+    ap.add_argument("--workload", choices=["decode_b1", "batched16", "prefill", "sample",
+                                           "layer_b1"],
                     default="decode_b1")
     ap.add_argument("--layers", type=int, default=40,
                     help="layers of the model (fewer only for profiling captures)")
     args = ap.parse_args()
     if args.steps is None:
-        args.steps = {"batched16": 32, "prefill": 5, "sample": 20}.get(args.workload, 48)
+        args.steps = {"batched16": 32, "prefill": 5, "sample": 20,
+                      "layer_b1": 40}.get(args.workload, 48)
     if args.warmup < 3:
         raise SystemExit("warmup must be >= 3")
     cfg = dict(synth.QWEN3_14B, num_layers=args.layers)
@@ -713,6 +795,8 @@ def main():
         run_prefill(args, cfg)
     elif args.workload == "sample":
         run_sample(args, cfg)
+    elif args.workload == "layer_b1":
+        run_layer_b1(args, cfg)
     else:
         run_ours(args, cfg)
 
