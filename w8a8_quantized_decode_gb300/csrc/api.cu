@@ -700,19 +700,10 @@ a8w8_status a8w8_prefill_layer(const a8w8_layer_weights* w, const a8w8_config* c
     if ((s = check_ptrs({hidden, slot_mapping, block_table, ctx_lens, k_cache, v_cache, rope},
                         "a8w8_prefill_layer")) != A8W8_OK)
         return s;
-    {
-        AttnParams probe = {};
-        probe.fused = true;
-        probe.tickets = reinterpret_cast<unsigned*>(16);   // shape check only
-        probe.Hq = cfg->num_q_heads;
-        probe.Hkv = cfg->num_kv_heads;
-        probe.D = cfg->head_dim;
-        probe.page = cfg->page_size;
-        probe.max_blocks = max_blocks;
-        if (!attn_group_supported(probe))
-            return fail(A8W8_ERR_UNSUPPORTED_SHAPE,
-                        "prefill attention needs Hq/Hkv <= 7 and at most 64 chunks of 128 tokens");
-    }
+    if (!attn_group_shape_ok(cfg->num_q_heads, cfg->num_kv_heads, cfg->head_dim,
+                             max_blocks * cfg->page_size))
+        return fail(A8W8_ERR_UNSUPPORTED_SHAPE,
+                    "prefill attention needs Hq/Hkv <= 7 and at most 64 chunks of 128 tokens");
     const WsLayout lay = ws_layout(*cfg, M, max_blocks);
     if (!ws || ws_bytes < lay.total || !aligned16(ws))
         return fail(A8W8_ERR_WORKSPACE, "prefill layer workspace needs %zu bytes", lay.total);

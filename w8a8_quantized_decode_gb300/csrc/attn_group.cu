@@ -430,10 +430,13 @@ cudaError_t launch_kv_prep(const AttnParams& p, const Launch& L) {
     return cudaLaunchKernelEx(&cfg, kv_prep_kernel<64>, p);
 }
 
+bool attn_group_shape_ok(int Hq, int Hkv, int D, int max_ctx) {
+    return Hkv > 0 && Hq % Hkv == 0 && Hq / Hkv <= kGrpMaxG && (D == 128 || D == 64) &&
+           (max_ctx + kGrpChunk - 1) / kGrpChunk <= kGrpMaxSplits;
+}
+
 bool attn_group_supported(const AttnParams& p) {
-    const int max_ctx = p.max_blocks * p.page;
-    return p.fused && p.tickets && p.Hq % p.Hkv == 0 && p.Hq / p.Hkv <= kGrpMaxG &&
-           (p.D == 128 || p.D == 64) && (max_ctx + kGrpChunk - 1) / kGrpChunk <= kGrpMaxSplits;
+    return p.fused && p.tickets && attn_group_shape_ok(p.Hq, p.Hkv, p.D, p.max_blocks * p.page);
 }
 
 int attn_group_splits(int max_ctx) { return max_ctx <= 0 ? 1 : (max_ctx + kGrpChunk - 1) / kGrpChunk; }

@@ -125,6 +125,7 @@ size_t attn_part_bytes(int B, int Hq, int D, int max_ctx, bool combine_in_kernel
 cudaError_t launch_attention(const AttnParams& p, const Launch& L);
 // Grouped form for large batches / long contexts (decode layer only): one CTA
 // per (request, KV head, 128-token chunk) for all query heads of the group.
+bool attn_group_shape_ok(int Hq, int Hkv, int D, int max_ctx);
 bool attn_group_supported(const AttnParams& p);
 int attn_group_splits(int max_ctx);
 cudaError_t launch_attn_group(const AttnParams& p, const Launch& L);
