@@ -768,7 +768,7 @@ def cpu_baseline(model, cfg):
                       f"head, batch 1, contexts {PROMPT_LEN + 1}..{PROMPT_LEN + len(times)})"}
 
 
-def main():
+def build_parser() -> argparse.ArgumentParser:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
@@ -780,7 +780,11 @@ def main():
                     default="decode_b1")
     ap.add_argument("--layers", type=int, default=40,
                     help="layers of the model (fewer only for profiling captures)")
-    args = ap.parse_args()
+    return ap
+
+
+def main():
+    args = build_parser().parse_args()
     if args.steps is None:
         args.steps = {"batched16": 32, "prefill": 5, "sample": 20,
                       "layer_b1": 40}.get(args.workload, 48)
