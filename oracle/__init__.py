@@ -98,7 +98,12 @@ def _declare(lib):
         "or_kv_write": (_i, [_p, _p, _i, _i, _i, _p, _p, _p, _l]),
         "or_paged_attention": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i,
                                     _d, _p]),
+        "or_kv_write_i8": (_i, [_p, _p, _i, _i, _i, _p, _p, _p, _p, _p, _l]),
+        "or_paged_attention_i8": (_i, [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i,
+                                       _i, _i, _d, _p]),
         "or_decode_layer": (_i, [_p, _p, _i, _p, _p, _p, _i, _i, _p, _p, _p, _p]),
+        "or_decode_layer_i8kv": (_i, [_p, _p, _i, _p, _p, _p, _i, _i, _p, _p, _p, _p, _p,
+                                      _p]),
         "or_argmax_f64": (None, [_p, _i, _i, _p]),
         "or_argmax_f32": (None, [_p, _i, _i, _p]),
         "or_lm_head": (None, [_p, _i, _i, _p, _i, _p]),
@@ -262,6 +267,44 @@ def paged_attention(q, k_cache, v_cache, block_table, ctx_lens, page: int,
     return out, rc
 
 
+def kv_write_i8(k, v, slot_mapping, k_codes, v_codes, k_scale, v_scale) -> int:
+    """INT8 KV variant: quantise each K/V head row of k, v [T, Hkv, D] into
+    codes [slots, Hkv, D] (int8) and row scales [slots, Hkv] (float32), in place."""
+    k = _c(k, U16)
+    v = _c(v, U16)
+    sm = _c(slot_mapping, I32)
+    for a, dt in ((k_codes, I8), (v_codes, I8), (k_scale, F32), (v_scale, F32)):
+        assert a.dtype == dt and a.flags["C_CONTIGUOUS"]
+    T, Hkv, D = k.shape
+    num_slots = k_codes.size // (Hkv * D)
+    assert k_scale.size == num_slots * Hkv and v_scale.size == num_slots * Hkv
+    return _load().or_kv_write_i8(_ptr(k), _ptr(v), T, Hkv, D, _ptr(sm), _ptr(k_codes),
+                                  _ptr(v_codes), _ptr(k_scale), _ptr(v_scale), num_slots)
+
+
+def paged_attention_i8(q, k_codes, v_codes, k_scale, v_scale, block_table, ctx_lens,
+                       page: int, scale: float | None = None):
+    """INT8 KV variant of paged_attention: codes [num_blocks*page, Hkv, D],
+    scales [num_blocks*page, Hkv]; returns (out [B,Hq,D], rc)."""
+    q = _c(q, U16)
+    k_codes = _c(k_codes, I8)
+    v_codes = _c(v_codes, I8)
+    k_scale = _c(k_scale, F32)
+    v_scale = _c(v_scale, F32)
+    bt = _c(block_table, I32)
+    cl = _c(ctx_lens, I32)
+    B, Hq, D = q.shape
+    Hkv = k_codes.shape[-2]
+    num_blocks = k_codes.size // (Hkv * D * page)
+    assert k_scale.size == num_blocks * page * Hkv == v_scale.size
+    scale = 1.0 / np.sqrt(D) if scale is None else scale
+    out = np.empty_like(q)
+    rc = _load().or_paged_attention_i8(_ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scale),
+                                       _ptr(v_scale), _ptr(bt), _ptr(cl), B, Hq, Hkv, D, page,
+                                       bt.shape[1], num_blocks, scale, _ptr(out))
+    return out, rc
+
+
 def make_config(cfg: dict) -> Config:
     return Config(cfg["hidden"], cfg["num_q_heads"], cfg["num_kv_heads"],
                   cfg["head_dim"], cfg["intermediate"], cfg.get("num_layers", 1),
@@ -284,9 +327,11 @@ def _layer_struct(w: dict, keep: list) -> LayerWeights:
 
 
 def decode_layer(w: dict, cfg: dict, hidden, slot_mapping, block_table, ctx_lens,
-                 k_cache, v_cache, taps: bool = False):
+                 k_cache, v_cache, taps: bool = False, k_scale=None, v_scale=None):
     """One layer; hidden [B,H] bf16 is returned updated (copy); caches updated in place.
 
+    With k_scale and v_scale ([slots, Hkv] float32) the caches are the INT8 KV
+    variant (int8 codes [slots, Hkv, D]); otherwise BF16 [slots, Hkv, D].
     Returns (hidden_out, taps_dict or None, rc)."""
     keep: list = []
     ws = _layer_struct(w, keep)
@@ -318,9 +363,20 @@ def decode_layer(w: dict, cfg: dict, hidden, slot_mapping, block_table, ctx_lens
         for n in TAP_NAMES:
             setattr(t, n, _ptr(tap_arrays[n]))
         tptr = ctypes.byref(t)
-    rc = _load().or_decode_layer(ctypes.byref(ws), ctypes.byref(c), B, _ptr(h), _ptr(sm),
-                                 _ptr(bt), bt.shape[1], num_blocks, _ptr(cl),
-                                 _ptr(k_cache), _ptr(v_cache), tptr)
+    if k_scale is None and v_scale is None:
+        assert k_cache.dtype == U16 and v_cache.dtype == U16
+        rc = _load().or_decode_layer(ctypes.byref(ws), ctypes.byref(c), B, _ptr(h), _ptr(sm),
+                                     _ptr(bt), bt.shape[1], num_blocks, _ptr(cl),
+                                     _ptr(k_cache), _ptr(v_cache), tptr)
+    else:
+        assert k_cache.dtype == I8 and v_cache.dtype == I8
+        for a in (k_scale, v_scale):
+            assert a.dtype == F32 and a.flags["C_CONTIGUOUS"]
+            assert a.size == num_blocks * cfg["page_size"] * Hkv
+        rc = _load().or_decode_layer_i8kv(ctypes.byref(ws), ctypes.byref(c), B, _ptr(h),
+                                          _ptr(sm), _ptr(bt), bt.shape[1], num_blocks,
+                                          _ptr(cl), _ptr(k_cache), _ptr(v_cache),
+                                          _ptr(k_scale), _ptr(v_scale), tptr)
     return h, tap_arrays, rc
 
 

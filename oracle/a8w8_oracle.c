@@ -349,6 +349,17 @@ int or_kv_write(const uint16_t* k, const uint16_t* v, int T, int Hkv, int D,
 /* a8: GQA decode attention over the paged BF16 cache                        */
 /* ------------------------------------------------------------------------- */
 
+/* One cached element as a real number: the BF16 value, or for the INT8 cache
+ * (scales != NULL) the code times its row's FP32 scale, exact in double. */
+static double cache_elem(const void* cache, const float* scales, long slot, int Hkv,
+                         int kvh, int D, int d)
+{
+    long r = slot * Hkv + kvh;
+    if (!scales)
+        return or_bf16_to_double(((const uint16_t*)cache)[r * D + d]);
+    return (double)((const int8_t*)cache)[r * D + d] * (double)scales[r];
+}
+
 /* For request b and query head h (KV head kvh = h / (Hq / Hkv)), over the
  * ctx_lens[b] cached tokens t, whose slot is
  *   block_table[b][t / page] * page + t % page:
@@ -361,15 +372,14 @@ int or_kv_write(const uint16_t* k, const uint16_t* v, int T, int Hkv, int D,
  * Pinned: single-token context returns V, q = 0 returns the mean of V, paged
  * equals contiguous, shuffled pages give identical output, Hkv = Hq reduces to
  * per-head attention (tests). */
-int or_paged_attention(const uint16_t* q, const uint16_t* k_cache,
-                       const uint16_t* v_cache, const int32_t* block_table,
-                       const int32_t* ctx_lens, int B, int Hq, int Hkv, int D,
-                       int page, int max_blocks, int num_blocks, double scale,
-                       uint16_t* out)
+static int attention(const uint16_t* q, const void* k_cache, const void* v_cache,
+                     const float* k_scale, const float* v_scale,
+                     const int32_t* block_table, const int32_t* ctx_lens, int B, int Hq,
+                     int Hkv, int D, int page, int max_blocks, int num_blocks,
+                     double scale, uint16_t* out)
 {
     int rc = 0;
     int G = Hq / Hkv;
-    long row = (long)Hkv * D;
     int max_ctx = max_blocks * page;
     double* s = (double*)malloc(sizeof(double) * (size_t)(max_ctx > 0 ? max_ctx : 1));
     double* o = (double*)malloc(sizeof(double) * (size_t)D);
@@ -395,10 +405,10 @@ int or_paged_attention(const uint16_t* q, const uint16_t* k_cache,
             double mx = -INFINITY;
             for (int t = 0; t < n; ++t) {
                 long slot = (long)block_table[(long)b * max_blocks + t / page] * page + t % page;
-                const uint16_t* kt = k_cache + slot * row + (long)kvh * D;
                 double dot = 0.0;
                 for (int d = 0; d < D; ++d)
-                    dot += or_bf16_to_double(qv[d]) * or_bf16_to_double(kt[d]);
+                    dot += or_bf16_to_double(qv[d]) *
+                           cache_elem(k_cache, k_scale, slot, Hkv, kvh, D, d);
                 s[t] = dot * scale;
                 if (s[t] > mx)
                     mx = s[t];
@@ -412,10 +422,9 @@ int or_paged_attention(const uint16_t* q, const uint16_t* k_cache,
                 o[d] = 0.0;
             for (int t = 0; t < n; ++t) {
                 long slot = (long)block_table[(long)b * max_blocks + t / page] * page + t % page;
-                const uint16_t* vt = v_cache + slot * row + (long)kvh * D;
                 double p = s[t] / l;
                 for (int d = 0; d < D; ++d)
-                    o[d] += p * or_bf16_to_double(vt[d]);
+                    o[d] += p * cache_elem(v_cache, v_scale, slot, Hkv, kvh, D, d);
             }
             for (int d = 0; d < D; ++d)
                 ob[d] = or_bf16_from_double(o[d]);
@@ -424,6 +433,72 @@ int or_paged_attention(const uint16_t* q, const uint16_t* k_cache,
     free(s);
     free(o);
     return rc;
+}
+
+int or_paged_attention(const uint16_t* q, const uint16_t* k_cache,
+                       const uint16_t* v_cache, const int32_t* block_table,
+                       const int32_t* ctx_lens, int B, int Hq, int Hkv, int D,
+                       int page, int max_blocks, int num_blocks, double scale,
+                       uint16_t* out)
+{
+    return attention(q, k_cache, v_cache, NULL, NULL, block_table, ctx_lens, B, Hq, Hkv,
+                     D, page, max_blocks, num_blocks, scale, out);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Variant: INT8 KV cache with FP32 row scales                               */
+/* ------------------------------------------------------------------------- */
+
+/* [LIB-810] "BF16 KV cache" names the storage that BF16 replaced: INT8 K/V
+ * cache rows with FP32 row scales, each token's K and V quantised when it is
+ * written (decode and prefill) and every row dequantised where attention reads
+ * it, the scales travelling in their own tensors.
+ * Reading: a row is one KV head's D values of one token, quantised by the
+ * activation formula (or_quant_rows: scale = absmax / 127, RNE, clamp +-127)
+ * from the BF16 values the BF16 cache would hold (after QK RMSNorm and RoPE).
+ * Codes [num_slots, Hkv, D] int8; scales [num_slots, Hkv] float. A negative
+ * slot skips the token; an out-of-range slot returns -3 and writes nothing
+ * for that token.
+ * Pinned: every written row equals the quantisation of its head row, the
+ * round trip stays within half a scale step, untouched slots stay untouched
+ * (tests). */
+int or_kv_write_i8(const uint16_t* k, const uint16_t* v, int T, int Hkv, int D,
+                   const int32_t* slot_mapping, int8_t* k_codes, int8_t* v_codes,
+                   float* k_scale, float* v_scale, long num_slots)
+{
+    int rc = 0;
+    long row = (long)Hkv * D;
+    for (int t = 0; t < T; ++t) {
+        long s = slot_mapping[t];
+        if (s < 0)
+            continue;
+        if (s >= num_slots) {
+            rc = -3;
+            continue;
+        }
+        or_quant_rows(k + (long)t * row, Hkv, D, k_codes + s * row, k_scale + s * Hkv);
+        or_quant_rows(v + (long)t * row, Hkv, D, v_codes + s * row, v_scale + s * Hkv);
+    }
+    return rc;
+}
+
+/* GQA decode attention over the INT8 cache: the BF16 form above with every
+ * K_t and V_t element read as code x row scale ([LIB-810] "BF16 KV cache":
+ * per-row K/V dequantisation inside attention). Same layout, bounds and
+ * return codes as or_paged_attention.
+ * Pinned: rows whose scale is a power of two (codes times 2^e exactly
+ * representable in BF16) give the BF16-cache result bit for bit, with
+ * different K and V scales per token and head; a single-token context
+ * returns the dequantised V row (tests). */
+int or_paged_attention_i8(const uint16_t* q, const int8_t* k_codes,
+                          const int8_t* v_codes, const float* k_scale,
+                          const float* v_scale, const int32_t* block_table,
+                          const int32_t* ctx_lens, int B, int Hq, int Hkv, int D,
+                          int page, int max_blocks, int num_blocks, double scale,
+                          uint16_t* out)
+{
+    return attention(q, k_codes, v_codes, k_scale, v_scale, block_table, ctx_lens, B, Hq,
+                     Hkv, D, page, max_blocks, num_blocks, scale, out);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -472,11 +547,11 @@ typedef struct {
  * Padded rows (slot -1, ctx_len 0) write no KV and attend to nothing.
  * Returns 0, or a negative code (-1 shapes, -3 bounds), or 1 on int32
  * overflow. */
-int or_decode_layer(const or_layer_weights* w, const or_config* cfg, int B,
-                    uint16_t* hidden, const int32_t* slot_mapping,
-                    const int32_t* block_table, int max_blocks, int num_blocks,
-                    const int32_t* ctx_lens, uint16_t* k_cache, uint16_t* v_cache,
-                    const or_layer_taps* taps)
+static int layer(const or_layer_weights* w, const or_config* cfg, int B,
+                 uint16_t* hidden, const int32_t* slot_mapping,
+                 const int32_t* block_table, int max_blocks, int num_blocks,
+                 const int32_t* ctx_lens, void* k_cache, void* v_cache, float* k_scale,
+                 float* v_scale, const or_layer_taps* taps)
 {
     const int H = cfg->hidden, Hq = cfg->num_q_heads, Hkv = cfg->num_kv_heads;
     const int D = cfg->head_dim, I = cfg->intermediate;
@@ -526,12 +601,16 @@ int or_decode_layer(const or_layer_weights* w, const or_config* cfg, int B,
     TAP(k_rot, k, sizeof(uint16_t) * (size_t)B * NK);
     /* a7 */
     long num_slots = (long)num_blocks * cfg->page_size;
-    if (or_kv_write(k, v, B, Hkv, D, slot_mapping, k_cache, v_cache, num_slots) != 0)
+    int wr = k_scale ? or_kv_write_i8(k, v, B, Hkv, D, slot_mapping, (int8_t*)k_cache,
+                                      (int8_t*)v_cache, k_scale, v_scale, num_slots)
+                     : or_kv_write(k, v, B, Hkv, D, slot_mapping, (uint16_t*)k_cache,
+                                   (uint16_t*)v_cache, num_slots);
+    if (wr != 0)
         rc = -3;
     /* a8 */
-    if (or_paged_attention(q, k_cache, v_cache, block_table, ctx_lens, B, Hq, Hkv, D,
-                           cfg->page_size, max_blocks, num_blocks, 1.0 / sqrt((double)D),
-                           attn) != 0)
+    if (attention(q, k_cache, v_cache, k_scale, v_scale, block_table, ctx_lens, B, Hq, Hkv,
+                  D, cfg->page_size, max_blocks, num_blocks, 1.0 / sqrt((double)D),
+                  attn) != 0)
         rc = -3;
     TAP(attn, attn, sizeof(uint16_t) * (size_t)B * NQ);
     /* a9, a10: the residual is the layer input */
@@ -566,6 +645,35 @@ int or_decode_layer(const or_layer_weights* w, const or_config* cfg, int B,
     free(xn); free(xq); free(xs); free(acc); free(qkv); free(q); free(k); free(v);
     free(attn); free(aq); free(as); free(act); free(pos);
     return rc != 0 ? rc : ov;
+}
+
+int or_decode_layer(const or_layer_weights* w, const or_config* cfg, int B,
+                    uint16_t* hidden, const int32_t* slot_mapping,
+                    const int32_t* block_table, int max_blocks, int num_blocks,
+                    const int32_t* ctx_lens, uint16_t* k_cache, uint16_t* v_cache,
+                    const or_layer_taps* taps)
+{
+    return layer(w, cfg, B, hidden, slot_mapping, block_table, max_blocks, num_blocks,
+                 ctx_lens, k_cache, v_cache, NULL, NULL, taps);
+}
+
+/* The same layer over the INT8 KV cache with FP32 row scales: a7 quantises
+ * each written K/V head row (or_kv_write_i8) and a8 dequantises every row it
+ * reads (or_paged_attention_i8); every other step is unchanged ([LIB-810]
+ * "BF16 KV cache", the storage it replaced). Codes [num_blocks * page, Hkv, D],
+ * scales [num_blocks * page, Hkv].
+ * Pinned: the steps before a7 equal the BF16-cache layer's bit for bit, the
+ * cache holds the quantised K/V rows of that layer at their slots (tests). */
+int or_decode_layer_i8kv(const or_layer_weights* w, const or_config* cfg, int B,
+                         uint16_t* hidden, const int32_t* slot_mapping,
+                         const int32_t* block_table, int max_blocks, int num_blocks,
+                         const int32_t* ctx_lens, int8_t* k_codes, int8_t* v_codes,
+                         float* k_scale, float* v_scale, const or_layer_taps* taps)
+{
+    if (!k_scale || !v_scale)
+        return -1;
+    return layer(w, cfg, B, hidden, slot_mapping, block_table, max_blocks, num_blocks,
+                 ctx_lens, k_codes, v_codes, k_scale, v_scale, taps);
 }
 
 /* Final RMSNorm, BF16 LM head and greedy argmax.

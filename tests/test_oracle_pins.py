@@ -448,6 +448,132 @@ def test_attention_padded_row_and_bounds():
 
 
 # ---------------------------------------------------------------------------
+# INT8 KV variant: INT8 cache rows with FP32 row scales
+# ---------------------------------------------------------------------------
+
+def _pow2_rows(rng, shape, e_lo=-6, e_hi=2):
+    """BF16 rows (last axis) whose absmax is 127 * 2^e: integer codes in
+    [-127, 127] with one +-127 per row, times a power of two per row. Returns
+    (bf16 bits, codes int8, scales float32); every value is exact in BF16."""
+    codes = rng.integers(-127, 128, shape)
+    flat = codes.reshape(-1, shape[-1])
+    at = rng.integers(0, shape[-1], flat.shape[0])
+    flat[np.arange(flat.shape[0]), at] = rng.choice([-127, 127], flat.shape[0])
+    e = rng.integers(e_lo, e_hi + 1, shape[:-1])
+    scales = np.ldexp(1.0, e)
+    vals = codes * scales[..., None]
+    return bf16_of(vals.astype(np.float32)), codes.astype(np.int8), scales.astype(np.float32)
+
+
+def test_kv_write_i8_quantises_each_head_row_at_its_slot():
+    Hkv, D, page, nblk = 2, 16, 4, 3
+    rng = np.random.default_rng(30)
+    mag = np.array([0.05, 7.0])[None, :, None]          # heads of different size
+    k = bf16_of((rng.standard_normal((3, Hkv, D)) * mag).astype(np.float32))
+    v = bf16_of((rng.standard_normal((3, Hkv, D)) * mag[:, ::-1]).astype(np.float32))
+    k[1, 0] = 0                                          # an all-zero row
+    n = nblk * page
+    kc = np.full((n, Hkv, D), 5, np.int8)
+    vc = np.full((n, Hkv, D), 5, np.int8)
+    ks = np.full((n, Hkv), -1.0, np.float32)
+    vs = np.full((n, Hkv), -1.0, np.float32)
+    rc = oracle.kv_write_i8(k, v, np.array([5, 2, 11], np.int32), kc, vc, ks, vs)
+    assert rc == 0
+    for t, sl in ((0, 5), (1, 2), (2, 11)):
+        for x, c, sc in ((k[t], kc[sl], ks[sl]), (v[t], vc[sl], vs[sl])):
+            q, qs = oracle.quant_rows(x)                 # the head rows of one token
+            assert np.array_equal(c, q) and np.array_equal(sc, qs)
+            xv = bf16_bits_to_f64(x)
+            for h in range(Hkv):
+                if sc[h] == 0:
+                    assert not xv[h].any() and not c[h].any()
+                    continue
+                # round to nearest: within half a step of the row's scale
+                err = np.abs(xv[h] - c[h].astype(np.float64) * float(sc[h]))
+                assert err.max() <= 0.5 * float(sc[h]) * (1 + 2.0 ** -20)
+                assert np.abs(c[h]).max() == 127
+    assert not kc[2, 0].any() and ks[2, 0] == 0          # the zero row (token 1, slot 2)
+    untouched = [i for i in range(n) if i not in (2, 5, 11)]
+    assert np.all(kc[untouched] == 5) and np.all(ks[untouched] == -1.0)
+    assert np.all(vc[untouched] == 5) and np.all(vs[untouched] == -1.0)
+    # an out-of-range slot writes nothing for that token and reports -3
+    kc2, ks2 = kc.copy(), ks.copy()
+    assert oracle.kv_write_i8(k, v, np.array([n, -1, -1], np.int32), kc2, vc.copy(), ks2,
+                              vs.copy()) == -3
+    assert np.array_equal(kc2, kc) and np.array_equal(ks2, ks)
+
+
+def test_kv_write_i8_recovers_codes_and_power_of_two_scales_exactly():
+    rng = np.random.default_rng(31)
+    T, Hkv, D = 6, 3, 32
+    k, kcodes, kscales = _pow2_rows(rng, (T, Hkv, D))
+    v, vcodes, vscales = _pow2_rows(rng, (T, Hkv, D))
+    kc = np.zeros((T, Hkv, D), np.int8)
+    vc = np.zeros_like(kc)
+    ks = np.zeros((T, Hkv), np.float32)
+    vs = np.zeros_like(ks)
+    assert oracle.kv_write_i8(k, v, np.arange(T, dtype=np.int32)[::-1].copy(), kc, vc, ks, vs) == 0
+    assert np.array_equal(kc[::-1], kcodes) and np.array_equal(ks[::-1], kscales)
+    assert np.array_equal(vc[::-1], vcodes) and np.array_equal(vs[::-1], vscales)
+
+
+def test_attention_i8_exact_cache_equals_bf16_attention():
+    """Rows that INT8 represents exactly reduce the variant to the BF16 form:
+    K and V scales differ per token, per head and between K and V, so a
+    misplaced or swapped scale, or a missing dequantisation, changes the result."""
+    rng = np.random.default_rng(32)
+    B, Hq, Hkv, D, page = 3, 8, 2, 64, 16
+    ctx = [1, 37, 64]
+    nb = 4
+    phys = B * nb
+    bt = rng.permutation(phys).astype(np.int32).reshape(B, nb)
+    kb, kcodes, kscales = _pow2_rows(rng, (phys * page, Hkv, D))
+    vb, vcodes, vscales = _pow2_rows(rng, (phys * page, Hkv, D), e_lo=-3, e_hi=5)
+    q = bf16_of(rng.standard_normal((B, Hq, D)).astype(np.float32) * 0.1)
+    cl = np.array(ctx, np.int32)
+    ref, rc0 = oracle.paged_attention(q, kb, vb, bt, cl, page)
+    out, rc1 = oracle.paged_attention_i8(q, kcodes, vcodes, kscales, vscales, bt, cl, page)
+    assert rc0 == 0 and rc1 == 0
+    assert np.array_equal(out, ref)
+    # the same cache with K and V scales exchanged is a different cache
+    swapped, _ = oracle.paged_attention_i8(q, kcodes, vcodes, vscales, kscales, bt, cl, page)
+    assert not np.array_equal(swapped, ref)
+
+
+def test_attention_i8_single_token_returns_dequantised_v():
+    rng = np.random.default_rng(33)
+    Hq, Hkv, D, page = 4, 2, 16, 4
+    q = bf16_of(rng.standard_normal((1, Hq, D)).astype(np.float32))
+    kc = rng.integers(-127, 128, (page, Hkv, D)).astype(np.int8)
+    vc = rng.integers(-127, 128, (page, Hkv, D)).astype(np.int8)
+    ks = rng.uniform(1e-3, 1e-1, (page, Hkv)).astype(np.float32)
+    vs = rng.uniform(1e-3, 1e-1, (page, Hkv)).astype(np.float32)
+    out, rc = oracle.paged_attention_i8(q, kc, vc, ks, vs, np.array([[0]], np.int32),
+                                        np.array([1], np.int32), page)
+    assert rc == 0
+    for h in range(Hq):
+        kvh = h // 2
+        want = oracle.bf16_from_f64(vc[0, kvh].astype(np.float64) * float(vs[0, kvh]))
+        assert np.array_equal(out[0, h], want)
+
+
+def test_attention_i8_padded_row_and_bounds():
+    rng = np.random.default_rng(34)
+    B, Hq, Hkv, D, page = 2, 2, 1, 8, 4
+    bt = np.array([[0], [1]], np.int32)
+    kc = rng.integers(-127, 128, (2 * page, Hkv, D)).astype(np.int8)
+    vc = rng.integers(-127, 128, (2 * page, Hkv, D)).astype(np.int8)
+    ks = np.full((2 * page, Hkv), 0.01, np.float32)
+    q = bf16_of(rng.standard_normal((B, Hq, D)).astype(np.float32))
+    out, rc = oracle.paged_attention_i8(q, kc, vc, ks, ks, bt, np.array([0, 4], np.int32), page)
+    assert rc == 0 and not out[0].any() and out[1].any()
+    bad = bt.copy()
+    bad[1, 0] = 2
+    out, rc = oracle.paged_attention_i8(q, kc, vc, ks, ks, bad, np.array([0, 4], np.int32), page)
+    assert rc == -3 and not out[1].any()
+
+
+# ---------------------------------------------------------------------------
 # Gate/Up + SwiGLU
 # ---------------------------------------------------------------------------
 
@@ -565,6 +691,74 @@ def test_layer_first_token_attends_to_itself():
     att = t["attn"][0].reshape(Hq, D)
     for h in range(Hq):
         assert np.array_equal(att[h], v[h // (Hq // Hkv)])
+
+
+def _i8_history(rng, like):
+    """A random INT8 KV history shaped like a BF16 cache [slots, Hkv, D]:
+    codes in [-127, 127], one positive FP32 scale per row."""
+    codes = rng.integers(-127, 128, like.shape).astype(np.int8)
+    scales = rng.uniform(0.002, 0.03, like.shape[:2]).astype(np.float32)
+    return codes, scales
+
+
+def test_layer_i8kv_shares_the_bf16_steps_and_quantises_the_written_rows():
+    cfg, case = _tiny_case(B=2, ctx=(16, 9))
+    _, tb, rc0, _, _ = _run_layer(cfg, case)
+    rng = np.random.default_rng(35)
+    kc, ks = _i8_history(rng, case["k_cache"])
+    vc, vs = _i8_history(rng, case["v_cache"])
+    kc0, vc0, ks0, vs0 = kc.copy(), vc.copy(), ks.copy(), vs.copy()
+    w = case["weights"]
+    h, t, rc = oracle.decode_layer(w, cfg, case["hidden"], case["slot_mapping"],
+                                   case["block_table"], case["ctx_lens"], kc, vc, taps=True,
+                                   k_scale=ks, v_scale=vs)
+    assert rc0 == 0 and rc == 0
+    # everything before the cache write is the BF16-cache layer's
+    for name in ("xn", "xq", "xs", "acc_qkv", "qkv", "q_rot", "k_rot"):
+        assert np.array_equal(t[name], tb[name]), name
+    Hq, Hkv, D = cfg["num_q_heads"], cfg["num_kv_heads"], cfg["head_dim"]
+    NQ, NK = Hq * D, Hkv * D
+    written = set()
+    for b in range(2):
+        sl = case["slot_mapping"][b]
+        written.add(int(sl))
+        q, qs = oracle.quant_rows(t["k_rot"][b])
+        assert np.array_equal(kc[sl], q) and np.array_equal(ks[sl], qs)
+        q, qs = oracle.quant_rows(t["qkv"][b, NQ + NK:].reshape(Hkv, D))
+        assert np.array_equal(vc[sl], q) and np.array_equal(vs[sl], qs)
+    rest = [i for i in range(kc.shape[0]) if i not in written]
+    assert np.array_equal(kc[rest], kc0[rest]) and np.array_equal(ks[rest], ks0[rest])
+    assert np.array_equal(vc[rest], vc0[rest]) and np.array_equal(vs[rest], vs0[rest])
+    # attention reads the INT8 cache; the steps after it are the pinned ones
+    att, _ = oracle.paged_attention_i8(t["q_rot"], kc, vc, ks, vs, case["block_table"],
+                                       case["ctx_lens"], cfg["page_size"])
+    assert np.array_equal(t["attn"], att.reshape(2, NQ))
+    aq, as_ = oracle.quant_rows(t["attn"])
+    h1, _ = oracle.linear(aq, as_, w["w_o"], w["s_o"], 1, case["hidden"])
+    assert np.array_equal(t["h1"], h1)
+    hq, hs = oracle.quant_rows(oracle.rmsnorm(h1, w["post_norm_w"], cfg["rms_eps"]))
+    act, _ = oracle.gate_up_swiglu(hq, hs, w["w_gate_up"], w["s_gate_up"])
+    dq, ds = oracle.quant_rows(act)
+    out, _ = oracle.linear(dq, ds, w["w_down"], w["s_down"], 2, h1)
+    assert np.array_equal(h, out)
+
+
+def test_layer_i8kv_first_token_attends_to_its_dequantised_v():
+    cfg, case = _tiny_case(ctx=(1,))
+    rng = np.random.default_rng(36)
+    kc, ks = _i8_history(rng, case["k_cache"])
+    vc, vs = _i8_history(rng, case["v_cache"])
+    _, t, rc = oracle.decode_layer(case["weights"], cfg, case["hidden"], case["slot_mapping"],
+                                   case["block_table"], case["ctx_lens"], kc, vc, taps=True,
+                                   k_scale=ks, v_scale=vs)
+    assert rc == 0
+    Hq, Hkv, D = cfg["num_q_heads"], cfg["num_kv_heads"], cfg["head_dim"]
+    sl = case["slot_mapping"][0]
+    att = t["attn"][0].reshape(Hq, D)
+    for h in range(Hq):
+        kvh = h // (Hq // Hkv)
+        want = oracle.bf16_from_f64(vc[sl, kvh].astype(np.float64) * float(vs[sl, kvh]))
+        assert np.array_equal(att[h], want)
 
 
 # ---------------------------------------------------------------------------
