@@ -69,6 +69,14 @@ class LayerWeights(ctypes.Structure):
         "post_norm_w", "w_gate_up", "s_gate_up", "w_down", "s_down")]
 
 
+BF16_WEIGHT_NAMES = ("input_norm_w", "w_qkv", "q_norm_w", "k_norm_w", "w_o", "post_norm_w",
+                     "w_gate_up", "w_down")
+
+
+class LayerWeightsBF16(ctypes.Structure):
+    _fields_ = [(n, _p) for n in BF16_WEIGHT_NAMES]
+
+
 TAP_NAMES = ("xn", "xq", "xs", "acc_qkv", "qkv", "q_rot", "k_rot", "attn", "aq",
              "as", "acc_o", "h1", "hn", "hq", "hs", "acc_gu", "act", "actq",
              "acts", "acc_down")
@@ -104,6 +112,9 @@ def _declare(lib):
         "or_decode_layer": (_i, [_p, _p, _i, _p, _p, _p, _i, _i, _p, _p, _p, _p]),
         "or_decode_layer_i8kv": (_i, [_p, _p, _i, _p, _p, _p, _i, _i, _p, _p, _p, _p, _p,
                                       _p]),
+        "or_linear_bf16": (None, [_p, _i, _i, _p, _i, _p, _p]),
+        "or_gate_up_swiglu_bf16": (None, [_p, _i, _i, _p, _i, _p]),
+        "or_decode_layer_bf16": (_i, [_p, _p, _i, _p, _p, _p, _i, _i, _p, _p, _p, _p]),
         "or_argmax_f64": (None, [_p, _i, _i, _p]),
         "or_argmax_f32": (None, [_p, _i, _i, _p]),
         "or_lm_head": (None, [_p, _i, _i, _p, _i, _p]),
@@ -393,6 +404,72 @@ def prefill_layer(w: dict, cfg: dict, hidden, slot_mapping, block_table, ctx_len
     chunk), which tests/test_oracle_pins.py checks."""
     return decode_layer(w, cfg, hidden, slot_mapping, block_table, ctx_lens, k_cache, v_cache,
                         taps)
+
+
+def linear_bf16(x, W, residual=None) -> np.ndarray:
+    """BF16 variant projection: bf16(x [M,K] . W [N,K]^T (+ residual)) -> [M,N]."""
+    x = _c(x, U16)
+    W = _c(W, U16)
+    M, K = x.shape
+    N = W.shape[0]
+    assert W.shape[1] == K
+    res = None if residual is None else _c(residual, U16)
+    y = np.empty((M, N), U16)
+    _load().or_linear_bf16(_ptr(x), M, K, _ptr(W), N, _ptr(res), _ptr(y))
+    return y
+
+
+def gate_up_swiglu_bf16(x, W_gu) -> np.ndarray:
+    """BF16 variant Gate/Up + SwiGLU: W_gu [2I, K] -> act [M, I] (bf16)."""
+    x = _c(x, U16)
+    W_gu = _c(W_gu, U16)
+    M, K = x.shape
+    I = W_gu.shape[0] // 2
+    act = np.empty((M, I), U16)
+    _load().or_gate_up_swiglu_bf16(_ptr(x), M, K, _ptr(W_gu), I, _ptr(act))
+    return act
+
+
+BF16_TAPS = ("xn", "qkv", "q_rot", "k_rot", "attn", "h1", "hn", "act")
+
+
+def decode_layer_bf16(w: dict, cfg: dict, hidden, slot_mapping, block_table, ctx_lens,
+                      k_cache, v_cache, taps: bool = False):
+    """BF16 (unquantised) layer; weights w hold the BF16 names of
+    BF16_WEIGHT_NAMES. hidden [B,H] is returned updated (copy); the BF16 caches
+    are updated in place. Returns (hidden_out, taps_dict or None, rc)."""
+    keep: list = []
+    ws = LayerWeightsBF16()
+    for name in BF16_WEIGHT_NAMES:
+        a = _c(w[name], U16)
+        keep.append(a)
+        setattr(ws, name, _ptr(a))
+    c = make_config(cfg)
+    h = _c(hidden, U16).copy()
+    B, H = h.shape
+    sm = _c(slot_mapping, I32)
+    bt = _c(block_table, I32)
+    cl = _c(ctx_lens, I32)
+    assert k_cache.dtype == U16 and v_cache.dtype == U16
+    assert k_cache.flags["C_CONTIGUOUS"] and v_cache.flags["C_CONTIGUOUS"]
+    Hq, Hkv, D, I = cfg["num_q_heads"], cfg["num_kv_heads"], cfg["head_dim"], cfg["intermediate"]
+    num_blocks = k_cache.size // (Hkv * D * cfg["page_size"])
+    tap_arrays = None
+    tptr = None
+    if taps:
+        NQ, NK = Hq * D, Hkv * D
+        shapes = {"xn": (B, H), "qkv": (B, NQ + 2 * NK), "q_rot": (B, Hq, D),
+                  "k_rot": (B, Hkv, D), "attn": (B, NQ), "h1": (B, H), "hn": (B, H),
+                  "act": (B, I)}
+        tap_arrays = {n: np.zeros(shp, dtype=U16) for n, shp in shapes.items()}
+        t = LayerTaps()
+        for n in BF16_TAPS:
+            setattr(t, n, _ptr(tap_arrays[n]))
+        tptr = ctypes.byref(t)
+    rc = _load().or_decode_layer_bf16(ctypes.byref(ws), ctypes.byref(c), B, _ptr(h), _ptr(sm),
+                                      _ptr(bt), bt.shape[1], num_blocks, _ptr(cl),
+                                      _ptr(k_cache), _ptr(v_cache), tptr)
+    return h, tap_arrays, rc
 
 
 def lm_head(hn, W_lm) -> np.ndarray:

@@ -676,6 +676,141 @@ int or_decode_layer_i8kv(const or_layer_weights* w, const or_config* cfg, int B,
                  ctx_lens, k_codes, v_codes, k_scale, v_scale, taps);
 }
 
+/* ------------------------------------------------------------------------- */
+/* Variant: BF16 (unquantised) decode layer                                  */
+/* ------------------------------------------------------------------------- */
+
+/* [LIB-810] (the kernel PR's summary quoted there) and [SRV-48] "Summary"
+ * keep the ordinary BF16 Qwen3-14B path beside the A8W8 one without spelling
+ * out its arithmetic. Reading: the same layer with BF16 weights and no
+ * quantisation, each projection the real-valued sum narrowed to BF16 once:
+ *   y[m][n] = bf16( sum_k x[m][k] W[n][k] (+ residual[m][n]) ),
+ * evaluated in double (each BF16 x BF16 product is exact there; the sum's
+ * rounding is far below the BF16 step). W is [N, K] row-major.
+ * Pinned: brute force in rational arithmetic; operands that are powers of two
+ * times INT8 codes reproduce the pinned A8W8 projection (tests). */
+void or_linear_bf16(const uint16_t* x, int M, int K, const uint16_t* W, int N,
+                    const uint16_t* residual, uint16_t* y)
+{
+    for (int m = 0; m < M; ++m) {
+        const uint16_t* xr = x + (long)m * K;
+#pragma omp parallel for schedule(static)
+        for (int n = 0; n < N; ++n) {
+            const uint16_t* wr = W + (long)n * K;
+            double s = 0.0;
+            for (int k = 0; k < K; ++k)
+                s += or_bf16_to_double(xr[k]) * or_bf16_to_double(wr[k]);
+            if (residual)
+                s += or_bf16_to_double(residual[(long)m * N + n]);
+            y[(long)m * N + n] = or_bf16_from_double(s);
+        }
+    }
+}
+
+/* Fused Gate/Up with SwiGLU on BF16 weights W_gu [2I, K] (gate rows, then up
+ * rows): g and u are the real-valued sums, not narrowed, and
+ * act = bf16( g / (1 + exp(-g)) * u ) in double, as in the A8W8 form.
+ * Pinned through the layer taps and the closed forms of the A8W8 form's SiLU
+ * (tests). */
+void or_gate_up_swiglu_bf16(const uint16_t* x, int M, int K, const uint16_t* W_gu, int I,
+                            uint16_t* act)
+{
+    for (int m = 0; m < M; ++m) {
+        const uint16_t* xr = x + (long)m * K;
+#pragma omp parallel for schedule(static)
+        for (int j = 0; j < I; ++j) {
+            const uint16_t* wg = W_gu + (long)j * K;
+            const uint16_t* wu = W_gu + (long)(I + j) * K;
+            double g = 0.0, u = 0.0;
+            for (int k = 0; k < K; ++k) {
+                double xv = or_bf16_to_double(xr[k]);
+                g += xv * or_bf16_to_double(wg[k]);
+                u += xv * or_bf16_to_double(wu[k]);
+            }
+            act[(long)m * I + j] = or_bf16_from_double(g / (1.0 + exp(-g)) * u);
+        }
+    }
+}
+
+typedef struct {
+    const uint16_t* input_norm_w;   /* [H] */
+    const uint16_t* w_qkv;          /* [Hq*D + 2*Hkv*D, H]: Q heads, K heads, V heads */
+    const uint16_t* q_norm_w;       /* [D] */
+    const uint16_t* k_norm_w;       /* [D] */
+    const uint16_t* w_o;            /* [H, Hq*D] */
+    const uint16_t* post_norm_w;    /* [H] */
+    const uint16_t* w_gate_up;      /* [2I, H]: gate rows then up rows */
+    const uint16_t* w_down;         /* [H, I] */
+} or_layer_weights_bf16;
+
+/* One BF16 decode layer on B rows: input RMSNorm, QKV projection, per-head QK
+ * RMSNorm, RoPE at position ctx_len - 1, KV write, paged GQA attention, O
+ * projection + residual, post-attention RMSNorm, Gate/Up + SwiGLU, down
+ * projection + residual; the A8W8 layer's order with every quantisation step
+ * removed and the projections by or_linear_bf16. Taps used: xn, qkv, q_rot,
+ * k_rot, attn, h1, hn, act (the others are left untouched). hidden [B, H] is
+ * updated in place; caches are BF16 [num_blocks * page, Hkv, D]. Returns 0,
+ * -1 on shapes, -3 on bounds.
+ * Pinned: every tap equals the pinned steps composed in order; zero O and
+ * down weights keep the residual; the first token attends to its own V. */
+int or_decode_layer_bf16(const or_layer_weights_bf16* w, const or_config* cfg, int B,
+                         uint16_t* hidden, const int32_t* slot_mapping,
+                         const int32_t* block_table, int max_blocks, int num_blocks,
+                         const int32_t* ctx_lens, uint16_t* k_cache, uint16_t* v_cache,
+                         const or_layer_taps* taps)
+{
+    const int H = cfg->hidden, Hq = cfg->num_q_heads, Hkv = cfg->num_kv_heads;
+    const int D = cfg->head_dim, I = cfg->intermediate;
+    const int NQ = Hq * D, NK = Hkv * D, NQKV = NQ + 2 * NK;
+    if (Hq % Hkv != 0 || D % 2 != 0)
+        return -1;
+    int rc = 0;
+    size_t bh = (size_t)B * H;
+    uint16_t* xn = malloc(sizeof(uint16_t) * bh);
+    uint16_t* qkv = malloc(sizeof(uint16_t) * (size_t)B * NQKV);
+    uint16_t* q = malloc(sizeof(uint16_t) * (size_t)B * NQ);
+    uint16_t* k = malloc(sizeof(uint16_t) * (size_t)B * NK);
+    uint16_t* v = malloc(sizeof(uint16_t) * (size_t)B * NK);
+    uint16_t* attn = malloc(sizeof(uint16_t) * (size_t)B * NQ);
+    uint16_t* act = malloc(sizeof(uint16_t) * (size_t)B * I);
+    int32_t* pos = malloc(sizeof(int32_t) * B);
+
+    or_rmsnorm(hidden, w->input_norm_w, B, H, cfg->rms_eps, xn);
+    TAP(xn, xn, sizeof(uint16_t) * bh);
+    or_linear_bf16(xn, B, H, w->w_qkv, NQKV, NULL, qkv);
+    TAP(qkv, qkv, sizeof(uint16_t) * (size_t)B * NQKV);
+    for (int b = 0; b < B; ++b) {
+        memcpy(q + (size_t)b * NQ, qkv + (size_t)b * NQKV, sizeof(uint16_t) * NQ);
+        memcpy(k + (size_t)b * NK, qkv + (size_t)b * NQKV + NQ, sizeof(uint16_t) * NK);
+        memcpy(v + (size_t)b * NK, qkv + (size_t)b * NQKV + NQ + NK, sizeof(uint16_t) * NK);
+        pos[b] = ctx_lens[b] - 1;
+    }
+    or_rmsnorm(q, w->q_norm_w, B * Hq, D, cfg->rms_eps, q);
+    or_rmsnorm(k, w->k_norm_w, B * Hkv, D, cfg->rms_eps, k);
+    or_rope(q, B, Hq, D, pos, cfg->rope_theta);
+    or_rope(k, B, Hkv, D, pos, cfg->rope_theta);
+    TAP(q_rot, q, sizeof(uint16_t) * (size_t)B * NQ);
+    TAP(k_rot, k, sizeof(uint16_t) * (size_t)B * NK);
+    long num_slots = (long)num_blocks * cfg->page_size;
+    if (or_kv_write(k, v, B, Hkv, D, slot_mapping, k_cache, v_cache, num_slots) != 0)
+        rc = -3;
+    if (or_paged_attention(q, k_cache, v_cache, block_table, ctx_lens, B, Hq, Hkv, D,
+                           cfg->page_size, max_blocks, num_blocks, 1.0 / sqrt((double)D),
+                           attn) != 0)
+        rc = -3;
+    TAP(attn, attn, sizeof(uint16_t) * (size_t)B * NQ);
+    or_linear_bf16(attn, B, NQ, w->w_o, H, hidden, hidden);
+    TAP(h1, hidden, sizeof(uint16_t) * bh);
+    or_rmsnorm(hidden, w->post_norm_w, B, H, cfg->rms_eps, xn);
+    TAP(hn, xn, sizeof(uint16_t) * bh);
+    or_gate_up_swiglu_bf16(xn, B, H, w->w_gate_up, I, act);
+    TAP(act, act, sizeof(uint16_t) * (size_t)B * I);
+    or_linear_bf16(act, B, I, w->w_down, H, hidden, hidden);
+
+    free(xn); free(qkv); free(q); free(k); free(v); free(attn); free(act); free(pos);
+    return rc;
+}
+
 /* Final RMSNorm, BF16 LM head and greedy argmax.
  * logits[b][v] = sum_k hn[b][k] * W_lm[v][k] in double (BF16 operands);
  * next[b] = the lowest index of the maximum logit. [SRV-48] "Performance"

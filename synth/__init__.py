@@ -9,7 +9,10 @@ Distributions (one generator per tensor, seeded ``seed_base + tensor_id``):
   * FP32 per-output-channel weight scales: uniform in [1e-3, 4e-3];
   * norm weights: BF16 1 + N(0, 0.02);
   * hidden states, cached K/V, embeddings: BF16 N(0, 1);
-  * LM head: BF16 N(0, 0.02^2).
+  * LM head: BF16 N(0, 0.02^2);
+  * BF16 (unquantised) layer projections: BF16 N(0, 0.02^2);
+  * INT8 KV history: codes uniform in [-127, 127], FP32 row scales uniform in
+    [2e-3, 3e-2].
 BF16 values are made by keeping the upper 16 bits of a float32 draw (a
 truncation, so no rounding rule of the method is involved).
 
@@ -105,6 +108,27 @@ def layer_weights(cfg: dict, seed_base: int, layer: int = 0) -> dict:
         else:
             out[name] = bf16_normal(seed, shape, mean=1.0, std=0.02)
     return out
+
+
+def bf16_layer_weights(cfg: dict, seed_base: int, layer: int = 0) -> dict:
+    """One BF16 (unquantised) layer's weights: the A8W8 layer's matrices in
+    BF16 N(0, 0.02^2), norm weights as there, no scales."""
+    out = {}
+    for i, (name, (kind, shape)) in enumerate(weight_shapes(cfg).items()):
+        seed = seed_base + 1000 * (layer + 1) + 500 + i
+        if kind == "i8":
+            out[name] = bf16_normal(seed, shape, std=0.02)
+        elif kind == "bf16":
+            out[name] = bf16_normal(seed, shape, mean=1.0, std=0.02)
+    return out
+
+
+def i8_kv_history(seed: int, num_slots: int, Hkv: int, D: int):
+    """Random INT8 KV cache contents: codes [slots, Hkv, D], scales [slots, Hkv]."""
+    g = _rng(seed)
+    codes = g.integers(-127, 128, size=(num_slots, Hkv, D), dtype=np.int8)
+    scales = g.uniform(2e-3, 3e-2, size=(num_slots, Hkv)).astype(np.float32)
+    return codes, scales
 
 
 def hidden_states(seed: int, B: int, H: int) -> np.ndarray:

@@ -693,20 +693,15 @@ def test_layer_first_token_attends_to_itself():
         assert np.array_equal(att[h], v[h // (Hq // Hkv)])
 
 
-def _i8_history(rng, like):
-    """A random INT8 KV history shaped like a BF16 cache [slots, Hkv, D]:
-    codes in [-127, 127], one positive FP32 scale per row."""
-    codes = rng.integers(-127, 128, like.shape).astype(np.int8)
-    scales = rng.uniform(0.002, 0.03, like.shape[:2]).astype(np.float32)
-    return codes, scales
+def _i8_history(seed, like):
+    return synth.i8_kv_history(seed, like.shape[0], like.shape[1], like.shape[2])
 
 
 def test_layer_i8kv_shares_the_bf16_steps_and_quantises_the_written_rows():
     cfg, case = _tiny_case(B=2, ctx=(16, 9))
     _, tb, rc0, _, _ = _run_layer(cfg, case)
-    rng = np.random.default_rng(35)
-    kc, ks = _i8_history(rng, case["k_cache"])
-    vc, vs = _i8_history(rng, case["v_cache"])
+    kc, ks = _i8_history(35, case["k_cache"])
+    vc, vs = _i8_history(36, case["v_cache"])
     kc0, vc0, ks0, vs0 = kc.copy(), vc.copy(), ks.copy(), vs.copy()
     w = case["weights"]
     h, t, rc = oracle.decode_layer(w, cfg, case["hidden"], case["slot_mapping"],
@@ -745,9 +740,8 @@ def test_layer_i8kv_shares_the_bf16_steps_and_quantises_the_written_rows():
 
 def test_layer_i8kv_first_token_attends_to_its_dequantised_v():
     cfg, case = _tiny_case(ctx=(1,))
-    rng = np.random.default_rng(36)
-    kc, ks = _i8_history(rng, case["k_cache"])
-    vc, vs = _i8_history(rng, case["v_cache"])
+    kc, ks = _i8_history(37, case["k_cache"])
+    vc, vs = _i8_history(38, case["v_cache"])
     _, t, rc = oracle.decode_layer(case["weights"], cfg, case["hidden"], case["slot_mapping"],
                                    case["block_table"], case["ctx_lens"], kc, vc, taps=True,
                                    k_scale=ks, v_scale=vs)
@@ -759,6 +753,148 @@ def test_layer_i8kv_first_token_attends_to_its_dequantised_v():
         kvh = h // (Hq // Hkv)
         want = oracle.bf16_from_f64(vc[sl, kvh].astype(np.float64) * float(vs[sl, kvh]))
         assert np.array_equal(att[h], want)
+
+
+# ---------------------------------------------------------------------------
+# BF16 (unquantised) layer variant
+# ---------------------------------------------------------------------------
+
+def test_linear_bf16_is_the_exact_sum_rounded_once():
+    rng = np.random.default_rng(40)
+    M, K, N = 2, 40, 5
+    x = bf16_of(rng.standard_normal((M, K)).astype(np.float32))
+    W = bf16_of((rng.standard_normal((N, K)) * 0.05).astype(np.float32))
+    res = bf16_of((rng.standard_normal((M, N)) * 3).astype(np.float32))
+    xv, Wv, rv = bf16_bits_to_f64(x), bf16_bits_to_f64(W), bf16_bits_to_f64(res)
+    for residual in (None, res):
+        y = oracle.linear_bf16(x, W, residual)
+        for m in range(M):
+            for n in range(N):
+                exact = sum(Fraction(float(xv[m, k])) * Fraction(float(Wv[n, k]))
+                            for k in range(K))
+                if residual is not None:
+                    exact += Fraction(float(rv[m, n]))
+                assert int(y[m, n]) == bf16_nearest_bruteforce(float(exact)), (m, n)
+    # one narrowing of (sum + residual): 1 + 2^-8 + 2^-20 rounds up to 1 + 2^-7,
+    # while narrowing the sum first (to 2^-8) would leave a tie that rounds to 1
+    x1 = bf16_of(np.array([[1.0, 1.0]], np.float32))
+    W1 = bf16_of(np.array([[2.0 ** -8, 2.0 ** -20]], np.float32))
+    y1 = oracle.linear_bf16(x1, W1, bf16_of(np.array([[1.0]], np.float32)))
+    assert bf16_bits_to_f64(y1)[0, 0] == 1.0 + 2.0 ** -7
+
+
+def test_linear_bf16_on_scaled_codes_equals_the_a8w8_projection():
+    """x = q 2^a and W = c 2^b (exact in BF16): the A8W8 projection of (q, 2^a,
+    c, 2^b) is bf16(acc 2^(a+b)) exactly while |acc| < 2^24, and so must be the
+    real-valued BF16 projection; a transposed or misrouted operand breaks it."""
+    rng = np.random.default_rng(41)
+    M, K, N = 3, 256, 24
+    q = rng.integers(-127, 128, (M, K)).astype(np.int8)
+    c = rng.integers(-127, 128, (N, K)).astype(np.int8)
+    a = rng.integers(-9, -3, M)
+    b = rng.integers(-12, -6, N)
+    x = bf16_of((q * np.ldexp(1.0, a)[:, None]).astype(np.float32))
+    W = bf16_of((c * np.ldexp(1.0, b)[:, None]).astype(np.float32))
+    y8, acc = oracle.linear(q, np.ldexp(1.0, a).astype(np.float32), c,
+                            np.ldexp(1.0, b).astype(np.float32))
+    assert np.abs(acc).max() < 2 ** 24
+    assert np.array_equal(oracle.linear_bf16(x, W), y8)
+
+
+def test_gate_up_swiglu_bf16_bruteforce():
+    """g and u are the exact sums, not narrowed; act = bf16(silu(g) u) once."""
+    rng = np.random.default_rng(43)
+    M, K, I = 2, 24, 6
+    x = bf16_of(rng.standard_normal((M, K)).astype(np.float32))
+    W = bf16_of((rng.standard_normal((2 * I, K)) * 0.3).astype(np.float32))
+    act = oracle.gate_up_swiglu_bf16(x, W)
+    xv, Wv = bf16_bits_to_f64(x), bf16_bits_to_f64(W)
+    for m in range(M):
+        for j in range(I):
+            g = float(sum(Fraction(float(xv[m, k])) * Fraction(float(Wv[j, k])) for k in range(K)))
+            u = float(sum(Fraction(float(xv[m, k])) * Fraction(float(Wv[I + j, k]))
+                          for k in range(K)))
+            assert int(act[m, j]) == bf16_nearest_bruteforce(g / (1.0 + math.exp(-g)) * u), (m, j)
+
+
+def test_gate_up_swiglu_bf16_closed_forms_and_row_layout():
+    I, K = 4, 8
+    x = np.zeros((1, K), np.float32)
+    x[0, 0] = 1.0
+    g_vals = [0.0, 1.0, 40.0, -40.0]
+    u_vals = [5.0, 2.0, 1.0, 1.0]
+    W = np.zeros((2 * I, K), np.float32)
+    for j in range(I):
+        W[j, 0] = g_vals[j]            # gate rows first
+        W[I + j, 0] = u_vals[j]        # then up rows
+    bits = oracle.gate_up_swiglu_bf16(bf16_of(x), bf16_of(W))[0]
+    act = bf16_bits_to_f64(bits)
+    assert act[0] == 0.0
+    assert int(bits[1]) == bf16_nearest_bruteforce(2.0 / (1.0 + math.exp(-1.0)))
+    assert act[2] == 40.0                                  # silu(40) = 40 to BF16
+    assert int(bits[3]) == bf16_nearest_bruteforce(-40.0 / (1.0 + math.exp(40.0)))
+    assert act[3] < 0
+
+
+def _bf16_case(B=2, ctx=(16, 9), seed=42):
+    cfg = synth.TINY
+    case = synth.decode_layer_case(cfg, B, list(ctx), seed_base=seed)
+    case["weights"] = synth.bf16_layer_weights(cfg, seed)
+    return cfg, case
+
+
+def _run_bf16_layer(cfg, case, weights=None):
+    kc, vc = case["k_cache"].copy(), case["v_cache"].copy()
+    h, t, rc = oracle.decode_layer_bf16(weights or case["weights"], cfg, case["hidden"],
+                                        case["slot_mapping"], case["block_table"],
+                                        case["ctx_lens"], kc, vc, taps=True)
+    return h, t, rc, kc, vc
+
+
+def test_layer_bf16_taps_compose_the_pinned_steps():
+    cfg, case = _bf16_case()
+    h, t, rc, kc, vc = _run_bf16_layer(cfg, case)
+    assert rc == 0
+    w = case["weights"]
+    eps, D = cfg["rms_eps"], cfg["head_dim"]
+    Hq, Hkv = cfg["num_q_heads"], cfg["num_kv_heads"]
+    NQ, NK = Hq * D, Hkv * D
+    assert np.array_equal(t["xn"], oracle.rmsnorm(case["hidden"], w["input_norm_w"], eps))
+    assert np.array_equal(t["qkv"], oracle.linear_bf16(t["xn"], w["w_qkv"]))
+    qh = oracle.rmsnorm(t["qkv"][:, :NQ].reshape(2, Hq, D), w["q_norm_w"], eps)
+    kh = oracle.rmsnorm(t["qkv"][:, NQ:NQ + NK].reshape(2, Hkv, D), w["k_norm_w"], eps)
+    pos = case["ctx_lens"] - 1
+    assert np.array_equal(t["q_rot"], oracle.rope(qh, pos, cfg["rope_theta"]))
+    assert np.array_equal(t["k_rot"], oracle.rope(kh, pos, cfg["rope_theta"]))
+    for b in range(2):
+        sl = case["slot_mapping"][b]
+        assert np.array_equal(kc[sl], t["k_rot"][b])
+        assert np.array_equal(vc[sl], t["qkv"][b, NQ + NK:].reshape(Hkv, D))
+    att, _ = oracle.paged_attention(t["q_rot"], kc, vc, case["block_table"], case["ctx_lens"],
+                                    cfg["page_size"])
+    assert np.array_equal(t["attn"], att.reshape(2, NQ))
+    h1 = oracle.linear_bf16(t["attn"], w["w_o"], case["hidden"])
+    assert np.array_equal(t["h1"], h1)
+    hn = oracle.rmsnorm(h1, w["post_norm_w"], eps)
+    assert np.array_equal(t["hn"], hn)
+    act = oracle.gate_up_swiglu_bf16(hn, w["w_gate_up"])
+    assert np.array_equal(t["act"], act)
+    assert np.array_equal(h, oracle.linear_bf16(act, w["w_down"], h1))
+
+
+def test_layer_bf16_zero_projections_keep_residual_and_first_token_attends_to_itself():
+    cfg, case = _bf16_case(B=1, ctx=(1,))
+    w = dict(case["weights"])
+    w["w_o"] = np.zeros_like(w["w_o"])
+    w["w_down"] = np.zeros_like(w["w_down"])
+    h, t, rc, _, _ = _run_bf16_layer(cfg, case, weights=w)
+    assert rc == 0
+    assert np.array_equal(t["h1"], case["hidden"]) and np.array_equal(h, case["hidden"])
+    Hq, Hkv, D = cfg["num_q_heads"], cfg["num_kv_heads"], cfg["head_dim"]
+    v = t["qkv"][0, (Hq + Hkv) * D:].reshape(Hkv, D)
+    att = t["attn"][0].reshape(Hq, D)
+    for h_ in range(Hq):
+        assert np.array_equal(att[h_], v[h_ // (Hq // Hkv)])
 
 
 # ---------------------------------------------------------------------------
