@@ -309,10 +309,13 @@ a8w8_status a8w8_decode_layer(const a8w8_layer_weights* w, const a8w8_config* cf
  * slot first, then each row attends over its own ctx_lens[r] tokens, so the
  * chunk is causal: row r sees the cache's earlier tokens and the chunk's rows
  * of its sequence up to its own position. Results equal those of decoding the
- * rows one at a time in position order. Projections run on the tensor cores
- * in tiles of 16 rows. 1 <= M <= 16384; attention supports Hq / Hkv <= 7 and
- * contexts of at most 64 chunks of 128 tokens (A8W8_ERR_UNSUPPORTED_SHAPE
- * otherwise). ws / ws_bytes: a8w8_workspace_bytes(cfg, M, max_blocks). */
+ * rows one at a time in position order. Projections: 1-2 rows stream the
+ * weights through the decode GEMV; 3-64 rows use INT8 tensor-core tiles of 16
+ * rows; above 64 rows, 128 x 128 tensor-core tiles on exact FP16 images of the
+ * codes with INT32 results in the workspace. 1 <= M <= 16384; attention
+ * supports Hq / Hkv <= 7 and contexts of at most 64 chunks of 128 tokens
+ * (A8W8_ERR_UNSUPPORTED_SHAPE otherwise). ws / ws_bytes:
+ * a8w8_workspace_bytes(cfg, M, max_blocks). */
 a8w8_status a8w8_prefill_layer(const a8w8_layer_weights* w, const a8w8_config* cfg, int M,
                                a8w8_bf16* hidden, const int32_t* slot_mapping,
                                const int32_t* block_table, int max_blocks, int num_blocks,
