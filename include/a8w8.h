@@ -245,6 +245,52 @@ a8w8_status paged_decode_attention_bf16_noalloc(const a8w8_bf16* q, const a8w8_b
                                                 int num_blocks, float softmax_scale,
                                                 a8w8_bf16* out, void* stream);
 
+/* ------------------------------------------------------------------------- */
+/* INT8 KV cache variant                                                     */
+/* ------------------------------------------------------------------------- */
+
+/* [LIB-810] "BF16 KV cache" names the storage that BF16 replaced: K/V cache
+ * rows held as INT8 plus FP32 row scales, each token's K/V quantised when
+ * written, each row dequantised where attention reads it, the scales in
+ * tensors of their own. A row is one KV head's D values of one token:
+ *   codes [num_blocks * page_size, Hkv, D] int8,
+ *   scales [num_blocks * page_size, Hkv] float,
+ * each row quantised by the activation formula of a8w8_quant_rows from its
+ * BF16 values (s = absmax / 127, q = clamp(rne(x / s), -127, 127)), and read
+ * back as code * s. D is 64 or 128. Status: built; not yet run on a GPU. */
+
+/* Quantises k, v ([T, Hkv, D] BF16) row by row into the INT8 cache at
+ * slot_mapping[t]. slot < 0 skips the token; slot >= num_blocks * page_size
+ * is skipped and flags A8W8_DEVERR_SLOT. */
+a8w8_status paged_kv_write_i8(const a8w8_bf16* k, const a8w8_bf16* v, int T, int Hkv, int D,
+                              const int32_t* slot_mapping, int8_t* k_codes, int8_t* v_codes,
+                              float* k_scale, float* v_scale, int num_blocks, int page_size,
+                              void* stream);
+
+/* paged_decode_attention_bf16 over the INT8 cache: K_t and V_t are the codes
+ * times their row scales. Same arguments, workspace
+ * (a8w8_attention_workspace_bytes), shape rules and errors. */
+a8w8_status paged_decode_attention_i8kv(const a8w8_bf16* q, const int8_t* k_codes,
+                                        const int8_t* v_codes, const float* k_scale,
+                                        const float* v_scale, const int32_t* block_table,
+                                        const int32_t* ctx_lens, int B, int Hq, int Hkv, int D,
+                                        int page_size, int max_blocks, int num_blocks,
+                                        float softmax_scale, a8w8_bf16* out, void* ws,
+                                        size_t ws_bytes, void* stream);
+
+/* a8w8_decode_layer over this layer's INT8 cache: the new token's rotated K
+ * and its V are quantised per row into the cache at slot_mapping[b] (codes and
+ * scale) and attention reads the dequantised rows; every other step and every
+ * argument as a8w8_decode_layer (taps included; k_rot holds the BF16 rotated
+ * K before quantisation). */
+a8w8_status a8w8_decode_layer_i8kv(const a8w8_layer_weights* w, const a8w8_config* cfg, int B,
+                                   a8w8_bf16* hidden, const int32_t* slot_mapping,
+                                   const int32_t* block_table, int max_blocks, int num_blocks,
+                                   const int32_t* ctx_lens, int8_t* k_codes, int8_t* v_codes,
+                                   float* k_scale, float* v_scale, const float* rope, int max_pos,
+                                   void* ws, size_t ws_bytes, const a8w8_layer_taps* taps,
+                                   void* stream);
+
 /* Fills the RoPE table used by the layer ([SRV-52] "Current behavior": Q/K
  * RoPE of the fused QK-norm path; reading: Qwen3 rotate-half, theta from the
  * model). With c = cos(p * theta^(-2i/D)) and s = sin(p * theta^(-2i/D))

@@ -183,3 +183,33 @@ def test_sample_validation(lib):
     need = L.a8w8_sample_workspace_bytes(2, 10)
     assert need >= 2 * 10 * 8 and L.a8w8_sample_workspace_bytes(2, 20) - need == 2 * 10 * 8
     assert call(wsb=need - 1) == a8w8.ERR_WORKSPACE
+
+
+def test_int8_kv_validation(lib):
+    L = lib
+    # quantise-on-write: head_dim 64 or 128, every pointer given and aligned
+    args = lambda D, k=FAKE, ks=FAKE: (k, FAKE, 2, 8, D, FAKE, FAKE, FAKE, ks, FAKE, 4, 16, None)
+    assert L.paged_kv_write_i8(*args(96)) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert L.paged_kv_write_i8(*args(128, k=None)) == a8w8.ERR_INVALID_ARG
+    assert L.paged_kv_write_i8(*args(128, ks=FAKE + 4)) == a8w8.ERR_INVALID_ARG
+    assert L.paged_kv_write_i8(None, None, 0, 8, 128, None, None, None, None, None, 4, 16,
+                               None) == a8w8.OK
+    # attention: the BF16 form's shape and workspace rules
+    att = lambda D, Hq, ws, wsb, vs=FAKE: (FAKE, FAKE, FAKE, FAKE, vs, FAKE, FAKE, 2, Hq, 2, D,
+                                           128, 40, 100, 0.1, FAKE, ws, wsb, None)
+    assert L.paged_decode_attention_i8kv(*att(96, 8, None, 0)) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert L.paged_decode_attention_i8kv(*att(128, 32, None, 0)) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert L.paged_decode_attention_i8kv(*att(128, 8, FAKE, 1 << 30, vs=None)) == a8w8.ERR_INVALID_ARG
+    need = L.a8w8_attention_workspace_bytes(2, 8, 128, 40 * 128)
+    assert L.paged_decode_attention_i8kv(*att(128, 8, FAKE, need - 1)) == a8w8.ERR_WORKSPACE
+    # layer: the decode layer's checks, plus the four cache pointers
+    q = synth.QWEN3_14B
+    w = a8w8.LayerWeights(*([FAKE] * len(a8w8.WEIGHT_FIELDS)))
+
+    def layer(cfg, B=1, kc=FAKE, wsb=1 << 30):
+        return L.a8w8_decode_layer_i8kv(ctypes.byref(w), _cfg(cfg), B, FAKE, FAKE, FAKE, 2, 4, FAKE,
+                                        kc, FAKE, FAKE, FAKE, FAKE, 256, FAKE, wsb, None, None)
+    assert layer(dict(q, head_dim=96)) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert layer(q, B=65) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert layer(q, kc=None) == a8w8.ERR_INVALID_ARG
+    assert layer(q, wsb=1000) == a8w8.ERR_WORKSPACE

@@ -78,6 +78,11 @@ _SIGNATURES = {
     "a8w8_attention_workspace_bytes": (_sz, [_i, _i, _i, _i]),
     "paged_decode_attention_bf16_noalloc": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i,
                                                  _f, _p, _p]),
+    "paged_kv_write_i8": (_i, [_p, _p, _i, _i, _i, _p, _p, _p, _p, _p, _i, _i, _p]),
+    "paged_decode_attention_i8kv": (_i, [_p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i,
+                                         _f, _p, _p, _sz, _p]),
+    "a8w8_decode_layer_i8kv": (_i, [_p, _p, _i, _p, _p, _p, _i, _i, _p, _p, _p, _p, _p, _p, _i,
+                                    _p, _sz, _p, _p]),
     "a8w8_rope_table": (_i, [_p, _i, _i, ctypes.c_double, _p]),
     "a8w8_workspace_bytes": (_sz, [_p, _i, _i]),
     "a8w8_sample_workspace_bytes": (_sz, [_i, _i]),
@@ -335,6 +340,59 @@ def a8w8_decode_layer(weights: dict, cfg: dict, hidden, slot_mapping, block_tabl
         ctypes.byref(w), ctypes.byref(c), B, _ptr(hidden), _ptr(slot_mapping), _ptr(block_table),
         block_table.shape[1], num_blocks, _ptr(ctx_lens), _ptr(k_cache), _ptr(v_cache),
         _ptr(rope), rope.shape[0], _ptr(ws), ws.numel(),
+        None if t is None else ctypes.byref(t), _stream(stream)))
+
+
+def paged_kv_write_i8(k, v, slot_mapping, k_codes, v_codes, k_scale, v_scale, page_size,
+                      stream=None):
+    """INT8 KV variant: quantise k, v [T, Hkv, D] bf16 row by row into codes
+    [slots, Hkv, D] int8 and row scales [slots, Hkv] float32."""
+    T, Hkv, D = k.shape
+    num_blocks = k_codes.numel() // (Hkv * D * page_size)
+    _check(lib().paged_kv_write_i8(_ptr(k), _ptr(v), T, Hkv, D, _ptr(slot_mapping),
+                                   _ptr(k_codes), _ptr(v_codes), _ptr(k_scale), _ptr(v_scale),
+                                   num_blocks, page_size, _stream(stream)))
+
+
+def paged_decode_attention_i8kv(q, k_codes, v_codes, k_scale, v_scale, block_table, ctx_lens,
+                                page_size, softmax_scale=None, ws=None, out=None, stream=None):
+    """Decode attention over the INT8 KV cache (codes times row scales)."""
+    torch = _torch()
+    B, Hq, D = q.shape
+    Hkv = k_codes.shape[-2]
+    num_blocks = k_codes.numel() // (Hkv * D * page_size)
+    max_blocks = block_table.shape[1]
+    scale = (1.0 / D ** 0.5) if softmax_scale is None else softmax_scale
+    need = attention_workspace_bytes(B, Hq, D, max_blocks * page_size)
+    if ws is None and need:
+        ws = torch.empty(need, dtype=torch.uint8, device=q.device)
+    o = out if out is not None else torch.empty_like(q)
+    _check(lib().paged_decode_attention_i8kv(
+        _ptr(q), _ptr(k_codes), _ptr(v_codes), _ptr(k_scale), _ptr(v_scale), _ptr(block_table),
+        _ptr(ctx_lens), B, Hq, Hkv, D, page_size, max_blocks, num_blocks, scale, _ptr(o),
+        _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+    return o
+
+
+def a8w8_decode_layer_i8kv(weights: dict, cfg: dict, hidden, slot_mapping, block_table, ctx_lens,
+                           k_codes, v_codes, k_scale, v_scale, rope, ws,
+                           taps: dict | None = None, stream=None):
+    """One decode layer over an INT8 KV cache; `hidden` [B, H] bf16 is updated
+    in place, the codes and row scales at the rows' slots are written."""
+    B = hidden.shape[0]
+    Hkv, D, page = cfg["num_kv_heads"], cfg["head_dim"], cfg["page_size"]
+    num_blocks = k_codes.numel() // (Hkv * D * page)
+    c = make_config(cfg)
+    w = layer_struct(weights)
+    t = None
+    if taps is not None:
+        t = LayerTaps()
+        for n in TAP_FIELDS:
+            setattr(t, n, _ptr(taps.get(n)))
+    _check(lib().a8w8_decode_layer_i8kv(
+        ctypes.byref(w), ctypes.byref(c), B, _ptr(hidden), _ptr(slot_mapping), _ptr(block_table),
+        block_table.shape[1], num_blocks, _ptr(ctx_lens), _ptr(k_codes), _ptr(v_codes),
+        _ptr(k_scale), _ptr(v_scale), _ptr(rope), rope.shape[0], _ptr(ws), ws.numel(),
         None if t is None else ctypes.byref(t), _stream(stream)))
 
 

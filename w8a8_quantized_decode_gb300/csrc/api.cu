@@ -231,12 +231,22 @@ cudaError_t run_gemv(int pro, int epi, int ks, GemvParams p, int M, const Launch
     return cudaSuccess;
 }
 
-// Enqueues one decode layer (no validation).
+// The INT8 KV cache of one layer: codes [slots, Hkv, D], row scales [slots, Hkv].
+struct KvI8 {
+    int8_t* k_codes;
+    int8_t* v_codes;
+    float* k_scale;
+    float* v_scale;
+};
+
+// Enqueues one decode layer (no validation). With `kv8` the layer's cache is
+// the INT8 one (k_cache / v_cache unused).
 a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int B, bf16* hidden,
                           const int32_t* slot_mapping, const int32_t* block_table, int max_blocks,
                           int num_blocks, const int32_t* ctx_lens, bf16* k_cache, bf16* v_cache,
                           const float* rope, int max_pos, unsigned char* ws, const WsLayout& lay,
-                          const a8w8_layer_taps* taps, const Launch& L, bool prefill = false) {
+                          const a8w8_layer_taps* taps, const Launch& L, bool prefill = false,
+                          const KvI8* kv8 = nullptr) {
     const int H = c.hidden, D = c.head_dim, Hq = c.num_q_heads, Hkv = c.num_kv_heads;
     const int I = c.intermediate, NQ = Hq * D, NQKV = NQ + 2 * Hkv * D;
     bf16* qkv = reinterpret_cast<bf16*>(ws + lay.qkv);
@@ -315,6 +325,14 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
         if (e != cudaSuccess) return cuda_fail(e, "prefill KV write");
         a.kv_in_cache = true;
         e = launch_attn_group(a, L);
+    } else if (kv8) {
+        AttnI8Params ai = {};
+        ai.a = a;
+        ai.k_codes = kv8->k_codes;
+        ai.v_codes = kv8->v_codes;
+        ai.k_scale = kv8->k_scale;
+        ai.v_scale = kv8->v_scale;
+        e = launch_attention_i8(ai, L);
     } else {
         e = launch_attention(a, L);
     }
@@ -540,6 +558,69 @@ a8w8_status paged_decode_attention_bf16(const a8w8_bf16* q, const a8w8_bf16* k_c
     return e == cudaSuccess ? A8W8_OK : cuda_fail(e, "paged_decode_attention_bf16");
 }
 
+a8w8_status paged_kv_write_i8(const a8w8_bf16* k, const a8w8_bf16* v, int T, int Hkv, int D,
+                              const int32_t* slot_mapping, int8_t* k_codes, int8_t* v_codes,
+                              float* k_scale, float* v_scale, int num_blocks, int page_size,
+                              void* stream) {
+    if (T < 0 || Hkv <= 0 || num_blocks < 0 || page_size <= 0)
+        return fail(A8W8_ERR_INVALID_ARG, "paged_kv_write_i8: bad size");
+    if (T == 0) return A8W8_OK;
+    if (D != 64 && D != 128) return fail(A8W8_ERR_UNSUPPORTED_SHAPE, "paged_kv_write_i8: head_dim %d not supported", D);
+    a8w8_status s = check_ptrs({k, v, slot_mapping, k_codes, v_codes, k_scale, v_scale}, "paged_kv_write_i8");
+    if (s != A8W8_OK) return s;
+    cudaError_t e = launch_kv_write_i8(reinterpret_cast<const bf16*>(k), reinterpret_cast<const bf16*>(v),
+                                       T, Hkv, D, slot_mapping, k_codes, v_codes, k_scale, v_scale,
+                                       (long)num_blocks * page_size, device_error_word(),
+                                       make_launch(stream, false));
+    return e == cudaSuccess ? A8W8_OK : cuda_fail(e, "paged_kv_write_i8");
+}
+
+a8w8_status paged_decode_attention_i8kv(const a8w8_bf16* q, const int8_t* k_codes,
+                                        const int8_t* v_codes, const float* k_scale,
+                                        const float* v_scale, const int32_t* block_table,
+                                        const int32_t* ctx_lens, int B, int Hq, int Hkv, int D,
+                                        int page_size, int max_blocks, int num_blocks,
+                                        float softmax_scale, a8w8_bf16* out, void* ws,
+                                        size_t ws_bytes, void* stream) {
+    if (B < 0 || Hq <= 0 || Hkv <= 0 || page_size <= 0 || max_blocks <= 0 || num_blocks <= 0)
+        return fail(A8W8_ERR_INVALID_ARG, "paged_decode_attention_i8kv: bad size");
+    if (B == 0) return A8W8_OK;
+    if (D != 64 && D != 128) return fail(A8W8_ERR_UNSUPPORTED_SHAPE, "head_dim %d not supported", D);
+    if (Hq % Hkv || Hq / Hkv > 8) return fail(A8W8_ERR_UNSUPPORTED_SHAPE, "Hq/Hkv must be an integer <= 8");
+    if ((long long)max_blocks * page_size > (1 << 24))
+        return fail(A8W8_ERR_UNSUPPORTED_SHAPE, "context longer than 2^24 tokens");
+    a8w8_status s = check_ptrs({q, k_codes, v_codes, k_scale, v_scale, block_table, ctx_lens, out},
+                               "paged_decode_attention_i8kv");
+    if (s != A8W8_OK) return s;
+    const size_t need = attn_part_bytes(B, Hq, D, max_blocks * page_size, false);
+    if (need > 0 && (!ws || ws_bytes < need || !aligned16(ws)))
+        return fail(A8W8_ERR_WORKSPACE, "attention workspace needs %zu bytes", need);
+    AttnI8Params ai = {};
+    AttnParams& a = ai.a;
+    a.q = reinterpret_cast<const bf16*>(q);
+    a.q_stride = Hq * D;
+    a.fused = false;
+    a.block_table = block_table;
+    a.ctx_lens = ctx_lens;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.D = D;
+    a.page = page_size;
+    a.max_blocks = max_blocks;
+    a.num_blocks = num_blocks;
+    a.scale = softmax_scale;
+    a.out = reinterpret_cast<bf16*>(out);
+    a.part = static_cast<float*>(ws);
+    a.err = device_error_word();
+    ai.k_codes = const_cast<int8_t*>(k_codes);
+    ai.v_codes = const_cast<int8_t*>(v_codes);
+    ai.k_scale = const_cast<float*>(k_scale);
+    ai.v_scale = const_cast<float*>(v_scale);
+    cudaError_t e = launch_attention_i8(ai, make_launch(stream, false));
+    return e == cudaSuccess ? A8W8_OK : cuda_fail(e, "paged_decode_attention_i8kv");
+}
+
 }  // extern "C"
 
 // Scratch of paged_decode_attention_bf16_noalloc: a fixed device array owned by
@@ -685,6 +766,31 @@ a8w8_status a8w8_decode_layer(const a8w8_layer_weights* w, const a8w8_config* cf
                          max_blocks, num_blocks, ctx_lens, reinterpret_cast<bf16*>(k_cache),
                          reinterpret_cast<bf16*>(v_cache), rope, max_pos,
                          static_cast<unsigned char*>(ws), lay, taps, L);
+}
+
+a8w8_status a8w8_decode_layer_i8kv(const a8w8_layer_weights* w, const a8w8_config* cfg, int B,
+                                   a8w8_bf16* hidden, const int32_t* slot_mapping,
+                                   const int32_t* block_table, int max_blocks, int num_blocks,
+                                   const int32_t* ctx_lens, int8_t* k_codes, int8_t* v_codes,
+                                   float* k_scale, float* v_scale, const float* rope, int max_pos,
+                                   void* ws, size_t ws_bytes, const a8w8_layer_taps* taps,
+                                   void* stream) {
+    a8w8_status s = check_layer_common(cfg, B, max_blocks, num_blocks, rope, max_pos);
+    if (s != A8W8_OK) return s;
+    if ((s = check_layer_weights(w)) != A8W8_OK) return s;
+    if ((s = check_ptrs({hidden, slot_mapping, block_table, ctx_lens, k_codes, v_codes, k_scale,
+                         v_scale, rope},
+                        "a8w8_decode_layer_i8kv")) != A8W8_OK)
+        return s;
+    const WsLayout lay = ws_layout(*cfg, B, max_blocks);
+    if (!ws || ws_bytes < lay.total || !aligned16(ws))
+        return fail(A8W8_ERR_WORKSPACE, "decode layer workspace needs %zu bytes", lay.total);
+    Launch L = make_launch(stream, true);
+    if (L.num_sms <= 0) return fail(A8W8_ERR_CUDA, "no CUDA device");
+    const KvI8 kv8 = {k_codes, v_codes, k_scale, v_scale};
+    return enqueue_layer(w, *cfg, B, reinterpret_cast<bf16*>(hidden), slot_mapping, block_table,
+                         max_blocks, num_blocks, ctx_lens, nullptr, nullptr, rope, max_pos,
+                         static_cast<unsigned char*>(ws), lay, taps, L, false, &kv8);
 }
 
 a8w8_status a8w8_prefill_layer(const a8w8_layer_weights* w, const a8w8_config* cfg, int M,

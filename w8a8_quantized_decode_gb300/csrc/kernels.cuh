@@ -129,6 +129,25 @@ bool attn_group_shape_ok(int Hq, int Hkv, int D, int max_ctx);
 bool attn_group_supported(const AttnParams& p);
 int attn_group_splits(int max_ctx);
 cudaError_t launch_attn_group(const AttnParams& p, const Launch& L);
+// Whether the decode-layer attention combines its split partials in the
+// kernel (tickets given and contexts up to 16384 tokens).
+bool in_kernel_combine(int max_ctx, bool tickets);
+
+// INT8 KV cache variant (attn_i8.cu): codes [num_blocks*page, Hkv, D] int8 and
+// row scales [num_blocks*page, Hkv] float; `a` as for the BF16 form with its
+// k_cache / v_cache unused. Per-head form only.
+struct AttnI8Params {
+    AttnParams a;
+    int8_t* k_codes;
+    int8_t* v_codes;
+    float* k_scale;
+    float* v_scale;
+};
+cudaError_t launch_attention_i8(const AttnI8Params& p, const Launch& L);
+cudaError_t launch_kv_write_i8(const bf16* k, const bf16* v, int T, int Hkv, int D,
+                               const int32_t* slot_mapping, int8_t* k_codes, int8_t* v_codes,
+                               float* k_scale, float* v_scale, long num_slots, unsigned* err,
+                               const Launch& L);
 // Prefill: per-head K RMSNorm + RoPE of every row's new token and the K/V
 // write into the cache, before the attention (fused QKV rows in p.q).
 cudaError_t launch_kv_prep(const AttnParams& p, const Launch& L);
