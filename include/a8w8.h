@@ -291,6 +291,52 @@ a8w8_status a8w8_decode_layer_i8kv(const a8w8_layer_weights* w, const a8w8_confi
                                    void* ws, size_t ws_bytes, const a8w8_layer_taps* taps,
                                    void* stream);
 
+/* ------------------------------------------------------------------------- */
+/* BF16 (unquantised) layer variant                                          */
+/* ------------------------------------------------------------------------- */
+
+/* [LIB-810] (the kernel PR summary it quotes) and [SRV-48] "Summary" keep the
+ * ordinary BF16 Qwen3-14B path beside the A8W8 one without giving its
+ * arithmetic. Reading: the A8W8 layer's steps with every quantisation step
+ * removed; each projection
+ *   y[m][n] = bf16_rne( sum_k x[m][k] * W[n][k] (+ residual[m][n]) )
+ * (products exact in float32, float32 sums), the SwiGLU epilogue
+ * act = bf16_rne( silu(g) * u ) on the float32 g and u. Status: built; not
+ * yet run on a GPU. */
+typedef struct {
+    const a8w8_bf16* input_norm_w;   /* [H] */
+    const a8w8_bf16* w_qkv;          /* [Hq*D + 2*Hkv*D, H]: Q heads, K heads, V heads */
+    const a8w8_bf16* q_norm_w;       /* [D] */
+    const a8w8_bf16* k_norm_w;       /* [D] */
+    const a8w8_bf16* w_o;            /* [H, Hq*D] */
+    const a8w8_bf16* post_norm_w;    /* [H] */
+    const a8w8_bf16* w_gate_up;      /* [2I, H]: gate rows [0, I), up rows [I, 2I) */
+    const a8w8_bf16* w_down;         /* [H, I] */
+} a8w8_bf16_layer_weights;
+
+/* BF16 projection: x [M, K], W [N, K], residual [M, N] (nullable; may alias
+ * y), y [M, N]. K a positive multiple of 8, at most 49152. */
+a8w8_status bf16_linear(const a8w8_bf16* x, int M, int K, const a8w8_bf16* W, int N,
+                        const a8w8_bf16* residual, a8w8_bf16* y, void* stream);
+
+/* BF16 fused Gate/Up with SwiGLU: W_gu [2I, K] (gate rows, then up rows),
+ * act [M, I]. Shape rules as bf16_linear. */
+a8w8_status bf16_gate_up_swiglu(const a8w8_bf16* x, int M, int K, const a8w8_bf16* W_gu, int I,
+                                a8w8_bf16* act, void* stream);
+
+/* One BF16 decode layer: input RMSNorm, QKV projection, per-head QK RMSNorm,
+ * RoPE, KV write, paged GQA attention (the A8W8 layer's kernels), O
+ * projection + residual, post-attention RMSNorm, Gate/Up + SwiGLU, down
+ * projection + residual. Arguments, caches, workspace (a8w8_workspace_bytes)
+ * and errors as a8w8_decode_layer (cfg->down_k_splits is not used); taps:
+ * the BF16 fields xn, qkv, q_rot, k_rot, attn, h1, hn, act. */
+a8w8_status bf16_decode_layer(const a8w8_bf16_layer_weights* w, const a8w8_config* cfg, int B,
+                              a8w8_bf16* hidden, const int32_t* slot_mapping,
+                              const int32_t* block_table, int max_blocks, int num_blocks,
+                              const int32_t* ctx_lens, a8w8_bf16* k_cache, a8w8_bf16* v_cache,
+                              const float* rope, int max_pos, void* ws, size_t ws_bytes,
+                              const a8w8_layer_taps* taps, void* stream);
+
 /* Fills the RoPE table used by the layer ([SRV-52] "Current behavior": Q/K
  * RoPE of the fused QK-norm path; reading: Qwen3 rotate-half, theta from the
  * model). With c = cos(p * theta^(-2i/D)) and s = sin(p * theta^(-2i/D))

@@ -213,3 +213,27 @@ def test_int8_kv_validation(lib):
     assert layer(q, B=65) == a8w8.ERR_UNSUPPORTED_SHAPE
     assert layer(q, kc=None) == a8w8.ERR_INVALID_ARG
     assert layer(q, wsb=1000) == a8w8.ERR_WORKSPACE
+
+
+def test_bf16_layer_validation(lib):
+    L = lib
+    assert L.bf16_linear(FAKE, 1, 20, FAKE, 4, None, FAKE, None) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert L.bf16_linear(FAKE, 1, 49160, FAKE, 4, None, FAKE, None) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert L.bf16_linear(None, 1, 32, FAKE, 4, None, FAKE, None) == a8w8.ERR_INVALID_ARG
+    assert L.bf16_linear(FAKE, 1, 32, FAKE, 4, FAKE + 2, FAKE, None) == a8w8.ERR_INVALID_ARG
+    assert L.bf16_linear(None, 0, 32, None, 4, None, None, None) == a8w8.OK
+    assert L.bf16_gate_up_swiglu(FAKE, 1, 12, FAKE, 4, FAKE, None) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert L.bf16_gate_up_swiglu(FAKE, 1, 32, None, 4, FAKE, None) == a8w8.ERR_INVALID_ARG
+    q = synth.QWEN3_14B
+    w = a8w8.Bf16LayerWeights(*([FAKE] * len(a8w8.BF16_WEIGHT_FIELDS)))
+
+    def layer(cfg, w=w, B=1, wsb=1 << 30):
+        return L.bf16_decode_layer(ctypes.byref(w), _cfg(cfg), B, FAKE, FAKE, FAKE, 2, 4, FAKE, FAKE,
+                                   FAKE, FAKE, 256, FAKE, wsb, None, None)
+    assert layer(dict(q, head_dim=96)) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert layer(q, B=65) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert layer(dict(q, intermediate=49168)) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert layer(q, wsb=1000) == a8w8.ERR_WORKSPACE
+    bad = a8w8.Bf16LayerWeights(*([FAKE] * len(a8w8.BF16_WEIGHT_FIELDS)))
+    bad.w_down = None
+    assert layer(q, w=bad) == a8w8.ERR_INVALID_ARG

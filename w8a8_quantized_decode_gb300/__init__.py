@@ -53,6 +53,14 @@ class LayerWeights(ctypes.Structure):
     _fields_ = [(n, _p) for n in WEIGHT_FIELDS]
 
 
+BF16_WEIGHT_FIELDS = ("input_norm_w", "w_qkv", "q_norm_w", "k_norm_w", "w_o", "post_norm_w",
+                      "w_gate_up", "w_down")
+
+
+class Bf16LayerWeights(ctypes.Structure):
+    _fields_ = [(n, _p) for n in BF16_WEIGHT_FIELDS]
+
+
 class Model(ctypes.Structure):
     _fields_ = [("embed", _p), ("layers", _p), ("final_norm_w", _p), ("lm_head", _p)]
 
@@ -83,6 +91,10 @@ _SIGNATURES = {
                                          _f, _p, _p, _sz, _p]),
     "a8w8_decode_layer_i8kv": (_i, [_p, _p, _i, _p, _p, _p, _i, _i, _p, _p, _p, _p, _p, _p, _i,
                                     _p, _sz, _p, _p]),
+    "bf16_linear": (_i, [_p, _i, _i, _p, _i, _p, _p, _p]),
+    "bf16_gate_up_swiglu": (_i, [_p, _i, _i, _p, _i, _p, _p]),
+    "bf16_decode_layer": (_i, [_p, _p, _i, _p, _p, _p, _i, _i, _p, _p, _p, _p, _i, _p, _sz, _p,
+                               _p]),
     "a8w8_rope_table": (_i, [_p, _i, _i, ctypes.c_double, _p]),
     "a8w8_workspace_bytes": (_sz, [_p, _i, _i]),
     "a8w8_sample_workspace_bytes": (_sz, [_i, _i]),
@@ -393,6 +405,49 @@ def a8w8_decode_layer_i8kv(weights: dict, cfg: dict, hidden, slot_mapping, block
         ctypes.byref(w), ctypes.byref(c), B, _ptr(hidden), _ptr(slot_mapping), _ptr(block_table),
         block_table.shape[1], num_blocks, _ptr(ctx_lens), _ptr(k_codes), _ptr(v_codes),
         _ptr(k_scale), _ptr(v_scale), _ptr(rope), rope.shape[0], _ptr(ws), ws.numel(),
+        None if t is None else ctypes.byref(t), _stream(stream)))
+
+
+def bf16_linear(x, W, residual=None, out=None, stream=None):
+    """BF16 projection: bf16(x [M,K] . W [N,K]^T (+ residual)) -> [M, N]."""
+    torch = _torch()
+    M, K = x.shape
+    N = W.shape[0]
+    y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _check(lib().bf16_linear(_ptr(x), M, K, _ptr(W), N, _ptr(residual), _ptr(y), _stream(stream)))
+    return y
+
+
+def bf16_gate_up_swiglu(x, W_gu, stream=None):
+    """BF16 fused Gate/Up + SwiGLU: W_gu [2I, K] -> act [M, I]."""
+    torch = _torch()
+    M, K = x.shape
+    I = W_gu.shape[0] // 2
+    act = torch.empty((M, I), dtype=torch.bfloat16, device=x.device)
+    _check(lib().bf16_gate_up_swiglu(_ptr(x), M, K, _ptr(W_gu), I, _ptr(act), _stream(stream)))
+    return act
+
+
+def bf16_decode_layer(weights: dict, cfg: dict, hidden, slot_mapping, block_table, ctx_lens,
+                      k_cache, v_cache, rope, ws, taps: dict | None = None, stream=None):
+    """One BF16 (unquantised) decode layer; `hidden` [B, H] bf16 is updated in
+    place; weights hold BF16_WEIGHT_FIELDS."""
+    B = hidden.shape[0]
+    Hkv, D, page = cfg["num_kv_heads"], cfg["head_dim"], cfg["page_size"]
+    num_blocks = k_cache.numel() // (Hkv * D * page)
+    c = make_config(cfg)
+    w = Bf16LayerWeights()
+    for n in BF16_WEIGHT_FIELDS:
+        setattr(w, n, _ptr(weights[n]))
+    t = None
+    if taps is not None:
+        t = LayerTaps()
+        for n in TAP_FIELDS:
+            setattr(t, n, _ptr(taps.get(n)))
+    _check(lib().bf16_decode_layer(
+        ctypes.byref(w), ctypes.byref(c), B, _ptr(hidden), _ptr(slot_mapping), _ptr(block_table),
+        block_table.shape[1], num_blocks, _ptr(ctx_lens), _ptr(k_cache), _ptr(v_cache),
+        _ptr(rope), rope.shape[0], _ptr(ws), ws.numel(),
         None if t is None else ctypes.byref(t), _stream(stream)))
 
 

@@ -402,6 +402,136 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     return A8W8_OK;
 }
 
+// Enqueues one BF16 (unquantised) decode layer (no validation): the A8W8
+// layer's steps without the quantisation, the same attention kernels.
+a8w8_status enqueue_bf16_layer(const a8w8_bf16_layer_weights* w, const a8w8_config& c, int B,
+                               bf16* hidden, const int32_t* slot_mapping,
+                               const int32_t* block_table, int max_blocks, int num_blocks,
+                               const int32_t* ctx_lens, bf16* k_cache, bf16* v_cache,
+                               const float* rope, int max_pos, unsigned char* ws,
+                               const WsLayout& lay, const a8w8_layer_taps* taps, const Launch& L) {
+    const int H = c.hidden, D = c.head_dim, Hq = c.num_q_heads, Hkv = c.num_kv_heads;
+    const int I = c.intermediate, NQ = Hq * D, NQKV = NQ + 2 * Hkv * D;
+    bf16* xn = reinterpret_cast<bf16*>(ws + lay.hid);
+    bf16* qkv = reinterpret_cast<bf16*>(ws + lay.qkv);
+    bf16* attn = reinterpret_cast<bf16*>(ws + lay.attn);
+    bf16* act = reinterpret_cast<bf16*>(ws + lay.act);
+    unsigned* att_tk = reinterpret_cast<unsigned*>(ws + lay.att_tk);
+    const a8w8_layer_taps none = {};
+    const a8w8_layer_taps& T = taps ? *taps : none;
+    auto tap = [&](void* dst, const void* src, size_t bytes, const char* what) -> a8w8_status {
+        if (!dst) return A8W8_OK;
+        cudaError_t e = cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, L.stream);
+        return e == cudaSuccess ? A8W8_OK : cuda_fail(e, what);
+    };
+    a8w8_status st;
+
+    // input RMSNorm, QKV projection
+    cudaError_t e = launch_rmsnorm_rows(hidden, B, H, reinterpret_cast<const bf16*>(w->input_norm_w),
+                                        c.rms_eps, xn, L);
+    if (e != cudaSuccess) return cuda_fail(e, "input RMSNorm");
+    if ((st = tap(T.xn, xn, (size_t)B * H * 2, "tap xn")) != A8W8_OK) return st;
+    e = cudaMemsetAsync(att_tk, 0, (size_t)B * Hq * 4, L.stream);   // attention split tickets
+    if (e != cudaSuccess) return cuda_fail(e, "clear tickets");
+    Bf16GemvParams g = {};
+    g.x = xn;
+    g.ldx = H;
+    g.W = reinterpret_cast<const bf16*>(w->w_qkv);
+    g.K = H;
+    g.N = NQKV;
+    g.M = B;
+    g.y = qkv;
+    g.ldy = NQKV;
+    e = launch_bf16_gemv(g, false, L);
+    if (e != cudaSuccess) return cuda_fail(e, "QKV projection");
+    if ((st = tap(T.qkv, qkv, (size_t)B * NQKV * 2, "tap qkv")) != A8W8_OK) return st;
+
+    // QK norm, RoPE, KV write, paged attention: the A8W8 layer's kernels
+    AttnParams a = {};
+    a.q = qkv;
+    a.q_stride = NQKV;
+    a.fused = true;
+    a.q_norm_w = reinterpret_cast<const bf16*>(w->q_norm_w);
+    a.k_norm_w = reinterpret_cast<const bf16*>(w->k_norm_w);
+    a.rope = rope;
+    a.max_pos = max_pos;
+    a.eps = c.rms_eps;
+    a.slot_mapping = slot_mapping;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_table = block_table;
+    a.ctx_lens = ctx_lens;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.D = D;
+    a.page = c.page_size;
+    a.max_blocks = max_blocks;
+    a.num_blocks = num_blocks;
+    {
+        const double sd = 1.0 / std::sqrt((double)D);
+        a.scale = (float)sd;
+        a.scale_lo = (float)(sd - (double)a.scale);
+    }
+    a.out = attn;
+    a.part = reinterpret_cast<float*>(ws + lay.part);
+    a.tickets = att_tk;
+    a.err = device_error_word();
+    a.tap_q_rot = reinterpret_cast<bf16*>(T.q_rot);
+    a.tap_k_rot = reinterpret_cast<bf16*>(T.k_rot);
+    e = launch_attention(a, L);
+    if (e != cudaSuccess) return cuda_fail(e, "attention");
+    if ((st = tap(T.attn, attn, (size_t)B * NQ * 2, "tap attn")) != A8W8_OK) return st;
+
+    // O projection + residual (in place)
+    g = Bf16GemvParams{};
+    g.x = attn;
+    g.ldx = NQ;
+    g.W = reinterpret_cast<const bf16*>(w->w_o);
+    g.K = NQ;
+    g.N = H;
+    g.M = B;
+    g.residual = hidden;
+    g.y = hidden;
+    g.ldy = H;
+    e = launch_bf16_gemv(g, false, L);
+    if (e != cudaSuccess) return cuda_fail(e, "O projection");
+    if ((st = tap(T.h1, hidden, (size_t)B * H * 2, "tap h1")) != A8W8_OK) return st;
+
+    // post-attention RMSNorm, Gate/Up + SwiGLU
+    e = launch_rmsnorm_rows(hidden, B, H, reinterpret_cast<const bf16*>(w->post_norm_w), c.rms_eps,
+                            xn, L);
+    if (e != cudaSuccess) return cuda_fail(e, "post-attention RMSNorm");
+    if ((st = tap(T.hn, xn, (size_t)B * H * 2, "tap hn")) != A8W8_OK) return st;
+    g = Bf16GemvParams{};
+    g.x = xn;
+    g.ldx = H;
+    g.W = reinterpret_cast<const bf16*>(w->w_gate_up);
+    g.K = H;
+    g.N = I;
+    g.M = B;
+    g.y = act;
+    g.ldy = I;
+    e = launch_bf16_gemv(g, true, L);
+    if (e != cudaSuccess) return cuda_fail(e, "Gate/Up projection");
+    if ((st = tap(T.act, act, (size_t)B * I * 2, "tap act")) != A8W8_OK) return st;
+
+    // down projection + residual (in place)
+    g = Bf16GemvParams{};
+    g.x = act;
+    g.ldx = I;
+    g.W = reinterpret_cast<const bf16*>(w->w_down);
+    g.K = I;
+    g.N = H;
+    g.M = B;
+    g.residual = hidden;
+    g.y = hidden;
+    g.ldy = H;
+    e = launch_bf16_gemv(g, false, L);
+    if (e != cudaSuccess) return cuda_fail(e, "down projection");
+    return A8W8_OK;
+}
+
 a8w8_status check_layer_common(const a8w8_config* cfg, int B, int max_blocks, int num_blocks,
                                const float* rope, int max_pos) {
     a8w8_status s = check_config(cfg);
@@ -791,6 +921,85 @@ a8w8_status a8w8_decode_layer_i8kv(const a8w8_layer_weights* w, const a8w8_confi
     return enqueue_layer(w, *cfg, B, reinterpret_cast<bf16*>(hidden), slot_mapping, block_table,
                          max_blocks, num_blocks, ctx_lens, nullptr, nullptr, rope, max_pos,
                          static_cast<unsigned char*>(ws), lay, taps, L, false, &kv8);
+}
+
+a8w8_status bf16_linear(const a8w8_bf16* x, int M, int K, const a8w8_bf16* W, int N,
+                        const a8w8_bf16* residual, a8w8_bf16* y, void* stream) {
+    if (M < 0 || K < 0 || N < 0) return fail(A8W8_ERR_INVALID_ARG, "bf16_linear: negative size");
+    if (M == 0 || N == 0) return A8W8_OK;
+    if (K == 0 || K % 8 || bf16_gemv_batch_tile(K) == 0)
+        return fail(A8W8_ERR_UNSUPPORTED_SHAPE, "bf16_linear: K must be a positive multiple of 8, at most 49152");
+    a8w8_status s = check_ptrs({x, W, y}, "bf16_linear");
+    if (s != A8W8_OK) return s;
+    if (residual && !aligned16(residual)) return fail(A8W8_ERR_INVALID_ARG, "bf16_linear: residual misaligned");
+    Launch L = make_launch(stream, false);
+    if (L.num_sms <= 0) return fail(A8W8_ERR_CUDA, "bf16_linear: no CUDA device");
+    Bf16GemvParams g = {};
+    g.x = reinterpret_cast<const bf16*>(x);
+    g.ldx = K;
+    g.W = reinterpret_cast<const bf16*>(W);
+    g.K = K;
+    g.N = N;
+    g.M = M;
+    g.residual = reinterpret_cast<const bf16*>(residual);
+    g.y = reinterpret_cast<bf16*>(y);
+    g.ldy = N;
+    cudaError_t e = launch_bf16_gemv(g, false, L);
+    return e == cudaSuccess ? A8W8_OK : cuda_fail(e, "bf16_linear");
+}
+
+a8w8_status bf16_gate_up_swiglu(const a8w8_bf16* x, int M, int K, const a8w8_bf16* W_gu, int I,
+                                a8w8_bf16* act, void* stream) {
+    if (M < 0 || K < 0 || I < 0) return fail(A8W8_ERR_INVALID_ARG, "bf16_gate_up_swiglu: negative size");
+    if (M == 0 || I == 0) return A8W8_OK;
+    if (K == 0 || K % 8 || bf16_gemv_batch_tile(K) == 0)
+        return fail(A8W8_ERR_UNSUPPORTED_SHAPE, "bf16_gate_up_swiglu: K must be a positive multiple of 8, at most 49152");
+    a8w8_status s = check_ptrs({x, W_gu, act}, "bf16_gate_up_swiglu");
+    if (s != A8W8_OK) return s;
+    Launch L = make_launch(stream, false);
+    if (L.num_sms <= 0) return fail(A8W8_ERR_CUDA, "bf16_gate_up_swiglu: no CUDA device");
+    Bf16GemvParams g = {};
+    g.x = reinterpret_cast<const bf16*>(x);
+    g.ldx = K;
+    g.W = reinterpret_cast<const bf16*>(W_gu);
+    g.K = K;
+    g.N = I;
+    g.M = M;
+    g.y = reinterpret_cast<bf16*>(act);
+    g.ldy = I;
+    cudaError_t e = launch_bf16_gemv(g, true, L);
+    return e == cudaSuccess ? A8W8_OK : cuda_fail(e, "bf16_gate_up_swiglu");
+}
+
+a8w8_status bf16_decode_layer(const a8w8_bf16_layer_weights* w, const a8w8_config* cfg, int B,
+                              a8w8_bf16* hidden, const int32_t* slot_mapping,
+                              const int32_t* block_table, int max_blocks, int num_blocks,
+                              const int32_t* ctx_lens, a8w8_bf16* k_cache, a8w8_bf16* v_cache,
+                              const float* rope, int max_pos, void* ws, size_t ws_bytes,
+                              const a8w8_layer_taps* taps, void* stream) {
+    a8w8_status s = check_layer_common(cfg, B, max_blocks, num_blocks, rope, max_pos);
+    if (s != A8W8_OK) return s;
+    if (!w) return fail(A8W8_ERR_INVALID_ARG, "layer weights are NULL");
+    if ((s = check_ptrs({w->input_norm_w, w->w_qkv, w->q_norm_w, w->k_norm_w, w->w_o,
+                         w->post_norm_w, w->w_gate_up, w->w_down},
+                        "BF16 layer weights")) != A8W8_OK)
+        return s;
+    const int D = cfg->head_dim;
+    const int kmax = std::max({cfg->hidden, cfg->num_q_heads * D, cfg->intermediate});
+    if (bf16_gemv_batch_tile(kmax) == 0)
+        return fail(A8W8_ERR_UNSUPPORTED_SHAPE, "bf16_decode_layer: projection K above 49152");
+    if ((s = check_ptrs({hidden, slot_mapping, block_table, ctx_lens, k_cache, v_cache, rope},
+                        "bf16_decode_layer")) != A8W8_OK)
+        return s;
+    const WsLayout lay = ws_layout(*cfg, B, max_blocks);
+    if (!ws || ws_bytes < lay.total || !aligned16(ws))
+        return fail(A8W8_ERR_WORKSPACE, "decode layer workspace needs %zu bytes", lay.total);
+    Launch L = make_launch(stream, true);
+    if (L.num_sms <= 0) return fail(A8W8_ERR_CUDA, "no CUDA device");
+    return enqueue_bf16_layer(w, *cfg, B, reinterpret_cast<bf16*>(hidden), slot_mapping,
+                              block_table, max_blocks, num_blocks, ctx_lens,
+                              reinterpret_cast<bf16*>(k_cache), reinterpret_cast<bf16*>(v_cache),
+                              rope, max_pos, static_cast<unsigned char*>(ws), lay, taps, L);
 }
 
 a8w8_status a8w8_prefill_layer(const a8w8_layer_weights* w, const a8w8_config* cfg, int M,

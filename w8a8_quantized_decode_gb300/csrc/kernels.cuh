@@ -148,6 +148,25 @@ cudaError_t launch_kv_write_i8(const bf16* k, const bf16* v, int T, int Hkv, int
                                const int32_t* slot_mapping, int8_t* k_codes, int8_t* v_codes,
                                float* k_scale, float* v_scale, long num_slots, unsigned* err,
                                const Launch& L);
+// BF16 (unquantised) layer (gemv_bf16.cu): y[m][n] = bf16(sum_k x[m][k]
+// W[n][k] (+ residual[m][n])), or with `swiglu` act[m][n] = bf16(silu(g) u)
+// from the gate row n and the up row N + n of W [2N, K]. K, ldx multiples
+// of 8; rows processed in tiles of bf16_gemv_batch_tile(K) (0: K too large).
+struct Bf16GemvParams {
+    const bf16* x;          // [M, ldx]
+    int ldx;
+    const bf16* W;          // [N, K] (or [2N, K] with swiglu)
+    int K, N, M;
+    const bf16* residual;   // [M, ldy] or null (may alias y)
+    bf16* y;                // [M, ldy]
+    int ldy;
+};
+int bf16_gemv_batch_tile(int K);
+cudaError_t launch_bf16_gemv(const Bf16GemvParams& p, bool swiglu, const Launch& L);
+// y[r] = bf16(x[r] / sqrt(mean(x[r]^2) + eps) * w), one CTA per row (H % 8 == 0).
+cudaError_t launch_rmsnorm_rows(const bf16* x, int rows, int H, const bf16* w, float eps, bf16* y,
+                                const Launch& L);
+
 // Prefill: per-head K RMSNorm + RoPE of every row's new token and the K/V
 // write into the cache, before the attention (fused QKV rows in p.q).
 cudaError_t launch_kv_prep(const AttnParams& p, const Launch& L);
