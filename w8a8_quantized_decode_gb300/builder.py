@@ -65,7 +65,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
         return obj
 
     srcs = sources()
-    with concurrent.futures.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
+    workers = max(1, min(os.cpu_count() or 8, len(srcs), 16))   # one wave where the cores allow
+    with concurrent.futures.ThreadPoolExecutor(max_workers=workers) as ex:
         objs = list(ex.map(compile_one, srcs))
     tmp = LIB + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"]
