@@ -184,6 +184,32 @@ def host_model(model) -> dict:
                 layers=[{k: h(v) for k, v in l.items()} for l in model["layers"]])
 
 
+def host_cpu(cpuinfo: str = "/proc/cpuinfo") -> dict:
+    """The host CPU's model and logical core count, for the oracle timings
+    (never raises: unknown fields read "unknown")."""
+    model = None
+    arm = {}
+    try:
+        with open(cpuinfo) as f:
+            for ln in f:
+                if ":" not in ln:
+                    continue
+                key, val = (x.strip() for x in ln.split(":", 1))
+                key = key.lower()
+                if key == "model name" and not model:
+                    model = val
+                elif key in ("cpu implementer", "cpu part") and key not in arm:
+                    arm[key] = val
+    except (OSError, UnicodeDecodeError):
+        pass
+    if not model and arm:
+        model = (f"implementer {arm.get('cpu implementer', '?')} "
+                 f"part {arm.get('cpu part', '?')}")
+    import platform
+    return {"model": model or platform.processor() or "unknown",
+            "arch": platform.machine() or "unknown", "nproc": os.cpu_count()}
+
+
 def time_oracle_steps(hm, cfg, n_steps: int, budget_s: float):
     """Oracle decode steps (batch 1) from a prompt of PROMPT_LEN tokens; returns
     (seconds per step list, threads)."""
@@ -239,6 +265,7 @@ def run_reference(args, cfg):
         "config": {"workload": WORKLOAD, "batch": 1, "prompt_len": PROMPT_LEN,
                    "max_seq_len": MAX_SEQ, "layers": cfg["num_layers"]},
         "cpu_baseline": {"value": tpot, "unit": "ms/token", "cores": threads, "kind": "oracle",
+                         "host": host_cpu(),
                          "sample": f"{len(timed)} oracle decode steps (40 layers + LM head, "
                                    f"batch 1, context {PROMPT_LEN + 1}..)"},
         "e2e": {"value": tpot, "unit": "ms/token", "h2d_bytes_per_step": 0,
@@ -763,7 +790,7 @@ def cpu_baseline(model, cfg):
     times, threads = time_oracle_steps(hm, cfg, n_steps=8, budget_s=20.0)
     del hm
     return {"value": 1000.0 * sum(times) / len(times), "unit": "ms/token", "cores": threads,
-            "kind": "oracle",
+            "kind": "oracle", "host": host_cpu(),
             "sample": f"{len(times)} oracle decode steps of the same workload (40 layers + LM "
                       f"head, batch 1, contexts {PROMPT_LEN + 1}..{PROMPT_LEN + len(times)})"}
 

@@ -56,3 +56,16 @@ def test_single_process_is_identity():
     import bench
     assert bench.max_over_ranks(3.5) == 3.5
     assert bench.job_rate(1, 2.0, 1) == 500.0
+
+
+def test_host_cpu_record(tmp_path):
+    import bench
+    x86 = tmp_path / "x86"
+    x86.write_text("processor\t: 0\nmodel name\t: Some CPU @ 2.0GHz\nflags\t: fpu\n")
+    assert bench.host_cpu(str(x86))["model"] == "Some CPU @ 2.0GHz"
+    arm = tmp_path / "arm"
+    arm.write_text("processor\t: 0\nBogoMIPS\t: 2000.00\nCPU implementer\t: 0x41\n"
+                   "CPU part\t: 0xd4f\n\nprocessor\t: 1\nCPU implementer\t: 0x41\n")
+    rec = bench.host_cpu(str(arm))
+    assert rec["model"] == "implementer 0x41 part 0xd4f" and rec["nproc"] >= 1
+    assert bench.host_cpu(str(tmp_path / "missing"))["model"]
