@@ -63,6 +63,7 @@ __device__ __forceinline__ void attn_i8_item(const AttnI8Params& P, int chunk, i
     const AttnParams& p = P.a;
     constexpr int NW = NT / 32;
     constexpr int DP = D + kI8TilePad;
+    static_assert(D % 32 == 0 && DP % 16 == 0, "16-byte code rows and tile pitch");
     int8_t* Ks = reinterpret_cast<int8_t*>(smem);
     int8_t* Vs = Ks + (size_t)chunk * DP;
     float* kss = reinterpret_cast<float*>(Vs + (size_t)chunk * DP);   // [chunk]
@@ -376,6 +377,7 @@ __global__ void __launch_bounds__(256) kv_write_i8_kernel(const bf16* __restrict
                                                           float* __restrict__ v_scale,
                                                           long num_slots, unsigned* err) {
     constexpr int E = D / 32;
+    static_assert(D % 32 == 0, "whole lanes per row");
     pdl_wait();
     pdl_trigger();
     const long row = (long)blockIdx.x * 8 + (threadIdx.x >> 5);   // token * Hkv + head
