@@ -990,6 +990,19 @@ def test_prefill_chunk_equals_sequential_decode():
 from oracle import sampling  # noqa: E402
 
 
+def test_philox_known_answer_vectors():
+    """The published known-answer vectors of Philox4x32-10
+    (tests/golden/philox4x32_10_kat.txt): a wrong multiplier, Weyl constant,
+    word permutation or round count changes every output word."""
+    rows = list(_golden_rows("philox4x32_10_kat.txt"))
+    assert len(rows) == 3
+    for ctr, key, want in rows:
+        c = [np.array([int(w, 16)], np.uint64) for w in ctr.split()]
+        k = [int(w, 16) for w in key.split()]
+        got = sampling.philox4x32_10(*c, *k)
+        assert [int(g[0]) for g in got] == [int(w, 16) for w in want.split()]
+
+
 def test_philox_is_a_deterministic_bijection_with_uniform_words():
     n = 1 << 16
     i = np.arange(n, dtype=np.uint64)
