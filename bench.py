@@ -659,28 +659,56 @@ def run_prefill(args, cfg):
         torch.distributed.destroy_process_group()
 
 
+LAYER_B1_VARIANTS = {
+    "layer_b1": ("a8w8", "A8W8 decode layer, batch 1, context 256 (us per layer)",
+                 "qwen3_14b_a8w8_layer_b1_ctx256",
+                 "int8 x int8 -> int32, f32 dequant, bf16 activations"),
+    "layer_b1_i8kv": ("i8kv", "A8W8 decode layer, INT8 KV cache, batch 1, context 256 (us per layer)",
+                      "qwen3_14b_a8w8_i8kv_layer_b1_ctx256",
+                      "int8 x int8 -> int32, f32 dequant, int8 KV codes x f32 row scales"),
+    "layer_b1_bf16": ("bf16", "BF16 decode layer, batch 1, context 256 (us per layer)",
+                      "qwen3_14b_bf16_layer_b1_ctx256",
+                      "bf16 x bf16 products, f32 sums, bf16 activations"),
+}
+
+
 def run_layer_b1(args, cfg):
     """One decode layer, batch 1, 255 cached tokens + the decoded one (context
     256, pages of 128), the layer's weights rotated over 4 copies so that L2
-    (129 MB) cannot serve a repeat (rank 0 only)."""
+    (129 MB) cannot serve a repeat (rank 0 only). Variants: the A8W8 layer
+    (BF16 KV cache), the A8W8 layer over the INT8 KV cache, the BF16 layer."""
     import torch
     import w8a8_quantized_decode_gb300 as a8w8
 
     rank, world, local = dist_env()
     if rank != 0:
         return
+    variant, metric, workload, dtype = LAYER_B1_VARIANTS[args.workload]
     device = torch.device(f"cuda:{local}")
     torch.cuda.set_device(device)
     a8w8.build()
     cfg = dict(cfg, num_layers=1)
     page, ctx = cfg["page_size"], 256
     Hkv, D, H = cfg["num_kv_heads"], cfg["head_dim"], cfg["hidden"]
-    copies = [synth.t_layer_weights(cfg, SEED + 50 + c, 0, device) for c in range(4)]
+    if variant == "bf16":
+        copies = [synth.t_bf16_layer_weights(cfg, SEED + 50 + c, 0, device) for c in range(4)]
+        # every matrix and norm weight in BF16, no scales
+        weight_bytes = sum(2 * int(np.prod(shape)) for kind, shape in synth.weight_shapes(cfg).values()
+                           if kind != "f32")
+    else:
+        copies = [synth.t_layer_weights(cfg, SEED + 50 + c, 0, device) for c in range(4)]
+        weight_bytes = synth.layer_weight_bytes(cfg)
     bt_np, nblk = synth.paged_layout(SEED + 51, [ctx], page, spare_blocks=1)
     gen = torch.Generator(device=device)
     gen.manual_seed(SEED + 52)
-    kc = torch.randn((nblk * page, Hkv, D), generator=gen, device=device).to(torch.bfloat16)
-    vc = torch.randn((nblk * page, Hkv, D), generator=gen, device=device).to(torch.bfloat16)
+    if variant == "i8kv":
+        kc, ks = synth.t_i8_kv_history(SEED + 53, nblk * page, Hkv, D, device)
+        vc, vs = synth.t_i8_kv_history(SEED + 55, nblk * page, Hkv, D, device)
+        kv_bytes = ctx * 2 * Hkv * (D + 4)
+    else:
+        kc = torch.randn((nblk * page, Hkv, D), generator=gen, device=device).to(torch.bfloat16)
+        vc = torch.randn((nblk * page, Hkv, D), generator=gen, device=device).to(torch.bfloat16)
+        kv_bytes = ctx * 2 * Hkv * D * 2
     hidden = torch.randn((1, H), generator=gen, device=device).to(torch.bfloat16)
     h0 = hidden.clone()
     bt = torch.from_numpy(bt_np).to(device)
@@ -689,19 +717,27 @@ def run_layer_b1(args, cfg):
     rope = a8w8.a8w8_rope_table(bt_np.shape[1] * page, D, cfg["rope_theta"], device=device)
     ws = a8w8.alloc_workspace(cfg, 1, bt_np.shape[1], device=device)
     stream = torch.cuda.Stream(device)
+
+    def layer(w):
+        if variant == "i8kv":
+            a8w8.a8w8_decode_layer_i8kv(w, cfg, hidden, sl, bt, cl, kc, vc, ks, vs, rope, ws,
+                                        stream=stream)
+        elif variant == "bf16":
+            a8w8.bf16_decode_layer(w, cfg, hidden, sl, bt, cl, kc, vc, rope, ws, stream=stream)
+        else:
+            a8w8.a8w8_decode_layer(w, cfg, hidden, sl, bt, cl, kc, vc, rope, ws, stream=stream)
+
     n = max(args.steps, 8)
     with torch.cuda.stream(stream):
         g = torch.cuda.CUDAGraph()
         # one graph replay = n layer calls over the 4 rotating copies
         for _ in range(2):
             for i in range(4):
-                a8w8.a8w8_decode_layer(copies[i], cfg, hidden, sl, bt, cl, kc, vc, rope, ws,
-                                       stream=stream)
+                layer(copies[i])
         stream.synchronize()
         with torch.cuda.graph(g, stream=stream):
             for i in range(n):
-                a8w8.a8w8_decode_layer(copies[i % 4], cfg, hidden, sl, bt, cl, kc, vc, rope, ws,
-                                       stream=stream)
+                layer(copies[i % 4])
         for _ in range(args.warmup):
             hidden.copy_(h0)
             g.replay()
@@ -723,16 +759,14 @@ def run_layer_b1(args, cfg):
             e1.synchronize()
         errs = a8w8.read_device_errors(stream)
     us = e0.elapsed_time(e1) * 1000.0 / (n * reps)
-    layer_bytes = synth.layer_weight_bytes(cfg) + ctx * 2 * Hkv * D * 2
+    layer_bytes = weight_bytes + kv_bytes
     peaks = measured_peaks()
-    line = {"metric": "A8W8 decode layer, batch 1, context 256 (us per layer)", "value": us,
+    line = {"metric": metric, "value": us,
             "unit": "us/layer", "n_gpus": 1, "steps": n * reps, "warmup": args.warmup,
-            "higher_is_better": False, "vs_baseline": None,
-            "dtype": "int8 x int8 -> int32, f32 dequant, bf16 activations",
-            "data": "synthetic (seeded random-init weights, 4 rotating copies; N(0,1) context K/V)",
-            "config": {"workload": "qwen3_14b_a8w8_layer_b1_ctx256", "batch": 1, "context": ctx,
-                       "weight_copies": 4,
-                       "l2": "weights rotated over 4 copies (1.32 GB), larger than L2"},
+            "higher_is_better": False, "vs_baseline": None, "dtype": dtype,
+            "data": "synthetic (seeded random-init weights, 4 rotating copies; random context K/V)",
+            "config": {"workload": workload, "batch": 1, "context": ctx, "weight_copies": 4,
+                       "l2": "weights rotated over 4 copies, larger than L2"},
             "layer_bytes": layer_bytes, "hbm_gbs": layer_bytes / (us * 1e-6) / 1e9,
             "frac_of_peak": layer_bytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
             "clocks": clocks.summary(), "device_errors": errs}
@@ -803,7 +837,7 @@ def build_parser() -> argparse.ArgumentParser:
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=["decode_b1", "batched16", "prefill", "sample",
-                                           "layer_b1"],
+                                           *LAYER_B1_VARIANTS],
                     default="decode_b1")
     ap.add_argument("--layers", type=int, default=40,
                     help="layers of the model (fewer only for profiling captures)")
@@ -814,7 +848,7 @@ def main():
     args = build_parser().parse_args()
     if args.steps is None:
         args.steps = {"batched16": 32, "prefill": 5, "sample": 20,
-                      "layer_b1": 40}.get(args.workload, 48)
+                      **{w: 40 for w in LAYER_B1_VARIANTS}}.get(args.workload, 48)
     if args.warmup < 3:
         raise SystemExit("warmup must be >= 3")
     cfg = dict(synth.QWEN3_14B, num_layers=args.layers)
@@ -826,7 +860,7 @@ def main():
         run_prefill(args, cfg)
     elif args.workload == "sample":
         run_sample(args, cfg)
-    elif args.workload == "layer_b1":
+    elif args.workload in LAYER_B1_VARIANTS:
         run_layer_b1(args, cfg)
     else:
         run_ours(args, cfg)

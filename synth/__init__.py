@@ -308,6 +308,29 @@ def t_layer_weights(cfg: dict, seed_base: int, layer: int, device) -> dict:
     return out
 
 
+def t_bf16_layer_weights(cfg: dict, seed_base: int, layer: int, device) -> dict:
+    """Device draw of one BF16 (unquantised) layer's weights (as
+    bf16_layer_weights: matrices N(0, 0.02^2), norm weights 1 + N(0, 0.02))."""
+    out = {}
+    for i, (name, (kind, shape)) in enumerate(weight_shapes(cfg).items()):
+        seed = seed_base + 1000 * (layer + 1) + 500 + i
+        if kind == "i8":
+            out[name] = t_bf16_normal(seed, shape, device, std=0.02)
+        elif kind == "bf16":
+            out[name] = t_bf16_normal(seed, shape, device, mean=1.0, std=0.02)
+    return out
+
+
+def t_i8_kv_history(seed: int, num_slots: int, Hkv: int, D: int, device):
+    """Device draw of INT8 KV cache contents (as i8_kv_history)."""
+    import torch
+    codes = torch.randint(-127, 128, (num_slots, Hkv, D), dtype=torch.int8, device=device,
+                          generator=_torch_gen(seed, device))
+    u = torch.rand((num_slots, Hkv), dtype=torch.float32, device=device,
+                   generator=_torch_gen(seed + 1, device))
+    return codes, u.mul_(2.8e-2).add_(2e-3)
+
+
 def t_model_weights(cfg: dict, seed_base: int, device) -> dict:
     H, V = cfg["hidden"], cfg["vocab"]
     return dict(
