@@ -408,6 +408,370 @@ __global__ void __launch_bounds__(256) kv_write_i8_kernel(const bf16* __restrict
     }
 }
 
+// ---------------------------------------------------------------------------
+// Grouped form (large batches, long contexts): one CTA per (request, KV head,
+// 128-token chunk) for every query head of the group, as attn_group.cu does for
+// the BF16 cache, over code tiles. Both row-scale arrays are read with the
+// block ids; the softmax stores p_t * v_scale_t (a pair product) for P.V while
+// the denominator l sums p_t alone, so P.V multiplies those pairs by the codes.
+// Decode only (the new token is quantised here, not by a prefill pre-pass).
+// ---------------------------------------------------------------------------
+constexpr int kG8Threads = 256;
+constexpr int kG8Chunk = 128;        // the BF16 grouped form's chunk ...
+constexpr int kG8MaxG = 7;           // ... heads per KV head ...
+constexpr int kG8MaxSplits = 64;     // ... and chunks per request (attn_group_shape_ok)
+
+__host__ __device__ inline size_t al16(size_t x) { return (x + 15) & ~size_t(15); }
+
+struct G8Smem {
+    size_t tile, vnew, ksc, vsc, q, pr, stat, blk, flag, total;
+};
+__host__ __device__ inline G8Smem g8_smem(int D, int G) {
+    G8Smem s;
+    s.tile = 0;
+    const size_t kv = (size_t)kG8Chunk * (D + kI8TilePad);
+    // combine scratch reuses the tile: per head 2*splits weights, 2 for L,
+    // splits active indices and their count
+    const size_t comb = (size_t)G * (2 * kG8MaxSplits + 2 + kG8MaxSplits + 1) * 4;
+    s.vnew = al16(kv > comb ? kv : comb);                // [D] int8: the new token's V codes
+    s.ksc = s.vnew + al16((size_t)D);                    // [chunk] K row scales
+    s.vsc = s.ksc + (size_t)kG8Chunk * 4;                // [chunk] V row scales
+    s.q = s.vsc + (size_t)kG8Chunk * 4;                  // [G][D] float
+    s.pr = s.q + (size_t)G * D * 4;                      // [G][chunk] (hi, lo) pairs
+    s.stat = s.pr + (size_t)G * kG8Chunk * 8;            // [G][4]: m hi, m lo, l hi, l lo
+    s.blk = s.stat + (size_t)G * 4 * 4;                  // [chunk] physical block per token
+    s.flag = s.blk + (size_t)kG8Chunk * 4;
+    s.total = s.flag + 16;
+    return s;
+}
+
+// acc += p * v with p a pair and v a float (Dot2 accumulation: the product's
+// high part by TwoSum, the rounding errors into acc.lo).
+__device__ __forceinline__ void dot2_acc8(f2& acc, const f2 p, float v) {
+    const float h = __fmul_rn(p.hi, v);
+    const float e = __fmaf_rn(p.hi, v, -h);
+    float s, err;
+    two_sum(acc.hi, h, s, err);
+    acc.hi = s;
+    acc.lo = __fadd_rn(acc.lo, __fadd_rn(err, __fmaf_rn(p.lo, v, e)));
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(kG8Threads) attn_i8_group_kernel(const AttnI8Params P, int splits) {
+    static_assert(G >= 1 && G <= kG8MaxG, "query heads per KV head");
+    static_assert(D % 32 == 0 && (D + kI8TilePad) % 16 == 0, "16-byte code rows and tile pitch");
+    const AttnParams& p = P.a;
+    extern __shared__ __align__(16) unsigned char smem[];
+    constexpr int NT = kG8Threads, C = kG8Chunk;
+    constexpr int DP = D + kI8TilePad;
+    constexpr int RV = D / 16;        // 16-byte code vectors per row
+    constexpr int E = D / 32;
+    const G8Smem L = g8_smem(D, G);
+    int8_t* Ts = reinterpret_cast<int8_t*>(smem + L.tile);   // K codes, then V codes
+    int8_t* vnew = reinterpret_cast<int8_t*>(smem + L.vnew);
+    float* ksc = reinterpret_cast<float*>(smem + L.ksc);
+    float* vsc = reinterpret_cast<float*>(smem + L.vsc);
+    float* qs = reinterpret_cast<float*>(smem + L.q);
+    float2* pr = reinterpret_cast<float2*>(smem + L.pr);
+    float* stat = reinterpret_cast<float*>(smem + L.stat);
+    int* blk = reinterpret_cast<int*>(smem + L.blk);
+    int* s_flag = reinterpret_cast<int*>(smem + L.flag);
+
+    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h0 = kvh * G;
+    const int t0 = split * C;
+    const int max_ctx = p.max_blocks * p.page;
+    const int ctx_raw = p.ctx_lens[b];
+    const bool bad_ctx = ctx_raw < 0 || ctx_raw > max_ctx;
+    const int pos = ctx_raw - 1;
+    const bool bad_pos = !bad_ctx && ctx_raw > 0 && pos >= p.max_pos;
+    const int ctx = (bad_ctx || bad_pos) ? 0 : ctx_raw;
+    const int n = max(min(t0 + C, ctx) - t0, 0);
+    const bool covers_new = ctx > 0 && pos >= t0 && pos < t0 + C;
+    const int n_old = covers_new ? n - 1 : n;
+    const int active = max(1, (ctx + C - 1) / C);
+    if (split >= active) return;   // the whole CTA, before any barrier
+    const bool single = active == 1;
+
+    // physical block and row scales of every cached token of the chunk
+    if (tid == 0) *s_flag = 0;
+    for (int t = tid; t < n_old; t += NT) {
+        const int tok = t0 + t;
+        const int bk = p.block_table[(size_t)b * p.max_blocks + tok / p.page];
+        const bool ok = bk >= 0 && bk < p.num_blocks;
+        blk[t] = ok ? bk : -1;
+        float ks = 0.0f, vs = 0.0f;
+        if (ok) {
+            const size_t row = ((size_t)bk * p.page + tok % p.page) * p.Hkv + kvh;
+            ks = __ldcg(P.k_scale + row);
+            vs = __ldcg(P.v_scale + row);
+        }
+        ksc[t] = ks;
+        vsc[t] = vs;
+    }
+    __syncthreads();
+    // code rows of the cached tokens of `cache` into the tile (zeros for a bad block)
+    auto load_tile = [&](const int8_t* cache) {
+        for (int i = tid; i < n_old * RV; i += NT) {
+            const int t = i / RV, c = i - t * RV;
+            const int bk = blk[t];
+            if (bk < 0) {
+                *reinterpret_cast<int4*>(Ts + (size_t)t * DP + 16 * c) = make_int4(0, 0, 0, 0);
+                *s_flag = 1;
+                continue;
+            }
+            const int tok = t0 + t;
+            const size_t off = (((size_t)bk * p.page + tok % p.page) * p.Hkv + kvh) * D + 16 * c;
+            cp_async16(Ts + (size_t)t * DP + 16 * c, cache + off);
+        }
+        cp_async_commit();
+    };
+    load_tile(P.k_codes);
+    // warps 0..G-1: query heads; warp G: the new token's K and V
+    const bool qwarp = warp < G;
+    const bool kwarp = warp == G && covers_new;
+    HeadPre<D> hp;
+    if (n > 0 && (qwarp || kwarp)) load_head_pre<D>(p, pos < p.max_pos ? pos : 0, lane, hp);
+
+    pdl_wait();
+    pdl_trigger();
+
+    if (tid == 0) {
+        if (bad_ctx) set_error(p.err, 0x4u);
+        if (bad_pos) set_error(p.err, 0x10u);
+    }
+    if (n > 0 && qwarp) {
+        const int h = h0 + warp;
+        float x[E], y[E];
+        load_bf16_lane<D>(p.q + (size_t)b * p.q_stride + (size_t)h * D + lane * E, x);
+        norm_rope_head<D>(x, hp.qw, hp, p.eps, lane, y);
+#pragma unroll
+        for (int e = 0; e < E; ++e) qs[warp * D + lane * E + e] = y[e];
+        if (p.tap_q_rot && split == 0) {
+#pragma unroll
+            for (int e = 0; e < E; ++e)
+                p.tap_q_rot[((size_t)b * p.Hq + h) * D + lane * E + e] = f2bf(y[e]);
+        }
+    } else if (n > 0 && kwarp) {
+        const int NQ = p.Hq * D, NK = p.Hkv * D;
+        const bf16* row = p.q + (size_t)b * p.q_stride;
+        float x[E], vv[E], y[E];
+        load_bf16_lane<D>(row + NQ + (size_t)kvh * D + lane * E, x);
+        load_bf16_lane<D>(row + NQ + NK + (size_t)kvh * D + lane * E, vv);
+        norm_rope_head<D>(x, hp.kw, hp, p.eps, lane, y);
+        int kc[E], vc[E];
+        const float ks = quant_row_warp<E>(y, kc);
+        const float vs = quant_row_warp<E>(vv, vc);
+        const int tr = pos - t0;
+        const long slot = p.slot_mapping[b];
+        const long num_slots = (long)p.num_blocks * p.page;
+        const bool slot_ok = slot >= 0 && slot < num_slots;
+        if (lane == 0) {
+            if (slot >= num_slots) set_error(p.err, 0x1u);
+            ksc[tr] = ks;
+            vsc[tr] = vs;
+            if (slot_ok) {
+                P.k_scale[(size_t)slot * p.Hkv + kvh] = ks;
+                P.v_scale[(size_t)slot * p.Hkv + kvh] = vs;
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const int d = lane * E + e;
+            Ts[(size_t)tr * DP + d] = (int8_t)kc[e];
+            vnew[d] = (int8_t)vc[e];
+            if (slot_ok) {
+                P.k_codes[((size_t)slot * p.Hkv + kvh) * D + d] = (int8_t)kc[e];
+                P.v_codes[((size_t)slot * p.Hkv + kvh) * D + d] = (int8_t)vc[e];
+            }
+            if (p.tap_k_rot) p.tap_k_rot[((size_t)b * p.Hkv + kvh) * D + d] = f2bf(y[e]);
+        }
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    if (tid == 0 && *s_flag) set_error(p.err, 0x2u);
+
+    // scores: warp w takes tokens 32 (w % 4) + lane and heads w / 4, +2, +4, +6
+    const f2 scale = {p.scale, p.scale_lo};
+    {
+        const int t = (warp & 3) * 32 + lane;
+        const int hb = warp >> 2;
+        constexpr int HW = (G + 1) / 2;    // heads per warp, at most
+        if (t < n) {
+            f2 acc[HW];
+#pragma unroll
+            for (int i = 0; i < HW; ++i) acc[i] = f2{0.0f, 0.0f};
+            const int8_t* krow = Ts + (size_t)t * DP;
+#pragma unroll 2
+            for (int dv = 0; dv < D / 8; ++dv) {
+                const uint2 raw = *reinterpret_cast<const uint2*>(krow + 8 * dv);
+                const char4 c0 = *reinterpret_cast<const char4*>(&raw.x);
+                const char4 c1 = *reinterpret_cast<const char4*>(&raw.y);
+                const float kf[8] = {(float)c0.x, (float)c0.y, (float)c0.z, (float)c0.w,
+                                     (float)c1.x, (float)c1.y, (float)c1.z, (float)c1.w};
+#pragma unroll
+                for (int i = 0; i < HW; ++i) {
+                    const int hh = hb + 2 * i;
+                    if (hh < G) {
+                        const float4 qa = *reinterpret_cast<const float4*>(qs + hh * D + 8 * dv);
+                        const float4 qb = *reinterpret_cast<const float4*>(qs + hh * D + 8 * dv + 4);
+                        f2_acc(acc[i], __fmul_rn(qa.x, kf[0]));
+                        f2_acc(acc[i], __fmul_rn(qa.y, kf[1]));
+                        f2_acc(acc[i], __fmul_rn(qa.z, kf[2]));
+                        f2_acc(acc[i], __fmul_rn(qa.w, kf[3]));
+                        f2_acc(acc[i], __fmul_rn(qb.x, kf[4]));
+                        f2_acc(acc[i], __fmul_rn(qb.y, kf[5]));
+                        f2_acc(acc[i], __fmul_rn(qb.z, kf[6]));
+                        f2_acc(acc[i], __fmul_rn(qb.w, kf[7]));
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < HW; ++i) {
+                const int hh = hb + 2 * i;
+                if (hh < G) {
+                    const f2 d = f2_mulf(fast_two_sum(acc[i].hi, acc[i].lo), ksc[t]);
+                    const f2 sv = f2_mul(d, scale);
+                    pr[hh * C + t] = make_float2(sv.hi, sv.lo);
+                }
+            }
+        }
+    }
+    __syncthreads();   // the K tile is no longer read
+
+    // the V codes into the same buffer, behind the softmax
+    load_tile(P.v_codes);
+    if (n > 0 && warp == G && covers_new) {
+        for (int d = lane; d < D; d += 32) Ts[(size_t)(pos - t0) * DP + d] = vnew[d];
+    }
+
+    // softmax of head w over the chunk: p = exp(s - m), l = sum p; the pairs
+    // kept for P.V are p * v_scale
+    if (warp < G) {
+        float2* ph = pr + warp * C;
+        f2 m = {-INFINITY, 0.0f};
+        for (int t = lane; t < n; t += 32) m = f2_max(m, f2{ph[t].x, ph[t].y});
+        m = warp_max_f2(m);
+        f2 l = {0.0f, 0.0f};
+        for (int t = lane; t < n; t += 32) {
+            const f2 e = f2_exp(f2_sub(f2{ph[t].x, ph[t].y}, m));
+            l = f2_add(l, e);
+            const f2 w = f2_mulf(e, vsc[t]);
+            ph[t] = make_float2(w.hi, w.lo);
+        }
+        l = warp_sum_f2(l);
+        if (lane == 0) {
+            stat[warp * 4 + 0] = m.hi;
+            stat[warp * 4 + 1] = m.lo;
+            stat[warp * 4 + 2] = l.hi;
+            stat[warp * 4 + 3] = l.lo;
+        }
+    }
+    cp_async_wait_all();
+    __syncthreads();
+
+    // P.V: TG consecutive threads share a column pair and split the tokens
+    {
+        constexpr int CP = D / 2;
+        constexpr int TG = NT / CP;
+        static_assert(TG >= 1 && TG <= 32 && (TG & (TG - 1)) == 0, "token groups");
+        const int cp = tid / TG, tg = tid % TG;
+        f2 o[G][2];
+#pragma unroll
+        for (int h = 0; h < G; ++h) o[h][0] = o[h][1] = f2{0.0f, 0.0f};
+        for (int t = tg; t < n; t += TG) {
+            const char2 v = *reinterpret_cast<const char2*>(Ts + (size_t)t * DP + 2 * cp);
+            const float v0 = (float)v.x, v1 = (float)v.y;
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float2 q = pr[h * C + t];
+                dot2_acc8(o[h][0], f2{q.x, q.y}, v0);
+                dot2_acc8(o[h][1], f2{q.x, q.y}, v1);
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            o[h][0] = fast_two_sum(o[h][0].hi, o[h][0].lo);
+            o[h][1] = fast_two_sum(o[h][1].hi, o[h][1].lo);
+#pragma unroll
+            for (int s = TG / 2; s > 0; s >>= 1) {
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    f2 r;
+                    r.hi = __shfl_xor_sync(0xffffffffu, o[h][c].hi, s);
+                    r.lo = __shfl_xor_sync(0xffffffffu, o[h][c].lo, s);
+                    o[h][c] = f2_add(o[h][c], r);
+                }
+            }
+        }
+        if (tg == 0) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const int hq = h0 + h;
+                const f2 l = {stat[h * 4 + 2], stat[h * 4 + 3]};
+                if (single) {
+                    bf16* out = p.out + ((size_t)b * p.Hq + hq) * D + 2 * cp;
+                    out[0] = n > 0 ? f2_to_bf16(f2_div(o[h][0], l)) : __float2bfloat16_rn(0.0f);
+                    out[1] = n > 0 ? f2_to_bf16(f2_div(o[h][1], l)) : __float2bfloat16_rn(0.0f);
+                } else {
+                    float* pp = p.part + (((size_t)b * p.Hq + hq) * splits + split) * (2 * D + 4);
+                    pp[2 * cp] = n > 0 ? o[h][0].hi : 0.0f;
+                    pp[2 * cp + 1] = n > 0 ? o[h][1].hi : 0.0f;
+                    pp[D + 2 * cp] = n > 0 ? o[h][0].lo : 0.0f;
+                    pp[D + 2 * cp + 1] = n > 0 ? o[h][1].lo : 0.0f;
+                    if (cp == 0) {
+                        pp[2 * D] = n > 0 ? stat[h * 4 + 0] : -INFINITY;
+                        pp[2 * D + 1] = n > 0 ? stat[h * 4 + 1] : 0.0f;
+                        pp[2 * D + 2] = n > 0 ? l.hi : 0.0f;
+                        pp[2 * D + 3] = n > 0 ? l.lo : 0.0f;
+                    }
+                }
+            }
+        }
+    }
+    if (single) return;   // no barrier follows on this path
+
+    // the last CTA of this (request, KV head) merges the chunks' partials
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        unsigned* tk = p.tickets + (size_t)b * p.Hq + kvh;
+        const unsigned prev = atomicAdd(tk, 1u);
+        *s_flag = prev == (unsigned)(active - 1);
+        if (*s_flag) *tk = 0u;   // ready for the next launch
+    }
+    __syncthreads();
+    if (!*s_flag) return;
+    __threadfence();
+    constexpr int CS = 2 * kG8MaxSplits + 2 + kG8MaxSplits + 1;   // floats per head
+    float* scratch = reinterpret_cast<float*>(smem + L.tile);
+    if (warp < G) {
+        float* cw = scratch + warp * CS;
+        int* act = reinterpret_cast<int*>(cw + 2 * kG8MaxSplits + 2);
+        const float* pb = p.part + ((size_t)b * p.Hq + h0 + warp) * splits * (2 * D + 4);
+        combine_weights<D>(pb, active, cw, cw + 2 * kG8MaxSplits, lane, act, act + kG8MaxSplits);
+    }
+    __syncthreads();
+    for (int i = tid; i < G * D; i += NT) {
+        const int h = i / D, d = i - h * D;
+        const float* cw = scratch + h * CS;
+        const float* cl = cw + 2 * kG8MaxSplits;
+        const int* act = reinterpret_cast<const int*>(cw + 2 * kG8MaxSplits + 2);
+        const int nact = act[kG8MaxSplits];
+        const float* pb = p.part + ((size_t)b * p.Hq + h0 + h) * splits * (2 * D + 4);
+        f2 acc = {0.0f, 0.0f};
+        for (int k = 0; k < nact; ++k) {
+            const int sp = act[k];
+            const float* q = pb + (size_t)sp * (2 * D + 4);
+            acc = f2_add(acc, f2_mul(f2{__ldcg(q + d), __ldcg(q + D + d)}, f2{cw[2 * sp], cw[2 * sp + 1]}));
+        }
+        const f2 l = {cl[0], cl[1]};
+        p.out[((size_t)b * p.Hq + h0 + h) * D + d] =
+            l.hi > 0.0f ? f2_to_bf16(f2_div(acc, l)) : __float2bfloat16_rn(0.0f);
+    }
+}
+
 template <typename Kern, typename... Args>
 cudaError_t launch_i8(Kern kern, dim3 grid, dim3 block, size_t smem, const Launch& L,
                       Args... args) {
@@ -454,12 +818,54 @@ cudaError_t launch_attn_i8_d(const AttnI8Params& P, const Launch& L) {
                      p.out);
 }
 
+template <int D, int G>
+cudaError_t launch_g8_t(const AttnI8Params& P, int splits, const Launch& L) {
+    const size_t smem = g8_smem(D, G).total;
+    static int configured_dev = -1;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (configured_dev != dev) {
+        cudaError_t e = cudaFuncSetAttribute(attn_i8_group_kernel<D, G>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        configured_dev = dev;
+    }
+    return launch_i8(attn_i8_group_kernel<D, G>, dim3(splits, P.a.Hkv, P.a.B), dim3(kG8Threads),
+                     smem, L, P, splits);
+}
+
+template <int D>
+cudaError_t launch_g8_d(const AttnI8Params& P, int splits, const Launch& L) {
+    switch (P.a.Hq / P.a.Hkv) {
+        case 1: return launch_g8_t<D, 1>(P, splits, L);
+        case 2: return launch_g8_t<D, 2>(P, splits, L);
+        case 3: return launch_g8_t<D, 3>(P, splits, L);
+        case 4: return launch_g8_t<D, 4>(P, splits, L);
+        case 5: return launch_g8_t<D, 5>(P, splits, L);
+        case 6: return launch_g8_t<D, 6>(P, splits, L);
+        case 7: return launch_g8_t<D, 7>(P, splits, L);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// Decode-layer attention over at least this many (request, cached token)
+// slots of the launch shape uses the grouped form (as for the BF16 cache).
+constexpr long kG8MinWork = 8192;
+
 }  // namespace
 
 cudaError_t launch_attention_i8(const AttnI8Params& P, const Launch& L) {
-    if (P.a.B == 0) return cudaSuccess;
-    if (P.a.D == 128) return launch_attn_i8_d<128>(P, L);
-    if (P.a.D == 64) return launch_attn_i8_d<64>(P, L);
+    const AttnParams& p = P.a;
+    if (p.B == 0) return cudaSuccess;
+    const int max_ctx = p.max_blocks * p.page;
+    if ((long)p.B * max_ctx >= kG8MinWork && p.fused && p.tickets && !p.kv_in_cache &&
+        attn_group_shape_ok(p.Hq, p.Hkv, p.D, max_ctx)) {
+        const int splits = (max_ctx + kG8Chunk - 1) / kG8Chunk;
+        if (splits > kG8MaxSplits) return cudaErrorInvalidValue;
+        return p.D == 128 ? launch_g8_d<128>(P, splits, L) : launch_g8_d<64>(P, splits, L);
+    }
+    if (p.D == 128) return launch_attn_i8_d<128>(P, L);
+    if (p.D == 64) return launch_attn_i8_d<64>(P, L);
     return cudaErrorInvalidValue;
 }
 
