@@ -291,6 +291,18 @@ a8w8_status a8w8_decode_layer_i8kv(const a8w8_layer_weights* w, const a8w8_confi
                                    void* ws, size_t ws_bytes, const a8w8_layer_taps* taps,
                                    void* stream);
 
+/* a8w8_prefill_layer over this layer's INT8 cache: every row's rotated K and
+ * its V are quantised per row into the cache at its slot first, then each
+ * row attends over its own ctx_lens[r] tokens (causal as a8w8_prefill_layer).
+ * Arguments, shape rules and workspace as a8w8_prefill_layer. */
+a8w8_status a8w8_prefill_layer_i8kv(const a8w8_layer_weights* w, const a8w8_config* cfg, int M,
+                                    a8w8_bf16* hidden, const int32_t* slot_mapping,
+                                    const int32_t* block_table, int max_blocks, int num_blocks,
+                                    const int32_t* ctx_lens, int8_t* k_codes, int8_t* v_codes,
+                                    float* k_scale, float* v_scale, const float* rope,
+                                    int max_pos, void* ws, size_t ws_bytes,
+                                    const a8w8_layer_taps* taps, void* stream);
+
 /* ------------------------------------------------------------------------- */
 /* BF16 (unquantised) layer variant                                          */
 /* ------------------------------------------------------------------------- */

@@ -392,7 +392,7 @@ def decode_layer(w: dict, cfg: dict, hidden, slot_mapping, block_table, ctx_lens
 
 
 def prefill_layer(w: dict, cfg: dict, hidden, slot_mapping, block_table, ctx_lens,
-                  k_cache, v_cache, taps: bool = False):
+                  k_cache, v_cache, taps: bool = False, k_scale=None, v_scale=None):
     """One layer over a prefill chunk: M token rows, row r the token at position
     ctx_lens[r] - 1 of the sequence whose block table row it carries.
 
@@ -403,7 +403,7 @@ def prefill_layer(w: dict, cfg: dict, hidden, slot_mapping, block_table, ctx_len
     (reading of "A8W8-compatible prefill chunk": the prompt decoded as a
     chunk), which tests/test_oracle_pins.py checks."""
     return decode_layer(w, cfg, hidden, slot_mapping, block_table, ctx_lens, k_cache, v_cache,
-                        taps)
+                        taps, k_scale=k_scale, v_scale=v_scale)
 
 
 def linear_bf16(x, W, residual=None) -> np.ndarray:

@@ -237,3 +237,20 @@ def test_bf16_layer_validation(lib):
     bad = a8w8.Bf16LayerWeights(*([FAKE] * len(a8w8.BF16_WEIGHT_FIELDS)))
     bad.w_down = None
     assert layer(q, w=bad) == a8w8.ERR_INVALID_ARG
+
+
+def test_int8_kv_prefill_validation(lib):
+    L = lib
+    q = synth.QWEN3_14B
+    w = a8w8.LayerWeights(*([FAKE] * len(a8w8.WEIGHT_FIELDS)))
+
+    def call(cfg, M=64, max_blocks=4, ks=FAKE, wsb=1 << 34):
+        return L.a8w8_prefill_layer_i8kv(ctypes.byref(w), _cfg(cfg), M, FAKE, FAKE, FAKE,
+                                         max_blocks, 8, FAKE, FAKE, FAKE, ks, FAKE, FAKE, 512,
+                                         FAKE, wsb, None, None)
+    assert call(q, M=0) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert call(dict(q, num_kv_heads=5)) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert call(q, max_blocks=65) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert call(q, ks=None) == a8w8.ERR_INVALID_ARG
+    need = L.a8w8_workspace_bytes(_cfg(q), 2048, 4)
+    assert call(q, M=2048, wsb=need - 1) == a8w8.ERR_WORKSPACE

@@ -983,6 +983,40 @@ def test_prefill_chunk_equals_sequential_decode():
     assert not np.array_equal(h_alone[0], out[4])
 
 
+def test_prefill_chunk_over_int8_cache_equals_sequential_decode():
+    # the same causal reading over the INT8 KV cache: every row's K/V is
+    # quantised into its slot before any row attends
+    cfg = synth.TINY
+    case = synth.prefill_case(cfg, seq_lens=[4, 6], prior_ctx=[5, 0], seed_base=33)
+    w = case["weights"]
+    n, Hkv, D = case["k_cache"].shape
+    kc0, ks0 = synth.i8_kv_history(34, n, Hkv, D)
+    vc0, vs0 = synth.i8_kv_history(35, n, Hkv, D)
+    c1 = [a.copy() for a in (kc0, vc0, ks0, vs0)]
+    out, _, rc = oracle.prefill_layer(w, cfg, case["hidden"], case["slot_mapping"],
+                                      case["block_table"], case["ctx_lens"], c1[0], c1[1],
+                                      k_scale=c1[2], v_scale=c1[3])
+    assert rc == 0
+    c2 = [a.copy() for a in (kc0, vc0, ks0, vs0)]
+    seq_of = np.repeat(np.arange(2), case["seq_lens"])
+    idx = np.arange(len(seq_of)) - np.concatenate([[0], np.cumsum(case["seq_lens"])[:-1]])[seq_of]
+    seq_out = np.empty_like(case["hidden"])
+    for i in range(int(case["seq_lens"].max())):
+        rows = np.nonzero(idx == i)[0]
+        h, _, rc = oracle.decode_layer(w, cfg, case["hidden"][rows], case["slot_mapping"][rows],
+                                       case["block_table"][rows], case["ctx_lens"][rows], c2[0],
+                                       c2[1], k_scale=c2[2], v_scale=c2[3])
+        assert rc == 0
+        seq_out[rows] = h
+    assert np.array_equal(out, seq_out)
+    assert all(np.array_equal(a, b) for a, b in zip(c1, c2))
+    # the chunk's slots hold codes and scales now, and only those changed
+    sl = case["slot_mapping"]
+    rest = np.setdiff1d(np.arange(n), sl)
+    assert np.array_equal(c1[0][rest], kc0[rest]) and np.array_equal(c1[2][rest], ks0[rest])
+    assert not np.array_equal(c1[2][sl], ks0[sl])
+
+
 # ---------------------------------------------------------------------------
 # Sampling beyond greedy (oracle/sampling.py)
 # ---------------------------------------------------------------------------

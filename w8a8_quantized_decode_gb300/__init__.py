@@ -91,6 +91,8 @@ _SIGNATURES = {
                                          _f, _p, _p, _sz, _p]),
     "a8w8_decode_layer_i8kv": (_i, [_p, _p, _i, _p, _p, _p, _i, _i, _p, _p, _p, _p, _p, _p, _i,
                                     _p, _sz, _p, _p]),
+    "a8w8_prefill_layer_i8kv": (_i, [_p, _p, _i, _p, _p, _p, _i, _i, _p, _p, _p, _p, _p, _p, _i,
+                                     _p, _sz, _p, _p]),
     "bf16_linear": (_i, [_p, _i, _i, _p, _i, _p, _p, _p]),
     "bf16_gate_up_swiglu": (_i, [_p, _i, _i, _p, _i, _p, _p]),
     "bf16_decode_layer": (_i, [_p, _p, _i, _p, _p, _p, _i, _i, _p, _p, _p, _p, _i, _p, _sz, _p,
@@ -403,6 +405,28 @@ def a8w8_decode_layer_i8kv(weights: dict, cfg: dict, hidden, slot_mapping, block
             setattr(t, n, _ptr(taps.get(n)))
     _check(lib().a8w8_decode_layer_i8kv(
         ctypes.byref(w), ctypes.byref(c), B, _ptr(hidden), _ptr(slot_mapping), _ptr(block_table),
+        block_table.shape[1], num_blocks, _ptr(ctx_lens), _ptr(k_codes), _ptr(v_codes),
+        _ptr(k_scale), _ptr(v_scale), _ptr(rope), rope.shape[0], _ptr(ws), ws.numel(),
+        None if t is None else ctypes.byref(t), _stream(stream)))
+
+
+def a8w8_prefill_layer_i8kv(weights: dict, cfg: dict, hidden, slot_mapping, block_table, ctx_lens,
+                            k_codes, v_codes, k_scale, v_scale, rope, ws,
+                            taps: dict | None = None, stream=None):
+    """One layer over a prefill chunk of M rows with the INT8 KV cache (rows as
+    a8w8_prefill_layer); `hidden` [M, H] bf16 is updated in place."""
+    M = hidden.shape[0]
+    Hkv, D, page = cfg["num_kv_heads"], cfg["head_dim"], cfg["page_size"]
+    num_blocks = k_codes.numel() // (Hkv * D * page)
+    c = make_config(cfg)
+    w = layer_struct(weights)
+    t = None
+    if taps is not None:
+        t = LayerTaps()
+        for n in TAP_FIELDS:
+            setattr(t, n, _ptr(taps.get(n)))
+    _check(lib().a8w8_prefill_layer_i8kv(
+        ctypes.byref(w), ctypes.byref(c), M, _ptr(hidden), _ptr(slot_mapping), _ptr(block_table),
         block_table.shape[1], num_blocks, _ptr(ctx_lens), _ptr(k_codes), _ptr(v_codes),
         _ptr(k_scale), _ptr(v_scale), _ptr(rope), rope.shape[0], _ptr(ws), ws.numel(),
         None if t is None else ctypes.byref(t), _stream(stream)))

@@ -318,21 +318,27 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     a.err = device_error_word();
     a.tap_q_rot = reinterpret_cast<bf16*>(T.q_rot);
     a.tap_k_rot = reinterpret_cast<bf16*>(T.k_rot);
-    if (prefill) {
-        // every token's K/V into the cache first: the chunk's rows attend to
-        // each other's earlier tokens (causal by their context lengths)
-        e = launch_kv_prep(a, L);
-        if (e != cudaSuccess) return cuda_fail(e, "prefill KV write");
-        a.kv_in_cache = true;
-        e = launch_attn_group(a, L);
-    } else if (kv8) {
+    if (kv8) {
         AttnI8Params ai = {};
         ai.a = a;
         ai.k_codes = kv8->k_codes;
         ai.v_codes = kv8->v_codes;
         ai.k_scale = kv8->k_scale;
         ai.v_scale = kv8->v_scale;
+        if (prefill) {
+            // every token's K/V quantised into the cache first (as below)
+            e = launch_kv_prep_i8(ai, L);
+            if (e != cudaSuccess) return cuda_fail(e, "prefill KV write");
+            ai.a.kv_in_cache = true;
+        }
         e = launch_attention_i8(ai, L);
+    } else if (prefill) {
+        // every token's K/V into the cache first: the chunk's rows attend to
+        // each other's earlier tokens (causal by their context lengths)
+        e = launch_kv_prep(a, L);
+        if (e != cudaSuccess) return cuda_fail(e, "prefill KV write");
+        a.kv_in_cache = true;
+        e = launch_attn_group(a, L);
     } else {
         e = launch_attention(a, L);
     }
@@ -1028,6 +1034,36 @@ a8w8_status a8w8_prefill_layer(const a8w8_layer_weights* w, const a8w8_config* c
                          max_blocks, num_blocks, ctx_lens, reinterpret_cast<bf16*>(k_cache),
                          reinterpret_cast<bf16*>(v_cache), rope, max_pos,
                          static_cast<unsigned char*>(ws), lay, taps, L, true);
+}
+
+a8w8_status a8w8_prefill_layer_i8kv(const a8w8_layer_weights* w, const a8w8_config* cfg, int M,
+                                    a8w8_bf16* hidden, const int32_t* slot_mapping,
+                                    const int32_t* block_table, int max_blocks, int num_blocks,
+                                    const int32_t* ctx_lens, int8_t* k_codes, int8_t* v_codes,
+                                    float* k_scale, float* v_scale, const float* rope,
+                                    int max_pos, void* ws, size_t ws_bytes,
+                                    const a8w8_layer_taps* taps, void* stream) {
+    if (M < 1 || M > 16384) return fail(A8W8_ERR_UNSUPPORTED_SHAPE, "M=%d outside [1, 16384]", M);
+    a8w8_status s = check_layer_common(cfg, 1, max_blocks, num_blocks, rope, max_pos);
+    if (s != A8W8_OK) return s;
+    if ((s = check_layer_weights(w)) != A8W8_OK) return s;
+    if ((s = check_ptrs({hidden, slot_mapping, block_table, ctx_lens, k_codes, v_codes, k_scale,
+                         v_scale, rope},
+                        "a8w8_prefill_layer_i8kv")) != A8W8_OK)
+        return s;
+    if (!attn_group_shape_ok(cfg->num_q_heads, cfg->num_kv_heads, cfg->head_dim,
+                             max_blocks * cfg->page_size))
+        return fail(A8W8_ERR_UNSUPPORTED_SHAPE,
+                    "prefill attention needs Hq/Hkv <= 7 and at most 64 chunks of 128 tokens");
+    const WsLayout lay = ws_layout(*cfg, M, max_blocks);
+    if (!ws || ws_bytes < lay.total || !aligned16(ws))
+        return fail(A8W8_ERR_WORKSPACE, "prefill layer workspace needs %zu bytes", lay.total);
+    Launch L = make_launch(stream, true);
+    if (L.num_sms <= 0) return fail(A8W8_ERR_CUDA, "no CUDA device");
+    const KvI8 kv8 = {k_codes, v_codes, k_scale, v_scale};
+    return enqueue_layer(w, *cfg, M, reinterpret_cast<bf16*>(hidden), slot_mapping, block_table,
+                         max_blocks, num_blocks, ctx_lens, nullptr, nullptr, rope, max_pos,
+                         static_cast<unsigned char*>(ws), lay, taps, L, true, &kv8);
 }
 
 static a8w8_status check_step(const a8w8_model* m, const a8w8_config* cfg, int B, int max_blocks,

@@ -495,6 +495,9 @@ __global__ void __launch_bounds__(kG8Threads) attn_i8_group_kernel(const AttnI8P
     const bool single = active == 1;
 
     // physical block and row scales of every cached token of the chunk
+    // (prefill: the scales and codes of this launch's tokens are written by the
+    // pre-pass before, so they are read only after the dependency wait)
+    if (p.kv_in_cache) pdl_wait();
     if (tid == 0) *s_flag = 0;
     for (int t = tid; t < n_old; t += NT) {
         const int tok = t0 + t;
@@ -566,9 +569,11 @@ __global__ void __launch_bounds__(kG8Threads) attn_i8_group_kernel(const AttnI8P
         const int tr = pos - t0;
         const long slot = p.slot_mapping[b];
         const long num_slots = (long)p.num_blocks * p.page;
-        const bool slot_ok = slot >= 0 && slot < num_slots;
+        // prefill: the pre-pass has written the cache (and flagged a bad slot)
+        const bool write = !p.kv_in_cache;
+        const bool slot_ok = write && slot >= 0 && slot < num_slots;
         if (lane == 0) {
-            if (slot >= num_slots) set_error(p.err, 0x1u);
+            if (write && slot >= num_slots) set_error(p.err, 0x1u);
             ksc[tr] = ks;
             vsc[tr] = vs;
             if (slot_ok) {
@@ -585,7 +590,7 @@ __global__ void __launch_bounds__(kG8Threads) attn_i8_group_kernel(const AttnI8P
                 P.k_codes[((size_t)slot * p.Hkv + kvh) * D + d] = (int8_t)kc[e];
                 P.v_codes[((size_t)slot * p.Hkv + kvh) * D + d] = (int8_t)vc[e];
             }
-            if (p.tap_k_rot) p.tap_k_rot[((size_t)b * p.Hkv + kvh) * D + d] = f2bf(y[e]);
+            if (p.tap_k_rot && write) p.tap_k_rot[((size_t)b * p.Hkv + kvh) * D + d] = f2bf(y[e]);
         }
     }
     cp_async_wait_all();
@@ -772,6 +777,56 @@ __global__ void __launch_bounds__(kG8Threads) attn_i8_group_kernel(const AttnI8P
     }
 }
 
+// Prefill pre-pass over the INT8 cache: one CTA per row, warp w handles KV
+// heads w, w + 8, ...: the row's new K (per-head RMSNorm and RoPE, the
+// attention's own code) and V quantised per head row into the row's slot.
+constexpr int kPrepI8Threads = 256;
+template <int D>
+__global__ void __launch_bounds__(kPrepI8Threads) kv_prep_i8_kernel(const AttnI8Params P) {
+    const AttnParams& p = P.a;
+    constexpr int E = D / 32;
+    const int b = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int max_ctx = p.max_blocks * p.page;
+    const int ctx_raw = p.ctx_lens[b];
+    const bool bad_ctx = ctx_raw < 0 || ctx_raw > max_ctx;
+    const int pos = ctx_raw - 1;
+    const bool bad_pos = !bad_ctx && ctx_raw > 0 && pos >= p.max_pos;
+    const bool live = !bad_ctx && !bad_pos && ctx_raw > 0;
+    HeadPre<D> hp;
+    if (live) load_head_pre<D>(p, pos, lane, hp);
+    pdl_wait();
+    pdl_trigger();
+    if (!live) return;   // the attention kernel flags bad contexts and positions
+    const long slot = p.slot_mapping[b];
+    const long num_slots = (long)p.num_blocks * p.page;
+    if (threadIdx.x == 0 && slot >= num_slots) set_error(p.err, 0x1u);
+    const bool slot_ok = slot >= 0 && slot < num_slots;
+    const int NQ = p.Hq * D, NK = p.Hkv * D;
+    const bf16* row = p.q + (size_t)b * p.q_stride;
+    for (int kvh = warp; kvh < p.Hkv; kvh += kPrepI8Threads / 32) {
+        float x[E], vv[E], y[E];
+        load_bf16_lane<D>(row + NQ + (size_t)kvh * D + lane * E, x);
+        load_bf16_lane<D>(row + NQ + NK + (size_t)kvh * D + lane * E, vv);
+        norm_rope_head<D>(x, hp.kw, hp, p.eps, lane, y);
+        int kc[E], vc[E];
+        const float ks = quant_row_warp<E>(y, kc);
+        const float vs = quant_row_warp<E>(vv, vc);
+        if (slot_ok && lane == 0) {
+            P.k_scale[(size_t)slot * p.Hkv + kvh] = ks;
+            P.v_scale[(size_t)slot * p.Hkv + kvh] = vs;
+        }
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const int d = lane * E + e;
+            if (slot_ok) {
+                P.k_codes[((size_t)slot * p.Hkv + kvh) * D + d] = (int8_t)kc[e];
+                P.v_codes[((size_t)slot * p.Hkv + kvh) * D + d] = (int8_t)vc[e];
+            }
+            if (p.tap_k_rot) p.tap_k_rot[((size_t)b * p.Hkv + kvh) * D + d] = f2bf(y[e]);
+        }
+    }
+}
+
 template <typename Kern, typename... Args>
 cudaError_t launch_i8(Kern kern, dim3 grid, dim3 block, size_t smem, const Launch& L,
                       Args... args) {
@@ -858,8 +913,9 @@ cudaError_t launch_attention_i8(const AttnI8Params& P, const Launch& L) {
     const AttnParams& p = P.a;
     if (p.B == 0) return cudaSuccess;
     const int max_ctx = p.max_blocks * p.page;
-    if ((long)p.B * max_ctx >= kG8MinWork && p.fused && p.tickets && !p.kv_in_cache &&
-        attn_group_shape_ok(p.Hq, p.Hkv, p.D, max_ctx)) {
+    const bool grouped_ok = p.fused && p.tickets && attn_group_shape_ok(p.Hq, p.Hkv, p.D, max_ctx);
+    if (p.kv_in_cache && !grouped_ok) return cudaErrorInvalidValue;   // prefill: grouped form only
+    if (grouped_ok && (p.kv_in_cache || (long)p.B * max_ctx >= kG8MinWork)) {
         const int splits = (max_ctx + kG8Chunk - 1) / kG8Chunk;
         if (splits > kG8MaxSplits) return cudaErrorInvalidValue;
         return p.D == 128 ? launch_g8_d<128>(P, splits, L) : launch_g8_d<64>(P, splits, L);
@@ -867,6 +923,14 @@ cudaError_t launch_attention_i8(const AttnI8Params& P, const Launch& L) {
     if (p.D == 128) return launch_attn_i8_d<128>(P, L);
     if (p.D == 64) return launch_attn_i8_d<64>(P, L);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_kv_prep_i8(const AttnI8Params& P, const Launch& L) {
+    if (P.a.B == 0) return cudaSuccess;
+    if (!P.a.fused || (P.a.D != 128 && P.a.D != 64)) return cudaErrorInvalidValue;
+    if (P.a.D == 128)
+        return launch_i8(kv_prep_i8_kernel<128>, dim3(P.a.B), dim3(kPrepI8Threads), 0, L, P);
+    return launch_i8(kv_prep_i8_kernel<64>, dim3(P.a.B), dim3(kPrepI8Threads), 0, L, P);
 }
 
 cudaError_t launch_kv_write_i8(const bf16* k, const bf16* v, int T, int Hkv, int D,

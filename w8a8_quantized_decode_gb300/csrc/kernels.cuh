@@ -135,7 +135,7 @@ bool in_kernel_combine(int max_ctx, bool tickets);
 
 // INT8 KV cache variant (attn_i8.cu): codes [num_blocks*page, Hkv, D] int8 and
 // row scales [num_blocks*page, Hkv] float; `a` as for the BF16 form with its
-// k_cache / v_cache unused. Per-head form only.
+// k_cache / v_cache unused. Per-head and grouped forms.
 struct AttnI8Params {
     AttnParams a;
     int8_t* k_codes;
@@ -144,6 +144,9 @@ struct AttnI8Params {
     float* v_scale;
 };
 cudaError_t launch_attention_i8(const AttnI8Params& p, const Launch& L);
+// Prefill pre-pass over the INT8 cache: every row's rotated K and its V
+// quantised into its slot (then launch_attention_i8 with a.kv_in_cache).
+cudaError_t launch_kv_prep_i8(const AttnI8Params& p, const Launch& L);
 cudaError_t launch_kv_write_i8(const bf16* k, const bf16* v, int T, int Hkv, int D,
                                const int32_t* slot_mapping, int8_t* k_codes, int8_t* v_codes,
                                float* k_scale, float* v_scale, long num_slots, unsigned* err,
