@@ -542,6 +542,110 @@ def run_batched(args, cfg):
         torch.distributed.destroy_process_group()
 
 
+def run_batched_i8kv(args, cfg):
+    """The batch-16 step over INT8 KV caches against the same step over BF16
+    caches, both at the seeded contexts (64..4096) held fixed: each replay
+    decodes the same positions, so both read the same number of cached rows
+    (rank 0 only)."""
+    import torch
+    import w8a8_quantized_decode_gb300 as a8w8
+
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    a8w8.build()
+    B, page = BATCHED_B, cfg["page_size"]
+    Hkv, D, L = cfg["num_kv_heads"], cfg["head_dim"], cfg["num_layers"]
+    ctx0 = synth.batched_ctx_lens(SEED + 20, B)
+    bt_np, nblk = synth.paged_layout(SEED + 21, ctx0, page)
+    max_blocks = bt_np.shape[1]
+    model = build_model(cfg, device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(SEED + 22)
+    kc, vc, k8, v8, ks, vs = [], [], [], [], [], []
+    for l in range(L):
+        kc.append(torch.randn((nblk * page, Hkv, D), generator=gen, device=device).to(torch.bfloat16))
+        vc.append(torch.randn((nblk * page, Hkv, D), generator=gen, device=device).to(torch.bfloat16))
+        c, sc = synth.t_i8_kv_history(SEED + 100 + 4 * l, nblk * page, Hkv, D, device)
+        k8.append(c)
+        ks.append(sc)
+        c, sc = synth.t_i8_kv_history(SEED + 102 + 4 * l, nblk * page, Hkv, D, device)
+        v8.append(c)
+        vs.append(sc)
+    rope = a8w8.a8w8_rope_table(max_blocks * page, D, cfg["rope_theta"], device=device)
+    ws = a8w8.alloc_workspace(cfg, B, max_blocks, device=device)
+    tok = torch.from_numpy(synth.prompt_ids(SEED + 23, B, cfg["vocab"])).to(device)
+    sl = torch.from_numpy(synth.slots_for(bt_np, ctx0 - 1, page)).to(device)
+    bt = torch.from_numpy(bt_np).to(device)
+    cl = torch.from_numpy(ctx0.astype(np.int32)).to(device)
+    nxt = torch.empty(B, dtype=torch.int32, device=device)
+    stream = torch.cuda.Stream(device)
+    n = max(args.steps, 4)
+
+    def step(int8):
+        if int8:
+            a8w8.a8w8_decode_step_i8kv(model, cfg, tok, sl, bt, cl, k8, v8, ks, vs, rope, ws, nxt,
+                                       stream=stream)
+        else:
+            a8w8.a8w8_decode_step(model, cfg, tok, sl, bt, cl, kc, vc, rope, ws, nxt, stream=stream)
+
+    gpu_uuid = None
+    try:
+        gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        pass
+    ms = {}
+    clock_runs = {}
+    with torch.cuda.stream(stream):
+        for int8 in (False, True):
+            step(int8)
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(n):
+                    step(int8)
+            for _ in range(args.warmup):
+                g.replay()
+            stream.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with ClockSampler(gpu_uuid) as clocks:
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+                e1.synchronize()
+            ms[int8] = e0.elapsed_time(e1) / n
+            clock_runs["int8_kv" if int8 else "bf16_kv"] = clocks.summary()
+            del g
+        errs = a8w8.read_device_errors(stream)
+    ctx_sum = int(ctx0.sum())
+    sb = step_bytes(cfg, [ctx_sum])
+    kv8 = ctx_sum * 2 * Hkv * (D + 4) * L    # codes and one f32 scale per row
+    bytes8 = sb["layers"] + sb["lm_head"] + kv8
+    bytes16 = sb["total"]
+    peaks = measured_peaks()
+    line = {"metric": "A8W8 batched decode step over an INT8 KV cache (ms/step, 40 layers, bs=16, "
+                      "fixed contexts 64..4096)",
+            "value": ms[True], "unit": "ms/step", "n_gpus": 1, "steps": n, "warmup": args.warmup,
+            "ms_per_step": ms[True], "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "int8 x int8 -> int32, f32 dequant, int8 KV codes x f32 row scales",
+            "data": "synthetic (seeded random-init weights; random KV codes and row scales)",
+            "config": {"workload": "qwen3_14b_a8w8_batched_decode_b16_int8_kv", "batch": B,
+                       "layers": L, "ctx_sum": ctx_sum, "page_size": page,
+                       "l2": "inputs larger than L2 (13.2 GB of weights + KV per step)"},
+            "tokens_per_s": job_rate(B, ms[True], 1),
+            "step_bytes": bytes8, "step_hbm_gbs": bytes8 / (ms[True] * 1e-3) / 1e9,
+            "step_frac_of_peak": bytes8 / (ms[True] * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "bf16_kv": {"ms_per_step": ms[False], "step_bytes": bytes16,
+                        "step_hbm_gbs": bytes16 / (ms[False] * 1e-3) / 1e9},
+            "kv_bytes": {"int8": kv8, "bf16": sb["kv"]},
+            "e2e": None, "clocks": clock_runs, "device_errors": errs}
+    print(json.dumps(line), flush=True)
+
+
 PREFILL_SEQS, PREFILL_LEN = 4, 512
 PREFILL_WORKLOAD = "qwen3_14b_a8w8_prefill_chunk_4x512"
 PREFILL_METRIC = "A8W8 prefill chunk through one layer (ms, 4 x 512 tokens)"
@@ -836,8 +940,8 @@ def build_parser() -> argparse.ArgumentParser:
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["decode_b1", "batched16", "prefill", "sample",
-                                           *LAYER_B1_VARIANTS],
+    ap.add_argument("--workload", choices=["decode_b1", "batched16", "batched16_i8kv", "prefill",
+                                           "sample", *LAYER_B1_VARIANTS],
                     default="decode_b1")
     ap.add_argument("--layers", type=int, default=40,
                     help="layers of the model (fewer only for profiling captures)")
@@ -847,7 +951,7 @@ def build_parser() -> argparse.ArgumentParser:
 def main():
     args = build_parser().parse_args()
     if args.steps is None:
-        args.steps = {"batched16": 32, "prefill": 5, "sample": 20,
+        args.steps = {"batched16": 32, "batched16_i8kv": 16, "prefill": 5, "sample": 20,
                       **{w: 40 for w in LAYER_B1_VARIANTS}}.get(args.workload, 48)
     if args.warmup < 3:
         raise SystemExit("warmup must be >= 3")
@@ -856,6 +960,8 @@ def main():
         run_reference(args, cfg)
     elif args.workload == "batched16":
         run_batched(args, cfg)
+    elif args.workload == "batched16_i8kv":
+        run_batched_i8kv(args, cfg)
     elif args.workload == "prefill":
         run_prefill(args, cfg)
     elif args.workload == "sample":

@@ -446,6 +446,20 @@ a8w8_status a8w8_decode_step(const a8w8_model* m, const a8w8_config* cfg, int B,
                              int32_t* next_tokens, float* logits, a8w8_bf16* final_hidden,
                              void* ws, size_t ws_bytes, void* stream);
 
+/* a8w8_decode_step over INT8 caches: k_codes / v_codes / k_scales / v_scales
+ * are HOST arrays of num_layers device pointers, each layer's cache laid out
+ * as for a8w8_decode_layer_i8kv; every other argument as a8w8_decode_step
+ * (A8W8_FLAG_PERSISTENT_STEP is ignored). Status: built; not yet run on a
+ * GPU. */
+a8w8_status a8w8_decode_step_i8kv(const a8w8_model* m, const a8w8_config* cfg, int B,
+                                  const int32_t* token_ids, const int32_t* slot_mapping,
+                                  const int32_t* block_table, int max_blocks, int num_blocks,
+                                  const int32_t* ctx_lens, int8_t* const* k_codes,
+                                  int8_t* const* v_codes, float* const* k_scales,
+                                  float* const* v_scales, const float* rope, int max_pos,
+                                  int32_t* next_tokens, float* logits, a8w8_bf16* final_hidden,
+                                  void* ws, size_t ws_bytes, void* stream);
+
 /* ------------------------------------------------------------------------- */
 /* Replayable decode step                                                    */
 /* ------------------------------------------------------------------------- */

@@ -254,3 +254,22 @@ def test_int8_kv_prefill_validation(lib):
     assert call(q, ks=None) == a8w8.ERR_INVALID_ARG
     need = L.a8w8_workspace_bytes(_cfg(q), 2048, 4)
     assert call(q, M=2048, wsb=need - 1) == a8w8.ERR_WORKSPACE
+
+
+def test_int8_kv_step_validation(lib):
+    L = lib
+    q = dict(synth.QWEN3_14B, num_layers=1)
+    w = a8w8.LayerWeights(*([FAKE] * len(a8w8.WEIGHT_FIELDS)))
+    layers = (a8w8.LayerWeights * 1)(w)
+    m = a8w8.Model(FAKE, ctypes.cast(layers, ctypes.c_void_p), FAKE, FAKE)
+    arr = (ctypes.c_void_p * 1)(FAKE)
+    nul = (ctypes.c_void_p * 1)(None)
+
+    def call(ks=arr, kc=arr, wsb=1 << 30):
+        return L.a8w8_decode_step_i8kv(ctypes.byref(m), _cfg(q), 1, FAKE, FAKE, FAKE, 2, 4, FAKE,
+                                       kc, arr, ks, arr, FAKE, 256, FAKE, None, None, FAKE, wsb,
+                                       None)
+    assert call(kc=nul) == a8w8.ERR_INVALID_ARG
+    assert call(ks=nul) == a8w8.ERR_INVALID_ARG
+    assert call(ks=None) == a8w8.ERR_INVALID_ARG
+    assert call(wsb=100) == a8w8.ERR_WORKSPACE

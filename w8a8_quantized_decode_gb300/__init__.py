@@ -93,6 +93,8 @@ _SIGNATURES = {
                                     _p, _sz, _p, _p]),
     "a8w8_prefill_layer_i8kv": (_i, [_p, _p, _i, _p, _p, _p, _i, _i, _p, _p, _p, _p, _p, _p, _i,
                                      _p, _sz, _p, _p]),
+    "a8w8_decode_step_i8kv": (_i, [_p, _p, _i, _p, _p, _p, _i, _i, _p, _p, _p, _p, _p, _p, _i, _p,
+                                   _p, _p, _p, _sz, _p]),
     "bf16_linear": (_i, [_p, _i, _i, _p, _i, _p, _p, _p]),
     "bf16_gate_up_swiglu": (_i, [_p, _i, _i, _p, _i, _p, _p]),
     "bf16_decode_layer": (_i, [_p, _p, _i, _p, _p, _p, _i, _i, _p, _p, _p, _p, _i, _p, _sz, _p,
@@ -526,6 +528,23 @@ def a8w8_decode_step(model: dict, cfg: dict, token_ids, slot_mapping, block_tabl
         _cache_array(k_caches), _cache_array(v_caches), _ptr(rope), rope.shape[0],
         _ptr(next_tokens), _ptr(logits), _ptr(final_hidden), _ptr(ws), ws.numel(),
         _stream(stream)))
+
+
+def a8w8_decode_step_i8kv(model: dict, cfg: dict, token_ids, slot_mapping, block_table, ctx_lens,
+                          k_codes, v_codes, k_scales, v_scales, rope, ws, next_tokens, logits=None,
+                          final_hidden=None, stream=None):
+    """One decode step over per-layer INT8 caches (lists of num_layers device
+    tensors: codes [slots, Hkv, D] int8, row scales [slots, Hkv] float32)."""
+    h = _ModelHandle(model, cfg)
+    B = token_ids.shape[0]
+    Hkv, D, page = cfg["num_kv_heads"], cfg["head_dim"], cfg["page_size"]
+    num_blocks = k_codes[0].numel() // (Hkv * D * page)
+    _check(lib().a8w8_decode_step_i8kv(
+        ctypes.byref(h.model), ctypes.byref(h.cfg), B, _ptr(token_ids), _ptr(slot_mapping),
+        _ptr(block_table), block_table.shape[1], num_blocks, _ptr(ctx_lens),
+        _cache_array(k_codes), _cache_array(v_codes), _cache_array(k_scales),
+        _cache_array(v_scales), _ptr(rope), rope.shape[0], _ptr(next_tokens), _ptr(logits),
+        _ptr(final_hidden), _ptr(ws), ws.numel(), _stream(stream)))
 
 
 class StepGraph:

@@ -1092,12 +1092,15 @@ static a8w8_status enqueue_step(const a8w8_model* m, const a8w8_config& c, int B
                                 const int32_t* ctx_lens, a8w8_bf16* const* k_caches,
                                 a8w8_bf16* const* v_caches, const float* rope, int max_pos,
                                 int32_t* next_tokens, float* logits, a8w8_bf16* final_hidden,
-                                unsigned char* ws, const Launch& L, bool device_loop) {
+                                unsigned char* ws, const Launch& L, bool device_loop,
+                                const KvI8* kv8 = nullptr) {
+    // kv8: the layers' INT8 caches (num_layers entries) instead of k_caches /
+    // v_caches; the per-operation kernels only
     const WsLayout lay = ws_layout(c, B, max_blocks);
     bf16* hidden = reinterpret_cast<bf16*>(ws + lay.hid);
     unsigned long long* keys = reinterpret_cast<unsigned long long*>(ws + lay.keys);
     unsigned* ticket = reinterpret_cast<unsigned*>(ws + lay.ticket);
-    if ((c.flags & A8W8_FLAG_PERSISTENT_STEP) &&
+    if (!kv8 && (c.flags & A8W8_FLAG_PERSISTENT_STEP) &&
         step_supported(B, c.head_dim, c.num_layers, c.hidden, c.intermediate, c.num_q_heads,
                        c.num_kv_heads, max_blocks * c.page_size, L.num_sms) &&
         c.down_k_splits == 2) {
@@ -1171,10 +1174,14 @@ static a8w8_status enqueue_step(const a8w8_model* m, const a8w8_config& c, int B
                                  B, hidden, keys, ticket, device_error_word(), L);
     if (e != cudaSuccess) return cuda_fail(e, "embedding");
     for (int l = 0; l < c.num_layers; ++l) {
-        a8w8_status s = enqueue_layer(&m->layers[l], c, B, hidden, slot_mapping, block_table, max_blocks,
-                                      num_blocks, ctx_lens, reinterpret_cast<bf16*>(k_caches[l]),
-                                      reinterpret_cast<bf16*>(v_caches[l]), rope, max_pos, ws, lay,
-                                      nullptr, L);
+        a8w8_status s = kv8
+            ? enqueue_layer(&m->layers[l], c, B, hidden, slot_mapping, block_table, max_blocks,
+                            num_blocks, ctx_lens, nullptr, nullptr, rope, max_pos, ws, lay, nullptr, L,
+                            false, &kv8[l])
+            : enqueue_layer(&m->layers[l], c, B, hidden, slot_mapping, block_table, max_blocks,
+                            num_blocks, ctx_lens, reinterpret_cast<bf16*>(k_caches[l]),
+                            reinterpret_cast<bf16*>(v_caches[l]), rope, max_pos, ws, lay,
+                            nullptr, L);
         if (s != A8W8_OK) return s;
     }
     const int tile = lmhead_max_batch_tile();
@@ -1202,6 +1209,38 @@ static a8w8_status enqueue_step(const a8w8_model* m, const a8w8_config& c, int B
         if (e != cudaSuccess) return cuda_fail(e, "advance kernel");
     }
     return A8W8_OK;
+}
+
+a8w8_status a8w8_decode_step_i8kv(const a8w8_model* m, const a8w8_config* cfg, int B,
+                                  const int32_t* token_ids, const int32_t* slot_mapping,
+                                  const int32_t* block_table, int max_blocks, int num_blocks,
+                                  const int32_t* ctx_lens, int8_t* const* k_codes,
+                                  int8_t* const* v_codes, float* const* k_scales,
+                                  float* const* v_scales, const float* rope, int max_pos,
+                                  int32_t* next_tokens, float* logits, a8w8_bf16* final_hidden,
+                                  void* ws, size_t ws_bytes, void* stream) {
+    // the code arrays get the BF16 caches' checks (present, 16-byte aligned)
+    a8w8_status s = check_step(m, cfg, B, max_blocks, num_blocks,
+                               reinterpret_cast<a8w8_bf16* const*>(k_codes),
+                               reinterpret_cast<a8w8_bf16* const*>(v_codes), rope, max_pos,
+                               ws_bytes, ws);
+    if (s != A8W8_OK) return s;
+    if (!k_scales || !v_scales) return fail(A8W8_ERR_INVALID_ARG, "scale arrays are NULL");
+    std::vector<KvI8> kv8((size_t)cfg->num_layers);
+    for (int l = 0; l < cfg->num_layers; ++l) {
+        if ((s = check_ptrs({k_scales[l], v_scales[l]}, "KV row scales")) != A8W8_OK) return s;
+        kv8[(size_t)l] = KvI8{k_codes[l], v_codes[l], k_scales[l], v_scales[l]};
+    }
+    if ((s = check_ptrs({token_ids, slot_mapping, block_table, ctx_lens, next_tokens},
+                        "a8w8_decode_step_i8kv")) != A8W8_OK)
+        return s;
+    if ((logits && !aligned16(logits)) || (final_hidden && !aligned16(final_hidden)))
+        return fail(A8W8_ERR_INVALID_ARG, "logits / final_hidden misaligned");
+    Launch L = make_launch(stream, true);
+    if (L.num_sms <= 0) return fail(A8W8_ERR_CUDA, "no CUDA device");
+    return enqueue_step(m, *cfg, B, token_ids, slot_mapping, block_table, max_blocks, num_blocks,
+                        ctx_lens, nullptr, nullptr, rope, max_pos, next_tokens, logits,
+                        final_hidden, static_cast<unsigned char*>(ws), L, false, kv8.data());
 }
 
 a8w8_status a8w8_decode_step(const a8w8_model* m, const a8w8_config* cfg, int B,
