@@ -763,6 +763,108 @@ def run_prefill(args, cfg):
         torch.distributed.destroy_process_group()
 
 
+TTFT_LEN = 512
+TTFT_WORKLOAD = "qwen3_14b_a8w8_ttft_prompt512"
+
+
+def run_ttft(args, cfg):
+    """Time to first token: one 512-token prompt through the 40 layers as one
+    prefill chunk, then the final norm, LM head and argmax on its last row
+    (a8w8_prefill_step); `e2e` adds the host->device copy of the prompt's
+    inputs and the device->host read of the token (rank 0 only)."""
+    import torch
+    import w8a8_quantized_decode_gb300 as a8w8
+
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    a8w8.build()
+    P, page = TTFT_LEN, cfg["page_size"]
+    Hkv, D, L = cfg["num_kv_heads"], cfg["head_dim"], cfg["num_layers"]
+    bt_seq, nblk = synth.paged_layout(SEED + 60, [P + 1], page, spare_blocks=1)
+    pos = np.arange(P)
+    bt = np.repeat(bt_seq, P, axis=0).astype(np.int32)
+    ctx = (pos + 1).astype(np.int32)
+    slots = (bt_seq[0, pos // page] * page + pos % page).astype(np.int32)
+    tok = synth.prompt_ids(SEED + 61, P, cfg["vocab"])
+    model = build_model(cfg, device)
+    kc = [torch.zeros((nblk * page, Hkv, D), dtype=torch.bfloat16, device=device) for _ in range(L)]
+    vc = [torch.zeros_like(k) for k in kc]
+    rope = a8w8.a8w8_rope_table(bt.shape[1] * page, D, cfg["rope_theta"], device=device)
+    ws = a8w8.alloc_workspace(cfg, P, bt.shape[1], device=device)
+    host = {n: torch.from_numpy(x).pin_memory() for n, x in
+            (("tok", tok), ("slot", slots), ("bt", bt), ("ctx", ctx))}
+    dev = {n: t.to(device) for n, t in host.items()}
+    last = torch.tensor([P - 1], dtype=torch.int32, device=device)
+    nxt = torch.empty(1, dtype=torch.int32, device=device)
+    nxt_host = torch.empty(1, dtype=torch.int32).pin_memory()
+    stream = torch.cuda.Stream(device)
+
+    def prefill():
+        a8w8.a8w8_prefill_step(model, cfg, dev["tok"], dev["slot"], dev["bt"], dev["ctx"], kc, vc,
+                               rope, ws, last, nxt, stream=stream)
+
+    gpu_uuid = None
+    try:
+        gpu_uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        pass
+    times, e2e_times = [], []
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            prefill()
+        stream.synchronize()
+        with ClockSampler(gpu_uuid) as clocks:
+            for _ in range(args.steps):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                prefill()
+                e1.record(stream)
+                e1.synchronize()
+                times.append(e0.elapsed_time(e1))
+            for _ in range(args.steps):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for n in host:
+                    dev[n].copy_(host[n], non_blocking=True)
+                prefill()
+                nxt_host.copy_(nxt, non_blocking=True)
+                e1.record(stream)
+                e1.synchronize()
+                e2e_times.append(e0.elapsed_time(e1))
+        errs = a8w8.read_device_errors(stream)
+    ms = sum(times) / len(times)
+    e2e_ms = sum(e2e_times) / len(e2e_times)
+    H, I, Hq = cfg["hidden"], cfg["intermediate"], cfg["num_q_heads"]
+    ops = 2.0 * P * L * (H * ((Hq + 2 * Hkv) * D) + Hq * D * H + 3 * I * H) + 2.0 * H * cfg["vocab"]
+    tops = ops / (ms * 1e-3) / 1e12
+    tpk = tensor_peak()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    # embed; per layer 15 (as the prefill layer); gather; LM head
+    n_launch = 1 + 15 * L + 1 + 1
+    line = {"metric": "A8W8 time to first token (ms, 512-token prompt, 40 layers, greedy)",
+            "value": ms, "unit": "ms", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": False, "vs_baseline": None,
+            "dtype": "int8 x int8 -> int32 (fp16 tensor-core images), f32 dequant, bf16 activations",
+            "data": "synthetic (seeded random-init weights; empty KV history)",
+            "config": {"workload": TTFT_WORKLOAD, "prompt_tokens": P, "layers": L,
+                       "page_size": page, "l2": "inputs larger than L2 (14.8 GB of weights)"},
+            "tokens_per_s": P / (ms * 1e-3),
+            "roofline": {"bound": "tensor",
+                         "kernel": "whole prefill (projections as FP16 mma.sync GEMMs on exact "
+                                   "images of the INT8 codes, epilogues, attention, LM head row)",
+                         "achieved": tops, "peak": tpk["tflops"], "unit": "TFLOP/s",
+                         "frac": tops / tpk["tflops"], "traffic": None, "peak_source": tpk["source"]},
+            "e2e": {"value": e2e_ms, "unit": "ms", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4},
+            "gpu_launches": n_launch * args.steps,
+            "clocks": clocks.summary(), "device_errors": errs}
+    print(json.dumps(line), flush=True)
+
+
 LAYER_B1_VARIANTS = {
     "layer_b1": ("a8w8", "A8W8 decode layer, batch 1, context 256 (us per layer)",
                  "qwen3_14b_a8w8_layer_b1_ctx256",
@@ -941,7 +1043,7 @@ def build_parser() -> argparse.ArgumentParser:
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--workload", choices=["decode_b1", "batched16", "batched16_i8kv", "prefill",
-                                           "sample", *LAYER_B1_VARIANTS],
+                                           "ttft", "sample", *LAYER_B1_VARIANTS],
                     default="decode_b1")
     ap.add_argument("--layers", type=int, default=40,
                     help="layers of the model (fewer only for profiling captures)")
@@ -951,7 +1053,7 @@ def build_parser() -> argparse.ArgumentParser:
 def main():
     args = build_parser().parse_args()
     if args.steps is None:
-        args.steps = {"batched16": 32, "batched16_i8kv": 16, "prefill": 5, "sample": 20,
+        args.steps = {"batched16": 32, "batched16_i8kv": 16, "prefill": 5, "ttft": 5, "sample": 20,
                       **{w: 40 for w in LAYER_B1_VARIANTS}}.get(args.workload, 48)
     if args.warmup < 3:
         raise SystemExit("warmup must be >= 3")
@@ -962,6 +1064,8 @@ def main():
         run_batched(args, cfg)
     elif args.workload == "batched16_i8kv":
         run_batched_i8kv(args, cfg)
+    elif args.workload == "ttft":
+        run_ttft(args, cfg)
     elif args.workload == "prefill":
         run_prefill(args, cfg)
     elif args.workload == "sample":

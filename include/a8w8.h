@@ -66,6 +66,7 @@ typedef enum {
 #define A8W8_DEVERR_TOKEN 0x8u       /* token id outside [0, vocab) */
 #define A8W8_DEVERR_POS 0x10u        /* RoPE position outside the table */
 #define A8W8_DEVERR_TIMEOUT 0x20u    /* a bounded wait on an asynchronous copy gave up */
+#define A8W8_DEVERR_ROW 0x40u        /* a8w8_prefill_step: last_rows entry outside [0, M) */
 
 /* Message of the last failed call on this host thread ("" if none). */
 const char* a8w8_last_error(void);
@@ -445,6 +446,24 @@ a8w8_status a8w8_decode_step(const a8w8_model* m, const a8w8_config* cfg, int B,
                              a8w8_bf16* const* v_caches, const float* rope, int max_pos,
                              int32_t* next_tokens, float* logits, a8w8_bf16* final_hidden,
                              void* ws, size_t ws_bytes, void* stream);
+
+/* The prompt through the model to the first generated token: embedding
+ * gather of token_ids [M], the num_layers layers as a8w8_prefill_layer (row
+ * r at position ctx_lens[r] - 1 of its sequence, causal over the chunk), then
+ * the final RMSNorm, BF16 LM head and greedy argmax on the S rows
+ * last_rows [S] (device; each sequence's last prompt row) into
+ * next_tokens [S] and, when not NULL, logits [S, vocab] float. The timed
+ * quantity of a time to first token. Shape rules as a8w8_prefill_layer
+ * (1 <= M <= 16384), 1 <= S <= M, intermediate or Hq*D + 2*Hkv*D at least
+ * hidden; ws / ws_bytes: a8w8_workspace_bytes(cfg, M, max_blocks); caches as
+ * a8w8_decode_step. Status: built; not yet run on a GPU. */
+a8w8_status a8w8_prefill_step(const a8w8_model* m, const a8w8_config* cfg, int M,
+                              const int32_t* token_ids, const int32_t* slot_mapping,
+                              const int32_t* block_table, int max_blocks, int num_blocks,
+                              const int32_t* ctx_lens, a8w8_bf16* const* k_caches,
+                              a8w8_bf16* const* v_caches, const float* rope, int max_pos, int S,
+                              const int32_t* last_rows, int32_t* next_tokens, float* logits,
+                              void* ws, size_t ws_bytes, void* stream);
 
 /* a8w8_decode_step over INT8 caches: k_codes / v_codes / k_scales / v_scales
  * are HOST arrays of num_layers device pointers, each layer's cache laid out

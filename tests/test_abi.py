@@ -273,3 +273,23 @@ def test_int8_kv_step_validation(lib):
     assert call(ks=nul) == a8w8.ERR_INVALID_ARG
     assert call(ks=None) == a8w8.ERR_INVALID_ARG
     assert call(wsb=100) == a8w8.ERR_WORKSPACE
+
+
+def test_prefill_step_validation(lib):
+    L = lib
+    q = dict(synth.QWEN3_14B, num_layers=1)
+    w = a8w8.LayerWeights(*([FAKE] * len(a8w8.WEIGHT_FIELDS)))
+    layers = (a8w8.LayerWeights * 1)(w)
+    m = a8w8.Model(FAKE, ctypes.cast(layers, ctypes.c_void_p), FAKE, FAKE)
+    arr = (ctypes.c_void_p * 1)(FAKE)
+
+    def call(cfg=q, M=512, S=1, max_blocks=8, last=FAKE, wsb=1 << 34):
+        return L.a8w8_prefill_step(ctypes.byref(m), _cfg(cfg), M, FAKE, FAKE, FAKE, max_blocks, 16,
+                                   FAKE, arr, arr, FAKE, 1024, S, last, FAKE, None, FAKE, wsb, None)
+    assert call(M=0) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert call(S=0) == a8w8.ERR_INVALID_ARG
+    assert call(S=513) == a8w8.ERR_INVALID_ARG
+    assert call(max_blocks=65) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert call(last=None) == a8w8.ERR_INVALID_ARG
+    need = L.a8w8_workspace_bytes(_cfg(q), 512, 8)
+    assert call(wsb=need - 1) == a8w8.ERR_WORKSPACE

@@ -953,6 +953,34 @@ def test_step_composes_embed_layers_norm_head():
     assert rc == -3
 
 
+def test_prompt_through_the_step_equals_decoding_it_token_by_token():
+    # the first generated token of a prompt (time to first token): the step
+    # over all prompt rows at once (each at its own position, causal) gives
+    # every row the next token and final hidden state of decoding the prompt
+    # one token at a time; the last row's token is the first generated one
+    cfg = dict(synth.TINY, num_layers=2, vocab=97)
+    model = synth.model_weights_host(cfg, 41)
+    page, P = cfg["page_size"], 21
+    Hkv, D = cfg["num_kv_heads"], cfg["head_dim"]
+    bt_seq, nblk = synth.paged_layout(42, [P + 1], page, spare_blocks=1)
+    pos = np.arange(P)
+    bt = np.repeat(bt_seq, P, axis=0).astype(np.int32)
+    ctx = (pos + 1).astype(np.int32)
+    slots = synth.slots_for(bt, pos, page)
+    tok = synth.prompt_ids(43, P, cfg["vocab"])
+    empty = lambda: [np.zeros((nblk * page, Hkv, D), np.uint16) for _ in range(2)]
+    kc1, vc1 = empty(), empty()
+    nxt, fh, _, rc = oracle.decode_step(model, cfg, tok, slots, bt, ctx, kc1, vc1)
+    assert rc == 0
+    kc2, vc2 = empty(), empty()
+    for i in range(P):
+        r = slice(i, i + 1)
+        n1, f1, _, rc = oracle.decode_step(model, cfg, tok[r], slots[r], bt[r], ctx[r], kc2, vc2)
+        assert rc == 0
+        assert n1[0] == nxt[i] and np.array_equal(f1[0], fh[i])
+    assert all(np.array_equal(a, b) for a, b in zip(kc1 + vc1, kc2 + vc2))
+
+
 def test_prefill_chunk_equals_sequential_decode():
     # a prefill chunk (all rows through the layer at once, each at its own
     # position) must equal decoding the rows one position at a time: same

@@ -95,6 +95,8 @@ _SIGNATURES = {
                                      _p, _sz, _p, _p]),
     "a8w8_decode_step_i8kv": (_i, [_p, _p, _i, _p, _p, _p, _i, _i, _p, _p, _p, _p, _p, _p, _i, _p,
                                    _p, _p, _p, _sz, _p]),
+    "a8w8_prefill_step": (_i, [_p, _p, _i, _p, _p, _p, _i, _i, _p, _p, _p, _p, _i, _i, _p, _p, _p,
+                               _p, _sz, _p]),
     "bf16_linear": (_i, [_p, _i, _i, _p, _i, _p, _p, _p]),
     "bf16_gate_up_swiglu": (_i, [_p, _i, _i, _p, _i, _p, _p]),
     "bf16_decode_layer": (_i, [_p, _p, _i, _p, _p, _p, _i, _i, _p, _p, _p, _p, _i, _p, _sz, _p,
@@ -528,6 +530,23 @@ def a8w8_decode_step(model: dict, cfg: dict, token_ids, slot_mapping, block_tabl
         _cache_array(k_caches), _cache_array(v_caches), _ptr(rope), rope.shape[0],
         _ptr(next_tokens), _ptr(logits), _ptr(final_hidden), _ptr(ws), ws.numel(),
         _stream(stream)))
+
+
+def a8w8_prefill_step(model: dict, cfg: dict, token_ids, slot_mapping, block_table, ctx_lens,
+                      k_caches, v_caches, rope, ws, last_rows, next_tokens, logits=None,
+                      stream=None):
+    """The prompt rows (as a8w8_prefill_layer) through every layer, then the
+    final norm, LM head and argmax on last_rows [S] -> next_tokens [S]."""
+    h = _ModelHandle(model, cfg)
+    M = token_ids.shape[0]
+    S = last_rows.shape[0]
+    Hkv, D, page = cfg["num_kv_heads"], cfg["head_dim"], cfg["page_size"]
+    num_blocks = k_caches[0].numel() // (Hkv * D * page)
+    _check(lib().a8w8_prefill_step(
+        ctypes.byref(h.model), ctypes.byref(h.cfg), M, _ptr(token_ids), _ptr(slot_mapping),
+        _ptr(block_table), block_table.shape[1], num_blocks, _ptr(ctx_lens),
+        _cache_array(k_caches), _cache_array(v_caches), _ptr(rope), rope.shape[0], S,
+        _ptr(last_rows), _ptr(next_tokens), _ptr(logits), _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def a8w8_decode_step_i8kv(model: dict, cfg: dict, token_ids, slot_mapping, block_table, ctx_lens,

@@ -1211,6 +1211,74 @@ static a8w8_status enqueue_step(const a8w8_model* m, const a8w8_config& c, int B
     return A8W8_OK;
 }
 
+a8w8_status a8w8_prefill_step(const a8w8_model* m, const a8w8_config* cfg, int M,
+                              const int32_t* token_ids, const int32_t* slot_mapping,
+                              const int32_t* block_table, int max_blocks, int num_blocks,
+                              const int32_t* ctx_lens, a8w8_bf16* const* k_caches,
+                              a8w8_bf16* const* v_caches, const float* rope, int max_pos, int S,
+                              const int32_t* last_rows, int32_t* next_tokens, float* logits,
+                              void* ws, size_t ws_bytes, void* stream) {
+    if (M < 1 || M > 16384) return fail(A8W8_ERR_UNSUPPORTED_SHAPE, "M=%d outside [1, 16384]", M);
+    if (S < 1 || S > M) return fail(A8W8_ERR_INVALID_ARG, "S=%d outside [1, M]", S);
+    // the model and caches as for a decode step of one row; the workspace for M rows
+    a8w8_status s = check_step(m, cfg, 1, max_blocks, num_blocks, k_caches, v_caches, rope,
+                               max_pos, ~(size_t)0, ws);
+    if (s != A8W8_OK) return s;
+    const int H = cfg->hidden, NQKV = (cfg->num_q_heads + 2 * cfg->num_kv_heads) * cfg->head_dim;
+    if (!attn_group_shape_ok(cfg->num_q_heads, cfg->num_kv_heads, cfg->head_dim,
+                             max_blocks * cfg->page_size))
+        return fail(A8W8_ERR_UNSUPPORTED_SHAPE,
+                    "prefill attention needs Hq/Hkv <= 7 and at most 64 chunks of 128 tokens");
+    if (cfg->intermediate < H && NQKV < H)
+        return fail(A8W8_ERR_UNSUPPORTED_SHAPE, "prefill step needs intermediate or QKV width >= hidden");
+    if ((s = check_ptrs({token_ids, slot_mapping, block_table, ctx_lens, last_rows, next_tokens},
+                        "a8w8_prefill_step")) != A8W8_OK)
+        return s;
+    if (logits && !aligned16(logits)) return fail(A8W8_ERR_INVALID_ARG, "logits misaligned");
+    const WsLayout lay = ws_layout(*cfg, M, max_blocks);
+    if (ws_bytes < lay.total) return fail(A8W8_ERR_WORKSPACE, "prefill step workspace needs %zu bytes", lay.total);
+    Launch L = make_launch(stream, true);
+    if (L.num_sms <= 0) return fail(A8W8_ERR_CUDA, "no CUDA device");
+    const a8w8_config& c = *cfg;
+    unsigned char* w = static_cast<unsigned char*>(ws);
+    bf16* hidden = reinterpret_cast<bf16*>(w + lay.hid);
+    unsigned long long* keys = reinterpret_cast<unsigned long long*>(w + lay.keys);
+    unsigned* ticket = reinterpret_cast<unsigned*>(w + lay.ticket);
+    cudaError_t e = launch_embed(reinterpret_cast<const bf16*>(m->embed), c.vocab, H, token_ids, M,
+                                 hidden, keys, ticket, device_error_word(), L);
+    if (e != cudaSuccess) return cuda_fail(e, "embedding");
+    for (int l = 0; l < c.num_layers; ++l) {
+        s = enqueue_layer(&m->layers[l], c, M, hidden, slot_mapping, block_table, max_blocks,
+                          num_blocks, ctx_lens, reinterpret_cast<bf16*>(k_caches[l]),
+                          reinterpret_cast<bf16*>(v_caches[l]), rope, max_pos, w, lay, nullptr, L,
+                          true);
+        if (s != A8W8_OK) return s;
+    }
+    // the last rows into a dense block (the SwiGLU or QKV buffer, free by now)
+    bf16* last = reinterpret_cast<bf16*>(w + (c.intermediate >= H ? lay.act : lay.qkv));
+    e = launch_gather_rows(hidden, H, last_rows, S, M, last, device_error_word(), L);
+    if (e != cudaSuccess) return cuda_fail(e, "gather last rows");
+    const int tile = lmhead_max_batch_tile();
+    for (int b0 = 0; b0 < S; b0 += tile) {
+        LmHeadParams p = {};
+        p.hidden = last + (size_t)b0 * H;
+        p.norm_w = reinterpret_cast<const bf16*>(m->final_norm_w);
+        p.eps = c.rms_eps;
+        p.W = reinterpret_cast<const bf16*>(m->lm_head);
+        p.H = H;
+        p.V = c.vocab;
+        p.M = S - b0 < tile ? S - b0 : tile;
+        p.logits = logits ? logits + (size_t)b0 * c.vocab : nullptr;
+        p.final_hidden = nullptr;
+        p.keys = keys + b0;
+        p.ticket = ticket;
+        p.next_tokens = next_tokens + b0;
+        e = launch_lmhead_argmax(p, L);
+        if (e != cudaSuccess) return cuda_fail(e, "LM head");
+    }
+    return A8W8_OK;
+}
+
 a8w8_status a8w8_decode_step_i8kv(const a8w8_model* m, const a8w8_config* cfg, int B,
                                   const int32_t* token_ids, const int32_t* slot_mapping,
                                   const int32_t* block_table, int max_blocks, int num_blocks,

@@ -170,6 +170,11 @@ cudaError_t launch_bf16_gemv(const Bf16GemvParams& p, bool swiglu, const Launch&
 cudaError_t launch_rmsnorm_rows(const bf16* x, int rows, int H, const bf16* w, float eps, bf16* y,
                                 const Launch& L);
 
+// Prefill step (gather.cu): dst[s] = src[rows[s]] ([S, H] BF16); a row index
+// outside [0, n_src) gives a zero row and device error bit 0x40.
+cudaError_t launch_gather_rows(const bf16* src, int H, const int32_t* rows, int S, int n_src,
+                               bf16* dst, unsigned* err, const Launch& L);
+
 // Prefill: per-head K RMSNorm + RoPE of every row's new token and the K/V
 // write into the cache, before the attention (fused QKV rows in p.q).
 cudaError_t launch_kv_prep(const AttnParams& p, const Launch& L);
