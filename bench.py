@@ -48,10 +48,10 @@ SEED = 2026
 WORKLOAD = "qwen3_14b_a8w8_decode_step_b1"
 METRIC = "A8W8 decode TPOT (ms/token, 40 layers, bs=1)"
 
-# DRAM bytes (read + write) per launch of the Gate/Up kernel, from an ncu
-# capture of the kernel as it is now built; None while no capture of the
-# current kernel exists.
-GATE_UP_NCU_TRAFFIC_BYTES = 181582848
+# DRAM bytes (read + write) per launch of the fused post-attention norm +
+# Gate/Up + SwiGLU kernel the step runs, from an ncu capture of the kernel as
+# it is now built; None while no capture of the current kernel exists.
+GATE_UP_NCU_TRAFFIC_BYTES = None
 
 
 def step_bytes(cfg, ctx_lens) -> dict:
@@ -65,9 +65,12 @@ def step_bytes(cfg, ctx_lens) -> dict:
     return {"layers": layer * L, "lm_head": head, "kv": kv, "total": layer * L + head + kv}
 
 
-def gate_up_bytes(cfg) -> int:
+def gate_up_bytes(cfg, B: int = 1) -> int:
+    """Algorithmic bytes of one launch of the fused a11-a12 kernel: the Gate/Up
+    weights and scales, the post-attention norm weight, the BF16 input rows
+    and the SwiGLU output rows."""
     H, I = cfg["hidden"], cfg["intermediate"]
-    return 2 * I * H + 2 * I * 4
+    return 2 * I * H + 2 * I * 4 + H * 2 + B * H * 2 + B * I * 2
 
 
 class ClockSampler:
@@ -371,31 +374,35 @@ def run_ours(args, cfg):
         d2h = B * 4
         e2e_graph.close()
 
-        # roofline of the dominant kernel: Gate/Up over the 40 layers' weights,
-        # its 40 launches replayed as one CUDA graph (no host launch overhead)
-        gu_bytes = gate_up_bytes(cfg)
-        xq = torch.randint(-127, 128, (B, cfg["hidden"]), dtype=torch.int8, device=device)
-        xs = torch.full((B,), 0.01, dtype=torch.float32, device=device)
+        # roofline of the dominant kernel, the one the step runs for a11-a12:
+        # post-attention RMSNorm and quantisation of the BF16 row in the
+        # prologue, Gate/Up + SwiGLU, over the 40 layers' weights (13.2 GB >
+        # L2), its 40 launches replayed as one CUDA graph on `stream`
+        gu_bytes = gate_up_bytes(cfg, B)
+        xrow = synth.t_bf16_normal(SEED + 40, (B, cfg["hidden"]), device, std=30.0)
+        act = torch.empty((B, cfg["intermediate"]), dtype=torch.bfloat16, device=device)
 
         def gate_up_all():
             for l in range(L):
-                a8w8.a8w8_gate_up_swiglu(xq, xs, model["layers"][l]["w_gate_up"],
-                                         model["layers"][l]["s_gate_up"])
+                lw = model["layers"][l]
+                a8w8.a8w8_rmsnorm_gate_up_swiglu(xrow, lw["post_norm_w"], cfg["rms_eps"],
+                                                 lw["w_gate_up"], lw["s_gate_up"], out=act,
+                                                 stream=stream)
         gate_up_all()
-        torch.cuda.synchronize()
+        stream.synchronize()
         gg = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gg):
+        with torch.cuda.graph(gg, stream=stream):
             gate_up_all()
         for _ in range(2):
             gg.replay()
         reps = 3
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        cs = torch.cuda.current_stream()
-        e0.record(cs)
+        stream.synchronize()
+        e0.record(stream)
         for _ in range(reps):
             gg.replay()
-        e1.record(cs)
+        e1.record(stream)
         e1.synchronize()
         gu_ms = e0.elapsed_time(e1) / (reps * L)
         del gg
@@ -424,10 +431,13 @@ def run_ours(args, cfg):
             "step_bytes": per_step_bytes,
             "step_hbm_gbs": per_step_bytes / (tpot * 1e-3) / 1e9,
             "step_frac_of_peak": per_step_bytes / (tpot * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "layers_frac": sb["layers"] / (tpot * 1e-3) / 1e9 / peaks["hbm_gbs"],
             "e2e": {"value": e2e_ms, "unit": "ms/token", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": n_launch * args.steps,
-            "roofline": {"bound": "hbm", "kernel": "Gate/Up projection + SwiGLU (gemv_stream_kernel)",
+            "roofline": {"bound": "hbm",
+                         "kernel": "post-attention RMSNorm + quant + Gate/Up + SwiGLU "
+                                   "(gemv_stream_kernel<1, PRO_NORM_QUANT, EPI_SWIGLU, 1>)",
                          "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / peaks["hbm_gbs"],
                          "traffic": GATE_UP_NCU_TRAFFIC_BYTES,

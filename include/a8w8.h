@@ -185,11 +185,27 @@ a8w8_status a8w8_linear(const int8_t* xq, const float* x_scale, int M, int K,
 /* Fused Gate/Up projection with SwiGLU ([LIB-810] "Gate/Up INT8 path"; [SRV-52]
  * "Measurement basis"). W_gu [2I, K]: rows [0, I) gate, [I, 2I) up.
  *   g = (float(acc_gate) * x_scale[m]) * s_gu[j],  u likewise with s_gu[I + j]
- *   act[m][j] = bf16_rne( silu(g) * u ),  silu(g) = g / (1 + exp(-g)), float32.
- * acc_out [M, 2I] int32 (nullable). Shape rules as a8w8_linear. */
+ *   act[m][j] = bf16_rne( silu(g) * u ),  silu(g) = g / (1 + exp(-g)),
+ * the product silu(g) * u of the float32 g and u evaluated in two-float
+ * arithmetic (about 2^-44 relative) and rounded to BF16 once, so act is the
+ * correctly rounded real value except within that distance of a rounding
+ * boundary. acc_out [M, 2I] int32 (nullable). Shape rules as a8w8_linear. */
 a8w8_status a8w8_gate_up_swiglu(const int8_t* xq, const float* x_scale, int M, int K,
                                 const int8_t* W_gu, const float* s_gu, int I,
                                 a8w8_bf16* act, int32_t* acc_out, void* stream);
+
+/* a11-a12 fused as the decode layer runs them for one or two rows: the
+ * post-attention RMSNorm of x [M, K] BF16 with weight norm_w [K] BF16,
+ *   xn = bf16_rne( x * 1/sqrt(mean(x^2) + eps) * norm_w ),
+ * its per-row INT8 quantisation (as a8w8_quant_rows), then Gate/Up + SwiGLU
+ * as a8w8_gate_up_swiglu ([LIB-810] "Gate/Up INT8 path": one activation
+ * quantisation per row feeding the fused gate/up projection). The row is
+ * normalised and quantised inside the projection kernel, never written out.
+ * act [M, I] BF16. K a positive multiple of 16 (at most 65536); every
+ * pointer 16-byte aligned. Errors as a8w8_linear. */
+a8w8_status a8w8_rmsnorm_gate_up_swiglu(const a8w8_bf16* x, int M, int K,
+                                        const a8w8_bf16* norm_w, float eps, const int8_t* W_gu,
+                                        const float* s_gu, int I, a8w8_bf16* act, void* stream);
 
 /* Writes k, v ([T, Hkv, D] BF16) into the paged caches at
  * slot_mapping[t] ([LIB-810] "BF16 KV cache": BF16 storage, no scale tensors;
@@ -204,8 +220,11 @@ a8w8_status paged_kv_write(const a8w8_bf16* k, const a8w8_bf16* v, int T, int Hk
  * attention loads BF16 K/V with no per-row dequantisation; [SRV-61]: block
  * table). For request b, query head h (KV head h / (Hq / Hkv)) and its
  * ctx_lens[b] tokens t at slot block_table[b][t / page] * page + t % page:
- *   out = sum_t softmax_t(softmax_scale * <q, K_t>) V_t   (float32, split-KV
- *   with online-softmax partials), narrowed to BF16 once.
+ *   out = sum_t softmax_t(softmax_scale * <q, K_t>) V_t
+ * evaluated in two-float arithmetic (scores, exponentials and sums carried
+ * as float pairs, about 2^-44 relative; split-KV partials merged with their
+ * maxima) and narrowed to BF16 once, so out is the correctly rounded real
+ * value except within that distance of a rounding boundary.
  * q [B, Hq, D]; block_table [B, max_blocks]; ctx_lens [B] (0 = padded row,
  * zero output); out [B, Hq, D]. ws: device workspace of at least
  * a8w8_attention_workspace_bytes(B, Hq, D, max_blocks * page_size) bytes

@@ -87,3 +87,64 @@ def bf16_close(gpu_bf16, ref_bf16, ulps: float, rel_floor: float) -> np.ndarray:
     mag = np.maximum(np.abs(b), max(rel_floor * rms, 1e-30))
     ulp = 2.0 ** (np.floor(np.log2(mag)) - 7)
     return np.abs(a - b) <= ulps * ulp
+
+
+# ---------------------------------------------------------------------------
+# Element-wise bounds for float32 sums of exact products
+# ---------------------------------------------------------------------------
+
+# The LM head multiplies BF16 operands on the tensor cores with float32
+# accumulation; each product is exact and the accumulated value is within a
+# small multiple of the float32 unit of the absolute sum. 2^-20 of sum |h w|
+# leaves room for a few dozen accumulation roundings in a row while a wrong
+# operand (a permuted column, a dropped K block) moves a logit by a sizeable
+# share of |h w| for that column, far above it.
+LM_HEAD_REL = 2.0 ** -20
+
+
+def abs_dot(x_bf16, W_bf16, chunk: int = 8192) -> np.ndarray:
+    """sum_k |x[m,k]| |W[n,k]| for BF16 operands, float64, W chunked by rows."""
+    xa = np.abs(bf16_to_f64(x_bf16)).astype(np.float32)
+    out = np.empty((xa.shape[0], W_bf16.shape[0]), np.float64)
+    for n0 in range(0, W_bf16.shape[0], chunk):
+        wa = np.abs(bf16_to_f64(W_bf16[n0:n0 + chunk])).astype(np.float32)
+        out[:, n0:n0 + chunk] = (xa @ wa.T).astype(np.float64)
+    return out
+
+
+def check_lm_head(fh_bf16, W_lm, g_logits, g_next, o_logits=None):
+    """GPU logits against the oracle's LM head evaluated on the GPU's own final
+    hidden rows, element by element within LM_HEAD_REL * sum |h w|, and the
+    GPU's token equal to the oracle's argmax except where the oracle's top two
+    are closer than twice that bound. Returns (max |diff| / bound, #near ties)."""
+    import oracle
+    if o_logits is None:
+        o_logits = oracle.lm_head(fh_bf16, W_lm)
+    bound = LM_HEAD_REL * abs_dot(fh_bf16, W_lm)
+    diff = np.abs(np.asarray(g_logits, np.float64) - o_logits)
+    worst = float(np.max(diff / np.maximum(bound, 1e-300)))
+    assert (diff <= bound).all(), f"LM head: logits beyond the float32 bound (worst {worst:.3g}x)"
+    o_next = oracle.argmax_f64(o_logits)
+    ties = 0
+    for b in range(o_logits.shape[0]):
+        if g_next[b] != o_next[b]:
+            gap = o_logits[b, o_next[b]] - o_logits[b, g_next[b]]
+            assert gap <= 2 * max(bound[b, o_next[b]], bound[b, g_next[b]]), \
+                f"row {b}: GPU token {g_next[b]} vs oracle {o_next[b]}, gap {gap:.3g}"
+            ties += 1
+    return worst, ties
+
+
+def proj_error_bound(x_bf16, W_bf16, K: int) -> np.ndarray:
+    """Bound on |float32 sum - exact sum| of sum_k x[m,k] W[n,k] with exact
+    products: gamma_K * sum |x w|, gamma_K = K u / (1 - K u), u = 2^-24
+    (any summation order), plus one more u for a residual add."""
+    u = 2.0 ** -24
+    gamma = (K + 1) * u / (1 - (K + 1) * u)
+    return gamma * abs_dot(x_bf16, W_bf16)
+
+
+def bf16_ulp_at(v) -> np.ndarray:
+    """One BF16 unit in the last place at |v| (normal range)."""
+    mag = np.maximum(np.abs(np.asarray(v, np.float64)), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(mag)) - 7)

@@ -44,6 +44,17 @@ def test_linear_validation(lib):
     assert L.a8w8_gate_up_swiglu(FAKE, FAKE, 1, 20, FAKE, FAKE, 4, FAKE, None, None) == a8w8.ERR_UNSUPPORTED_SHAPE
 
 
+def test_rmsnorm_gate_up_validation(lib):
+    L = lib
+    f = L.a8w8_rmsnorm_gate_up_swiglu
+    assert f(FAKE, 1, 20, FAKE, 1e-6, FAKE, FAKE, 4, FAKE, None) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert f(FAKE, 1, 65552, FAKE, 1e-6, FAKE, FAKE, 4, FAKE, None) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert f(FAKE, 1, 32, None, 1e-6, FAKE, FAKE, 4, FAKE, None) == a8w8.ERR_INVALID_ARG
+    assert f(FAKE, 1, 32, FAKE, -1.0, FAKE, FAKE, 4, FAKE, None) == a8w8.ERR_INVALID_ARG
+    assert f(FAKE, -1, 32, FAKE, 1e-6, FAKE, FAKE, 4, FAKE, None) == a8w8.ERR_INVALID_ARG
+    assert f(None, 0, 32, None, 1e-6, None, None, 4, None, None) == a8w8.OK
+
+
 def test_quant_and_kv_validation(lib):
     L = lib
     assert L.a8w8_quant_rows(FAKE, 2, 12, 12, FAKE, FAKE, None) == a8w8.ERR_UNSUPPORTED_SHAPE

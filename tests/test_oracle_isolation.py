@@ -26,16 +26,24 @@ ORACLE_RUNNERS = {"bench.py": ({"time_oracle_steps"}, {"run_reference", "cpu_bas
 
 
 def _py_files():
-    skip = ("tests", "oracle", "_work", "gpurun_out", "baseline")
-    for dirpath, dirnames, files in os.walk(ROOT):
-        rel = os.path.relpath(dirpath, ROOT)
-        top = rel.split(os.sep)[0]
-        if rel != "." and (top in skip or top.startswith(".") or top.startswith("_")):
-            dirnames[:] = []
-            continue
-        for f in files:
-            if f.endswith(".py"):
-                yield os.path.join(dirpath, f)
+    """Python files of the repository outside tests/ and oracle/: the files
+    git tracks, or, in a copy without git metadata, the top-level scripts and
+    the product packages."""
+    import subprocess
+    skip = ("tests", "oracle", "baseline")
+    try:
+        out = subprocess.run(["git", "ls-files", "*.py"], cwd=ROOT, capture_output=True,
+                             text=True, check=True).stdout.split()
+    except (OSError, subprocess.CalledProcessError):
+        out = []
+    if not out:
+        out = [f for f in os.listdir(ROOT) if f.endswith(".py")]
+        for pkg in ("w8a8_quantized_decode_gb300", "synth"):
+            out += [os.path.relpath(p, ROOT)
+                    for p in glob.glob(os.path.join(ROOT, pkg, "**", "*.py"), recursive=True)]
+    for rel in out:
+        if rel.split("/")[0] not in skip:
+            yield os.path.join(ROOT, rel)
 
 
 def _imports_oracle(node) -> bool:

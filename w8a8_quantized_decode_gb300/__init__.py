@@ -80,6 +80,7 @@ _SIGNATURES = {
     "a8w8_quant_rows": (_i, [_p, _i, _i, _i, _p, _p, _p]),
     "a8w8_linear": (_i, [_p, _p, _i, _i, _p, _p, _i, _i, _p, _p, _p, _p]),
     "a8w8_gate_up_swiglu": (_i, [_p, _p, _i, _i, _p, _p, _i, _p, _p, _p]),
+    "a8w8_rmsnorm_gate_up_swiglu": (_i, [_p, _i, _i, _p, _f, _p, _p, _i, _p, _p]),
     "paged_kv_write": (_i, [_p, _p, _i, _i, _i, _p, _p, _p, _i, _i, _p]),
     "paged_decode_attention_bf16": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p,
                                          _p, _sz, _p]),
@@ -239,6 +240,18 @@ def a8w8_gate_up_swiglu(xq, x_scale, W_gu, s_gu, acc_out=False, stream=None):
     _check(lib().a8w8_gate_up_swiglu(_ptr(xq), _ptr(x_scale), M, K, _ptr(W_gu), _ptr(s_gu), I,
                                      _ptr(act), _ptr(acc), _stream(stream)))
     return (act, acc) if acc_out else act
+
+
+def a8w8_rmsnorm_gate_up_swiglu(x, norm_w, eps, W_gu, s_gu, out=None, stream=None):
+    """Post-attention RMSNorm + per-row quantisation + fused Gate/Up + SwiGLU
+    of x [M, K] bf16 in one kernel: W_gu [2I, K] int8 -> act [M, I] bf16."""
+    torch = _torch()
+    M, K = x.shape
+    I = W_gu.shape[0] // 2
+    act = out if out is not None else torch.empty((M, I), dtype=torch.bfloat16, device=x.device)
+    _check(lib().a8w8_rmsnorm_gate_up_swiglu(_ptr(x), M, K, _ptr(norm_w), float(eps), _ptr(W_gu),
+                                             _ptr(s_gu), I, _ptr(act), _stream(stream)))
+    return act
 
 
 def paged_kv_write(k, v, slot_mapping, k_cache, v_cache, page_size, stream=None):

@@ -632,6 +632,37 @@ a8w8_status a8w8_gate_up_swiglu(const int8_t* xq, const float* x_scale, int M, i
                          "a8w8_gate_up_swiglu");
 }
 
+a8w8_status a8w8_rmsnorm_gate_up_swiglu(const a8w8_bf16* x, int M, int K,
+                                        const a8w8_bf16* norm_w, float eps, const int8_t* W_gu,
+                                        const float* s_gu, int I, a8w8_bf16* act, void* stream) {
+    const char* name = "a8w8_rmsnorm_gate_up_swiglu";
+    if (M < 0 || K < 0 || I < 0) return fail(A8W8_ERR_INVALID_ARG, "%s: negative size", name);
+    if (M == 0 || I == 0) return A8W8_OK;
+    if (K == 0 || K % 16 || K > 65536)
+        return fail(A8W8_ERR_UNSUPPORTED_SHAPE, "%s: K must be a positive multiple of 16, at most 65536", name);
+    if (!(eps >= 0.0f)) return fail(A8W8_ERR_INVALID_ARG, "%s: eps must be >= 0", name);
+    a8w8_status s = check_ptrs({x, norm_w, W_gu, s_gu, act}, name);
+    if (s != A8W8_OK) return s;
+    Launch L = make_launch(stream, false);
+    if (L.num_sms <= 0) return fail(A8W8_ERR_CUDA, "%s: no CUDA device", name);
+    GemvParams g = {};
+    g.W = W_gu;
+    g.w_scale = s_gu;
+    g.K = K;
+    g.N = I;
+    g.x = reinterpret_cast<const bf16*>(x);
+    g.ldx = K;
+    g.norm_w = reinterpret_cast<const bf16*>(norm_w);
+    g.eps = eps;
+    g.y = reinterpret_cast<bf16*>(act);
+    g.ldy = I;
+    // no code buffers: every batch tile runs the streaming kernel with the
+    // normalisation and quantisation in its prologue, as the decode layer
+    // does for one or two rows
+    cudaError_t e = run_gemv(PRO_NORM_QUANT, EPI_SWIGLU, 1, g, M, L);
+    return e == cudaSuccess ? A8W8_OK : cuda_fail(e, name);
+}
+
 a8w8_status paged_kv_write(const a8w8_bf16* k, const a8w8_bf16* v, int T, int Hkv, int D,
                            const int32_t* slot_mapping, a8w8_bf16* k_cache, a8w8_bf16* v_cache,
                            int num_blocks, int page_size, void* stream) {
