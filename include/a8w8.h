@@ -253,9 +253,11 @@ size_t a8w8_attention_workspace_bytes(int B, int Hq, int D, int max_ctx);
  * loads the library until the process exits. A call whose partials would
  * exceed it (a8w8_attention_workspace_bytes(B, Hq, D, max_blocks * page_size)
  * > A8W8_NOALLOC_SCRATCH_BYTES) is rejected with A8W8_ERR_WORKSPACE before
- * anything is launched. The first call on a device looks up the array's
- * device address for that device (with that device current); make that first
- * call before any stream capture. Every call shares the one array: calls that
+ * anything is launched. The first call in each CUDA context (once per
+ * device, and again after a device reset, which replaces the context) looks
+ * up the array's device address with that device current, under a lock that
+ * makes concurrent first calls safe; make that first call before any stream
+ * capture. Every call shares the one array: calls that
  * overlap on the GPU (other streams, other host threads) race on it and must
  * be serialised by the caller. Nothing in it needs to start at zero: each call
  * writes every partial it later reads. */

@@ -3,10 +3,15 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
+#include <map>
+#include <mutex>
+#include <set>
 #include <string>
 #include <vector>
 
@@ -14,6 +19,60 @@
 #include "kernels.cuh"
 
 using namespace a8w8;
+
+namespace a8w8 {
+namespace {
+
+// The id of the current CUDA context, read through the driver entry points
+// (cuCtxGetCurrent, cuCtxGetId); every context gets a distinct id, so a value
+// looked up in one context is stale exactly when the id differs. 0 when no
+// context is current or the ids cannot be read.
+using CtxGetCurrentFn = int (*)(void**);
+using CtxGetIdFn = int (*)(void*, unsigned long long*);
+
+unsigned long long current_context_id() {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag resolved;
+    std::call_once(resolved, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+        f = nullptr;
+        q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(f);
+    });
+    void* ctx = nullptr;
+    if (!get_current || get_current(&ctx) != 0 || !ctx) return 0;
+    unsigned long long id = 0;
+    if (!get_id || get_id(ctx, &id) != 0) return 0;
+    return id;
+}
+
+std::mutex g_ctx_mutex;
+// (context id, key) pairs whose setup has succeeded, and the symbol
+// addresses looked up, per context id.
+std::set<std::pair<unsigned long long, const void*>> g_ctx_done;
+std::map<std::pair<unsigned long long, const void*>, void*> g_ctx_symbols;
+
+}  // namespace
+
+cudaError_t once_per_context(const void* key, const std::function<cudaError_t()>& setup) {
+    const unsigned long long id = current_context_id();
+    std::lock_guard<std::mutex> lock(g_ctx_mutex);
+    if (id && g_ctx_done.count({id, key})) return cudaSuccess;
+    const cudaError_t e = setup();
+    // the setup may have created the context: remember it under its id
+    const unsigned long long after = current_context_id();
+    if (e == cudaSuccess && after) g_ctx_done.insert({after, key});
+    return e;
+}
+
+}  // namespace a8w8
 
 namespace {
 
@@ -42,30 +101,40 @@ a8w8_status cuda_fail(cudaError_t e, const char* what) {
 
 __device__ unsigned g_device_error;
 
+// Device address of a __device__ variable in the current context, looked up
+// once per context (nullptr if the lookup fails).
+void* symbol_address(const void* symbol) {
+    const unsigned long long id = current_context_id();
+    {
+        std::lock_guard<std::mutex> lock(g_ctx_mutex);
+        auto it = g_ctx_symbols.find({id, symbol});
+        if (id && it != g_ctx_symbols.end()) return it->second;
+    }
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, symbol) != cudaSuccess) return nullptr;
+    const unsigned long long after = current_context_id();
+    if (after) {
+        std::lock_guard<std::mutex> lock(g_ctx_mutex);
+        g_ctx_symbols[{after, symbol}] = p;
+    }
+    return p;
+}
+
 int num_sms_current() {
-    static int cached[64];
+    // a property of the device, not of the context
+    static std::atomic<int> cached[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (dev < 0 || dev >= 64) return 0;
-    if (cached[dev] == 0) {
-        int n = 0;
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        cached[dev] = n;
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cached[dev].store(n, std::memory_order_relaxed);
     }
-    return cached[dev];
+    return n;
 }
 
-unsigned* device_error_word() {
-    static unsigned* cached[64];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    if (!cached[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
-        cached[dev] = static_cast<unsigned*>(p);
-    }
-    return cached[dev];
-}
+unsigned* device_error_word() { return static_cast<unsigned*>(symbol_address(&g_device_error)); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -239,6 +308,23 @@ struct KvI8 {
     float* v_scale;
 };
 
+// L2 prefetch depths of the batch-1/2 decode layer: 512-byte units of each
+// warp's weight run that the QKV, O, Gate/Up and down kernels ask of L2 before
+// their dependency wait, and whether the attention kernel asks for the O
+// projection's weights.
+struct PrefetchDepths {
+    int qkv, o, gate_up, down, attn_o;
+};
+const PrefetchDepths& prefetch_depths() {
+    static const PrefetchDepths d = [] {
+        PrefetchDepths v = {16, 16, 16, 16, 1};
+        if (const char* s = std::getenv("A8W8_PF"))
+            std::sscanf(s, "%d,%d,%d,%d,%d", &v.qkv, &v.o, &v.gate_up, &v.down, &v.attn_o);
+        return v;
+    }();
+    return d;
+}
+
 // Enqueues one decode layer (no validation). With `kv8` the layer's cache is
 // the INT8 one (k_cache / v_cache unused).
 a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int B, bf16* hidden,
@@ -277,6 +363,8 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     g.tap_s = T.xs;
     g.clear = att_tk;   // the attention that follows counts its splits there
     g.clear_n = B * Hq;
+    const PrefetchDepths& pf = prefetch_depths();
+    g.pf_units = pf.qkv;
     cudaError_t e = run_gemv(PRO_NORM_QUANT, EPI_STORE, 1, g, B, L, qx, qs, gacc);
     if (e != cudaSuccess) return cuda_fail(e, "QKV projection");
     if (T.qkv) {
@@ -340,6 +428,11 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
         a.kv_in_cache = true;
         e = launch_attn_group(a, L);
     } else {
+        if (pf.attn_o) {
+            // the O projection's weights, asked of L2 while attention runs
+            a.pf = w->w_o;
+            a.pf_bytes = ((size_t)H * NQ) & ~size_t(15);
+        }
         e = launch_attention(a, L);
     }
     if (e != cudaSuccess) return cuda_fail(e, "attention");
@@ -361,6 +454,7 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     g.ldy = H;
     g.tap_q = T.aq;
     g.tap_s = T.as;
+    g.pf_units = pf.o;
     e = run_gemv(PRO_QUANT, EPI_STORE, 1, g, B, L, qx, qs, gacc);
     if (e != cudaSuccess) return cuda_fail(e, "O projection");
     if (T.h1) {
@@ -383,6 +477,7 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     g.tap_x = reinterpret_cast<bf16*>(T.hn);
     g.tap_q = T.hq;
     g.tap_s = T.hs;
+    g.pf_units = pf.gate_up;
     e = run_gemv(PRO_NORM_QUANT, EPI_SWIGLU, 1, g, B, L, qx, qs, gacc);
     if (e != cudaSuccess) return cuda_fail(e, "Gate/Up projection");
     if (T.act) {
@@ -403,6 +498,7 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     g.ldy = H;
     g.tap_q = T.actq;
     g.tap_s = T.acts;
+    g.pf_units = pf.down;
     e = run_gemv(PRO_QUANT, EPI_STORE, c.down_k_splits, g, B, L, qx, qs, gacc);
     if (e != cudaSuccess) return cuda_fail(e, "down projection");
     return A8W8_OK;
@@ -799,21 +895,16 @@ static __device__ __align__(256) float g_noalloc_attn_scratch[A8W8_NOALLOC_SCRAT
 
 namespace {
 
-// Device address of the scratch array on the current device (looked up on
-// the first use per device), or nullptr with the error message set.
-float* noalloc_scratch_address(int dev) {
-    static float* addr[64];
-    if (dev < 0 || dev >= 64) return nullptr;
-    if (!addr[dev]) {
-        void* p = nullptr;
-        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_attn_scratch);
-        if (e != cudaSuccess) {
-            cuda_fail(e, "paged_decode_attention_bf16_noalloc: scratch address");
-            return nullptr;
-        }
-        addr[dev] = static_cast<float*>(p);
+// Device address of the scratch array in the current context (looked up on
+// the first use in each context, under the library's lock), or nullptr with
+// the error message set.
+float* noalloc_scratch_address() {
+    void* p = symbol_address(g_noalloc_attn_scratch);
+    if (!p) {
+        fail(A8W8_ERR_CUDA, "paged_decode_attention_bf16_noalloc: scratch address lookup failed");
+        return nullptr;
     }
-    return addr[dev];
+    return static_cast<float*>(p);
 }
 
 }  // namespace
@@ -843,11 +934,9 @@ a8w8_status paged_decode_attention_bf16_noalloc(const a8w8_bf16* q, const a8w8_b
                     "paged_decode_attention_bf16_noalloc: split-KV partials need %zu bytes, more than "
                     "the %zu-byte built-in scratch; use paged_decode_attention_bf16 with a workspace",
                     need, (size_t)A8W8_NOALLOC_SCRATCH_BYTES);
-    int dev = 0;
-    CUDA_TRY(cudaGetDevice(&dev), "paged_decode_attention_bf16_noalloc: current device");
     float* scratch = nullptr;
     if (need > 0) {
-        scratch = noalloc_scratch_address(dev);
+        scratch = noalloc_scratch_address();
         if (!scratch) return A8W8_ERR_CUDA;
     }
     AttnParams a = {};

@@ -29,6 +29,14 @@ template <int D>
 __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnParams p, int chunk,
                                                             int splits) {
     extern __shared__ __align__(16) unsigned char smem[];
+    if (p.pf && threadIdx.x == 0) {
+        // this CTA's share of the next kernel's weights, asked of L2 (no wait)
+        const size_t nb = (size_t)gridDim.x * gridDim.y * gridDim.z;
+        const size_t id = ((size_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+        const size_t units = p.pf_bytes / 16;
+        const size_t u0 = units * id / nb, u1 = units * (id + 1) / nb;
+        if (u1 > u0) l2_prefetch_bulk(static_cast<const char*>(p.pf) + u0 * 16, (u1 - u0) * 16);
+    }
     attn_item<D, kAttnThreads>(p, chunk, splits, blockIdx.x, blockIdx.y, blockIdx.z, smem, true);
 }
 
@@ -92,15 +100,15 @@ cudaError_t launch_attn_d(const AttnParams& p, const Launch& L) {
     const int chunk = attn_chunk(max_ctx, in_kernel);
     const int splits = attn_splits(max_ctx, in_kernel);
     const size_t smem = attn_item_smem_bytes(chunk, D);
-    static int configured_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(attn_kernel<D>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)attn_item_smem_bytes(256, 128));
+    {
+        // the shared-memory limit, set once per CUDA context
+        cudaError_t e = once_per_context(reinterpret_cast<const void*>(attn_kernel<D>), [&]() -> cudaError_t {
+            cudaError_t e = cudaFuncSetAttribute(attn_kernel<D>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)attn_item_smem_bytes(256, 128));
+            return e;
+        });
         if (e != cudaSuccess) return e;
-        configured_dev = dev;
     }
     AttnParams q = p;
     if (!in_kernel) q.tickets = nullptr;   // partials go to the combine kernel

@@ -444,14 +444,14 @@ int attn_group_splits(int max_ctx) { return max_ctx <= 0 ? 1 : (max_ctx + kGrpCh
 template <int D, int G>
 cudaError_t launch_grp_t(const AttnParams& p, int splits, const Launch& L) {
     const size_t smem = grp_smem(D, G).total;
-    static int configured_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(attn_group_kernel<D, G>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    {
+        // the shared-memory limit, set once per CUDA context
+        cudaError_t e = once_per_context(reinterpret_cast<const void*>(attn_group_kernel<D, G>), [&]() -> cudaError_t {
+            cudaError_t e = cudaFuncSetAttribute(attn_group_kernel<D, G>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            return e;
+        });
         if (e != cudaSuccess) return e;
-        configured_dev = dev;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(splits, p.Hkv, p.B);

@@ -851,15 +851,15 @@ cudaError_t launch_attn_i8_d(const AttnI8Params& P, const Launch& L) {
     const int chunk = attn_chunk(max_ctx, in_kernel);
     const int splits = attn_splits(max_ctx, in_kernel);
     const size_t smem = i8_item_smem_bytes(chunk, D);
-    static int configured_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(attn_i8_kernel<D>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)i8_item_smem_bytes(256, 128));
+    {
+        // the shared-memory limit, set once per CUDA context
+        cudaError_t e = once_per_context(reinterpret_cast<const void*>(attn_i8_kernel<D>), [&]() -> cudaError_t {
+            cudaError_t e = cudaFuncSetAttribute(attn_i8_kernel<D>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)i8_item_smem_bytes(256, 128));
+            return e;
+        });
         if (e != cudaSuccess) return e;
-        configured_dev = dev;
     }
     if (smem > i8_item_smem_bytes(256, 128)) return cudaErrorInvalidValue;
     AttnI8Params q = P;
@@ -876,14 +876,14 @@ cudaError_t launch_attn_i8_d(const AttnI8Params& P, const Launch& L) {
 template <int D, int G>
 cudaError_t launch_g8_t(const AttnI8Params& P, int splits, const Launch& L) {
     const size_t smem = g8_smem(D, G).total;
-    static int configured_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(attn_i8_group_kernel<D, G>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    {
+        // the shared-memory limit, set once per CUDA context
+        cudaError_t e = once_per_context(reinterpret_cast<const void*>(attn_i8_group_kernel<D, G>), [&]() -> cudaError_t {
+            cudaError_t e = cudaFuncSetAttribute(attn_i8_group_kernel<D, G>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            return e;
+        });
         if (e != cudaSuccess) return e;
-        configured_dev = dev;
     }
     return launch_i8(attn_i8_group_kernel<D, G>, dim3(splits, P.a.Hkv, P.a.B), dim3(kG8Threads),
                      smem, L, P, splits);

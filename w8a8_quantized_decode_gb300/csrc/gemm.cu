@@ -289,14 +289,14 @@ cudaError_t launch_gemm_projection(int epilogue, int k_splits, const GemvParams&
     if (epilogue == EPI_SWIGLU && k_splits != 1) return cudaErrorInvalidValue;
     const int Nc = epilogue == EPI_SWIGLU ? 2 * p.N : p.N;
     const size_t smem = gemm_smem().total;
-    static int configured_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_i8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)smem);
+    {
+        // the shared-memory limit, set once per CUDA context
+        cudaError_t e = once_per_context(reinterpret_cast<const void*>(gemm_i8_kernel), [&]() -> cudaError_t {
+            cudaError_t e = cudaFuncSetAttribute(gemm_i8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)smem);
+            return e;
+        });
         if (e != cudaSuccess) return e;
-        configured_dev = dev;
     }
     const dim3 grid((p.M + kBM - 1) / kBM, (Nc + kBN - 1) / kBN);
     const int Ks = p.K / k_splits;

@@ -204,17 +204,17 @@ cudaError_t launch_t(const GemvParams& p, const Launch& L) {
     const size_t smem =
         stream ? smem_layout(BT, nseg, KS, p.K, p.N, G, stream_threads(BT), stream_ring_bytes<BT>()).total
                : smem_layout(BT, nseg, KS, p.K, p.N, G, kGenThreads).total;
-    static int configured_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(gemv_kernel<BT, PRO, EPI, KS>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(gemv_stream_kernel<BT, PRO, EPI, KS>,
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+    {
+        // the shared-memory limit, set once per CUDA context
+        cudaError_t e = once_per_context(reinterpret_cast<const void*>(gemv_kernel<BT, PRO, EPI, KS>), [&]() -> cudaError_t {
+            cudaError_t e = cudaFuncSetAttribute(gemv_kernel<BT, PRO, EPI, KS>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(gemv_stream_kernel<BT, PRO, EPI, KS>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+            return e;
+        });
         if (e != cudaSuccess) return e;
-        configured_dev = dev;
     }
     if (smem > (size_t)kMaxDynSmem) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};

@@ -183,15 +183,15 @@ cudaError_t launch_bf(Kern kern, dim3 grid, dim3 block, size_t smem, const Launc
 
 template <int BT, bool SWIGLU>
 cudaError_t launch_bf_t(const Bf16GemvParams& p, const Launch& L) {
-    static int configured_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(gemv_bf16_kernel<BT, SWIGLU>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kBfSmemMax);
+    {
+        // the shared-memory limit, set once per CUDA context
+        cudaError_t e = once_per_context(reinterpret_cast<const void*>(gemv_bf16_kernel<BT, SWIGLU>), [&]() -> cudaError_t {
+            cudaError_t e = cudaFuncSetAttribute(gemv_bf16_kernel<BT, SWIGLU>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)kBfSmemMax);
+            return e;
+        });
         if (e != cudaSuccess) return e;
-        configured_dev = dev;
     }
     const size_t smem = (size_t)BT * p.K * 2;
     if (smem > kBfSmemMax) return cudaErrorInvalidValue;

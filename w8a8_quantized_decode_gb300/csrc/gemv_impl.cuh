@@ -436,6 +436,21 @@ __device__ __forceinline__ bool stream_gemv(const GemvParams& p, unsigned char* 
 #pragma unroll
     for (int b = 0; b < NBPRE; ++b) issue_batch(b);
 
+    // and the head of this warp's run asked of L2, so that HBM keeps
+    // streaming while the CTA waits for its producer and runs the prologue
+    // (the ring alone holds NB batches per lane)
+    if (p.pf_units > 0 && lane == 0 && n > 0) {
+        int u = u0, left = min(n, p.pf_units);
+        while (left > 0) {
+            const int seg = u / useg, off = u - seg * useg;
+            const int cnt = min(left, useg - off);
+            l2_prefetch_bulk(p.W + (size_t)(seg * N + o0) * K + (size_t)off * kUnit,
+                             (size_t)cnt * kUnit);
+            u += cnt;
+            left -= cnt;
+        }
+    }
+
     if (!wait()) {
         cp_async_wait_all();
         return false;

@@ -298,14 +298,14 @@ cudaError_t launch_mma_t(const GemvParams& p, const Launch& L) {
     const int G = L.num_sms;
     const size_t smem = mma_smem(EPI == EPI_SWIGLU ? 2 : 1, KS, p.N, G).total;
     if (smem > (size_t)kMaxDynSmem) return cudaErrorInvalidValue;
-    static int configured_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(gemv_mma_kernel<EPI, KS>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+    {
+        // the shared-memory limit, set once per CUDA context
+        cudaError_t e = once_per_context(reinterpret_cast<const void*>(gemv_mma_kernel<EPI, KS>), [&]() -> cudaError_t {
+            cudaError_t e = cudaFuncSetAttribute(gemv_mma_kernel<EPI, KS>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+            return e;
+        });
         if (e != cudaSuccess) return e;
-        configured_dev = dev;
     }
     return launch_k(gemv_mma_kernel<EPI, KS>, G, kMmaThreads, smem, p, L);
 }
@@ -314,14 +314,14 @@ template <int PRO>
 cudaError_t launch_prep_t(const GemvParams& p, int8_t* xq, float* xs, const Launch& L) {
     const size_t smem = smem_layout(1, 1, 1, p.K, 1, 1, kPrepThreads).total;
     if (smem > (size_t)kMaxDynSmem) return cudaErrorInvalidValue;
-    static int configured_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_dev != dev) {
-        cudaError_t e = cudaFuncSetAttribute(quant_prep_kernel<PRO>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+    {
+        // the shared-memory limit, set once per CUDA context
+        cudaError_t e = once_per_context(reinterpret_cast<const void*>(quant_prep_kernel<PRO>), [&]() -> cudaError_t {
+            cudaError_t e = cudaFuncSetAttribute(quant_prep_kernel<PRO>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
+            return e;
+        });
         if (e != cudaSuccess) return e;
-        configured_dev = dev;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.M);

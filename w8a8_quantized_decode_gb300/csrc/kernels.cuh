@@ -2,6 +2,7 @@
 #pragma once
 
 #include <stddef.h>
+#include <functional>
 #include <stdint.h>
 
 #include "common.cuh"
@@ -15,6 +16,12 @@ struct Launch {
     int num_sms;
     bool pdl;
 };
+
+// Runs `setup` (a cudaFuncSetAttribute, a symbol lookup) once per CUDA
+// context and key, under a lock: later calls in the same context return at
+// once; a failed setup is retried on the next call. A device reset destroys
+// the context, so the setup runs again in the new one.
+cudaError_t once_per_context(const void* key, const std::function<cudaError_t()>& setup);
 
 // ---------------------------------------------------------------------------
 // Per-row quantisation
@@ -54,6 +61,8 @@ struct GemvParams {
     unsigned* err;          // device error word (timeouts)
     unsigned* clear;        // CTA 0 zeroes clear[0, clear_n) after the wait (or null)
     int clear_n;
+    int pf_units;           // streaming kernel: 512-byte units of each warp's run
+                            // asked of L2 before the dependency wait (0: none)
 };
 
 // Largest batch tile one launch handles; bigger batches are tiled by the host.
@@ -112,6 +121,9 @@ struct AttnParams {
     bf16* tap_k_rot;        // [B, Hkv, D] or null
     bool kv_in_cache;       // every row's new K/V was written by launch_kv_prep
                             // (prefill: rows attend to each other's tokens)
+    const void* pf;         // decode layer: bytes the next kernel streams (the O
+    size_t pf_bytes;        // projection's weights), asked of L2 by the CTAs
+                            // in equal shares at their start (null: none)
 };
 
 // Tokens per attention CTA and the number of CTAs per (request, KV head).

@@ -64,14 +64,14 @@ __global__ void __launch_bounds__(kLmThreads, 1) lmhead_kernel(const LmHeadParam
 template <int BT>
 cudaError_t launch_lm_t(const LmHeadParams& p, const Launch& L) {
     auto kern = lmhead_kernel<BT>;
-    static int configured_dev = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_dev != dev) {
-        cudaError_t e =
-            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    {
+        // the shared-memory limit, set once per CUDA context
+        cudaError_t e = once_per_context(reinterpret_cast<const void*>(kern), [&]() -> cudaError_t {
+            cudaError_t e =
+                cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+            return e;
+        });
         if (e != cudaSuccess) return e;
-        configured_dev = dev;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(L.num_sms);
