@@ -260,8 +260,9 @@ def _check_swiglu(gpu, ref, x, W_gu, what):
     E = proj_error_bound(x, W_gu, K)
     Eg, Eu = E[:, :I], E[:, I:]
     xf = bf16_to_f64(x)
-    g = np.concatenate([xf @ bf16_to_f64(W_gu[i:i + 4096]).T for i in range(0, I, 4096)], 1)
-    u = np.concatenate([xf @ bf16_to_f64(W_gu[I + i:I + i + 4096]).T for i in range(0, I, 4096)], 1)
+    g = np.concatenate([xf @ bf16_to_f64(W_gu[i:min(i + 4096, I)]).T for i in range(0, I, 4096)], 1)
+    u = np.concatenate([xf @ bf16_to_f64(W_gu[I + i:I + min(i + 4096, I)]).T
+                        for i in range(0, I, 4096)], 1)
     a, b = bf16_to_f64(gpu), bf16_to_f64(ref)
     lim = (bf16_ulp_at(np.maximum(np.abs(a), np.abs(b))) + 1.1 * (np.abs(u) + Eu) * Eg
            + (np.abs(g) + Eg) * Eu)
