@@ -308,23 +308,6 @@ struct KvI8 {
     float* v_scale;
 };
 
-// L2 prefetch depths of the batch-1/2 decode layer: 512-byte units of each
-// warp's weight run that the QKV, O, Gate/Up and down kernels ask of L2 before
-// their dependency wait, and whether the attention kernel asks for the O
-// projection's weights.
-struct PrefetchDepths {
-    int qkv, o, gate_up, down, attn_o;
-};
-const PrefetchDepths& prefetch_depths() {
-    static const PrefetchDepths d = [] {
-        PrefetchDepths v = {16, 16, 16, 16, 1};
-        if (const char* s = std::getenv("A8W8_PF"))
-            std::sscanf(s, "%d,%d,%d,%d,%d", &v.qkv, &v.o, &v.gate_up, &v.down, &v.attn_o);
-        return v;
-    }();
-    return d;
-}
-
 // Enqueues one decode layer (no validation). With `kv8` the layer's cache is
 // the INT8 one (k_cache / v_cache unused).
 a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int B, bf16* hidden,
@@ -363,8 +346,6 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     g.tap_s = T.xs;
     g.clear = att_tk;   // the attention that follows counts its splits there
     g.clear_n = B * Hq;
-    const PrefetchDepths& pf = prefetch_depths();
-    g.pf_units = pf.qkv;
     cudaError_t e = run_gemv(PRO_NORM_QUANT, EPI_STORE, 1, g, B, L, qx, qs, gacc);
     if (e != cudaSuccess) return cuda_fail(e, "QKV projection");
     if (T.qkv) {
@@ -428,11 +409,6 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
         a.kv_in_cache = true;
         e = launch_attn_group(a, L);
     } else {
-        if (pf.attn_o) {
-            // the O projection's weights, asked of L2 while attention runs
-            a.pf = w->w_o;
-            a.pf_bytes = ((size_t)H * NQ) & ~size_t(15);
-        }
         e = launch_attention(a, L);
     }
     if (e != cudaSuccess) return cuda_fail(e, "attention");
@@ -454,7 +430,6 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     g.ldy = H;
     g.tap_q = T.aq;
     g.tap_s = T.as;
-    g.pf_units = pf.o;
     e = run_gemv(PRO_QUANT, EPI_STORE, 1, g, B, L, qx, qs, gacc);
     if (e != cudaSuccess) return cuda_fail(e, "O projection");
     if (T.h1) {
@@ -477,7 +452,6 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     g.tap_x = reinterpret_cast<bf16*>(T.hn);
     g.tap_q = T.hq;
     g.tap_s = T.hs;
-    g.pf_units = pf.gate_up;
     e = run_gemv(PRO_NORM_QUANT, EPI_SWIGLU, 1, g, B, L, qx, qs, gacc);
     if (e != cudaSuccess) return cuda_fail(e, "Gate/Up projection");
     if (T.act) {
@@ -498,7 +472,6 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     g.ldy = H;
     g.tap_q = T.actq;
     g.tap_s = T.acts;
-    g.pf_units = pf.down;
     e = run_gemv(PRO_QUANT, EPI_STORE, c.down_k_splits, g, B, L, qx, qs, gacc);
     if (e != cudaSuccess) return cuda_fail(e, "down projection");
     return A8W8_OK;

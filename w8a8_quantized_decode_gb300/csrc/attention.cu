@@ -29,14 +29,6 @@ template <int D>
 __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnParams p, int chunk,
                                                             int splits) {
     extern __shared__ __align__(16) unsigned char smem[];
-    if (p.pf && threadIdx.x == 0) {
-        // this CTA's share of the next kernel's weights, asked of L2 (no wait)
-        const size_t nb = (size_t)gridDim.x * gridDim.y * gridDim.z;
-        const size_t id = ((size_t)blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
-        const size_t units = p.pf_bytes / 16;
-        const size_t u0 = units * id / nb, u1 = units * (id + 1) / nb;
-        if (u1 > u0) l2_prefetch_bulk(static_cast<const char*>(p.pf) + u0 * 16, (u1 - u0) * 16);
-    }
     attn_item<D, kAttnThreads>(p, chunk, splits, blockIdx.x, blockIdx.y, blockIdx.z, smem, true);
 }
 

@@ -77,24 +77,6 @@ __device__ __forceinline__ int4 lds_v4(uint32_t s) {
 }
 
 // L2 policy for data read once per step (weights): evict first.
-// Asks L2 to fetch [p, p + bytes) from HBM without waiting for it: no
-// registers, shared memory or completion tracking are involved, so a kernel
-// can queue the weights it will stream before its dependency wait and let
-// HBM work through that wait and the activation prologue. p 16-byte aligned,
-// bytes a multiple of 16; issued in pieces of at most 32 KB.
-__device__ __forceinline__ void l2_prefetch_bulk(const void* p, size_t bytes) {
-    const char* a = static_cast<const char*>(p);
-    while (bytes > 0) {
-        const uint32_t n = bytes > 32768 ? 32768u : (uint32_t)bytes;
-        asm volatile(
-            "{\n\t.reg .u64 g;\n\tcvta.to.global.u64 g, %0;\n\t"
-            "cp.async.bulk.prefetch.L2.global [g], %1;\n\t}" ::"l"(a), "r"(n)
-            : "memory");
-        a += n;
-        bytes -= n;
-    }
-}
-
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));

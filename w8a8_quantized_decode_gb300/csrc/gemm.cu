@@ -20,6 +20,8 @@
 //     accumulators are exact; they are converted to INT32 and added into an
 //     INT32 tile in shared memory every 16 steps, which is written out at the
 //     end.
+#include <cstdlib>
+
 #include "gemv_impl.cuh"
 
 namespace a8w8 {
@@ -300,10 +302,17 @@ cudaError_t launch_gemm_projection(int epilogue, int k_splits, const GemvParams&
     }
     const dim3 grid((p.M + kBM - 1) / kBM, (Nc + kBN - 1) / kBN);
     const int Ks = p.K / k_splits;
+    static const bool use_mma_sync = [] {
+        const char* v = std::getenv("A8W8_GEMM");
+        return v && v[0] == 'm';
+    }();
     for (int s = 0; s < k_splits; ++s) {
-        cudaError_t e = launch_pdl(gemm_i8_kernel, grid, dim3(kGemmThreads), smem, L, p.xq, p.K, p.W,
-                                   p.K, p.M, Nc, s * Ks, (s + 1) * Ks,
-                                   acc + (size_t)s * p.M * Nc, Nc);
+        cudaError_t e = use_mma_sync
+                            ? launch_pdl(gemm_i8_kernel, grid, dim3(kGemmThreads), smem, L, p.xq, p.K,
+                                         p.W, p.K, p.M, Nc, s * Ks, (s + 1) * Ks,
+                                         acc + (size_t)s * p.M * Nc, Nc)
+                            : launch_gemm_tc(p.xq, p.M, p.W, Nc, p.K, s * Ks, (s + 1) * Ks,
+                                             acc + (size_t)s * p.M * Nc, Nc, p.err, L);
         if (e != cudaSuccess) return e;
     }
     const long total = (long)p.M * p.N;

@@ -1,0 +1,365 @@
+// gemm_tc.cu -- INT8 x INT8 -> INT32 projections of a prefill chunk on the
+// fifth-generation tensor cores (tcgen05, accumulators in tensor memory).
+//
+// Arithmetic ("perf(qwen3-a8w8): optimize decode scheduling and data paths",
+// pypto-lib PR #810, "Gate/Up INT8 path": INT8 x INT8 products accumulated
+// exactly, dequantised in FP32 afterwards): C[m][n] = sum_{k in [k0, k1)}
+// X[m][k] * W[n][k], X the INT8 activation codes [M, K], W the INT8 weights
+// [N, K]. sm_103a has no INT8 kind of tcgen05.mma, so each code is fed as its
+// FP16 image (exact: |code| <= 128 needs 8 significant bits) to the kind::f16
+// MMA with FP32 accumulators. Every product is an integer of magnitude below
+// 2^14 and 1024 of them sum to below 2^24, where FP32 holds every integer, so
+// each 1024-column chunk of K accumulates exactly; the chunk's FP32 result is
+// converted to INT32 and added to an INT32 running sum.
+//
+// One CTA computes a 128 x 128 tile of C^T (128 weight rows = the MMA's M and
+// the tensor-memory lanes, 128 activation rows = the MMA's N and columns) over
+// K steps of 64 columns, with warp roles:
+//   warp 0      TMA: the INT8 tiles of W and X for each step (cp.async.bulk
+//               .tensor, 8 KB each) into a 4-stage ring;
+//   warp 1      allocates 512 tensor-memory columns; one thread issues the
+//               four m128 n128 k16 MMAs of a step and commits them;
+//   warps 2-5   convert each step's INT8 tiles to FP16 in the 128-byte
+//               swizzled K-major layout the MMA reads (a 3-stage ring);
+//   warps 6-9   drain each finished chunk: FP32 accumulators (two buffers of
+//               128 columns, so the MMAs of the next chunk proceed meanwhile)
+//               to INT32, added into a 128-column INT32 sum in tensor memory;
+//               after the last chunk they write C.
+// Every wait is bounded (2 s): on a timeout the CTA sets the device error
+// word's timeout bit, every role stops, the in-flight copies and MMAs are
+// waited for (again bounded) and the tensor memory is freed.
+#include <cuda.h>
+
+#include "kernels.cuh"
+#include "tc_common.cuh"
+
+namespace a8w8 {
+
+namespace {
+
+using namespace tc;
+
+constexpr int kTM = 128;          // weight rows per tile
+constexpr int kTN = 128;          // activation rows per tile
+constexpr int kTK = 64;           // K columns per step
+constexpr int kS8 = 4;            // INT8 stages
+constexpr int kS16 = 3;           // FP16 stages
+constexpr int kChunkSteps = 16;   // steps per exact FP32 chunk (1024 columns)
+constexpr int kTcThreads = 320;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSumCol = 256;  // INT32 sums at columns [256, 384)
+constexpr int kTile8 = kTM * kTK;          // 8192 bytes
+constexpr int kTile16 = kTM * kTK * 2;     // 16384 bytes
+
+struct TcSmem {
+    size_t w8, x8, w16, x16, bars, total;
+};
+__host__ __device__ constexpr TcSmem tc_smem() {
+    TcSmem s{};
+    s.w16 = 0;                                        // [kS16][16 KB], 1024-aligned
+    s.x16 = s.w16 + (size_t)kS16 * kTile16;
+    s.w8 = s.x16 + (size_t)kS16 * kTile16;            // [kS8][8 KB]
+    s.x8 = s.w8 + (size_t)kS8 * kTile8;
+    s.bars = s.x8 + (size_t)kS8 * kTile8;
+    // barriers: full8, empty8 [kS8]; full16, empty16 [kS16]; accfull,
+    // accempty [2]; done; then the tensor-memory base and the abort flag
+    s.total = s.bars + (size_t)(2 * kS8 + 2 * kS16 + 4 + 1) * 8 + 16;
+    return s;
+}
+// dynamic shared memory requested: the layout plus room to align it to 1024
+constexpr size_t kTcSmemBytes = tc_smem().total + 1024;
+
+// 16 INT8 codes -> 16 FP16 values (exact): byte v becomes the FP16 number
+// 1024 + (v + 128), from which 1152 is subtracted.
+__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    const uint32_t l = __byte_perm(u, 0x64646464u, 0x4140);
+    const uint32_t h = __byte_perm(u, 0x64646464u, 0x4342);
+    const __half2 off = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+    const __half2 lf = __hsub2(*reinterpret_cast<const __half2*>(&l), off);
+    const __half2 hf = __hsub2(*reinterpret_cast<const __half2*>(&h), off);
+    lo = *reinterpret_cast<const uint32_t*>(&lf);
+    hi = *reinterpret_cast<const uint32_t*>(&hf);
+}
+
+// Converts one 128 x 64 INT8 tile (row pitch 64 bytes) into the FP16
+// 128-byte-swizzled K-major tile, thread t of 128 taking the 16-byte pieces
+// t, t + 128, t + 256, t + 384 (piece p: row p / 4, columns 16 (p % 4) ..).
+__device__ __forceinline__ void convert_tile(const int8_t* src, unsigned char* dst, int t) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int p = t + 128 * i;
+        const int r = p >> 2, q = p & 3;
+        const int4 v = *reinterpret_cast<const int4*>(src + r * kTK + 16 * q);
+        uint4 a, b;
+        i8x4_to_f16x4((uint32_t)v.x, a.x, a.y);
+        i8x4_to_f16x4((uint32_t)v.y, a.z, a.w);
+        i8x4_to_f16x4((uint32_t)v.z, b.x, b.y);
+        i8x4_to_f16x4((uint32_t)v.w, b.z, b.w);
+        // FP16 chunks 2q and 2q + 1 of row r, swizzled within the 8-row atom
+        unsigned char* row = dst + (r >> 3) * 1024 + (r & 7) * 128;
+        *reinterpret_cast<uint4*>(row + (((2 * q) ^ (r & 7)) << 4)) = a;
+        *reinterpret_cast<uint4*>(row + (((2 * q + 1) ^ (r & 7)) << 4)) = b;
+    }
+}
+
+// The timeout bit of the device error word (A8W8_DEVERR_TIMEOUT).
+constexpr unsigned kErrTimeout = 0x20u;
+
+__device__ __forceinline__ void set_timeout(unsigned* err, volatile int* abort) {
+    *abort = 1;
+    set_error(err, kErrTimeout);
+}
+
+}  // namespace
+
+namespace {
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
+                   int M, int N, int k0, int steps, int32_t* __restrict__ C, int ldc,
+                   unsigned* err) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // the swizzled tiles need 1024-byte aligned bases
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    constexpr TcSmem L = tc_smem();
+    unsigned char* w16 = smem + L.w16;
+    unsigned char* x16 = smem + L.x16;
+    int8_t* w8 = reinterpret_cast<int8_t*>(smem + L.w8);
+    int8_t* x8 = reinterpret_cast<int8_t*>(smem + L.x8);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
+    uint64_t* full8 = bars;
+    uint64_t* empty8 = full8 + kS8;
+    uint64_t* full16 = empty8 + kS8;
+    uint64_t* empty16 = full16 + kS16;
+    uint64_t* accfull = empty16 + kS16;
+    uint64_t* accempty = accfull + 2;
+    uint64_t* done = accempty + 2;
+    uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(done + 1);
+    volatile int* abort = reinterpret_cast<volatile int*>(tmem_base_smem + 1);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int m0 = blockIdx.x * kTN;      // activation rows of the tile
+    const int n0 = blockIdx.y * kTM;      // weight rows of the tile
+    const int nchunks = (steps + kChunkSteps - 1) / kChunkSteps;
+
+    if (tid == 0) {
+        for (int i = 0; i < kS8; ++i) {
+            mbar_init(&full8[i], 1);      // the producer's expect-tx arrival
+            mbar_init(&empty8[i], 4);     // one arrival per converter warp
+        }
+        for (int i = 0; i < kS16; ++i) {
+            mbar_init(&full16[i], 4);     // one arrival per converter warp
+            mbar_init(&empty16[i], 1);    // the MMA commit
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&accfull[i], 1);    // the MMA commit
+            mbar_init(&accempty[i], 4);   // one arrival per drain warp
+        }
+        mbar_init(done, 1);
+        *abort = 0;
+        mbar_init_fence();
+        tma_prefetch_map(&map_w);
+        tma_prefetch_map(&map_x);
+    }
+    if (warp == 1) tmem_alloc(tmem_base_smem, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_base_smem;
+
+    // the activation codes come from the preceding kernel
+    pdl_wait();
+    pdl_trigger();
+
+    if (warp == 0) {
+        // ---- TMA producer ----
+        int issued = 0;
+        if (lane == 0) {
+            for (int s = 0; s < steps; ++s) {
+                const int st = s % kS8;
+                if (s >= kS8 && !mbar_wait(&empty8[st], ((s / kS8) - 1) & 1, abort)) {
+                    if (!*abort) set_timeout(err, abort);
+                    break;
+                }
+                mbar_arrive_expect_tx(&full8[st], 2 * kTile8);
+                tma_load_2d(w8 + (size_t)st * kTile8, &map_w, k0 + s * kTK, n0, &full8[st]);
+                tma_load_2d(x8 + (size_t)st * kTile8, &map_x, k0 + s * kTK, m0, &full8[st]);
+                issued = s + 1;
+            }
+            // every issued copy has landed before the CTA may exit (immediate
+            // on the normal path, where the converters consumed them all)
+            for (int s = issued > kS8 ? issued - kS8 : 0; s < issued; ++s)
+                mbar_wait(&full8[s % kS8], (s / kS8) & 1, nullptr);
+        }
+    } else if (warp == 1) {
+        // ---- MMA issuer ----
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16_f32(kTM, kTN);
+            for (int s = 0; s < steps; ++s) {
+                const int c = s / kChunkSteps, buf = c & 1;
+                const bool first = s % kChunkSteps == 0;
+                if (first && c >= 2 && !mbar_wait(&accempty[buf], ((c >> 1) - 1) & 1, abort)) {
+                    if (!*abort) set_timeout(err, abort);
+                    break;
+                }
+                const int st = s % kS16;
+                if (!mbar_wait(&full16[st], (s / kS16) & 1, abort)) {
+                    if (!*abort) set_timeout(err, abort);
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t ad = sw128_kmajor_desc(smem_u32(w16 + (size_t)st * kTile16));
+                const uint64_t bd = sw128_kmajor_desc(smem_u32(x16 + (size_t)st * kTile16));
+                const uint32_t d = tmem + (uint32_t)(buf * kTN);
+#pragma unroll
+                for (int j = 0; j < kTK / 16; ++j)
+                    mma_f16(d, ad + 2 * j, bd + 2 * j, idesc, (first && j == 0) ? 0u : 1u);
+                mma_commit(&empty16[st]);
+                if (s % kChunkSteps == kChunkSteps - 1 || s == steps - 1) mma_commit(&accfull[buf]);
+            }
+            // no MMA may still be running when the tensor memory is freed
+            mma_commit(done);
+            mbar_wait(done, 0, nullptr);
+        }
+    } else if (warp < 6) {
+        // ---- converters: INT8 tiles -> FP16 swizzled tiles ----
+        const int t = tid - 64;
+        for (int s = 0; s < steps; ++s) {
+            const int st8 = s % kS8, st16 = s % kS16;
+            bool ok = mbar_wait(&full8[st8], (s / kS8) & 1, abort);
+            if (ok && s >= kS16) ok = mbar_wait(&empty16[st16], ((s / kS16) - 1) & 1, abort);
+            if (!ok) {
+                if (!*abort) set_timeout(err, abort);
+                break;
+            }
+            convert_tile(w8 + (size_t)st8 * kTile8, w16 + (size_t)st16 * kTile16, t);
+            convert_tile(x8 + (size_t)st8 * kTile8, x16 + (size_t)st16 * kTile16, t);
+            fence_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&empty8[st8]);
+                mbar_arrive(&full16[st16]);
+            }
+        }
+    } else {
+        // ---- drain: FP32 chunk -> INT32 sum; after the last chunk, C ----
+        const int q = warp & 3;                       // lanes 32q .. 32q + 31
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
+        const int n = n0 + 32 * q + lane;             // this thread's weight row
+        for (int c = 0; c < nchunks; ++c) {
+            const int buf = c & 1;
+            if (!mbar_wait(&accfull[buf], (c >> 1) & 1, abort)) {
+                if (!*abort) set_timeout(err, abort);
+                break;
+            }
+            tc_fence_after();
+            const bool last = c == nchunks - 1;
+#pragma unroll 1
+            for (int g = 0; g < kTN / 32; ++g) {
+                uint32_t f[32], a[32];
+                tmem_ld32(lane_base + (uint32_t)(buf * kTN + 32 * g), f);
+                if (c > 0) {
+                    tmem_ld32(lane_base + kSumCol + (uint32_t)(32 * g), a);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) a[i] = 0u;
+                }
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    a[i] = (uint32_t)((int)a[i] + __float2int_rn(__uint_as_float(f[i])));
+                if (!last) {
+                    tmem_st32(lane_base + kSumCol + (uint32_t)(32 * g), a);
+                } else if (n < N) {
+                    // C[m][n]: for each column the warp's lanes write 32
+                    // consecutive words
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const int m = m0 + 32 * g + i;
+                        if (m < M) C[(size_t)m * ldc + n] = (int32_t)a[i];
+                    }
+                }
+            }
+            if (!last) {
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&accempty[buf]);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// Driver entry point that encodes tensor maps (resolved once per process).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return static_cast<EncodeTiledFn>(nullptr);
+        return reinterpret_cast<EncodeTiledFn>(f);
+    }();
+    return fn;
+}
+
+// Tensor map of an INT8 matrix [rows, cols] (row pitch `ld` bytes) read in
+// boxes of 128 rows x 64 bytes, zero-filled beyond the matrix.
+bool make_i8_map(CUtensorMap* map, const int8_t* base, int rows, int cols, int ld) {
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld};
+    const cuuint32_t box[2] = {(cuuint32_t)kTK, 128u};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<int8_t*>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool gemm_tc_supported(int K, int k_splits) { return K > 0 && K % (kTK * k_splits) == 0; }
+
+cudaError_t launch_gemm_tc(const int8_t* X, int M, const int8_t* W, int N, int K, int k0, int k1,
+                           int32_t* C, int ldc, unsigned* err, const Launch& L) {
+    if (M <= 0 || N <= 0 || k1 <= k0) return cudaSuccess;
+    if ((k1 - k0) % kTK || k0 % kTK || K % 16 || (reinterpret_cast<uintptr_t>(X) & 15) ||
+        (reinterpret_cast<uintptr_t>(W) & 15))
+        return cudaErrorInvalidValue;
+    CUtensorMap mw, mx;
+    if (!make_i8_map(&mw, W, N, K, K) || !make_i8_map(&mx, X, M, K, K)) return cudaErrorInvalidValue;
+    {
+        // the shared-memory limit, set once per CUDA context
+        cudaError_t e = once_per_context(reinterpret_cast<const void*>(gemm_tc_kernel), [&]() {
+            return cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)kTcSmemBytes);
+        });
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((M + kTN - 1) / kTN, (N + kTM - 1) / kTM);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = kTcSmemBytes;
+    cfg.stream = L.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = L.pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, mw, mx, M, N, k0, (k1 - k0) / kTK, C, ldc, err);
+}
+
+}  // namespace a8w8

@@ -389,30 +389,12 @@ __device__ __forceinline__ bool stream_gemv(const GemvParams& p, unsigned char* 
     }
     int issued = 0;   // units requested so far
     const uint64_t pol = l2_evict_first_policy();
-    // L2 prefetch of run units [k, k + cnt) (clipped to the run), lane 0 only
-    const int pf = p.pf_units;
-    auto prefetch_units = [&](int k, int cnt) {
-        cnt = min(cnt, n - k);
-        int u = u0 + k;
-        while (cnt > 0) {
-            const int seg = u / useg, off = u - seg * useg;
-            const int c = min(cnt, useg - off);
-            l2_prefetch_bulk(p.W + (size_t)(seg * N + o0) * K + (size_t)off * kUnit,
-                             (size_t)c * kUnit);
-            u += c;
-            cnt -= c;
-        }
-    };
-    // one copy group per batch (empty when the stream is exhausted); with
-    // L2 prefetch on, every kPfStep units the prefetch window moves ahead
-    constexpr int kPfStep = 8;
+    // one copy group per batch (empty when the stream is exhausted)
     auto issue_batch = [&](int slot) {
 #pragma unroll
         for (int i = 0; i < UNR; ++i) {
             if (issued < n) {
                 cp_async16_s(ring + (uint32_t)((slot * UNR + i) * NT * 16), lp, pol);
-                if (pf > 0 && lane == 0 && issued % kPfStep == 0 && issued + pf < n)
-                    prefetch_units(issued + pf, kPfStep);
                 ++issued;
                 lp += kUnit;
                 if (--lleft == 0) {
@@ -453,12 +435,6 @@ __device__ __forceinline__ bool stream_gemv(const GemvParams& p, unsigned char* 
     // the activation loads of the prologue
 #pragma unroll
     for (int b = 0; b < NBPRE; ++b) issue_batch(b);
-
-    // and the head of this warp's run asked of L2, so that HBM keeps
-    // streaming while the CTA waits for its producer and runs the prologue
-    // (the ring alone holds NB batches per lane); the window then moves
-    // ahead with the stream (issue_batch)
-    if (pf > 0 && lane == 0 && n > 0) prefetch_units(0, pf);
 
     if (!wait()) {
         cp_async_wait_all();

@@ -61,8 +61,6 @@ struct GemvParams {
     unsigned* err;          // device error word (timeouts)
     unsigned* clear;        // CTA 0 zeroes clear[0, clear_n) after the wait (or null)
     int clear_n;
-    int pf_units;           // streaming kernel: 512-byte units of each warp's run
-                            // asked of L2 before the dependency wait (0: none)
 };
 
 // Largest batch tile one launch handles; bigger batches are tiled by the host.
@@ -83,6 +81,12 @@ cudaError_t launch_quant_prep(int prologue, const GemvParams& p, int8_t* xq, flo
 // INT32 result in acc (gemm_acc_bytes), then the dequantisation epilogue.
 // PRO_I8 input (p.xq, p.x_scale); K a multiple of 64 * k_splits.
 bool gemm_supported(int K, int k_splits);
+// tcgen05 form of the prefill GEMM: C[m][n] = sum_{k in [k0, k1)} X[m][k] *
+// W[n][k] (INT32, exact) for X [M, K], W [N, K] INT8 (rows of K bytes), into
+// C [M, ldc]; k0 and k1 - k0 multiples of 64.
+bool gemm_tc_supported(int K, int k_splits);
+cudaError_t launch_gemm_tc(const int8_t* X, int M, const int8_t* W, int N, int K, int k0, int k1,
+                           int32_t* C, int ldc, unsigned* err, const Launch& L);
 size_t gemm_acc_bytes(int M, int N, int epilogue, int k_splits);
 cudaError_t launch_gemm_projection(int epilogue, int k_splits, const GemvParams& p, int32_t* acc,
                                    const Launch& L);
@@ -121,9 +125,6 @@ struct AttnParams {
     bf16* tap_k_rot;        // [B, Hkv, D] or null
     bool kv_in_cache;       // every row's new K/V was written by launch_kv_prep
                             // (prefill: rows attend to each other's tokens)
-    const void* pf;         // decode layer: bytes the next kernel streams (the O
-    size_t pf_bytes;        // projection's weights), asked of L2 by the CTAs
-                            // in equal shares at their start (null: none)
 };
 
 // Tokens per attention CTA and the number of CTAs per (request, KV head).
