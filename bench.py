@@ -732,8 +732,28 @@ def run_prefill(args, cfg):
                 e1.synchronize()
                 times.append(e0.elapsed_time(e1))
         errs = a8w8.read_device_errors(stream)
+        # the dominant contraction alone: the Gate/Up GEMM's exact INT32
+        # product (tcgen05) on the chunk's quantised rows, CUDA events on
+        # `stream` around `reps` back-to-back launches
+        xq = torch.randint(-127, 128, (M, H), dtype=torch.int8, device=device)
+        acc = torch.empty((M, 2 * cfg["intermediate"]), dtype=torch.int32, device=device)
+        for _ in range(2):
+            a8w8.a8w8_matmul_i8(xq, w["w_gate_up"], out=acc, stream=stream)
+        reps = 5
+        g0 = torch.cuda.Event(enable_timing=True)
+        g1 = torch.cuda.Event(enable_timing=True)
+        stream.synchronize()
+        g0.record(stream)
+        for _ in range(reps):
+            a8w8.a8w8_matmul_i8(xq, w["w_gate_up"], out=acc, stream=stream)
+        g1.record(stream)
+        g1.synchronize()
+        gu_ms = g0.elapsed_time(g1) / reps
+        del acc
     ms = sum(times) / len(times)
     ms = max_over_ranks(ms, device)
+    gu_flop = 2.0 * M * 2 * cfg["intermediate"] * H
+    gu_tflops = gu_flop / (gu_ms * 1e-3) / 1e12
     ops = 2.0 * M * (cfg["hidden"] * ((cfg["num_q_heads"] + 2 * Hkv) * D) +
                       cfg["num_q_heads"] * D * cfg["hidden"] + 2 * cfg["intermediate"] * cfg["hidden"]
                       + cfg["intermediate"] * cfg["hidden"])
@@ -757,11 +777,14 @@ def run_prefill(args, cfg):
             "tokens_per_s": job_rate(M, ms, world),
             "int8_ops_per_s_e12": tops,
             "attention_flop": attn_flops,
+            "layer_tflops": tops, "layer_frac_of_tensor_peak": tops / tpk["tflops"],
             "roofline": {"bound": "tensor",
-                         "kernel": "whole prefill layer (4 projections as FP16 mma.sync GEMMs on "
-                                   "exact images of the INT8 codes, epilogues, attention)",
-                         "achieved": tops, "peak": tpk["tflops"], "unit": "TFLOP/s",
-                         "frac": tops / tpk["tflops"], "traffic": None,
+                         "kernel": "Gate/Up GEMM, exact INT32 product of 2048 x 5120 by "
+                                   "34816 x 5120 INT8 (gemm_tc_kernel: tcgen05.mma kind::f16 on "
+                                   "exact FP16 images, TMA-fed, TMEM accumulators)",
+                         "achieved": gu_tflops, "peak": tpk["tflops"], "unit": "TFLOP/s",
+                         "frac": gu_tflops / tpk["tflops"], "traffic": None,
+                         "flop_per_launch": gu_flop, "ms_per_launch": gu_ms,
                          "peak_source": tpk["source"]},
             "e2e": None,
             "gpu_launches": n_launch * args.steps,
@@ -865,7 +888,7 @@ def run_ttft(args, cfg):
                        "page_size": page, "l2": "inputs larger than L2 (14.8 GB of weights)"},
             "tokens_per_s": P / (ms * 1e-3),
             "roofline": {"bound": "tensor",
-                         "kernel": "whole prefill (projections as FP16 mma.sync GEMMs on exact "
+                         "kernel": "whole prefill (projections as tcgen05 GEMMs on exact "
                                    "images of the INT8 codes, epilogues, attention, LM head row)",
                          "achieved": tops, "peak": tpk["tflops"], "unit": "TFLOP/s",
                          "frac": tops / tpk["tflops"], "traffic": None, "peak_source": tpk["source"]},

@@ -194,6 +194,18 @@ a8w8_status a8w8_gate_up_swiglu(const int8_t* xq, const float* x_scale, int M, i
                                 const int8_t* W_gu, const float* s_gu, int I,
                                 a8w8_bf16* act, int32_t* acc_out, void* stream);
 
+/* The exact INT32 product of a prefill chunk's quantised rows with an INT8
+ * weight matrix, on the tensor cores ([LIB-810] "Gate/Up INT8 path": INT8 x
+ * INT8 -> INT32 matmuls; the step of a8w8_linear before dequantisation):
+ *   acc[m][n] = sum_{k in [k0, k1)} xq[m][k] * W[n][k]     (int32, exact)
+ * xq [M, K] int8, W [N, K] int8 (rows of K bytes), acc [M, N] int32 (dense).
+ * K, k0 and k1 - k0 positive multiples of 64 with k1 <= K (a K split of the
+ * down projection is one call per half); every pointer 16-byte aligned.
+ * Exact for codes in [-128, 127] whenever |acc| < 2^31. A bounded wait that
+ * gives up sets A8W8_DEVERR_TIMEOUT in the device error word. */
+a8w8_status a8w8_matmul_i8(const int8_t* xq, int M, int K, const int8_t* W, int N, int k0, int k1,
+                           int32_t* acc, void* stream);
+
 /* a11-a12 fused as the decode layer runs them for one or two rows: the
  * post-attention RMSNorm of x [M, K] BF16 with weight norm_w [K] BF16,
  *   xn = bf16_rne( x * 1/sqrt(mean(x^2) + eps) * norm_w ),

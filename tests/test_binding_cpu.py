@@ -124,6 +124,7 @@ def test_measured_path_wrappers(rec):
     D, H, I = CFG["head_dim"], CFG["hidden"], CFG["intermediate"]
     a8w8.a8w8_rmsnorm_gate_up_swiglu(_t((2, H)), _t((H,)), 1e-6, _t((2 * I, H), torch.int8),
                                      _t((2 * I,), torch.float32))
+    a8w8.a8w8_matmul_i8(_t((3, H), torch.int8), _t((5, H), torch.int8), 0, H)
     tok, slot, bt, ctx = _rows(2)
     rope, ws = _t((32, 2 * D), torch.float32), _t((64,), torch.uint8)
     a8w8.a8w8_decode_layer(_weights(), CFG, _t((2, CFG["hidden"])), slot, bt, ctx, _caches(),
@@ -134,5 +135,5 @@ def test_measured_path_wrappers(rec):
              "lm_head": _t((64, CFG["hidden"])), "layers": [_weights(), _weights()]}
     a8w8.a8w8_decode_step(model, CFG, tok, slot, bt, ctx, [_caches()] * 2, [_caches()] * 2, rope,
                           ws, _t((2,), torch.int32))
-    assert rec.calls == ["a8w8_rmsnorm_gate_up_swiglu", "a8w8_decode_layer", "a8w8_prefill_layer",
-                         "a8w8_decode_step"]
+    assert rec.calls == ["a8w8_rmsnorm_gate_up_swiglu", "a8w8_matmul_i8", "a8w8_decode_layer",
+                         "a8w8_prefill_layer", "a8w8_decode_step"]

@@ -169,6 +169,37 @@ def test_rmsnorm_gate_up_swiglu(a8w8, M, K, I):
 
 
 # ---------------------------------------------------------------------------
+# Exact INT32 product of prefill rows on the tensor cores (tcgen05)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("M,K,N,k0,k1", [
+    (130, 320, 300, 0, 320),          # ragged M and N tiles, one partial chunk
+    (200, 2112, 136, 0, 2112),        # 33 K steps: chunks of 16, 16 and 1 steps
+    (64, 1024, 128, 0, 1024),         # exactly one chunk, one tile
+    (257, 17408, 260, 8704, 17408),   # the down projection's second K half
+    (2048, 5120, 256, 0, 5120),       # the prefill chunk's rows, Qwen3-14B K
+])
+def test_matmul_i8_exact(a8w8, M, K, N, k0, k1):
+    x = synth.int8_uniform(M + K, (M, K))
+    W = synth.int8_uniform(N + K + 1, (N, K))
+    acc = to_host(a8w8.a8w8_matmul_i8(to_dev(x), to_dev(W), k0, k1))
+    assert np.array_equal(acc, oracle.matmul_i8(x, W, k0, k1))
+    assert a8w8.read_device_errors() == 0
+
+
+@pytest.mark.parametrize("a,b", [(127, 127), (-128, -128), (127, -127), (-128, 127)])
+def test_matmul_i8_extreme_chunks(a8w8, a, b):
+    # every product at the extreme: each 1024-column chunk sums to +-2^24 or
+    # just below, the largest FP32 partial the exact accumulation meets
+    M, K, N = 130, 5120, 136
+    x = np.full((M, K), a, np.int8)
+    W = np.full((N, K), b, np.int8)
+    x[3, ::7] = -a if a != -128 else 127
+    acc = to_host(a8w8.a8w8_matmul_i8(to_dev(x), to_dev(W)))
+    assert np.array_equal(acc, oracle.matmul_i8(x, W))
+
+
+# ---------------------------------------------------------------------------
 # KV write and attention
 # ---------------------------------------------------------------------------
 

@@ -80,6 +80,7 @@ _SIGNATURES = {
     "a8w8_quant_rows": (_i, [_p, _i, _i, _i, _p, _p, _p]),
     "a8w8_linear": (_i, [_p, _p, _i, _i, _p, _p, _i, _i, _p, _p, _p, _p]),
     "a8w8_gate_up_swiglu": (_i, [_p, _p, _i, _i, _p, _p, _i, _p, _p, _p]),
+    "a8w8_matmul_i8": (_i, [_p, _i, _i, _p, _i, _i, _i, _p, _p]),
     "a8w8_rmsnorm_gate_up_swiglu": (_i, [_p, _i, _i, _p, _f, _p, _p, _i, _p, _p]),
     "paged_kv_write": (_i, [_p, _p, _i, _i, _i, _p, _p, _p, _i, _i, _p]),
     "paged_decode_attention_bf16": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p,
@@ -240,6 +241,19 @@ def a8w8_gate_up_swiglu(xq, x_scale, W_gu, s_gu, acc_out=False, stream=None):
     _check(lib().a8w8_gate_up_swiglu(_ptr(xq), _ptr(x_scale), M, K, _ptr(W_gu), _ptr(s_gu), I,
                                      _ptr(act), _ptr(acc), _stream(stream)))
     return (act, acc) if acc_out else act
+
+
+def a8w8_matmul_i8(xq, W, k0=0, k1=None, out=None, stream=None):
+    """Exact INT32 product on the tensor cores: xq [M, K] int8 . W [N, K]^T
+    over K columns [k0, k1) -> [M, N] int32."""
+    torch = _torch()
+    M, K = xq.shape
+    N = W.shape[0]
+    k1 = K if k1 is None else k1
+    acc = out if out is not None else torch.empty((M, N), dtype=torch.int32, device=xq.device)
+    _check(lib().a8w8_matmul_i8(_ptr(xq), M, K, _ptr(W), N, int(k0), int(k1), _ptr(acc),
+                                _stream(stream)))
+    return acc
 
 
 def a8w8_rmsnorm_gate_up_swiglu(x, norm_w, eps, W_gu, s_gu, out=None, stream=None):

@@ -430,6 +430,9 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     g.ldy = H;
     g.tap_q = T.aq;
     g.tap_s = T.as;
+    // the O matrix (26 MB) fits the grid's shared memory: each CTA requests
+    // its whole share before waiting for the attention output
+    g.deep = 1;
     e = run_gemv(PRO_QUANT, EPI_STORE, 1, g, B, L, qx, qs, gacc);
     if (e != cudaSuccess) return cuda_fail(e, "O projection");
     if (T.h1) {
@@ -699,6 +702,22 @@ a8w8_status a8w8_gate_up_swiglu(const int8_t* xq, const float* x_scale, int M, i
                                 int32_t* acc_out, void* stream) {
     return linear_common(xq, x_scale, M, K, W_gu, s_gu, I, 1, nullptr, act, acc_out, true, stream,
                          "a8w8_gate_up_swiglu");
+}
+
+a8w8_status a8w8_matmul_i8(const int8_t* xq, int M, int K, const int8_t* W, int N, int k0, int k1,
+                           int32_t* acc, void* stream) {
+    const char* name = "a8w8_matmul_i8";
+    if (M < 0 || N < 0 || K < 0) return fail(A8W8_ERR_INVALID_ARG, "%s: negative size", name);
+    if (M == 0 || N == 0) return A8W8_OK;
+    if (K == 0 || K % 64 || k0 < 0 || k1 > K || k0 % 64 || (k1 - k0) <= 0 || (k1 - k0) % 64)
+        return fail(A8W8_ERR_UNSUPPORTED_SHAPE,
+                    "%s: K, k0 and k1 - k0 must be positive multiples of 64 with k1 <= K", name);
+    a8w8_status s = check_ptrs({xq, W, acc}, name);
+    if (s != A8W8_OK) return s;
+    Launch L = make_launch(stream, false);
+    if (L.num_sms <= 0) return fail(A8W8_ERR_CUDA, "%s: no CUDA device", name);
+    cudaError_t e = launch_gemm_tc(xq, M, W, N, K, k0, k1, acc, N, device_error_word(), L);
+    return e == cudaSuccess ? A8W8_OK : cuda_fail(e, name);
 }
 
 a8w8_status a8w8_rmsnorm_gate_up_swiglu(const a8w8_bf16* x, int M, int K,

@@ -16,12 +16,15 @@
 // the tensor-memory lanes, 128 activation rows = the MMA's N and columns) over
 // K steps of 64 columns, with warp roles:
 //   warp 0      TMA: the INT8 tiles of W and X for each step (cp.async.bulk
-//               .tensor, 8 KB each) into a 4-stage ring;
+//               .tensor, 8 KB each) into a 6-stage ring;
 //   warp 1      allocates 512 tensor-memory columns; one thread issues the
 //               four m128 n128 k16 MMAs of a step and commits them;
-//   warps 2-5   convert each step's INT8 tiles to FP16 in the 128-byte
-//               swizzled K-major layout the MMA reads (a 3-stage ring);
-//   warps 6-9   drain each finished chunk: FP32 accumulators (two buffers of
+//   warps 2-9   convert each step's INT8 tiles to FP16 in the 128-byte
+//               swizzled K-major layout the MMA reads (a 4-stage ring), in two
+//               groups of 4 warps that take alternate steps (a group's
+//               conversion of one step is a latency chain of shared-memory
+//               loads, conversions, stores and a proxy fence);
+//   warps 10-13 drain each finished chunk: FP32 accumulators (two buffers of
 //               128 columns, so the MMAs of the next chunk proceed meanwhile)
 //               to INT32, added into a 128-column INT32 sum in tensor memory;
 //               after the last chunk they write C.
@@ -42,10 +45,10 @@ using namespace tc;
 constexpr int kTM = 128;          // weight rows per tile
 constexpr int kTN = 128;          // activation rows per tile
 constexpr int kTK = 64;           // K columns per step
-constexpr int kS8 = 4;            // INT8 stages
-constexpr int kS16 = 3;           // FP16 stages
 constexpr int kChunkSteps = 16;   // steps per exact FP32 chunk (1024 columns)
-constexpr int kTcThreads = 320;
+constexpr int kStages8 = 6;       // INT8 TMA stages (W and X tiles)
+constexpr int kStages16 = 4;      // FP16 operand stages
+constexpr int kConvGroups = 2;    // converter groups of 4 warps, alternating K steps
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSumCol = 256;  // INT32 sums at columns [256, 384)
 constexpr int kTile8 = kTM * kTK;          // 8192 bytes
@@ -54,6 +57,8 @@ constexpr int kTile16 = kTM * kTK * 2;     // 16384 bytes
 struct TcSmem {
     size_t w8, x8, w16, x16, bars, total;
 };
+// kS8 INT8 stages (TMA), kS16 FP16 stages (converted operands)
+template <int kS8, int kS16>
 __host__ __device__ constexpr TcSmem tc_smem() {
     TcSmem s{};
     s.w16 = 0;                                        // [kS16][16 KB], 1024-aligned
@@ -67,7 +72,8 @@ __host__ __device__ constexpr TcSmem tc_smem() {
     return s;
 }
 // dynamic shared memory requested: the layout plus room to align it to 1024
-constexpr size_t kTcSmemBytes = tc_smem().total + 1024;
+template <int kS8, int kS16>
+constexpr size_t tc_smem_bytes() { return tc_smem<kS8, kS16>().total + 1024; }
 
 // 16 INT8 codes -> 16 FP16 values (exact): byte v becomes the FP16 number
 // 1024 + (v + 128), from which 1152 is subtracted.
@@ -85,12 +91,19 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
 // Converts one 128 x 64 INT8 tile (row pitch 64 bytes) into the FP16
 // 128-byte-swizzled K-major tile, thread t of 128 taking the 16-byte pieces
 // t, t + 128, t + 256, t + 384 (piece p: row p / 4, columns 16 (p % 4) ..).
+// All four pieces are loaded before any is converted.
 __device__ __forceinline__ void convert_tile(const int8_t* src, unsigned char* dst, int t) {
+    int4 vs[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int p = t + 128 * i;
+        vs[i] = *reinterpret_cast<const int4*>(src + (p >> 2) * kTK + 16 * (p & 3));
+    }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int p = t + 128 * i;
         const int r = p >> 2, q = p & 3;
-        const int4 v = *reinterpret_cast<const int4*>(src + r * kTK + 16 * q);
+        const int4 v = vs[i];
         uint4 a, b;
         i8x4_to_f16x4((uint32_t)v.x, a.x, a.y);
         i8x4_to_f16x4((uint32_t)v.y, a.z, a.w);
@@ -115,7 +128,11 @@ __device__ __forceinline__ void set_timeout(unsigned* err, volatile int* abort) 
 
 namespace {
 
-__global__ void __launch_bounds__(kTcThreads, 1)
+// warps: TMA, MMA, kG groups of 4 converter warps, 4 drain warps
+__host__ __device__ constexpr int tc_threads(int kG) { return (2 + 4 * kG + 4) * 32; }
+
+template <int kS8, int kS16, int kG>
+__global__ void __launch_bounds__(tc_threads(kG), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
                    int M, int N, int k0, int steps, int32_t* __restrict__ C, int ldc,
                    unsigned* err) {
@@ -123,7 +140,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // the swizzled tiles need 1024-byte aligned bases
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    constexpr TcSmem L = tc_smem();
+    constexpr TcSmem L = tc_smem<kS8, kS16>();
     unsigned char* w16 = smem + L.w16;
     unsigned char* x16 = smem + L.x16;
     int8_t* w8 = reinterpret_cast<int8_t*>(smem + L.w8);
@@ -147,10 +164,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (tid == 0) {
         for (int i = 0; i < kS8; ++i) {
             mbar_init(&full8[i], 1);      // the producer's expect-tx arrival
-            mbar_init(&empty8[i], 4);     // one arrival per converter warp
+            mbar_init(&empty8[i], 4);     // one arrival per warp of the converting group
         }
         for (int i = 0; i < kS16; ++i) {
-            mbar_init(&full16[i], 4);     // one arrival per converter warp
+            mbar_init(&full16[i], 4);     // one arrival per warp of the converting group
             mbar_init(&empty16[i], 1);    // the MMA commit
         }
         for (int i = 0; i < 2; ++i) {
@@ -223,10 +240,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mma_commit(done);
             mbar_wait(done, 0, nullptr);
         }
-    } else if (warp < 6) {
-        // ---- converters: INT8 tiles -> FP16 swizzled tiles ----
-        const int t = tid - 64;
-        for (int s = 0; s < steps; ++s) {
+    } else if (warp < 2 + 4 * kG) {
+        // ---- converters: INT8 tiles -> FP16 swizzled tiles; group g of 4
+        // warps takes the steps s = g (mod kG), so kG steps convert at once ----
+        const int grp = (warp - 2) >> 2;
+        const int t = tid - 64 - 128 * grp;
+        for (int s = grp; s < steps; s += kG) {
             const int st8 = s % kS8, st16 = s % kS16;
             bool ok = mbar_wait(&full8[st8], (s / kS8) & 1, abort);
             if (ok && s >= kS16) ok = mbar_wait(&empty16[st16], ((s / kS16) - 1) & 1, abort);
@@ -329,6 +348,32 @@ bool make_i8_map(CUtensorMap* map, const int8_t* base, int rows, int cols, int l
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+template <int kS8, int kS16, int kG>
+cudaError_t launch_tc_t(const CUtensorMap& mw, const CUtensorMap& mx, int M, int N, int k0, int steps,
+                        int32_t* C, int ldc, unsigned* err, const Launch& L) {
+    auto kern = gemm_tc_kernel<kS8, kS16, kG>;
+    constexpr size_t smem = tc_smem_bytes<kS8, kS16>();
+    static_assert(smem <= 227 * 1024, "shared memory");
+    {
+        // the shared-memory limit, set once per CUDA context
+        cudaError_t e = once_per_context(reinterpret_cast<const void*>(kern), [&]() {
+            return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        });
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((M + kTN - 1) / kTN, (N + kTM - 1) / kTM);
+    cfg.blockDim = dim3(tc_threads(kG));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = L.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = L.pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, mw, mx, M, N, k0, steps, C, ldc, err);
+}
+
 }  // namespace
 
 bool gemm_tc_supported(int K, int k_splits) { return K > 0 && K % (kTK * k_splits) == 0; }
@@ -341,25 +386,8 @@ cudaError_t launch_gemm_tc(const int8_t* X, int M, const int8_t* W, int N, int K
         return cudaErrorInvalidValue;
     CUtensorMap mw, mx;
     if (!make_i8_map(&mw, W, N, K, K) || !make_i8_map(&mx, X, M, K, K)) return cudaErrorInvalidValue;
-    {
-        // the shared-memory limit, set once per CUDA context
-        cudaError_t e = once_per_context(reinterpret_cast<const void*>(gemm_tc_kernel), [&]() {
-            return cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)kTcSmemBytes);
-        });
-        if (e != cudaSuccess) return e;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((M + kTN - 1) / kTN, (N + kTM - 1) / kTM);
-    cfg.blockDim = dim3(kTcThreads);
-    cfg.dynamicSmemBytes = kTcSmemBytes;
-    cfg.stream = L.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = L.pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, gemm_tc_kernel, mw, mx, M, N, k0, (k1 - k0) / kTK, C, ldc, err);
+    return launch_tc_t<kStages8, kStages16, kConvGroups>(mw, mx, M, N, k0, (k1 - k0) / kTK, C, ldc,
+                                                         err, L);
 }
 
 }  // namespace a8w8

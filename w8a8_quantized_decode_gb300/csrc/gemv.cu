@@ -33,9 +33,15 @@ constexpr size_t kSmemActBudget = 72 * 1024;
 __host__ __device__ constexpr int ring_unr(int BT) { return BT >= 8 ? 2 : 1; }
 constexpr int kRingNB = 6;
 constexpr int kRingPre = 2;
-template <int BT>
+// Deep form (1-2 rows): 11 batches (176 KB per CTA), all requested before
+// the dependency wait. A projection whose share is at most 11 units per warp
+// (O: 5120 x 5120) then has all of its weights in flight, or landed, while
+// the kernel before it runs; larger ones keep the first 11 units of each
+// warp's run ahead of the activation prologue.
+constexpr int kDeepNB = 11;
+template <int BT, int NB>
 constexpr size_t stream_ring_bytes() {
-    return ring_bytes<stream_threads(BT), ring_unr(BT), kRingNB>();
+    return ring_bytes<stream_threads(BT), ring_unr(BT), NB>();
 }
 // General kernel (any K multiple of 16).
 constexpr int kGenThreads = 512;
@@ -44,10 +50,10 @@ constexpr int kGenUnroll = 8;
 // ---------------------------------------------------------------------------
 // Streaming kernel (K a multiple of 512 * KS).
 // ---------------------------------------------------------------------------
-template <int BT, int PRO, int EPI, int KS>
+template <int BT, int PRO, int EPI, int KS, int NB, int NBPRE>
 __global__ void __launch_bounds__(stream_threads(BT), 1) gemv_stream_kernel(const GemvParams p) {
     extern __shared__ __align__(16) unsigned char smem[];
-    stream_gemv<BT, PRO, EPI, KS, stream_threads(BT), ring_unr(BT), kRingNB, kRingPre>(p, smem, [] {
+    stream_gemv<BT, PRO, EPI, KS, stream_threads(BT), ring_unr(BT), NB, NBPRE>(p, smem, [] {
         pdl_wait();
         pdl_trigger();
         return true;
@@ -195,24 +201,18 @@ __global__ void __launch_bounds__(kGenThreads, 1) gemv_kernel(const GemvParams p
 
 bool use_stream(int K, int KS) { return K % (kUnit * KS) == 0; }
 
-template <int BT, int PRO, int EPI, int KS>
-cudaError_t launch_t(const GemvParams& p, const Launch& L) {
-    const bool stream = use_stream(p.K, KS);
-    auto kern = stream ? gemv_stream_kernel<BT, PRO, EPI, KS> : gemv_kernel<BT, PRO, EPI, KS>;
+template <int BT, int PRO, int EPI, int KS, int NB, int NBPRE>
+cudaError_t launch_ring(const GemvParams& p, const Launch& L, bool stream) {
+    auto kern = stream ? gemv_stream_kernel<BT, PRO, EPI, KS, NB, NBPRE> : gemv_kernel<BT, PRO, EPI, KS>;
     const int G = L.num_sms;
     const int nseg = EPI == EPI_SWIGLU ? 2 : 1;
     const size_t smem =
-        stream ? smem_layout(BT, nseg, KS, p.K, p.N, G, stream_threads(BT), stream_ring_bytes<BT>()).total
+        stream ? smem_layout(BT, nseg, KS, p.K, p.N, G, stream_threads(BT), stream_ring_bytes<BT, NB>()).total
                : smem_layout(BT, nseg, KS, p.K, p.N, G, kGenThreads).total;
     {
         // the shared-memory limit, set once per CUDA context
-        cudaError_t e = once_per_context(reinterpret_cast<const void*>(gemv_kernel<BT, PRO, EPI, KS>), [&]() -> cudaError_t {
-            cudaError_t e = cudaFuncSetAttribute(gemv_kernel<BT, PRO, EPI, KS>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
-            if (e == cudaSuccess)
-                e = cudaFuncSetAttribute(gemv_stream_kernel<BT, PRO, EPI, KS>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
-            return e;
+        cudaError_t e = once_per_context(reinterpret_cast<const void*>(kern), [&]() -> cudaError_t {
+            return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxDynSmem);
         });
         if (e != cudaSuccess) return e;
     }
@@ -228,6 +228,21 @@ cudaError_t launch_t(const GemvParams& p, const Launch& L) {
     cfg.attrs = attr;
     cfg.numAttrs = L.pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+template <int BT, int PRO, int EPI, int KS>
+cudaError_t launch_t(const GemvParams& p, const Launch& L) {
+    const bool stream = use_stream(p.K, KS);
+    if constexpr (BT <= 2) {
+        if (stream && p.deep) {
+            const int nseg = EPI == EPI_SWIGLU ? 2 : 1;
+            const size_t deep = smem_layout(BT, nseg, KS, p.K, p.N, L.num_sms, stream_threads(BT),
+                                            stream_ring_bytes<BT, kDeepNB>()).total;
+            if (deep <= (size_t)kMaxDynSmem)
+                return launch_ring<BT, PRO, EPI, KS, kDeepNB, kDeepNB>(p, L, stream);
+        }
+    }
+    return launch_ring<BT, PRO, EPI, KS, kRingNB, kRingPre>(p, L, stream);
 }
 
 template <int PRO, int EPI, int KS>

@@ -61,6 +61,9 @@ struct GemvParams {
     unsigned* err;          // device error word (timeouts)
     unsigned* clear;        // CTA 0 zeroes clear[0, clear_n) after the wait (or null)
     int clear_n;
+    int deep;               // streaming kernel, 1-2 rows: a ring deep enough for the
+                            // CTA's whole share (up to 11 units per warp), all of it
+                            // requested before the dependency wait, where it fits
 };
 
 // Largest batch tile one launch handles; bigger batches are tiled by the host.
