@@ -257,3 +257,32 @@ def test_persistent_device_loop(a8w8):
     g.close()
 
 
+
+
+def test_qwen3_14b_lm_head_full_vocab_vs_oracle(a8w8):
+    """The final norm, the 151936-row BF16 LM head and the argmax at full
+    size (one Qwen3-14B-shaped layer in front, batch 2), element by element
+    on the GPU's own final hidden rows."""
+    import torch
+    cfg = dict(synth.QWEN3_14B, num_layers=1)
+    dev = torch.device("cuda")
+    model = synth.t_model_weights(cfg, 77, dev)
+    B, page, Hkv, D = 2, cfg["page_size"], cfg["num_kv_heads"], cfg["head_dim"]
+    kc = [torch.zeros((2 * page, Hkv, D), dtype=torch.bfloat16, device=dev)]
+    vc = [torch.zeros_like(kc[0])]
+    rope = a8w8.a8w8_rope_table(page, D, cfg["rope_theta"])
+    ws = a8w8.alloc_workspace(cfg, B, 1)
+    nxt = torch.empty(B, dtype=torch.int32, device=dev)
+    logits = torch.empty((B, cfg["vocab"]), dtype=torch.float32, device=dev)
+    fh = torch.empty((B, cfg["hidden"]), dtype=torch.bfloat16, device=dev)
+    bt = np.array([[0], [1]], np.int32)
+    tok = synth.prompt_ids(78, B, cfg["vocab"])
+    ctx = np.array([1, 1], np.int32)
+    slots = synth.slots_for(bt, ctx - 1, page)
+    a8w8.a8w8_decode_step(model, cfg, to_dev(tok), to_dev(slots), to_dev(bt), to_dev(ctx), kc, vc,
+                          rope, ws, nxt, logits=logits, final_hidden=fh)
+    torch.cuda.synchronize()
+    W = model["lm_head"].detach().cpu().view(torch.int16).numpy().view(np.uint16)
+    worst, ties = check_lm_head(to_host(fh), W, to_host(logits), to_host(nxt))
+    print("LM head: worst |diff| / bound", worst, "near ties", ties)
+    assert a8w8.read_device_errors() == 0
