@@ -294,7 +294,7 @@ a8w8_status paged_decode_attention_bf16_noalloc(const a8w8_bf16* q, const a8w8_b
  *   scales [num_blocks * page_size, Hkv] float,
  * each row quantised by the activation formula of a8w8_quant_rows from its
  * BF16 values (s = absmax / 127, q = clamp(rne(x / s), -127, 127)), and read
- * back as code * s. D is 64 or 128. Status: built; not yet run on a GPU. */
+ * back as code * s. D is 64 or 128. */
 
 /* Quantises k, v ([T, Hkv, D] BF16) row by row into the INT8 cache at
  * slot_mapping[t]. slot < 0 skips the token; slot >= num_blocks * page_size
@@ -350,8 +350,7 @@ a8w8_status a8w8_prefill_layer_i8kv(const a8w8_layer_weights* w, const a8w8_conf
  * removed; each projection
  *   y[m][n] = bf16_rne( sum_k x[m][k] * W[n][k] (+ residual[m][n]) )
  * (products exact in float32, float32 sums), the SwiGLU epilogue
- * act = bf16_rne( silu(g) * u ) on the float32 g and u. Status: built; not
- * yet run on a GPU. */
+ * act = bf16_rne( silu(g) * u ) on the float32 g and u. */
 typedef struct {
     const a8w8_bf16* input_norm_w;   /* [H] */
     const a8w8_bf16* w_qkv;          /* [Hq*D + 2*Hkv*D, H]: Q heads, K heads, V heads */
@@ -492,7 +491,7 @@ a8w8_status a8w8_decode_step(const a8w8_model* m, const a8w8_config* cfg, int B,
  * quantity of a time to first token. Shape rules as a8w8_prefill_layer
  * (1 <= M <= 16384), 1 <= S <= M, intermediate or Hq*D + 2*Hkv*D at least
  * hidden; ws / ws_bytes: a8w8_workspace_bytes(cfg, M, max_blocks); caches as
- * a8w8_decode_step. Status: built; not yet run on a GPU. */
+ * a8w8_decode_step. */
 a8w8_status a8w8_prefill_step(const a8w8_model* m, const a8w8_config* cfg, int M,
                               const int32_t* token_ids, const int32_t* slot_mapping,
                               const int32_t* block_table, int max_blocks, int num_blocks,
@@ -504,8 +503,7 @@ a8w8_status a8w8_prefill_step(const a8w8_model* m, const a8w8_config* cfg, int M
 /* a8w8_decode_step over INT8 caches: k_codes / v_codes / k_scales / v_scales
  * are HOST arrays of num_layers device pointers, each layer's cache laid out
  * as for a8w8_decode_layer_i8kv; every other argument as a8w8_decode_step
- * (A8W8_FLAG_PERSISTENT_STEP is ignored). Status: built; not yet run on a
- * GPU. */
+ * (A8W8_FLAG_PERSISTENT_STEP is ignored). */
 a8w8_status a8w8_decode_step_i8kv(const a8w8_model* m, const a8w8_config* cfg, int B,
                                   const int32_t* token_ids, const int32_t* slot_mapping,
                                   const int32_t* block_table, int max_blocks, int num_blocks,
