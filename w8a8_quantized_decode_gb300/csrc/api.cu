@@ -329,7 +329,7 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     const a8w8_layer_taps none = {};
     const a8w8_layer_taps& T = taps ? *taps : none;
 
-    // a2-a4: input RMSNorm + quantisation (prologue) + QKV projection
+    // parameter blocks of a2-a4 (QKV), a5-a8 (attention) and a9-a10 (O)
     GemvParams g = {};
     g.W = w->w_qkv;
     g.w_scale = w->s_qkv;
@@ -346,14 +346,18 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     g.tap_s = T.xs;
     g.clear = att_tk;   // the attention that follows counts its splits there
     g.clear_n = B * Hq;
-    cudaError_t e = run_gemv(PRO_NORM_QUANT, EPI_STORE, 1, g, B, L, qx, qs, gacc);
-    if (e != cudaSuccess) return cuda_fail(e, "QKV projection");
-    if (T.qkv) {
-        e = cudaMemcpyAsync(T.qkv, qkv, (size_t)B * NQKV * 2, cudaMemcpyDeviceToDevice, L.stream);
-        if (e != cudaSuccess) return cuda_fail(e, "tap qkv");
-    }
-
-    // a5-a8: QK norm, RoPE, KV write, paged attention
+    GemvParams go = {};
+    go.W = w->w_o;
+    go.w_scale = w->s_o;
+    go.K = NQ;
+    go.N = H;
+    go.x = attn;
+    go.ldx = NQ;
+    go.residual = hidden;
+    go.y = hidden;
+    go.ldy = H;
+    go.tap_q = T.aq;
+    go.tap_s = T.as;
     AttnParams a = {};
     a.q = qkv;
     a.q_stride = NQKV;
@@ -387,54 +391,53 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     a.err = device_error_word();
     a.tap_q_rot = reinterpret_cast<bf16*>(T.q_rot);
     a.tap_k_rot = reinterpret_cast<bf16*>(T.k_rot);
-    if (kv8) {
-        AttnI8Params ai = {};
-        ai.a = a;
-        ai.k_codes = kv8->k_codes;
-        ai.v_codes = kv8->v_codes;
-        ai.k_scale = kv8->k_scale;
-        ai.v_scale = kv8->v_scale;
-        if (prefill) {
-            // every token's K/V quantised into the cache first (as below)
-            e = launch_kv_prep_i8(ai, L);
+
+    cudaError_t e = cudaSuccess;
+    {
+        // a2-a4: input RMSNorm + quantisation (prologue) + QKV projection
+        e = run_gemv(PRO_NORM_QUANT, EPI_STORE, 1, g, B, L, qx, qs, gacc);
+        if (e != cudaSuccess) return cuda_fail(e, "QKV projection");
+        // a5-a8: QK norm, RoPE, KV write, paged attention
+        if (kv8) {
+            AttnI8Params ai = {};
+            ai.a = a;
+            ai.k_codes = kv8->k_codes;
+            ai.v_codes = kv8->v_codes;
+            ai.k_scale = kv8->k_scale;
+            ai.v_scale = kv8->v_scale;
+            if (prefill) {
+                // every token's K/V quantised into the cache first (as below)
+                e = launch_kv_prep_i8(ai, L);
+                if (e != cudaSuccess) return cuda_fail(e, "prefill KV write");
+                ai.a.kv_in_cache = true;
+            }
+            e = launch_attention_i8(ai, L);
+        } else if (prefill) {
+            // every token's K/V into the cache first: the chunk's rows attend to
+            // each other's earlier tokens (causal by their context lengths)
+            e = launch_kv_prep(a, L);
             if (e != cudaSuccess) return cuda_fail(e, "prefill KV write");
-            ai.a.kv_in_cache = true;
+            a.kv_in_cache = true;
+            e = launch_attn_group(a, L);
+        } else {
+            e = launch_attention(a, L);
         }
-        e = launch_attention_i8(ai, L);
-    } else if (prefill) {
-        // every token's K/V into the cache first: the chunk's rows attend to
-        // each other's earlier tokens (causal by their context lengths)
-        e = launch_kv_prep(a, L);
-        if (e != cudaSuccess) return cuda_fail(e, "prefill KV write");
-        a.kv_in_cache = true;
-        e = launch_attn_group(a, L);
-    } else {
-        e = launch_attention(a, L);
+        if (e != cudaSuccess) return cuda_fail(e, "attention");
+        // a9-a10: quantisation (prologue) + O projection + residual (in place);
+        // the O matrix (26 MB) fits the grid's shared memory: each CTA
+        // requests its whole share before waiting for the attention output
+        go.deep = 1;
+        e = run_gemv(PRO_QUANT, EPI_STORE, 1, go, B, L, qx, qs, gacc);
+        if (e != cudaSuccess) return cuda_fail(e, "O projection");
     }
-    if (e != cudaSuccess) return cuda_fail(e, "attention");
+    if (T.qkv) {
+        e = cudaMemcpyAsync(T.qkv, qkv, (size_t)B * NQKV * 2, cudaMemcpyDeviceToDevice, L.stream);
+        if (e != cudaSuccess) return cuda_fail(e, "tap qkv");
+    }
     if (T.attn) {
         e = cudaMemcpyAsync(T.attn, attn, (size_t)B * NQ * 2, cudaMemcpyDeviceToDevice, L.stream);
         if (e != cudaSuccess) return cuda_fail(e, "tap attn");
     }
-
-    // a9-a10: quantisation (prologue) + O projection + residual (in place)
-    g = GemvParams{};
-    g.W = w->w_o;
-    g.w_scale = w->s_o;
-    g.K = NQ;
-    g.N = H;
-    g.x = attn;
-    g.ldx = NQ;
-    g.residual = hidden;
-    g.y = hidden;
-    g.ldy = H;
-    g.tap_q = T.aq;
-    g.tap_s = T.as;
-    // the O matrix (26 MB) fits the grid's shared memory: each CTA requests
-    // its whole share before waiting for the attention output
-    g.deep = 1;
-    e = run_gemv(PRO_QUANT, EPI_STORE, 1, g, B, L, qx, qs, gacc);
-    if (e != cudaSuccess) return cuda_fail(e, "O projection");
     if (T.h1) {
         e = cudaMemcpyAsync(T.h1, hidden, (size_t)B * H * 2, cudaMemcpyDeviceToDevice, L.stream);
         if (e != cudaSuccess) return cuda_fail(e, "tap h1");
@@ -1282,8 +1285,8 @@ static a8w8_status enqueue_step(const a8w8_model* m, const a8w8_config& c, int B
         if (e != cudaSuccess) return cuda_fail(e, "persistent decode step");
         return A8W8_OK;
     }
-    cudaError_t e = launch_embed(reinterpret_cast<const bf16*>(m->embed), c.vocab, c.hidden, token_ids,
-                                 B, hidden, keys, ticket, device_error_word(), L);
+    cudaError_t e = launch_embed(reinterpret_cast<const bf16*>(m->embed), c.vocab, c.hidden,
+                                 token_ids, B, hidden, keys, ticket, device_error_word(), L);
     if (e != cudaSuccess) return cuda_fail(e, "embedding");
     for (int l = 0; l < c.num_layers; ++l) {
         a8w8_status s = kv8
