@@ -18,12 +18,14 @@
 //   warp 0      TMA: the INT8 tiles of W and X for each step (cp.async.bulk
 //               .tensor, 8 KB each) into a 6-stage ring;
 //   warp 1      allocates 512 tensor-memory columns; one thread issues the
-//               four m128 n128 k16 MMAs of a step and commits them;
-//   warps 2-9   convert each step's INT8 tiles to FP16 in the 128-byte
-//               swizzled K-major layout the MMA reads (a 4-stage ring), in two
-//               groups of 4 warps that take alternate steps (a group's
-//               conversion of one step is a latency chain of shared-memory
-//               loads, conversions, stores and a proxy fence);
+//               MMAs (m128 n128 k16, four per step) and commits once per pair
+//               of steps (a commit costs the issuing thread about as much as
+//               three MMAs);
+//   warps 2-9   convert the INT8 tiles to FP16 in the 128-byte swizzled
+//               K-major layout the MMA reads, in two groups of 4 warps that
+//               take alternate pairs of steps, each into its own slot of two
+//               step tiles (a group's conversion is a latency chain of
+//               shared-memory loads, conversions, stores and a proxy fence);
 //   warps 10-13 drain each finished chunk: FP32 accumulators (two buffers of
 //               128 columns, so the MMAs of the next chunk proceed meanwhile)
 //               to INT32, added into a 128-column INT32 sum in tensor memory;
@@ -136,6 +138,7 @@ __global__ void __launch_bounds__(tc_threads(kG), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
                    int M, int N, int k0, int steps, int32_t* __restrict__ C, int ldc,
                    unsigned* err) {
+    static_assert(kS16 == 2 * kG, "one FP16 slot of two step tiles per converter group");
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // the swizzled tiles need 1024-byte aligned bases
     unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -166,7 +169,7 @@ __global__ void __launch_bounds__(tc_threads(kG), 1)
             mbar_init(&full8[i], 1);      // the producer's expect-tx arrival
             mbar_init(&empty8[i], 4);     // one arrival per warp of the converting group
         }
-        for (int i = 0; i < kS16; ++i) {
+        for (int i = 0; i < kG; ++i) {
             mbar_init(&full16[i], 4);     // one arrival per warp of the converting group
             mbar_init(&empty16[i], 1);    // the MMA commit
         }
@@ -214,27 +217,35 @@ __global__ void __launch_bounds__(tc_threads(kG), 1)
         // ---- MMA issuer ----
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16_f32(kTM, kTN);
-            for (int s = 0; s < steps; ++s) {
-                const int c = s / kChunkSteps, buf = c & 1;
-                const bool first = s % kChunkSteps == 0;
+            // one wait and one commit per pair of steps: a commit costs the
+            // issuing thread about as much as three of these MMAs
+            for (int P = 0; 2 * P < steps; ++P) {
+                const int s0 = 2 * P, ns = min(2, steps - s0);
+                const int c = s0 / kChunkSteps, buf = c & 1;
+                const bool first = s0 % kChunkSteps == 0;
                 if (first && c >= 2 && !mbar_wait(&accempty[buf], ((c >> 1) - 1) & 1, abort)) {
                     if (!*abort) set_timeout(err, abort);
                     break;
                 }
-                const int st = s % kS16;
-                if (!mbar_wait(&full16[st], (s / kS16) & 1, abort)) {
+                const int slot = P % kG;
+                if (!mbar_wait(&full16[slot], (P / kG) & 1, abort)) {
                     if (!*abort) set_timeout(err, abort);
                     break;
                 }
                 tc_fence_after();
-                const uint64_t ad = sw128_kmajor_desc(smem_u32(w16 + (size_t)st * kTile16));
-                const uint64_t bd = sw128_kmajor_desc(smem_u32(x16 + (size_t)st * kTile16));
                 const uint32_t d = tmem + (uint32_t)(buf * kTN);
+                for (int u = 0; u < ns; ++u) {
+                    const int tile = 2 * slot + u;
+                    const uint64_t ad = sw128_kmajor_desc(smem_u32(w16 + (size_t)tile * kTile16));
+                    const uint64_t bd = sw128_kmajor_desc(smem_u32(x16 + (size_t)tile * kTile16));
 #pragma unroll
-                for (int j = 0; j < kTK / 16; ++j)
-                    mma_f16(d, ad + 2 * j, bd + 2 * j, idesc, (first && j == 0) ? 0u : 1u);
-                mma_commit(&empty16[st]);
-                if (s % kChunkSteps == kChunkSteps - 1 || s == steps - 1) mma_commit(&accfull[buf]);
+                    for (int j = 0; j < kTK / 16; ++j)
+                        mma_f16(d, ad + 2 * j, bd + 2 * j, idesc,
+                                (first && u == 0 && j == 0) ? 0u : 1u);
+                }
+                mma_commit(&empty16[slot]);
+                const int s1 = s0 + ns - 1;
+                if (s1 % kChunkSteps == kChunkSteps - 1 || s1 == steps - 1) mma_commit(&accfull[buf]);
             }
             // no MMA may still be running when the tensor memory is freed
             mma_commit(done);
@@ -242,24 +253,29 @@ __global__ void __launch_bounds__(tc_threads(kG), 1)
         }
     } else if (warp < 2 + 4 * kG) {
         // ---- converters: INT8 tiles -> FP16 swizzled tiles; group g of 4
-        // warps takes the steps s = g (mod kG), so kG steps convert at once ----
+        // warps takes the step pairs P = g (mod kG) into its own FP16 slot
+        // (tiles 2g, 2g + 1), so kG pairs convert at once ----
         const int grp = (warp - 2) >> 2;
         const int t = tid - 64 - 128 * grp;
-        for (int s = grp; s < steps; s += kG) {
-            const int st8 = s % kS8, st16 = s % kS16;
-            bool ok = mbar_wait(&full8[st8], (s / kS8) & 1, abort);
-            if (ok && s >= kS16) ok = mbar_wait(&empty16[st16], ((s / kS16) - 1) & 1, abort);
+        for (int P = grp; 2 * P < steps; P += kG) {
+            const int s0 = 2 * P, ns = min(2, steps - s0), use = P / kG;
+            bool ok = use == 0 || mbar_wait(&empty16[grp], (use - 1) & 1, abort);
+            for (int u = 0; u < ns && ok; ++u)
+                ok = mbar_wait(&full8[(s0 + u) % kS8], ((s0 + u) / kS8) & 1, abort);
             if (!ok) {
                 if (!*abort) set_timeout(err, abort);
                 break;
             }
-            convert_tile(w8 + (size_t)st8 * kTile8, w16 + (size_t)st16 * kTile16, t);
-            convert_tile(x8 + (size_t)st8 * kTile8, x16 + (size_t)st16 * kTile16, t);
+            for (int u = 0; u < ns; ++u) {
+                const int st8 = (s0 + u) % kS8, tile = 2 * grp + u;
+                convert_tile(w8 + (size_t)st8 * kTile8, w16 + (size_t)tile * kTile16, t);
+                convert_tile(x8 + (size_t)st8 * kTile8, x16 + (size_t)tile * kTile16, t);
+            }
             fence_async_shared();
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(&empty8[st8]);
-                mbar_arrive(&full16[st16]);
+                for (int u = 0; u < ns; ++u) mbar_arrive(&empty8[(s0 + u) % kS8]);
+                mbar_arrive(&full16[grp]);
             }
         }
     } else {
