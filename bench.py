@@ -739,19 +739,20 @@ def run_prefill(args, cfg):
         # `stream` around `reps` back-to-back launches
         xq = torch.randint(-127, 128, (M, H), dtype=torch.int8, device=device)
         acc = torch.empty((M, 2 * cfg["intermediate"]), dtype=torch.int32, device=device)
+        scratch = torch.empty((M * H,), dtype=torch.float16, device=device)
         for _ in range(2):
-            a8w8.a8w8_matmul_i8(xq, w["w_gate_up"], out=acc, stream=stream)
+            a8w8.a8w8_matmul_i8(xq, w["w_gate_up"], out=acc, scratch=scratch, stream=stream)
         reps = 5
         g0 = torch.cuda.Event(enable_timing=True)
         g1 = torch.cuda.Event(enable_timing=True)
         stream.synchronize()
         g0.record(stream)
         for _ in range(reps):
-            a8w8.a8w8_matmul_i8(xq, w["w_gate_up"], out=acc, stream=stream)
+            a8w8.a8w8_matmul_i8(xq, w["w_gate_up"], out=acc, scratch=scratch, stream=stream)
         g1.record(stream)
         g1.synchronize()
         gu_ms = g0.elapsed_time(g1) / reps
-        del acc
+        del acc, scratch
     ms = sum(times) / len(times)
     ms = max_over_ranks(ms, device)
     gu_flop = 2.0 * M * 2 * cfg["intermediate"] * H

@@ -201,10 +201,13 @@ a8w8_status a8w8_gate_up_swiglu(const int8_t* xq, const float* x_scale, int M, i
  * xq [M, K] int8, W [N, K] int8 (rows of K bytes), acc [M, N] int32 (dense).
  * K, k0 and k1 - k0 positive multiples of 64 with k1 <= K (a K split of the
  * down projection is one call per half); every pointer 16-byte aligned.
+ * scratch: device memory of at least 2 * M * K bytes, owned by the caller,
+ * that receives the FP16 images of xq (the tensor cores' activation operand)
+ * and may be reused after the call completes on the stream.
  * Exact for codes in [-128, 127] whenever |acc| < 2^31. A bounded wait that
  * gives up sets A8W8_DEVERR_TIMEOUT in the device error word. */
 a8w8_status a8w8_matmul_i8(const int8_t* xq, int M, int K, const int8_t* W, int N, int k0, int k1,
-                           int32_t* acc, void* stream);
+                           int32_t* acc, void* scratch, void* stream);
 
 /* a11-a12 fused as the decode layer runs them for one or two rows: the
  * post-attention RMSNorm of x [M, K] BF16 with weight norm_w [K] BF16,

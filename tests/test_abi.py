@@ -46,14 +46,15 @@ def test_linear_validation(lib):
 
 def test_matmul_i8_validation(lib):
     f = lib.a8w8_matmul_i8
-    assert f(FAKE, 4, 96, FAKE, 4, 0, 96, FAKE, None) == a8w8.ERR_UNSUPPORTED_SHAPE   # K % 64
-    assert f(FAKE, 4, 128, FAKE, 4, 32, 128, FAKE, None) == a8w8.ERR_UNSUPPORTED_SHAPE
-    assert f(FAKE, 4, 128, FAKE, 4, 0, 192, FAKE, None) == a8w8.ERR_UNSUPPORTED_SHAPE
-    assert f(FAKE, 4, 128, FAKE, 4, 64, 64, FAKE, None) == a8w8.ERR_UNSUPPORTED_SHAPE
-    assert f(FAKE + 8, 4, 128, FAKE, 4, 0, 128, FAKE, None) == a8w8.ERR_INVALID_ARG
-    assert f(FAKE, 4, 128, None, 4, 0, 128, FAKE, None) == a8w8.ERR_INVALID_ARG
-    assert f(FAKE, -1, 128, FAKE, 4, 0, 128, FAKE, None) == a8w8.ERR_INVALID_ARG
-    assert f(None, 0, 128, None, 4, 0, 128, None, None) == a8w8.OK
+    assert f(FAKE, 4, 96, FAKE, 4, 0, 96, FAKE, FAKE, None) == a8w8.ERR_UNSUPPORTED_SHAPE   # K % 64
+    assert f(FAKE, 4, 128, FAKE, 4, 32, 128, FAKE, FAKE, None) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert f(FAKE, 4, 128, FAKE, 4, 0, 192, FAKE, FAKE, None) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert f(FAKE, 4, 128, FAKE, 4, 64, 64, FAKE, FAKE, None) == a8w8.ERR_UNSUPPORTED_SHAPE
+    assert f(FAKE + 8, 4, 128, FAKE, 4, 0, 128, FAKE, FAKE, None) == a8w8.ERR_INVALID_ARG
+    assert f(FAKE, 4, 128, None, 4, 0, 128, FAKE, FAKE, None) == a8w8.ERR_INVALID_ARG
+    assert f(FAKE, -1, 128, FAKE, 4, 0, 128, FAKE, FAKE, None) == a8w8.ERR_INVALID_ARG
+    assert f(FAKE, 4, 128, FAKE, 4, 0, 128, FAKE, None, None) == a8w8.ERR_INVALID_ARG   # scratch
+    assert f(None, 0, 128, None, 4, 0, 128, None, None, None) == a8w8.OK
 
 
 def test_rmsnorm_gate_up_validation(lib):

@@ -80,7 +80,7 @@ _SIGNATURES = {
     "a8w8_quant_rows": (_i, [_p, _i, _i, _i, _p, _p, _p]),
     "a8w8_linear": (_i, [_p, _p, _i, _i, _p, _p, _i, _i, _p, _p, _p, _p]),
     "a8w8_gate_up_swiglu": (_i, [_p, _p, _i, _i, _p, _p, _i, _p, _p, _p]),
-    "a8w8_matmul_i8": (_i, [_p, _i, _i, _p, _i, _i, _i, _p, _p]),
+    "a8w8_matmul_i8": (_i, [_p, _i, _i, _p, _i, _i, _i, _p, _p, _p]),
     "a8w8_rmsnorm_gate_up_swiglu": (_i, [_p, _i, _i, _p, _f, _p, _p, _i, _p, _p]),
     "paged_kv_write": (_i, [_p, _p, _i, _i, _i, _p, _p, _p, _i, _i, _p]),
     "paged_decode_attention_bf16": (_i, [_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _f, _p,
@@ -243,16 +243,19 @@ def a8w8_gate_up_swiglu(xq, x_scale, W_gu, s_gu, acc_out=False, stream=None):
     return (act, acc) if acc_out else act
 
 
-def a8w8_matmul_i8(xq, W, k0=0, k1=None, out=None, stream=None):
+def a8w8_matmul_i8(xq, W, k0=0, k1=None, out=None, scratch=None, stream=None):
     """Exact INT32 product on the tensor cores: xq [M, K] int8 . W [N, K]^T
-    over K columns [k0, k1) -> [M, N] int32."""
+    over K columns [k0, k1) -> [M, N] int32. `scratch` (>= 2 M K bytes on the
+    device) receives the FP16 images of xq; allocated when not given."""
     torch = _torch()
     M, K = xq.shape
     N = W.shape[0]
     k1 = K if k1 is None else k1
     acc = out if out is not None else torch.empty((M, N), dtype=torch.int32, device=xq.device)
+    if scratch is None:
+        scratch = torch.empty((max(M * K, 1),), dtype=torch.float16, device=xq.device)
     _check(lib().a8w8_matmul_i8(_ptr(xq), M, K, _ptr(W), N, int(k0), int(k1), _ptr(acc),
-                                _stream(stream)))
+                                _ptr(scratch), _stream(stream)))
     return acc
 
 

@@ -150,7 +150,7 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Workspace layout shared by the layer and the step.
 struct WsLayout {
-    size_t hid, qkv, attn, act, qx, qs, gacc, part, att_tk, keys, ticket, bar, total;
+    size_t hid, qkv, attn, act, qx, qs, gacc, x16, part, att_tk, keys, ticket, bar, total;
 };
 
 // Row counts above this use the tiled GEMM (prefill chunks).
@@ -179,6 +179,11 @@ WsLayout ws_layout(const a8w8_config& c, int B, int max_blocks) {
     if (B > kGemmMinRows)
         o = round_up(o + (size_t)B * std::max({nqkv, (size_t)2 * c.intermediate,
                                                (size_t)2 * c.hidden}) * 4, 256);
+    // FP16 images of the INT8 activation rows, the GEMM's activation operand
+    w.x16 = o;
+    if (B > kGemmMinRows)
+        o = round_up(o + (size_t)B * std::max({c.hidden, c.num_q_heads * D, c.intermediate}) * 2,
+                     256);
     w.part = o;
     const int max_ctx = max_blocks * c.page_size;
     o = round_up(o + std::max(attn_part_bytes(B, c.num_q_heads, D, max_ctx, true),
@@ -241,9 +246,10 @@ bool use_mma(int M, int K, int ks) { return M >= kMmaMinBatch && gemv_mma_suppor
 // Runs a projection over batch tiles. `qx` / `qs` (room for M rows of K
 // codes and M scales) receive the quantised rows on the tensor-core path.
 cudaError_t run_gemv(int pro, int epi, int ks, GemvParams p, int M, const Launch& L,
-                     int8_t* qx = nullptr, float* qs = nullptr, int32_t* gacc = nullptr) {
+                     int8_t* qx = nullptr, float* qs = nullptr, int32_t* gacc = nullptr,
+                     uint16_t* x16 = nullptr) {
     const int Ntot = (epi == EPI_SWIGLU) ? 2 * p.N : p.N;
-    if (M > kGemmMinRows && gacc && gemm_supported(p.K, ks) && (pro == PRO_I8 || (qx && qs)) &&
+    if (M > kGemmMinRows && gacc && x16 && gemm_supported(p.K, ks) && (pro == PRO_I8 || (qx && qs)) &&
         !p.acc_out) {
         p.err = device_error_word();
         p.M = M;
@@ -253,7 +259,7 @@ cudaError_t run_gemv(int pro, int epi, int ks, GemvParams p, int M, const Launch
             p.xq = qx;
             p.x_scale = qs;
         }
-        return launch_gemm_projection(epi, ks, p, gacc, L);
+        return launch_gemm_projection(epi, ks, p, gacc, x16, L);
     }
     if (use_mma(M, p.K, ks) && (pro == PRO_I8 || (qx && qs))) {
         p.err = device_error_word();
@@ -326,6 +332,7 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     int8_t* qx = reinterpret_cast<int8_t*>(ws + lay.qx);
     float* qs = reinterpret_cast<float*>(ws + lay.qs);
     int32_t* gacc = B > kGemmMinRows ? reinterpret_cast<int32_t*>(ws + lay.gacc) : nullptr;
+    uint16_t* x16 = B > kGemmMinRows ? reinterpret_cast<uint16_t*>(ws + lay.x16) : nullptr;
     const a8w8_layer_taps none = {};
     const a8w8_layer_taps& T = taps ? *taps : none;
 
@@ -395,7 +402,7 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     cudaError_t e = cudaSuccess;
     {
         // a2-a4: input RMSNorm + quantisation (prologue) + QKV projection
-        e = run_gemv(PRO_NORM_QUANT, EPI_STORE, 1, g, B, L, qx, qs, gacc);
+        e = run_gemv(PRO_NORM_QUANT, EPI_STORE, 1, g, B, L, qx, qs, gacc, x16);
         if (e != cudaSuccess) return cuda_fail(e, "QKV projection");
         // a5-a8: QK norm, RoPE, KV write, paged attention
         if (kv8) {
@@ -427,7 +434,7 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
         // the O matrix (26 MB) fits the grid's shared memory: each CTA
         // requests its whole share before waiting for the attention output
         go.deep = 1;
-        e = run_gemv(PRO_QUANT, EPI_STORE, 1, go, B, L, qx, qs, gacc);
+        e = run_gemv(PRO_QUANT, EPI_STORE, 1, go, B, L, qx, qs, gacc, x16);
         if (e != cudaSuccess) return cuda_fail(e, "O projection");
     }
     if (T.qkv) {
@@ -458,7 +465,7 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     g.tap_x = reinterpret_cast<bf16*>(T.hn);
     g.tap_q = T.hq;
     g.tap_s = T.hs;
-    e = run_gemv(PRO_NORM_QUANT, EPI_SWIGLU, 1, g, B, L, qx, qs, gacc);
+    e = run_gemv(PRO_NORM_QUANT, EPI_SWIGLU, 1, g, B, L, qx, qs, gacc, x16);
     if (e != cudaSuccess) return cuda_fail(e, "Gate/Up projection");
     if (T.act) {
         e = cudaMemcpyAsync(T.act, act, (size_t)B * I * 2, cudaMemcpyDeviceToDevice, L.stream);
@@ -478,7 +485,7 @@ a8w8_status enqueue_layer(const a8w8_layer_weights* w, const a8w8_config& c, int
     g.ldy = H;
     g.tap_q = T.actq;
     g.tap_s = T.acts;
-    e = run_gemv(PRO_QUANT, EPI_STORE, c.down_k_splits, g, B, L, qx, qs, gacc);
+    e = run_gemv(PRO_QUANT, EPI_STORE, c.down_k_splits, g, B, L, qx, qs, gacc, x16);
     if (e != cudaSuccess) return cuda_fail(e, "down projection");
     return A8W8_OK;
 }
@@ -708,18 +715,20 @@ a8w8_status a8w8_gate_up_swiglu(const int8_t* xq, const float* x_scale, int M, i
 }
 
 a8w8_status a8w8_matmul_i8(const int8_t* xq, int M, int K, const int8_t* W, int N, int k0, int k1,
-                           int32_t* acc, void* stream) {
+                           int32_t* acc, void* scratch, void* stream) {
     const char* name = "a8w8_matmul_i8";
     if (M < 0 || N < 0 || K < 0) return fail(A8W8_ERR_INVALID_ARG, "%s: negative size", name);
     if (M == 0 || N == 0) return A8W8_OK;
     if (K == 0 || K % 64 || k0 < 0 || k1 > K || k0 % 64 || (k1 - k0) <= 0 || (k1 - k0) % 64)
         return fail(A8W8_ERR_UNSUPPORTED_SHAPE,
                     "%s: K, k0 and k1 - k0 must be positive multiples of 64 with k1 <= K", name);
-    a8w8_status s = check_ptrs({xq, W, acc}, name);
+    a8w8_status s = check_ptrs({xq, W, acc, scratch}, name);
     if (s != A8W8_OK) return s;
     Launch L = make_launch(stream, false);
     if (L.num_sms <= 0) return fail(A8W8_ERR_CUDA, "%s: no CUDA device", name);
-    cudaError_t e = launch_gemm_tc(xq, M, W, N, K, k0, k1, acc, N, device_error_word(), L);
+    uint16_t* x16 = static_cast<uint16_t*>(scratch);
+    cudaError_t e = launch_i8_to_f16(xq, (size_t)M * K, x16, L);
+    if (e == cudaSuccess) e = launch_gemm_tc(x16, M, W, N, K, k0, k1, acc, N, device_error_word(), L);
     return e == cudaSuccess ? A8W8_OK : cuda_fail(e, name);
 }
 

@@ -76,14 +76,18 @@ size_t gemm_acc_bytes(int M, int N, int epilogue, int k_splits) {
 }
 
 cudaError_t launch_gemm_projection(int epilogue, int k_splits, const GemvParams& p, int32_t* acc,
-                                   const Launch& L) {
+                                   uint16_t* x16, const Launch& L) {
     if (p.M <= 0) return cudaSuccess;
-    if (!p.xq || !p.x_scale || !gemm_supported(p.K, k_splits)) return cudaErrorInvalidValue;
+    if (!p.xq || !p.x_scale || !x16 || !gemm_supported(p.K, k_splits)) return cudaErrorInvalidValue;
+    {
+        cudaError_t e = launch_i8_to_f16(p.xq, (size_t)p.M * p.K, x16, L);
+        if (e != cudaSuccess) return e;
+    }
     if (epilogue == EPI_SWIGLU && k_splits != 1) return cudaErrorInvalidValue;
     const int Nc = epilogue == EPI_SWIGLU ? 2 * p.N : p.N;
     const int Ks = p.K / k_splits;
     for (int s = 0; s < k_splits; ++s) {
-        cudaError_t e = launch_gemm_tc(p.xq, p.M, p.W, Nc, p.K, s * Ks, (s + 1) * Ks,
+        cudaError_t e = launch_gemm_tc(x16, p.M, p.W, Nc, p.K, s * Ks, (s + 1) * Ks,
                                        acc + (size_t)s * p.M * Nc, Nc, p.err, L);
         if (e != cudaSuccess) return e;
     }

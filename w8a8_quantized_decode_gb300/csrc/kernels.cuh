@@ -85,14 +85,18 @@ cudaError_t launch_quant_prep(int prologue, const GemvParams& p, int8_t* xq, flo
 // PRO_I8 input (p.xq, p.x_scale); K a multiple of 64 * k_splits.
 bool gemm_supported(int K, int k_splits);
 // tcgen05 form of the prefill GEMM: C[m][n] = sum_{k in [k0, k1)} X[m][k] *
-// W[n][k] (INT32, exact) for X [M, K], W [N, K] INT8 (rows of K bytes), into
-// C [M, ldc]; k0 and k1 - k0 multiples of 64.
+// W[n][k] (INT32, exact) for the INT8 codes X [M, K] given as their FP16
+// images X16 (launch_i8_to_f16), W [N, K] INT8 (rows of K bytes), into C [M,
+// ldc]; k0 and k1 - k0 multiples of 64.
 bool gemm_tc_supported(int K, int k_splits);
-cudaError_t launch_gemm_tc(const int8_t* X, int M, const int8_t* W, int N, int K, int k0, int k1,
+cudaError_t launch_gemm_tc(const uint16_t* X16, int M, const int8_t* W, int N, int K, int k0, int k1,
                            int32_t* C, int ldc, unsigned* err, const Launch& L);
+// y[i] = the FP16 image of the code x[i] (exact), n a multiple of 16.
+cudaError_t launch_i8_to_f16(const int8_t* x, size_t n, uint16_t* y, const Launch& L);
 size_t gemm_acc_bytes(int M, int N, int epilogue, int k_splits);
+// x16: room for the FP16 images of p.xq (p.M * p.K values).
 cudaError_t launch_gemm_projection(int epilogue, int k_splits, const GemvParams& p, int32_t* acc,
-                                   const Launch& L);
+                                   uint16_t* x16, const Launch& L);
 
 // ---------------------------------------------------------------------------
 // KV write and paged decode attention
