@@ -75,9 +75,9 @@ __host__ __device__ constexpr TcSmem tc_smem() {
     s.w16 = s.x16 + (size_t)kS8 * kTileX16;           // [kS16][16 KB], 1024-aligned
     s.w8 = s.w16 + (size_t)kS16 * kTileW16;           // [kS8][8 KB]
     s.bars = s.w8 + (size_t)kS8 * kTileW8;
-    // barriers: full8 [kS8]; full16, empty16 [kConvGroups]; accfull,
-    // accempty; done; then the tensor-memory base and the abort flag
-    s.total = s.bars + (size_t)(kS8 + 2 * kConvGroups + 2 + 1) * 8 + 16;
+    // barriers: full8, empty8 [kS8]; full16 [kS16]; empty16 [kConvGroups];
+    // accfull, accempty; done; then the tensor-memory base and the abort flag
+    s.total = s.bars + (size_t)(2 * kS8 + kS16 + kConvGroups + 2 + 1) * 8 + 16;
     return s;
 }
 // dynamic shared memory requested: the layout plus room to align it to 1024
@@ -157,8 +157,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     int8_t* w8 = reinterpret_cast<int8_t*>(smem + L.w8);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L.bars);
     uint64_t* full8 = bars;                   // TMA stage landed
-    uint64_t* full16 = full8 + kS8;           // converter group's slot written
-    uint64_t* empty16 = full16 + kConvGroups; // MMAs of the slot's pair done
+    uint64_t* empty8 = full8 + kS8;           // MMAs of the stage's step done
+    uint64_t* full16 = empty8 + kS8;          // converted W tile written
+    uint64_t* empty16 = full16 + kS16;        // MMAs of the slot's pair done
     uint64_t* accfull = empty16 + kConvGroups;
     uint64_t* accempty = accfull + 1;
     uint64_t* done = accempty + 1;
@@ -172,11 +173,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int nchunks = (steps + kChunkSteps - 1) / kChunkSteps;
 
     if (tid == 0) {
-        for (int i = 0; i < kS8; ++i) mbar_init(&full8[i], 1);   // the producer's expect-tx arrival
-        for (int i = 0; i < kConvGroups; ++i) {
-            mbar_init(&full16[i], 4);     // one arrival per warp of the converting group
-            mbar_init(&empty16[i], 1);    // the MMA commit
+        for (int i = 0; i < kS8; ++i) {
+            mbar_init(&full8[i], 1);      // the producer's expect-tx arrival
+            mbar_init(&empty8[i], 1);     // the MMA commit
         }
+        for (int i = 0; i < kS16; ++i) mbar_init(&full16[i], 4);   // one per converter warp
+        for (int i = 0; i < kConvGroups; ++i) mbar_init(&empty16[i], 1);   // the MMA commit
         mbar_init(accfull, 1);            // the MMA commit
         mbar_init(accempty, kDrainWarps); // one arrival per drain warp
         mbar_init(done, 1);
@@ -196,14 +198,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     pdl_trigger();
 
     if (warp == 0) {
-        // ---- TMA producer: step s into stage s % kS8, once the MMAs of the
-        // pair that last used the stage (pair s / 2 - 2) are done ----
+        // ---- TMA producer: step s into stage s % kS8, once the MMAs of step
+        // s - kS8 are done ----
         int issued = 0;
         if (lane == 0) {
             for (int s = 0; s < steps; ++s) {
-                const int st = s % kS8, P = s / 2;
-                if (P >= 2 &&
-                    !mbar_wait(&empty16[P % kConvGroups], ((P / kConvGroups) - 1) & 1, abort)) {
+                const int st = s % kS8;
+                if (s >= kS8 && !mbar_wait(&empty8[st], ((s / kS8) - 1) & 1, abort)) {
                     if (!*abort) set_timeout(err, abort);
                     break;
                 }
@@ -230,15 +231,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 // drain of the previous chunk must have read them
                 if (first && c >= 1) ok = mbar_wait(accempty, (c - 1) & 1, abort);
                 const int slot = P % kConvGroups;
-                if (ok) ok = mbar_wait(&full16[slot], (P / kConvGroups) & 1, abort);
-                for (int u = 0; u < ns && ok; ++u)
-                    ok = mbar_wait(&full8[(s0 + u) % kS8], ((s0 + u) / kS8) & 1, abort);
-                if (!ok) {
-                    if (!*abort) set_timeout(err, abort);
-                    break;
-                }
-                tc_fence_after();
-                for (int u = 0; u < ns; ++u) {
+                for (int u = 0; u < ns && ok; ++u) {
+                    ok = mbar_wait(&full16[2 * slot + u], (P / kConvGroups) & 1, abort) &&
+                         mbar_wait(&full8[(s0 + u) % kS8], ((s0 + u) / kS8) & 1, abort);
+                    if (!ok) break;
+                    tc_fence_after();
                     const uint64_t ad =
                         sw128_kmajor_desc(smem_u32(w16 + (size_t)(2 * slot + u) * kTileW16));
                     const uint64_t bd =
@@ -247,9 +244,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     for (int j = 0; j < kTK / 16; ++j)
                         mma_f16(tmem, ad + 2 * j, bd + 2 * j, idesc,
                                 (first && u == 0 && j == 0) ? 0u : 1u);
+                    // the TMA stage is free once this step's MMAs are done
+                    mma_commit(&empty8[(s0 + u) % kS8]);
                 }
-                // one commit per pair: frees the converted slot and the pair's
-                // TMA stages
+                if (!ok) {
+                    if (!*abort) set_timeout(err, abort);
+                    break;
+                }
+                // the converted slot is free once the pair's MMAs are done
                 mma_commit(&empty16[slot]);
                 const int s1 = s0 + ns - 1;
                 if (s1 % kChunkSteps == kChunkSteps - 1 || s1 == steps - 1) mma_commit(accfull);
@@ -267,18 +269,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int P = grp; P < npairs; P += kConvGroups) {
             const int s0 = 2 * P, ns = min(2, steps - s0), use = P / kConvGroups;
             bool ok = use == 0 || mbar_wait(&empty16[grp], (use - 1) & 1, abort);
-            for (int u = 0; u < ns && ok; ++u)
+            for (int u = 0; u < ns && ok; ++u) {
                 ok = mbar_wait(&full8[(s0 + u) % kS8], ((s0 + u) / kS8) & 1, abort);
+                if (!ok) break;
+                convert_tile(w8 + (size_t)((s0 + u) % kS8) * kTileW8,
+                             w16 + (size_t)(2 * grp + u) * kTileW16, t);
+                fence_async_shared();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&full16[2 * grp + u]);
+            }
             if (!ok) {
                 if (!*abort) set_timeout(err, abort);
                 break;
             }
-            for (int u = 0; u < ns; ++u)
-                convert_tile(w8 + (size_t)((s0 + u) % kS8) * kTileW8,
-                             w16 + (size_t)(2 * grp + u) * kTileW16, t);
-            fence_async_shared();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&full16[grp]);
         }
     } else {
         // ---- drain: FP32 chunk -> INT32 sum; after the last chunk, C. Warp
@@ -298,10 +301,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int g = 0; g < 4; ++g) {
                 const uint32_t col = (uint32_t)(128 * h + 32 * g);
                 uint32_t f[32], a[32];
-                tmem_ld32(lane_base + col, f);
                 if (c > 0) {
-                    tmem_ld32(lane_base + kSumCol + col, a);
+                    tmem_ld32x2(lane_base + col, f, lane_base + kSumCol + col, a);
                 } else {
+                    tmem_ld32(lane_base + col, f);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) a[i] = 0u;
                 }
