@@ -282,6 +282,21 @@ __device__ __forceinline__ f2 rms_inv(f2 ss, int n, float eps) {
 __device__ __forceinline__ bf16 norm_bf16(float x, float w, f2 inv) {
     return f2_to_bf16(f2_mulf(inv, __fmul_rn(x, w)));
 }
+// The same rounding of xw * inv for an exact float32 xw (= x w), taking the
+// float product p = RN(xw inv.hi) where it decides: the exact value differs
+// from p by at most 1.5 float32 units (the product's rounding error and
+// xw inv.lo), and BF16 rounding changes only at the midpoints between BF16
+// values, where the low 16 bits of a float are 0x8000. Away from them
+// (more than 4 units) and for normal finite p, RN_bf16(p) is the answer;
+// otherwise the two-float product decides.
+__device__ __forceinline__ bf16 norm_bf16_fast(float xw, f2 inv) {
+    const float pr = __fmul_rn(xw, inv.hi);
+    const unsigned u = __float_as_uint(pr);
+    const unsigned ex = u & 0x7F800000u;
+    const unsigned d = (u & 0xFFFFu) - 0x7FFCu;   // < 9 within 4 units of the midpoint
+    if (d >= 9u && ex != 0u && ex != 0x7F800000u) return __float2bfloat16_rn(pr);
+    return f2_to_bf16(f2_mulf(inv, xw));
+}
 
 __device__ __forceinline__ void set_error(unsigned* err, unsigned bit) {
     if (err) atomicOr(err, bit);

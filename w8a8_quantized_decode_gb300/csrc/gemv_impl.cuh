@@ -96,13 +96,76 @@ __device__ __forceinline__ void block_rms_inv(f2 (&ss)[BT], float* red, int K, f
 // enough for K = 8192 with 1024 or 512 threads.
 __host__ __device__ constexpr int norm_pre_slots(int NT) { return NT >= 1024 ? 1 : 2; }
 
+// Row statistics with one barrier: per row the sum of squares (a float
+// pair) and a maximum, reduced over the block. red: 3 * kMaxWarps * BT floats.
+template <int BT>
+__device__ __forceinline__ void block_stats(f2 (&ss)[BT], float (&mx)[BT], float* red) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+#pragma unroll
+    for (int b = 0; b < BT; ++b) {
+        const f2 t = warp_sum_f2(ss[b]);
+        const float m = warp_max(mx[b]);
+        if (lane == 0) {
+            red[2 * (b * kMaxWarps + warp)] = t.hi;
+            red[2 * (b * kMaxWarps + warp) + 1] = t.lo;
+            red[2 * kMaxWarps * BT + b * kMaxWarps + warp] = m;
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int b = 0; b < BT; ++b) {
+        f2 t = {0.0f, 0.0f};
+        float m = 0.0f;
+        if (lane < nw) {
+            t.hi = red[2 * (b * kMaxWarps + lane)];
+            t.lo = red[2 * (b * kMaxWarps + lane) + 1];
+            m = red[2 * kMaxWarps * BT + b * kMaxWarps + lane];
+        }
+        ss[b] = warp_sum_f2(t);
+        mx[b] = warp_max(m);
+    }
+}
+
+// The INT8 codes of eight consecutive values of one row, packed into two
+// words. `fast` (the row's s > 0 with a finite R, decided once per row) takes
+// quant_code's division-free form without its per-element checks; the
+// results are quant_code's.
+__device__ __forceinline__ uint2 quant8(const float (&f)[8], float s, float R, bool fast) {
+    int c[8];
+    if (fast) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float q0 = __fmul_rn(f[e], R);
+            const float q = __fmaf_rn(__fmaf_rn(-q0, s, f[e]), R, q0);
+            c[e] = max(-127, min(127, __float2int_rn(q)));
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) c[e] = quant_code(f[e], s, R);
+    }
+    const unsigned lo = __byte_perm(__byte_perm(c[0], c[1], 0x0040), __byte_perm(c[2], c[3], 0x0040), 0x5410);
+    const unsigned hi = __byte_perm(__byte_perm(c[4], c[5], 0x0040), __byte_perm(c[6], c[7], 0x0040), 0x5410);
+    return make_uint2(lo, hi);
+}
+
 // Quantised activation rows into act[BT][K] and their scales into xs[BT].
 // The BF16 rows are read from L2 once (each thread issues up to four 16-byte
 // loads before using any); when `stage` is given they are kept in shared
-// memory for the later passes (normalisation, quantisation). With `nw_pre`
-// the RMSNorm weight is taken from `nwr` (loaded before the wait).
-// `issued()` is called once, right after the first activation loads have been
-// issued (the caller can queue more weight loads behind them).
+// memory for the second pass. With `nw_pre` the RMSNorm weight is taken from
+// `nwr` (loaded before the wait). `issued()` is called once, right after the
+// first activation loads have been issued (the caller can queue more weight
+// loads behind them). With RMSNorm the stage holds the normalised BF16 rows
+// afterwards.
+//
+// Two passes and one block reduction. Pass 1 forms each row's sum of squares
+// and the maximum of |x| (plain quantisation) or of |x w| (RMSNorm). The
+// second is enough for the absmax of the normalised row: x w is exact in
+// float32 (two 8-bit significands), and the normalised value is the BF16
+// rounding of x w times the two-float 1/rms, whose error (about 2^-47
+// relative) is far below the 2^-24 gap between distinct float32 values of
+// x w, so that value is a non-decreasing function of |x w| and its largest
+// magnitude belongs to the largest |x w|. Pass 2 normalises (norm_bf16_fast)
+// and quantises each element in one go.
 template <int BT, int PRO, int NP, class Hook>
 __device__ __forceinline__ void prologue(const GemvParams& p, int8_t* act, float* xs, float* red,
                                          bf16* stage, const int4 (&nwr)[NP], bool nw_pre,
@@ -123,13 +186,28 @@ __device__ __forceinline__ void prologue(const GemvParams& p, int8_t* act, float
         return;
     }
     const int vec = K / 8;
-    // pass 1 (L2): sum of squares (RMSNorm) or absmax (plain quantisation)
-    constexpr int C = BT == 1 ? 4 : (BT == 2 ? 2 : 1);   // loads in flight per row
-    float st[BT];    // absmax (plain quantisation)
-    f2 ss[BT];       // sum of squares (RMSNorm)
+    // the RMSNorm weight of vector j: from the registers loaded before the
+    // wait (slot (j - thread) / nt) or from memory
+    auto norm_w = [&](int j) -> int4 {
+        if (nw_pre) {
+            const int slot = (j - (int)threadIdx.x) / nt;
+            int4 w = make_int4(0, 0, 0, 0);
+#pragma unroll
+            for (int i = 0; i < NP; ++i)
+                if (slot == i) w = nwr[i];
+            return w;
+        }
+        return ld_nc_v4(p.norm_w + 8 * j);
+    };
+    // pass 1 (L2): sum of squares and max |x w| (RMSNorm) or max |x|; loads
+    // in flight per row (a normalised row of K <= 8192 is one vector per
+    // thread at 1024 threads, so its loads are all in flight with C = 1 or 2)
+    constexpr int C = PRO == PRO_NORM_QUANT ? (BT == 1 ? 2 : 1) : (BT == 1 ? 4 : (BT == 2 ? 2 : 1));
+    float mx[BT];
+    f2 ss[BT];
 #pragma unroll
     for (int b = 0; b < BT; ++b) {
-        st[b] = 0.0f;
+        mx[b] = 0.0f;
         ss[b].hi = ss[b].lo = 0.0f;
     }
     bool first = true;
@@ -151,6 +229,8 @@ __device__ __forceinline__ void prologue(const GemvParams& p, int8_t* act, float
         for (int c = 0; c < C; ++c) {
             const int j = j0 + c * nt;
             if (j < vec) {
+                float w[8];
+                if (PRO == PRO_NORM_QUANT) unpack8(norm_w(j), w);
 #pragma unroll
                 for (int b = 0; b < BT; ++b) {
                     if (b < M) {
@@ -159,8 +239,12 @@ __device__ __forceinline__ void prologue(const GemvParams& p, int8_t* act, float
                         unpack8(raw[c][b], f);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
-                            if (PRO == PRO_NORM_QUANT) f2_acc(ss[b], __fmul_rn(f[e], f[e]));
-                            else st[b] = fmaxf(st[b], fabsf(f[e]));
+                            if (PRO == PRO_NORM_QUANT) {
+                                f2_acc(ss[b], __fmul_rn(f[e], f[e]));
+                                mx[b] = fmaxf(mx[b], fabsf(__fmul_rn(f[e], w[e])));
+                            } else {
+                                mx[b] = fmaxf(mx[b], fabsf(f[e]));
+                            }
                         }
                     }
                 }
@@ -168,52 +252,19 @@ __device__ __forceinline__ void prologue(const GemvParams& p, int8_t* act, float
         }
     }
     if (first) issued();
-    float sc[BT];
+    float sc[BT], rc[BT];
     f2 inv[BT];
     if (PRO == PRO_NORM_QUANT) {
-        block_rms_inv<BT>(ss, red, K, p.eps, inv);            // red[0, 2 W BT)
-        // pass 2: normalised BF16 row (kept in the stage) and its absmax
-        const bool tapx = (blockIdx.x == 0) && p.tap_x != nullptr;
-        float am[BT];
+        block_stats<BT>(ss, mx, red);
 #pragma unroll
-        for (int b = 0; b < BT; ++b) am[b] = 0.0f;
-        auto pass2 = [&](int j, const int4 wraw) {
-            float w[8];
-            unpack8(wraw, w);
-#pragma unroll
-            for (int b = 0; b < BT; ++b) {
-                if (b < M) {
-                    const int4 raw = stage ? *reinterpret_cast<const int4*>(stage + (size_t)b * K + 8 * j)
-                                           : ld_cg_v4(p.x + (size_t)b * p.ldx + 8 * j);
-                    float f[8];
-                    unpack8(raw, f);
-                    __align__(16) bf16 y[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        y[e] = norm_bf16(f[e], w[e], inv[b]);
-                        am[b] = fmaxf(am[b], fabsf(bf2f(y[e])));
-                    }
-                    if (stage) *reinterpret_cast<int4*>(stage + (size_t)b * K + 8 * j) = *reinterpret_cast<const int4*>(y);
-                    if (tapx) *reinterpret_cast<int4*>(p.tap_x + (size_t)b * K + 8 * j) = *reinterpret_cast<const int4*>(y);
-                }
-            }
-        };
-        if (nw_pre) {
-#pragma unroll
-            for (int i = 0; i < NP; ++i) {
-                const int j = threadIdx.x + i * nt;
-                if (j < vec) pass2(j, nwr[i]);
-            }
-        } else {
-            for (int j = threadIdx.x; j < vec; j += nt) pass2(j, ld_nc_v4(p.norm_w + 8 * j));
+        for (int b = 0; b < BT; ++b) {
+            inv[b] = rms_inv(ss[b], K, p.eps);
+            sc[b] = __fdiv_rn(bf2f(f2_to_bf16(f2_mulf(inv[b], mx[b]))), 127.0f);
         }
-        block_max<BT>(am, red + 2 * kMaxWarps * BT);          // red[2 W BT, 3 W BT)
-#pragma unroll
-        for (int b = 0; b < BT; ++b) sc[b] = __fdiv_rn(am[b], 127.0f);
     } else {
-        block_max<BT>(st, red);
+        block_max<BT>(mx, red);
 #pragma unroll
-        for (int b = 0; b < BT; ++b) sc[b] = __fdiv_rn(st[b], 127.0f);
+        for (int b = 0; b < BT; ++b) sc[b] = __fdiv_rn(mx[b], 127.0f);
     }
     if (threadIdx.x < BT) {
 #pragma unroll
@@ -221,41 +272,43 @@ __device__ __forceinline__ void prologue(const GemvParams& p, int8_t* act, float
             if (b == (int)threadIdx.x) xs[b] = sc[b];
     }
     const bool tap = (blockIdx.x == 0) && p.tap_q != nullptr;
+    const bool tapx = PRO == PRO_NORM_QUANT && (blockIdx.x == 0) && p.tap_x != nullptr;
     if (tap && threadIdx.x < M && p.tap_s) {
 #pragma unroll
         for (int b = 0; b < BT; ++b)
             if (b == (int)threadIdx.x) p.tap_s[b] = sc[b];
     }
-    // pass 3: INT8 codes of the BF16 row that is quantised
-    float rc[BT];
+    bool fast[BT];
 #pragma unroll
-    for (int b = 0; b < BT; ++b) rc[b] = quant_recip(sc[b]);
+    for (int b = 0; b < BT; ++b) {
+        rc[b] = quant_recip(sc[b]);
+        fast[b] = sc[b] != 0.0f && isfinite(rc[b]);
+    }
+    // pass 2: normalised BF16 values (RMSNorm) and their INT8 codes
     for (int j = threadIdx.x; j < vec; j += nt) {
         float w[8];
-        if (PRO == PRO_NORM_QUANT && !stage) unpack8(ld_nc_v4(p.norm_w + 8 * j), w);
+        if (PRO == PRO_NORM_QUANT) unpack8(norm_w(j), w);
 #pragma unroll
         for (int b = 0; b < BT; ++b) {
-            uint32_t lo = 0, hi = 0;
+            uint2 code = make_uint2(0u, 0u);
             if (b < M) {
                 float f[8];
-                if (stage) {
-                    unpack8(*reinterpret_cast<const int4*>(stage + (size_t)b * K + 8 * j), f);
-                } else {
-                    unpack8(ld_cg_v4(p.x + (size_t)b * p.ldx + 8 * j), f);
-                    if (PRO == PRO_NORM_QUANT) {
+                unpack8(stage ? *reinterpret_cast<const int4*>(stage + (size_t)b * K + 8 * j)
+                              : ld_cg_v4(p.x + (size_t)b * p.ldx + 8 * j), f);
+                if (PRO == PRO_NORM_QUANT) {
+                    __align__(16) bf16 y[8];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) f[e] = bf2f(norm_bf16(f[e], w[e], inv[b]));
+                    for (int e = 0; e < 8; ++e) {
+                        y[e] = norm_bf16_fast(__fmul_rn(f[e], w[e]), inv[b]);
+                        f[e] = bf2f(y[e]);
                     }
+                    if (stage) *reinterpret_cast<int4*>(stage + (size_t)b * K + 8 * j) = *reinterpret_cast<const int4*>(y);
+                    if (tapx) *reinterpret_cast<int4*>(p.tap_x + (size_t)b * K + 8 * j) = *reinterpret_cast<const int4*>(y);
                 }
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const uint32_t c = (uint32_t)(quant_code(f[e], sc[b], rc[b]) & 0xff);
-                    if (e < 4) lo |= c << (8 * e);
-                    else hi |= c << (8 * (e - 4));
-                }
+                code = quant8(f, sc[b], rc[b], fast[b]);
             }
-            *reinterpret_cast<uint2*>(act + (size_t)b * K + 8 * j) = make_uint2(lo, hi);
-            if (tap && b < M) *reinterpret_cast<uint2*>(p.tap_q + (size_t)b * K + 8 * j) = make_uint2(lo, hi);
+            *reinterpret_cast<uint2*>(act + (size_t)b * K + 8 * j) = code;
+            if (tap && b < M) *reinterpret_cast<uint2*>(p.tap_q + (size_t)b * K + 8 * j) = code;
         }
     }
     __syncthreads();
