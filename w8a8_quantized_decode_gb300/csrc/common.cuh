@@ -238,55 +238,26 @@ __device__ __forceinline__ f2 f2_rsqrt(f2 s) {
     const float e = __fsub_rn(__fsub_rn(1.0f, t.hi), t.lo);   // 1 - t.hi is exact
     return fast_two_sum(y, __fmul_rn(__fmul_rn(y, e), 0.5f));
 }
-// One of four two-float constants by a 2-bit index (0 gives 1).
-__device__ __forceinline__ f2 f2_pick4(int i, f2 a1, f2 a2, f2 a3) {
-    return i == 0 ? f2{1.0f, 0.0f} : (i == 1 ? a1 : (i == 2 ? a2 : a3));
-}
-// exp(x) for x.hi <= 88.5 (0 below x.hi = -104), table-driven in the manner of
-// Tang (ACM TOMS 15(2), 1989) with the table replaced by products:
-//   x = k ln2/64 + r, |r| <= ln2/128; k = 64 m + j;
-//   exp(x) = 2^m * 2^(j/64) * (1 + expm1(r)).
-// ln2/64 = c1 + c2 + c3 with c1 = 710/2^16 (10 significant bits), so k c1 is
-// exact for |k| < 2^14 and x.hi - k c1 is exact (Sterbenz); r is formed as a
-// pair. expm1(r) = r + r^2/2 + r^3/6 + r^4/24 + r^5/120 (the next term is
-// below 3.5e-17): r^2/2 as a pair, the rest in float (below 2.6e-8). 2^(j/64)
-// is the product of three two-float factors 2^(j0/64) 2^(4 j1/64) 2^(16 j2/64)
-// for the 2-bit digits of j, each hi = RN(v), lo = RN(v - hi) of the
-// exact power. Relative error about 2^-46 (a float32 model of these steps
-// against a 40-digit reference: worst 2^-46.3 over [-104, 88]).
-__device__ __forceinline__ f2 f2_exp(f2 x) {
+// exp(x) for x.hi <= 88 (underflows to 0 below about -103): x = k ln2 + r,
+// exp(r) = (1 + p)^(2^8) with p = expm1(r / 2^8) from its Taylor series to
+// the fourth power, squared eight times in expm1 form (1 + p)^2 = 1 + (2p +
+// p^2); then scaled by 2^k.
+static __device__ __noinline__ f2 f2_exp(f2 x) {
     if (x.hi < -104.0f) return f2{0.0f, 0.0f};
     if (x.hi > 88.5f) return f2{INFINITY, 0.0f};
-    const float kf = rintf(__fmul_rn(x.hi, 92.33248138427734f));   // 64 / ln2
-    const int k = (int)kf;
-    const float t = __fsub_rn(x.hi, __fmul_rn(kf, 0.010833740234375f));
-    f2 r = f2_add(f2{t, 0.0f}, f2{x.lo, 0.0f});
-    r = f2_sub(r, two_prod(kf, -3.3155381515825866e-06f));
-    r = f2_addf(r, -__fmul_rn(kf, 2.572804640231345e-14f));
-    f2 r2 = two_prod(r.hi, r.hi);
-    r2.lo = __fmaf_rn(__fmul_rn(2.0f, r.hi), r.lo, r2.lo);
-    const f2 half = {__fmul_rn(r2.hi, 0.5f), __fmul_rn(r2.lo, 0.5f)};
-    const float tail = __fmul_rn(__fmul_rn(r.hi, r2.hi),
-                                 __fmaf_rn(r.hi, __fmaf_rn(r.hi, 0.008333333767950535f, 0.0416666679084301f),
-                                           0.1666666716337204f));
-    const f2 em1 = f2_add(r, f2_addf(half, tail));
-    const int j = k & 63, m = k >> 6;
-    const f2 a = f2_pick4(j & 3, f2{1.0108892917633057f, -5.7116054108519165e-09f},
-                          f2{1.0218971967697144f, -4.811559861650494e-08f},
-                          f2{1.0330249071121216f, -2.809089316713198e-08f});
-    const f2 b = f2_pick4((j >> 2) & 3, f2{1.0442737340927124f, 4.8334701574503924e-08f},
-                          f2{1.0905077457427979f, -1.3077539939843064e-08f},
-                          f2{1.1387885808944702f, 5.386222312608879e-08f});
-    const f2 c = f2_pick4(j >> 4, f2{1.1892070770263672f, 3.797635272917432e-08f},
-                          f2{1.4142135381698608f, 2.4203234971764687e-08f},
-                          f2{1.6817928552627563f, -2.4755326677450284e-08f});
-    const f2 T = f2_mul(f2_mul(a, b), c);
-    const f2 e = f2_add(T, f2_mul(T, em1));
-    if (m >= -126) {
-        const float sc = __int_as_float((m + 127) << 23);   // 2^m, exact
-        return f2{__fmul_rn(e.hi, sc), __fmul_rn(e.lo, sc)};
-    }
-    return f2{ldexpf(e.hi, m), ldexpf(e.lo, m)};
+    const float k = rintf(__fmul_rn(x.hi, 1.44269504088896341f));
+    const f2 ln2 = {0.693147182464599609375f, -1.904654323148236e-09f};   // ln 2 = hi + lo
+    const f2 r = f2_sub(x, f2_mulf(ln2, k));
+    const f2 t = f2{__fmul_rn(r.hi, 0.00390625f), __fmul_rn(r.lo, 0.00390625f)};   // r / 2^8
+    const f2 t2 = f2_mul(t, t);
+    const float t3 = __fmul_rn(t2.hi, t.hi);
+    const float tail = __fmaf_rn(__fmul_rn(t3, t.hi), 1.0f / 24.0f, __fmul_rn(t3, 1.0f / 6.0f));
+    f2 p = f2_addf(f2_add(t, f2{__fmul_rn(t2.hi, 0.5f), __fmul_rn(t2.lo, 0.5f)}), tail);
+#pragma unroll 1
+    for (int i = 0; i < 8; ++i) p = f2_add(f2{__fmul_rn(p.hi, 2.0f), __fmul_rn(p.lo, 2.0f)}, f2_mul(p, p));
+    const f2 e = f2_addf(p, 1.0f);
+    const int ki = (int)k;
+    return f2{ldexpf(e.hi, ki), ldexpf(e.lo, ki)};
 }
 // BF16 nearest-even rounding of the value hi + lo.
 __device__ __forceinline__ bf16 f2_to_bf16(f2 v) {
