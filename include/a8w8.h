@@ -546,6 +546,34 @@ a8w8_status a8w8_step_graph_create(a8w8_step_graph** out, const a8w8_model* m,
                                    a8w8_bf16* final_hidden, int device_loop, void* ws,
                                    size_t ws_bytes, void* stream);
 
+/* The same replayable step with sampling beyond greedy inside the graph
+ * ([SRV-61] "Related": device-side embedding and sampling; [SRV-48]
+ * "Performance": temperature and top_p are sampling parameters of the
+ * decode). After the LM head writes the step's logits, the graph runs the
+ * sampler of a8w8_sample on them (same rule: temperature <= 0 is the argmax,
+ * otherwise the Gumbel-max draw over the top_p nucleus) and writes the drawn
+ * tokens to next_tokens; with device_loop they are fed back as the next
+ * step's tokens. The draw of a replay uses the Philox step read from
+ * step_counter (device, one uint64, 8-byte aligned, caller-owned: set it
+ * before the first replay), which the graph advances by one at the end of
+ * every replay, so replay n of a graph whose counter started at s draws
+ * exactly what a8w8_sample(logits, ..., seed, s + n) would on that replay's
+ * logits. logits (device [B, vocab] float32) is required here.
+ * sample_ws / sample_ws_bytes: at least a8w8_sample_workspace_bytes(B, vocab)
+ * bytes of 16-byte aligned device memory owned by the caller, used by every
+ * replay (replays of graphs that share it must not overlap). The persistent
+ * step form (A8W8_FLAG_PERSISTENT_STEP) is not used for a sampled graph.
+ * Errors: as a8w8_step_graph_create, plus a NULL logits or step_counter, a
+ * non-finite temperature, top_p outside (0, 1] and a small sampling
+ * workspace. */
+a8w8_status a8w8_step_graph_create_sampled(
+    a8w8_step_graph** out, const a8w8_model* m, const a8w8_config* cfg, int B, int max_blocks,
+    int num_blocks, a8w8_bf16* const* k_caches, a8w8_bf16* const* v_caches, const float* rope,
+    int max_pos, int32_t* token_ids, int32_t* slot_mapping, int32_t* block_table,
+    int32_t* ctx_lens, int32_t* next_tokens, float* logits, a8w8_bf16* final_hidden,
+    int device_loop, float temperature, float top_p, uint64_t seed, uint64_t* step_counter,
+    void* sample_ws, size_t sample_ws_bytes, void* ws, size_t ws_bytes, void* stream);
+
 /* Replays the step on `stream`. */
 a8w8_status a8w8_step_graph_launch(a8w8_step_graph* g, void* stream);
 

@@ -159,6 +159,27 @@ def test_layer_and_step_validation(lib):
     assert L.a8w8_step_graph_launch(None, None) == a8w8.ERR_INVALID_ARG
     L.a8w8_step_graph_destroy(None)
 
+    # sampled graph: its own arguments are checked before anything is captured
+    def sampled(**kw):
+        a = dict(logits=FAKE, T=1.0, top_p=0.9, ctr=FAKE, sws=FAKE, swsb=1 << 30, wsb=1 << 30)
+        a.update(kw)
+        o = ctypes.c_void_p(123)
+        r = L.a8w8_step_graph_create_sampled(
+            ctypes.byref(o), ctypes.byref(m), _cfg(dict(q, num_layers=1)), 1, 2, 4, caches, caches,
+            FAKE, 256, FAKE, FAKE, FAKE, FAKE, FAKE, a["logits"], None, 1, a["T"], a["top_p"], 7,
+            a["ctr"], a["sws"], a["swsb"], FAKE, a["wsb"], None)
+        assert o.value is None
+        return r
+    assert sampled(logits=None) == a8w8.ERR_INVALID_ARG
+    assert sampled(ctr=None) == a8w8.ERR_INVALID_ARG
+    assert sampled(ctr=FAKE + 4) == a8w8.ERR_INVALID_ARG
+    assert sampled(T=float("nan")) == a8w8.ERR_INVALID_ARG
+    assert sampled(top_p=0.0) == a8w8.ERR_INVALID_ARG
+    assert sampled(top_p=1.5) == a8w8.ERR_INVALID_ARG
+    assert sampled(sws=None) == a8w8.ERR_WORKSPACE
+    assert sampled(swsb=100) == a8w8.ERR_WORKSPACE
+    assert sampled(wsb=100) == a8w8.ERR_WORKSPACE   # then the step's own checks
+
 
 def test_rope_table_validation(lib):
     assert lib.a8w8_rope_table(FAKE, 16, 63, 1e6, None) == a8w8.ERR_INVALID_ARG

@@ -6,6 +6,7 @@ import pytest
 
 import oracle
 import synth
+from oracle import sampling
 from gpu_util import STEP_REL_L2, bf16_to_f64, check_lm_head, rel_l2, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
@@ -286,3 +287,41 @@ def test_qwen3_14b_lm_head_full_vocab_vs_oracle(a8w8):
     worst, ties = check_lm_head(to_host(fh), W, to_host(logits), to_host(nxt))
     print("LM head: worst |diff| / bound", worst, "near ties", ties)
     assert a8w8.read_device_errors() == 0
+
+
+@pytest.mark.parametrize("T,top_p", [(0.8, 0.9), (1.3, 1.0), (0.0, 1.0)])
+def test_sampled_device_loop_graph(a8w8, T, top_p):
+    """Sampling inside the replayed step graph: replay i draws exactly what
+    a8w8_sample draws from that replay's logits at step s0 + i (the same
+    kernels), which agrees with the oracle's sampling rule; the drawn tokens
+    are fed back as the next step's tokens and the step counter advances by
+    one per replay; temperature 0 gives the argmax of the logits."""
+    import torch
+    cfg = dict(synth.TINY, num_layers=2, vocab=777)
+    B, n, seed, s0 = 3, 8, 0xABCDEF12345, 5
+    s = Session(a8w8, cfg, B, max_seq=48, seed=460)
+    tok0, slots0, ctx0 = s.inputs(synth.prompt_ids(461, B, cfg["vocab"]))
+    g = a8w8.StepGraph(s.gm, cfg, B, s.max_blocks, s.gkc, s.gvc, s.rope, s.ws, logits=s.logits,
+                       device_loop=True,
+                       sampling=dict(temperature=T, top_p=top_p, seed=seed, step=s0))
+    g.set_inputs(to_dev(tok0), to_dev(slots0), to_dev(s.bt), to_dev(ctx0))
+    agree = 0
+    for i in range(n):
+        g.launch()
+        torch.cuda.synchronize()
+        got = to_host(g.next_tokens)
+        lg = to_host(s.logits)
+        same = to_host(a8w8.a8w8_sample(s.logits, T, top_p, seed=seed, step=s0 + i))
+        assert np.array_equal(got, same), (i, got, same)
+        if T > 0:
+            agree += int((got == sampling.sample_rows(lg, T, top_p, seed, s0 + i)).sum())
+        else:
+            assert np.array_equal(got, np.argmax(lg, axis=1))
+        assert np.array_equal(to_host(g.token_ids), got)        # fed back on the device
+    if T > 0:
+        # float32 Gumbel keys on the device, float64 in the oracle (as for a8w8_sample)
+        assert agree >= n * B - 1, (agree, n * B)
+    assert int(to_host(g.step_counter)[0]) == s0 + n
+    assert np.array_equal(to_host(g.ctx_lens), ctx0 + n)
+    g.close()
+

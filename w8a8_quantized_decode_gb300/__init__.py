@@ -116,6 +116,9 @@ _SIGNATURES = {
                               _sz, _p]),
     "a8w8_step_graph_create": (_i, [ctypes.POINTER(_p), _p, _p, _i, _i, _i, _p, _p, _p, _i, _p,
                                     _p, _p, _p, _p, _p, _p, _i, _p, _sz, _p]),
+    "a8w8_step_graph_create_sampled": (_i, [ctypes.POINTER(_p), _p, _p, _i, _i, _i, _p, _p, _p,
+                                            _i, _p, _p, _p, _p, _p, _p, _p, _i, _f, _f,
+                                            ctypes.c_uint64, _p, _p, _sz, _p, _sz, _p]),
     "a8w8_step_graph_launch": (_i, [_p, _p]),
     "a8w8_step_graph_run_host": (_i, [_p, _p, _p, _p, _p, _p, _p]),
     "a8w8_step_graph_destroy": (None, [_p]),
@@ -603,10 +606,17 @@ class StepGraph:
     ``token_ids``, ``slot_mapping``, ``block_table``, ``ctx_lens`` (write them
     between replays) and ``next_tokens`` (read after a replay). With
     ``device_loop=True`` each replay also prepares the next step on the
-    device (greedy feedback, context advanced by one token)."""
+    device (the drawn token fed back, context advanced by one token).
+
+    ``sampling=dict(temperature=T, top_p=P, seed=S, step=s0)`` samples inside
+    the graph (``a8w8_step_graph_create_sampled``): this object then owns the
+    Philox step counter (``step_counter``, int64 [1], starting at s0 and
+    advanced by each replay) and the sampling workspace, and ``logits`` is
+    required."""
 
     def __init__(self, model: dict, cfg: dict, B: int, max_blocks: int, k_caches, v_caches, rope,
-                 ws, logits=None, final_hidden=None, device_loop=False, stream=None):
+                 ws, logits=None, final_hidden=None, device_loop=False, stream=None,
+                 sampling=None):
         torch = _torch()
         dev = k_caches[0].device
         self._h = _ModelHandle(model, cfg)
@@ -622,12 +632,25 @@ class StepGraph:
         self.next_tokens = torch.zeros(B, dtype=i32, device=dev)
         self._g = None
         g = _p()
-        _check(lib().a8w8_step_graph_create(
-            ctypes.byref(g), ctypes.byref(self._h.model), ctypes.byref(self._h.cfg), B, max_blocks,
-            num_blocks, _cache_array(k_caches), _cache_array(v_caches), _ptr(rope), rope.shape[0],
-            _ptr(self.token_ids), _ptr(self.slot_mapping), _ptr(self.block_table),
-            _ptr(self.ctx_lens), _ptr(self.next_tokens), _ptr(logits), _ptr(final_hidden),
-            1 if device_loop else 0, _ptr(ws), ws.numel(), _stream(stream)))
+        common = (ctypes.byref(g), ctypes.byref(self._h.model), ctypes.byref(self._h.cfg), B,
+                  max_blocks, num_blocks, _cache_array(k_caches), _cache_array(v_caches),
+                  _ptr(rope), rope.shape[0], _ptr(self.token_ids), _ptr(self.slot_mapping),
+                  _ptr(self.block_table), _ptr(self.ctx_lens), _ptr(self.next_tokens),
+                  _ptr(logits), _ptr(final_hidden), 1 if device_loop else 0)
+        if sampling is None:
+            _check(lib().a8w8_step_graph_create(*common, _ptr(ws), ws.numel(), _stream(stream)))
+        else:
+            if logits is None:
+                raise ValueError("sampling inside the step needs a logits buffer")
+            self.step_counter = torch.full((1,), int(sampling.get("step", 0)), dtype=torch.int64,
+                                           device=dev)
+            need = lib().a8w8_sample_workspace_bytes(B, cfg["vocab"])
+            self._sample_ws = torch.empty(need, dtype=torch.uint8, device=dev)
+            _check(lib().a8w8_step_graph_create_sampled(
+                *common, float(sampling.get("temperature", 1.0)), float(sampling.get("top_p", 1.0)),
+                int(sampling.get("seed", 0)) & (2 ** 64 - 1), _ptr(self.step_counter),
+                _ptr(self._sample_ws),
+                need, _ptr(ws), ws.numel(), _stream(stream)))
         self._g = g
         self._torch = torch
 

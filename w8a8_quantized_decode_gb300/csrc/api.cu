@@ -1210,6 +1210,16 @@ static a8w8_status check_step(const a8w8_model* m, const a8w8_config* cfg, int B
     return A8W8_OK;
 }
 
+// Sampling inside a captured step: the sampler runs on the step's logits and
+// overwrites the argmax, reading its Philox step from `step` (advanced by one
+// per step on the device).
+struct StepSampling {
+    float T, top_p;
+    uint64_t seed;
+    uint64_t* step;
+    float* ws;
+};
+
 static a8w8_status enqueue_step(const a8w8_model* m, const a8w8_config& c, int B,
                                 const int32_t* token_ids, const int32_t* slot_mapping,
                                 const int32_t* block_table, int max_blocks, int num_blocks,
@@ -1217,14 +1227,14 @@ static a8w8_status enqueue_step(const a8w8_model* m, const a8w8_config& c, int B
                                 a8w8_bf16* const* v_caches, const float* rope, int max_pos,
                                 int32_t* next_tokens, float* logits, a8w8_bf16* final_hidden,
                                 unsigned char* ws, const Launch& L, bool device_loop,
-                                const KvI8* kv8 = nullptr) {
+                                const KvI8* kv8 = nullptr, const StepSampling* smp = nullptr) {
     // kv8: the layers' INT8 caches (num_layers entries) instead of k_caches /
     // v_caches; the per-operation kernels only
     const WsLayout lay = ws_layout(c, B, max_blocks);
     bf16* hidden = reinterpret_cast<bf16*>(ws + lay.hid);
     unsigned long long* keys = reinterpret_cast<unsigned long long*>(ws + lay.keys);
     unsigned* ticket = reinterpret_cast<unsigned*>(ws + lay.ticket);
-    if (!kv8 && (c.flags & A8W8_FLAG_PERSISTENT_STEP) &&
+    if (!kv8 && !smp && (c.flags & A8W8_FLAG_PERSISTENT_STEP) &&
         step_supported(B, c.head_dim, c.num_layers, c.hidden, c.intermediate, c.num_q_heads,
                        c.num_kv_heads, max_blocks * c.page_size, L.num_sms) &&
         c.down_k_splits == 2) {
@@ -1325,6 +1335,11 @@ static a8w8_status enqueue_step(const a8w8_model* m, const a8w8_config& c, int B
         p.next_tokens = next_tokens + b0;
         e = launch_lmhead_argmax(p, L);
         if (e != cudaSuccess) return cuda_fail(e, "LM head");
+    }
+    if (smp) {
+        e = launch_sample(logits, B, c.vocab, c.vocab, smp->T, smp->top_p, smp->seed, 0, smp->ws,
+                          next_tokens, L, smp->step);
+        if (e != cudaSuccess) return cuda_fail(e, "sampling");
     }
     if (device_loop) {
         e = launch_advance(const_cast<int32_t*>(token_ids), const_cast<int32_t*>(slot_mapping),
@@ -1468,13 +1483,14 @@ struct a8w8_step_graph {
     cudaGraphExec_t exec;
 };
 
-a8w8_status a8w8_step_graph_create(a8w8_step_graph** out, const a8w8_model* m,
-                                   const a8w8_config* cfg, int B, int max_blocks, int num_blocks,
-                                   a8w8_bf16* const* k_caches, a8w8_bf16* const* v_caches,
-                                   const float* rope, int max_pos, int32_t* token_ids,
-                                   int32_t* slot_mapping, int32_t* block_table, int32_t* ctx_lens,
-                                   int32_t* next_tokens, float* logits, a8w8_bf16* final_hidden,
-                                   int device_loop, void* ws, size_t ws_bytes, void* stream) {
+static a8w8_status step_graph_create(a8w8_step_graph** out, const a8w8_model* m,
+                                     const a8w8_config* cfg, int B, int max_blocks, int num_blocks,
+                                     a8w8_bf16* const* k_caches, a8w8_bf16* const* v_caches,
+                                     const float* rope, int max_pos, int32_t* token_ids,
+                                     int32_t* slot_mapping, int32_t* block_table, int32_t* ctx_lens,
+                                     int32_t* next_tokens, float* logits, a8w8_bf16* final_hidden,
+                                     int device_loop, void* ws, size_t ws_bytes, void* stream,
+                                     const StepSampling* smp) {
     if (!out) return fail(A8W8_ERR_INVALID_ARG, "out is NULL");
     *out = nullptr;
     a8w8_status s = check_step(m, cfg, B, max_blocks, num_blocks, k_caches, v_caches, rope, max_pos,
@@ -1506,7 +1522,7 @@ a8w8_status a8w8_step_graph_create(a8w8_step_graph** out, const a8w8_model* m,
         Launch L = make_launch(cap, true);
         s = enqueue_step(m, *cfg, B, g->tok, g->slot, g->table, max_blocks, num_blocks, g->ctx,
                          k_caches, v_caches, rope, max_pos, g->next, logits, final_hidden,
-                         static_cast<unsigned char*>(ws), L, device_loop != 0);
+                         static_cast<unsigned char*>(ws), L, device_loop != 0, nullptr, smp);
         cudaGraph_t graph = nullptr;
         cudaError_t e2 = cudaStreamEndCapture(cap, &graph);
         if (s == A8W8_OK && e2 != cudaSuccess) s = cuda_fail(e2, "end capture");
@@ -1528,6 +1544,48 @@ a8w8_status a8w8_step_graph_create(a8w8_step_graph** out, const a8w8_model* m,
     }
     *out = g;
     return A8W8_OK;
+}
+
+a8w8_status a8w8_step_graph_create(a8w8_step_graph** out, const a8w8_model* m,
+                                   const a8w8_config* cfg, int B, int max_blocks, int num_blocks,
+                                   a8w8_bf16* const* k_caches, a8w8_bf16* const* v_caches,
+                                   const float* rope, int max_pos, int32_t* token_ids,
+                                   int32_t* slot_mapping, int32_t* block_table, int32_t* ctx_lens,
+                                   int32_t* next_tokens, float* logits, a8w8_bf16* final_hidden,
+                                   int device_loop, void* ws, size_t ws_bytes, void* stream) {
+    return step_graph_create(out, m, cfg, B, max_blocks, num_blocks, k_caches, v_caches, rope,
+                             max_pos, token_ids, slot_mapping, block_table, ctx_lens, next_tokens,
+                             logits, final_hidden, device_loop, ws, ws_bytes, stream, nullptr);
+}
+
+a8w8_status a8w8_step_graph_create_sampled(
+    a8w8_step_graph** out, const a8w8_model* m, const a8w8_config* cfg, int B, int max_blocks,
+    int num_blocks, a8w8_bf16* const* k_caches, a8w8_bf16* const* v_caches, const float* rope,
+    int max_pos, int32_t* token_ids, int32_t* slot_mapping, int32_t* block_table,
+    int32_t* ctx_lens, int32_t* next_tokens, float* logits, a8w8_bf16* final_hidden,
+    int device_loop, float temperature, float top_p, uint64_t seed, uint64_t* step_counter,
+    void* sample_ws, size_t sample_ws_bytes, void* ws, size_t ws_bytes, void* stream) {
+    if (out) *out = nullptr;
+    if (!logits) return fail(A8W8_ERR_INVALID_ARG, "a8w8_step_graph_create_sampled: logits is NULL");
+    if (!step_counter || (reinterpret_cast<uintptr_t>(step_counter) & 7))
+        return fail(A8W8_ERR_INVALID_ARG, "step_counter NULL or not 8-byte aligned");
+    if (!std::isfinite(temperature))
+        return fail(A8W8_ERR_INVALID_ARG, "temperature is not finite");
+    if (!(top_p > 0.0f && top_p <= 1.0f))
+        return fail(A8W8_ERR_INVALID_ARG, "top_p=%g outside (0, 1]", (double)top_p);
+    if (cfg && B > 0 && cfg->vocab > 0 &&
+        (!sample_ws || !aligned16(sample_ws) || sample_ws_bytes < a8w8_sample_workspace_bytes(B, cfg->vocab)))
+        return fail(A8W8_ERR_WORKSPACE, "sampling workspace NULL, misaligned or below %zu bytes",
+                    a8w8_sample_workspace_bytes(B, cfg->vocab));
+    StepSampling smp;
+    smp.T = temperature;
+    smp.top_p = top_p;
+    smp.seed = seed;
+    smp.step = step_counter;
+    smp.ws = static_cast<float*>(sample_ws);
+    return step_graph_create(out, m, cfg, B, max_blocks, num_blocks, k_caches, v_caches, rope,
+                             max_pos, token_ids, slot_mapping, block_table, ctx_lens, next_tokens,
+                             logits, final_hidden, device_loop, ws, ws_bytes, stream, &smp);
 }
 
 a8w8_status a8w8_step_graph_launch(a8w8_step_graph* g, void* stream) {

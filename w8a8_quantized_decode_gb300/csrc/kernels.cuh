@@ -209,10 +209,13 @@ cudaError_t launch_embed(const bf16* embed, int vocab, int H, const int32_t* tok
 cudaError_t launch_rope_table(float* rope, int max_pos, int D, double theta, cudaStream_t s);
 
 // Sampling beyond greedy (sample.cu): temperature and top-p by the Gumbel-max
-// rule with Philox4x32-10 noise; ws [B][V][2] floats when 0 < top_p < 1.
+// rule with Philox4x32-10 noise; ws [B][V][2] floats when 0 < top_p < 1. With
+// step_ptr the step is read on the device and advanced by one after the
+// token is picked (the form a captured step graph replays).
 size_t sample_workspace_bytes(int B, int V);
 cudaError_t launch_sample(const float* logits, int B, int V, int ld, float T, float top_p,
-                          uint64_t seed, uint64_t step, float* ws, int32_t* out, const Launch& L);
+                          uint64_t seed, uint64_t step, float* ws, int32_t* out, const Launch& L,
+                          uint64_t* step_ptr = nullptr);
 
 struct LmHeadParams {
     const bf16* hidden;     // [M, H] (pre final norm)

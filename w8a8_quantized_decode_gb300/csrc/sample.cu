@@ -92,6 +92,7 @@ struct SampArgs {
     int V, ld;
     float T, top_p;
     uint64_t seed, step;
+    const uint64_t* step_ptr;   // when set, the step is read from here (captured graphs)
     unsigned char* ws;        // [B][kStateBytes], then [B][V][2] floats
     int32_t* out;
 };
@@ -312,7 +313,9 @@ __global__ void __launch_bounds__(kSampThreads) samp_pick_kernel(const SampArgs 
     const bool nucleus = !greedy && a.top_p < 1.0f;
     const float tau = nucleus ? __uint_as_float(__ldcg(&st->sel[3])) : 0.0f;
     const uint32_t k0 = (uint32_t)a.seed, k1 = (uint32_t)(a.seed >> 32);
-    const uint32_t s0 = (uint32_t)a.step, s1 = (uint32_t)(a.step >> 32);
+    const uint64_t step = a.step_ptr ? __ldcg(reinterpret_cast<const unsigned long long*>(a.step_ptr))
+                                     : a.step;
+    const uint32_t s0 = (uint32_t)step, s1 = (uint32_t)(step >> 32);
     const int i0 = (int)((long long)a.V * c / kChunks), i1 = (int)((long long)a.V * (c + 1) / kChunks);
     unsigned long long best = 0ull;
     for (int i = i0 + threadIdx.x; i < i1; i += kSampThreads) {
@@ -335,6 +338,14 @@ __global__ void __launch_bounds__(kSampThreads) samp_pick_kernel(const SampArgs 
     if (threadIdx.x == 0) a.out[b] = (int32_t)(0xffffffffu - (unsigned)(__ldcg(&st->best) & 0xffffffffull));
 }
 
+// Advances a captured graph's step counter once the pick pass (which read
+// it) has completed.
+__global__ void __launch_bounds__(32) samp_step_kernel(uint64_t* step_ptr) {
+    pdl_wait();
+    pdl_trigger();
+    if (threadIdx.x == 0) *step_ptr += 1;
+}
+
 template <typename Kern>
 cudaError_t launch_pass(Kern kern, int B, const SampArgs& a, const Launch& L) {
     cudaLaunchConfig_t cfg = {};
@@ -355,9 +366,11 @@ cudaError_t launch_pass(Kern kern, int B, const SampArgs& a, const Launch& L) {
 size_t sample_workspace_bytes(int B, int V) { return (size_t)B * (kStateBytes + (size_t)V * 8); }
 
 cudaError_t launch_sample(const float* logits, int B, int V, int ld, float T, float top_p,
-                          uint64_t seed, uint64_t step, float* ws, int32_t* out, const Launch& L) {
+                          uint64_t seed, uint64_t step, float* ws, int32_t* out, const Launch& L,
+                          uint64_t* step_ptr) {
     if (B <= 0) return cudaSuccess;
     SampArgs a;
+    a.step_ptr = step_ptr;
     a.logits = logits;
     a.V = V;
     a.ld = ld;
@@ -377,7 +390,18 @@ cudaError_t launch_sample(const float* logits, int B, int V, int ld, float T, fl
         if ((e = launch_pass(samp_level_kernel<1>, B, a, L)) != cudaSuccess) return e;
         if ((e = launch_pass(samp_level_kernel<2>, B, a, L)) != cudaSuccess) return e;
     }
-    return launch_pass(samp_pick_kernel, B, a, L);
+    if ((e = launch_pass(samp_pick_kernel, B, a, L)) != cudaSuccess) return e;
+    if (!step_ptr) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(32);
+    cfg.stream = L.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = L.pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, samp_step_kernel, step_ptr);
 }
 
 }  // namespace a8w8
