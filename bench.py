@@ -355,13 +355,16 @@ def run_ours(args, cfg):
         h_bt = torch.from_numpy(bt.copy()).pin_memory()
         h_ctx = torch.zeros(B, dtype=torch.int32).pin_memory()
         h_next = torch.zeros(B, dtype=torch.int32).pin_memory()
-        h_tok[0] = int(prompt[-1])
+        # numpy views of the pinned buffers: the per-step host updates are
+        # plain stores into the memory the copies read
+        n_tok, n_slot, n_ctx, n_next = (t.numpy() for t in (h_tok, h_slot, h_ctx, h_next))
+        n_tok[0] = int(prompt[-1])
 
         def e2e_step(pos):
-            h_ctx[0] = pos + 1
-            h_slot[0] = int(bt[0, pos // page]) * page + pos % page
+            n_ctx[0] = pos + 1
+            n_slot[0] = int(bt[0, pos // page]) * page + pos % page
             e2e_graph.run_host(h_tok, h_slot, h_bt, h_ctx, h_next, stream=stream)
-            h_tok[0] = int(h_next[0])
+            n_tok[0] = n_next[0]
 
         for i in range(args.warmup):
             e2e_step(PROMPT_LEN + i)

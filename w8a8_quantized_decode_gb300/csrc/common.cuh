@@ -298,6 +298,33 @@ __device__ __forceinline__ bf16 norm_bf16_fast(float xw, f2 inv) {
     return f2_to_bf16(f2_mulf(inv, xw));
 }
 
+// act = RN_bf16(silu(g) u) for float32 g, u: g u / (1 + e) for g >= 0 and
+// g u e / (1 + e) for g < 0, e = exp(-|g|), evaluated in two-float
+// arithmetic (f2_exp, f2_div) so that the BF16 rounding is that of the exact
+// value. A float32 evaluation decides first where it can: with expf within a
+// few units of its result, the three float roundings and e <= 1, it is within
+// about 10 float32 units of the exact value, so where it lies more than 64
+// units from a BF16 midpoint (low 16 bits 0x8000), is normal and finite, its
+// own BF16 rounding is the exact value's; elsewhere (about 0.2 % of values)
+// the two-float form decides.
+__device__ __forceinline__ bf16 swiglu_bf16(float g, float u) {
+    {
+        const float ef = expf(-fabsf(g));
+        float r = __fdiv_rn(__fmul_rn(g, u), __fadd_rn(1.0f, ef));
+        if (g < 0.0f) r = __fmul_rn(r, ef);
+        const unsigned ur = __float_as_uint(r);
+        const unsigned ex = ur & 0x7F800000u;
+        const unsigned d = (ur & 0xFFFFu) - (0x8000u - 64u);   // < 129 near the midpoint
+        // (g > -80: for g < 0 the result is scaled by e, which must be a
+        // normal float, not a subnormal with few significant bits)
+        if (d >= 129u && ex != 0u && ex != 0x7F800000u && g > -80.0f) return __float2bfloat16_rn(r);
+    }
+    const f2 e = f2_exp(f2_make(-fabsf(g)));
+    f2 num = two_prod(g, u);
+    if (g < 0.0f) num = f2_mul(num, e);
+    return f2_to_bf16(f2_div(num, f2_addf(e, 1.0f)));
+}
+
 __device__ __forceinline__ void set_error(unsigned* err, unsigned bit) {
     if (err) atomicOr(err, bit);
 }

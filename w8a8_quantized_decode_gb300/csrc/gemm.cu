@@ -43,10 +43,7 @@ __global__ void __launch_bounds__(256) gemm_epilogue_kernel(const GemvParams p, 
         const int au = acc[(size_t)b * ldacc + p.N + o];
         const float gv = __fmul_rn(__fmul_rn(__int2float_rn(ag), xs), p.w_scale[o]);
         const float uv = __fmul_rn(__fmul_rn(__int2float_rn(au), xs), p.w_scale[p.N + o]);
-        const f2 e = f2_exp(f2_make(-fabsf(gv)));
-        f2 num = two_prod(gv, uv);
-        if (gv < 0.0f) num = f2_mul(num, e);
-        p.y[(size_t)b * p.ldy + o] = f2_to_bf16(f2_div(num, f2_addf(e, 1.0f)));
+        p.y[(size_t)b * p.ldy + o] = swiglu_bf16(gv, uv);
     }
 }
 

@@ -113,13 +113,9 @@ __global__ void __launch_bounds__(kBfThreads) gemv_bf16_kernel(const Bf16GemvPar
                     if (p.residual) sum = __fadd_rn(sum, bf2f(ld_cg_bf16(p.residual + (size_t)m * p.ldy + n)));
                     p.y[(size_t)m * p.ldy + n] = f2bf(sum);
                 } else {
-                    // silu(g) u = g u sigmoid(g) in two-float arithmetic, the
-                    // exponential taken of -|g| (as in the A8W8 epilogue)
+                    // silu(g) u correctly rounded (as in the A8W8 epilogue)
                     const float g = acc[0][m], u = acc[NSEG - 1][m];
-                    const f2 e = f2_exp(f2_make(-fabsf(g)));
-                    f2 num = two_prod(g, u);
-                    if (g < 0.0f) num = f2_mul(num, e);
-                    p.y[(size_t)m * p.ldy + n] = f2_to_bf16(f2_div(num, f2_addf(e, 1.0f)));
+                    p.y[(size_t)m * p.ldy + n] = swiglu_bf16(g, u);
                 }
             }
         }

@@ -351,13 +351,7 @@ __device__ __forceinline__ void epilogue(const GemvParams& p, const int32_t* acc
                                       use_pre ? pre[i] : p.w_scale[o]);
             const float u = __fmul_rn(__fmul_rn(__int2float_rn(au), xs[b]),
                                       use_pre ? pre[nt + i] : p.w_scale[N + o]);
-            // silu(g) * u = g u sigmoid(g) in two-float arithmetic (see f2),
-            // with the exponential taken of -|g|: g u / (1 + e) for g >= 0,
-            // g u e / (1 + e) for g < 0, e = exp(-|g|)
-            const f2 e = f2_exp(f2_make(-fabsf(g)));
-            f2 num = two_prod(g, u);
-            if (g < 0.0f) num = f2_mul(num, e);
-            p.y[(size_t)b * p.ldy + o] = f2_to_bf16(f2_div(num, f2_addf(e, 1.0f)));
+            p.y[(size_t)b * p.ldy + o] = swiglu_bf16(g, u);
             if (p.acc_out) {
                 p.acc_out[(size_t)b * 2 * N + o] = ag;
                 p.acc_out[(size_t)b * 2 * N + N + o] = au;
