@@ -207,7 +207,8 @@ cudaError_t launch_ring(const GemvParams& p, const Launch& L, bool stream) {
     const int G = L.num_sms;
     const int nseg = EPI == EPI_SWIGLU ? 2 : 1;
     const size_t smem =
-        stream ? smem_layout(BT, nseg, KS, p.K, p.N, G, stream_threads(BT), stream_ring_bytes<BT, NB>()).total
+        stream ? smem_layout(BT, nseg, KS, p.K, p.N, G, stream_threads(BT), stream_ring_bytes<BT, NB>(),
+                             p.late_ctas, p.late_w).total
                : smem_layout(BT, nseg, KS, p.K, p.N, G, kGenThreads).total;
     {
         // the shared-memory limit, set once per CUDA context
@@ -217,6 +218,8 @@ cudaError_t launch_ring(const GemvParams& p, const Launch& L, bool stream) {
         if (e != cudaSuccess) return e;
     }
     if (smem > (size_t)kMaxDynSmem) return cudaErrorInvalidValue;
+    GemvParams q = p;
+    if (!stream) q.late_ctas = 0;   // the general kernel keeps equal shares
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(G);
     cfg.blockDim = dim3(stream ? stream_threads(BT) : kGenThreads);
@@ -227,7 +230,7 @@ cudaError_t launch_ring(const GemvParams& p, const Launch& L, bool stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = L.pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, kern, p);
+    return cudaLaunchKernelEx(&cfg, kern, q);
 }
 
 template <int BT, int PRO, int EPI, int KS>
@@ -237,7 +240,8 @@ cudaError_t launch_t(const GemvParams& p, const Launch& L) {
         if (stream && p.deep) {
             const int nseg = EPI == EPI_SWIGLU ? 2 : 1;
             const size_t deep = smem_layout(BT, nseg, KS, p.K, p.N, L.num_sms, stream_threads(BT),
-                                            stream_ring_bytes<BT, kDeepNB>()).total;
+                                            stream_ring_bytes<BT, kDeepNB>(), p.late_ctas,
+                                            p.late_w).total;
             if (deep <= (size_t)kMaxDynSmem)
                 return launch_ring<BT, PRO, EPI, KS, kDeepNB, kDeepNB>(p, L, stream);
         }

@@ -360,6 +360,29 @@ __device__ __forceinline__ void epilogue(const GemvParams& p, const int32_t* acc
     }
 }
 
+// Row partition of the streaming kernel: equal shares, or with `late` > 0
+// the last `late` CTAs (the ones dispatched last, onto the SMs that free up
+// last) take shares of relative size w and the others the rest evenly. Each
+// output row is still reduced and finished by one CTA, so where the rows run
+// changes no result.
+__host__ __device__ __forceinline__ bool part_skewed(int G, int late, float w) {
+    return late > 0 && late < G && w > 0.0f && w < 1.0f;
+}
+__host__ __device__ __forceinline__ int part_bound(int N, int c, int G, int late, float w) {
+    if (c <= 0) return 0;
+    if (c >= G) return N;
+    if (!part_skewed(G, late, w)) return (int)(((long long)N * c) / G);
+    const int e = G - late;
+    const float wc = c <= e ? (float)c : (float)e + (float)(c - e) * w;
+    const float wg = (float)e + (float)late * w;
+    return min(N, (int)((float)N * wc / wg));
+}
+// Rows of the largest share.
+__host__ __device__ __forceinline__ int part_rows_max(int N, int G, int late, float w) {
+    if (!part_skewed(G, late, w)) return (N + G - 1) / G;
+    return (int)ceilf((float)N / ((float)(G - late) + (float)late * w)) + 1;
+}
+
 // Shared-memory layout common to both kernels. `stage` (BF16 copy of the
 // activation rows) is present when it fits in kStageBudget (stage == 0: none).
 constexpr size_t kStageBudget = 48 * 1024;
@@ -368,8 +391,9 @@ struct SmemLayout {
 };
 __host__ __device__ __forceinline__ SmemLayout smem_layout(int BT, int nseg, int KS, int K, int N,
                                                            int G, int nthreads,
-                                                           size_t ring_bytes = 0) {
-    const int rows_max = (N + G - 1) / G;
+                                                           size_t ring_bytes = 0, int late = 0,
+                                                           float late_w = 0.0f) {
+    const int rows_max = part_rows_max(N, G, late, late_w);
     SmemLayout s;
     s.act = 0;
     s.accs = align16((size_t)BT * K);
@@ -408,10 +432,10 @@ __device__ __forceinline__ bool stream_gemv(const GemvParams& p, unsigned char* 
     constexpr int NW = NT / 32;
     const int K = p.K, N = p.N;
     const int G = gridDim.x;
-    const int o0 = (int)(((long long)N * blockIdx.x) / G);
-    const int o1 = (int)(((long long)N * (blockIdx.x + 1)) / G);
+    const int o0 = part_bound(N, blockIdx.x, G, p.late_ctas, p.late_w);
+    const int o1 = part_bound(N, blockIdx.x + 1, G, p.late_ctas, p.late_w);
     const int nrows = o1 - o0;
-    const int rows_max = (N + G - 1) / G;
+    const int rows_max = part_rows_max(N, G, p.late_ctas, p.late_w);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int upr = K / kUnit;            // units per row
@@ -422,7 +446,8 @@ __device__ __forceinline__ bool stream_gemv(const GemvParams& p, unsigned char* 
     const int u1 = (int)(((long long)U * (warp + 1)) / NW);
     const int n = u1 - u0;
 
-    const SmemLayout L = smem_layout(BT, NSEG, KS, K, N, G, NT, ring_bytes<NT, UNR, NB>());
+    const SmemLayout L = smem_layout(BT, NSEG, KS, K, N, G, NT, ring_bytes<NT, UNR, NB>(), p.late_ctas,
+                                     p.late_w);
     const uint32_t ring = (uint32_t)__cvta_generic_to_shared(smem + L.ring) + threadIdx.x * 16u;
 
     // load stream: contiguous bytes inside a segment

@@ -64,6 +64,8 @@ struct GemvParams {
     int deep;               // streaming kernel, 1-2 rows: a ring deep enough for the
                             // CTA's whole share (up to 11 units per warp), all of it
                             // requested before the dependency wait, where it fits
+    int late_ctas;          // streaming kernel: the last late_ctas CTAs take shares of
+    float late_w;           // relative size late_w (0 / 1: equal shares)
 };
 
 // Largest batch tile one launch handles; bigger batches are tiled by the host.
