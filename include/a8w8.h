@@ -5,10 +5,11 @@
  * INT8 weights and dynamically quantised INT8 activations on one GPU:
  * per-row activation quantisation, INT8 x INT8 -> INT32 projections with FP32
  * dequantisation, RMSNorm, per-head QK-RMSNorm + RoPE, a paged BF16 KV cache,
- * GQA decode attention, SwiGLU, and the LM head with greedy argmax; also a
- * prefill chunk, the prompt-to-first-token step, sampling beyond greedy, and
- * two variants: the INT8 KV cache with FP32 row scales and the BF16
- * (unquantised) layer.
+ * GQA decode attention, SwiGLU, and the LM head with greedy argmax; the step
+ * as a replayable CUDA graph (optionally decoding on the device, greedily or
+ * with sampling inside the graph); also a prefill chunk, the
+ * prompt-to-first-token step, sampling beyond greedy, and two variants: the
+ * INT8 KV cache with FP32 row scales and the BF16 (unquantised) layer.
  *
  * Sources, cited by page title and section:
  *   [LIB-810] "perf(qwen3-a8w8): optimize decode scheduling and data paths"
