@@ -457,6 +457,74 @@ def run_ours(args, cfg):
         torch.distributed.destroy_process_group()
 
 
+SAMPLED_T, SAMPLED_TOP_P = 0.8, 0.95
+
+
+def run_sampled(args, cfg):
+    """The headline workload (40 layers, batch 1, 16-token prompt, max_seq_len
+    256) decoded with temperature / top-p sampling inside the replayed
+    device-loop graph (a8w8_step_graph_create_sampled): TPOT with the sampler
+    over the full vocabulary in every step."""
+    import torch
+    import w8a8_quantized_decode_gb300 as a8w8
+
+    device = torch.device("cuda:0")
+    torch.cuda.set_device(device)
+    a8w8.build()
+    B, page = 1, cfg["page_size"]
+    max_blocks = MAX_SEQ // page
+    if PROMPT_LEN + args.warmup + args.steps > MAX_SEQ:
+        raise SystemExit("prompt + warmup + steps exceeds max_seq_len")
+    model = build_model(cfg, device)
+    Hkv, D, L = cfg["num_kv_heads"], cfg["head_dim"], cfg["num_layers"]
+    nblk = max_blocks + 1
+    bt = np.random.default_rng(SEED + 1).permutation(nblk).astype(np.int32)[:max_blocks][None, :]
+    kc = [torch.zeros((nblk * page, Hkv, D), dtype=torch.bfloat16, device=device) for _ in range(L)]
+    vc = [torch.zeros((nblk * page, Hkv, D), dtype=torch.bfloat16, device=device) for _ in range(L)]
+    rope = a8w8.a8w8_rope_table(MAX_SEQ, D, cfg["rope_theta"], device=device)
+    ws = a8w8.alloc_workspace(cfg, B, max_blocks, device=device)
+    logits = torch.empty((B, cfg["vocab"]), dtype=torch.float32, device=device)
+    stream = torch.cuda.Stream(device)
+    with torch.cuda.stream(stream):
+        g = a8w8.StepGraph(model, cfg, B, max_blocks, kc, vc, rope, ws, logits=logits,
+                           device_loop=True, stream=stream,
+                           sampling=dict(temperature=SAMPLED_T, top_p=SAMPLED_TOP_P, seed=SEED,
+                                         step=0))
+        prompt = synth.prompt_ids(SEED + 5, PROMPT_LEN, cfg["vocab"])
+        g.block_table.copy_(torch.from_numpy(bt))
+        for i in range(PROMPT_LEN):
+            ctx = np.array([i + 1], np.int32)
+            g.token_ids.copy_(torch.from_numpy(prompt[i:i + 1]))
+            g.ctx_lens.copy_(torch.from_numpy(ctx))
+            g.slot_mapping.copy_(torch.from_numpy(synth.slots_for(bt, ctx - 1, page)))
+            g.launch(stream)
+        for _ in range(args.warmup):
+            g.launch(stream)
+        stream.synchronize()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        with ClockSampler(None) as clocks:
+            ev0.record(stream)
+            for _ in range(args.steps):
+                g.launch(stream)
+            ev1.record(stream)
+            ev1.synchronize()
+        tpot = ev0.elapsed_time(ev1) / args.steps
+        errs = a8w8.read_device_errors(stream)
+        g.close()
+    print(json.dumps({
+        "metric": "A8W8 decode TPOT with in-graph sampling (ms/token, 40 layers, bs=1)",
+        "value": tpot, "unit": "ms/token", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "higher_is_better": False, "vs_baseline": None,
+        "dtype": "int8 x int8 -> int32, f32 dequant, bf16 activations; two-float sampling masses",
+        "data": "synthetic (seeded random-init weights drawn on the device)",
+        "config": {"workload": "qwen3_14b_a8w8_decode_step_b1_sampled", "batch": 1, "layers": L,
+                   "vocab": cfg["vocab"], "temperature": SAMPLED_T, "top_p": SAMPLED_TOP_P,
+                   "prompt_len": PROMPT_LEN, "max_seq_len": MAX_SEQ},
+        "tokens_per_s": 1000.0 / tpot, "gpu_launches": None, "clocks": clocks.summary(),
+        "device_errors": errs}), flush=True)
+
+
 BATCHED_B = 16
 BATCHED_WORKLOAD = "qwen3_14b_a8w8_batched_decode_b16"
 BATCHED_METRIC = "A8W8 batched decode step (ms/step, 40 layers, bs=16, contexts 64..4096)"
@@ -1081,8 +1149,9 @@ def build_parser() -> argparse.ArgumentParser:
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--workload", choices=["decode_b1", "batched16", "batched16_i8kv", "prefill",
-                                           "ttft", "sample", *LAYER_B1_VARIANTS],
+    ap.add_argument("--workload", choices=["decode_b1", "decode_b1_sampled", "batched16",
+                                           "batched16_i8kv", "prefill", "ttft", "sample",
+                                           *LAYER_B1_VARIANTS],
                     default="decode_b1")
     ap.add_argument("--layers", type=int, default=40,
                     help="layers of the model (fewer only for profiling captures)")
@@ -1109,6 +1178,8 @@ def main():
         run_prefill(args, cfg)
     elif args.workload == "sample":
         run_sample(args, cfg)
+    elif args.workload == "decode_b1_sampled":
+        run_sampled(args, cfg)
     elif args.workload in LAYER_B1_VARIANTS:
         run_layer_b1(args, cfg)
     else:
